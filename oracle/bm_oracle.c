@@ -1,0 +1,179 @@
+/*
+ * CPU oracle for the BF16 BLAS3 hot path: GEMM and SYRK, plain triple loops
+ * accumulating in double.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing in the product path links, loads or calls
+ * this file; only the tests, the smoke check and the bench's CPU-baseline leg
+ * do. It shares no code with the CUDA library.
+ *
+ * What is computed (the BLAS3 statement of the local compute in "BLASMp
+ * development notes", section 1, and the GEMM that the "cp.async / ldmatrix
+ * ablation plan", section 2, dissects):
+ *
+ *   GEMM:  C[i][j] = alpha * sum_p op(A)[i][p] * op(B)[p][j] + beta * C[i][j]
+ *          op(A) is m x k, op(B) is k x n, all matrices row-major.
+ *   SYRK:  C[i][j] = alpha * sum_p op(A)[i][p] * op(A)[j][p] + beta * C[i][j]
+ *          for (i, j) in one triangle of the n x n matrix C; op(A) is n x k
+ *          ("SYRK main compute done with a GEMM", BLASMp notes, stage B).
+ *
+ * Alongside each value the oracle returns bound[i][j] = sum_p |product|, the
+ * scale against which the tolerance max|C - C_ref| <= 1e-3 * |alpha| * bound
+ * is stated.
+ *
+ * BLAS conventions (the plainest reading of "BLAS3"): when alpha == 0 or
+ * k == 0 the products are not formed and A is not read; when beta == 0 the
+ * input C is not read. Storage: element (r, c) of a row-major matrix X with
+ * leading dimension ld sits at X[r * ld + c]. op(X) = X for trans == 0 and
+ * X^T for trans == 1.
+ *
+ * Products of two bf16 values are exact in double (8 + 8 significant bits),
+ * and the sum runs over p in ascending order; no blocking or reordering.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* bf16 bit pattern -> double, exact (bf16 is the top half of a float32). */
+static double bf16_value(uint16_t bits)
+{
+    uint32_t word = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &word, sizeof f);
+    return (double)f;
+}
+
+/* Element (r, c) of op(X), X stored row-major with leading dimension ld. */
+static double op_at(const uint16_t *X, int64_t ld, int trans, int64_t r, int64_t c)
+{
+    if (trans)
+        return bf16_value(X[c * ld + r]);
+    return bf16_value(X[r * ld + c]);
+}
+
+/* Element (i, j) of the input C, float32 or bf16. */
+static double c_input(const void *C, int64_t ldc, int c_is_bf16, int64_t i, int64_t j)
+{
+    if (c_is_bf16)
+        return bf16_value(((const uint16_t *)C)[i * ldc + j]);
+    return (double)((const float *)C)[i * ldc + j];
+}
+
+/* One output element of GEMM. */
+static void gemm_element(int64_t i, int64_t j, int64_t k, int transA, int transB, double alpha,
+                         const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb,
+                         double beta, const void *C, int64_t ldc, int c_is_bf16,
+                         double *ref, double *bound)
+{
+    double acc = 0.0, mag = 0.0;
+    if (alpha != 0.0) {
+        for (int64_t p = 0; p < k; ++p) {
+            double prod = op_at(A, lda, transA, i, p) * op_at(B, ldb, transB, p, j);
+            acc += prod;
+            mag += fabs(prod);
+        }
+    }
+    double value = alpha * acc;
+    if (beta != 0.0)
+        value += beta * c_input(C, ldc, c_is_bf16, i, j);
+    *ref = value;
+    *bound = mag;
+}
+
+/* One output element of SYRK: the product of rows i and j of op(A). */
+static void syrk_element(int64_t i, int64_t j, int64_t k, int trans, double alpha,
+                         const uint16_t *A, int64_t lda, double beta, const void *C,
+                         int64_t ldc, int c_is_bf16, double *ref, double *bound)
+{
+    double acc = 0.0, mag = 0.0;
+    if (alpha != 0.0) {
+        for (int64_t p = 0; p < k; ++p) {
+            double prod = op_at(A, lda, trans, i, p) * op_at(A, lda, trans, j, p);
+            acc += prod;
+            mag += fabs(prod);
+        }
+    }
+    double value = alpha * acc;
+    if (beta != 0.0)
+        value += beta * c_input(C, ldc, c_is_bf16, i, j);
+    *ref = value;
+    *bound = mag;
+}
+
+/* Is (i, j) in the referenced triangle? uplo 0 = lower (i >= j), 1 = upper (i <= j). */
+static int in_triangle(int uplo, int64_t i, int64_t j)
+{
+    return uplo == 0 ? (i >= j) : (i <= j);
+}
+
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* Full GEMM: ref and bound are m x n row-major with leading dimension ldr. */
+void oracle_gemm(int64_t m, int64_t n, int64_t k, int transA, int transB, double alpha,
+                 const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb, double beta,
+                 const void *C, int64_t ldc, int c_is_bf16, double *ref, double *bound,
+                 int64_t ldr)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < m; ++i)
+        for (int64_t j = 0; j < n; ++j)
+            gemm_element(i, j, k, transA, transB, alpha, A, lda, B, ldb, beta, C, ldc,
+                         c_is_bf16, &ref[i * ldr + j], &bound[i * ldr + j]);
+}
+
+/* GEMM at `count` chosen positions (rows[t], cols[t]). */
+void oracle_gemm_entries(int64_t k, int transA, int transB, double alpha, const uint16_t *A,
+                         int64_t lda, const uint16_t *B, int64_t ldb, double beta, const void *C,
+                         int64_t ldc, int c_is_bf16, int64_t count, const int64_t *rows,
+                         const int64_t *cols, double *ref, double *bound)
+{
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t t = 0; t < count; ++t)
+        gemm_element(rows[t], cols[t], k, transA, transB, alpha, A, lda, B, ldb, beta, C, ldc,
+                     c_is_bf16, &ref[t], &bound[t]);
+}
+
+/* Full SYRK: entries outside the triangle are set to NaN (not referenced). */
+void oracle_syrk(int uplo, int trans, int64_t n, int64_t k, double alpha, const uint16_t *A,
+                 int64_t lda, double beta, const void *C, int64_t ldc, int c_is_bf16,
+                 double *ref, double *bound, int64_t ldr)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < n; ++i)
+        for (int64_t j = 0; j < n; ++j) {
+            if (in_triangle(uplo, i, j)) {
+                syrk_element(i, j, k, trans, alpha, A, lda, beta, C, ldc, c_is_bf16,
+                             &ref[i * ldr + j], &bound[i * ldr + j]);
+            } else {
+                ref[i * ldr + j] = NAN;
+                bound[i * ldr + j] = NAN;
+            }
+        }
+}
+
+/* SYRK at chosen positions; positions outside the triangle give NaN. */
+void oracle_syrk_entries(int uplo, int trans, int64_t k, double alpha, const uint16_t *A,
+                         int64_t lda, double beta, const void *C, int64_t ldc, int c_is_bf16,
+                         int64_t count, const int64_t *rows, const int64_t *cols, double *ref,
+                         double *bound)
+{
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t t = 0; t < count; ++t) {
+        if (in_triangle(uplo, rows[t], cols[t])) {
+            syrk_element(rows[t], cols[t], k, trans, alpha, A, lda, beta, C, ldc, c_is_bf16,
+                         &ref[t], &bound[t]);
+        } else {
+            ref[t] = NAN;
+            bound[t] = NAN;
+        }
+    }
+}

@@ -1,0 +1,259 @@
+"""Pins for the CPU oracle: checks that tie it to something other than itself.
+
+Each pin takes an ``oracle.Oracle`` handle and raises AssertionError when the
+oracle disagrees with
+
+* brute force in exact rational arithmetic on tiny integer inputs,
+* NumPy's float64 matmul on the decoded operands (a library routine),
+* closed forms (ones, rank one, identity),
+* the invariants (A*B)^T = B^T*A^T, SYRK = one triangle of GEMM(A, A^T),
+  beta=1 accumulation = C0 + a beta=0 call, exact power-of-two alpha scaling,
+* the BLAS conventions for alpha = 0, beta = 0 and k = 0.
+
+``tests/test_oracle_mutants.py`` plants plausible mistakes in copies of the
+oracle's C source and checks that every one of them fails at least one pin.
+"""
+
+from __future__ import annotations
+
+from fractions import Fraction
+import itertools
+
+import numpy as np
+
+import bm_inputs as gen
+
+BF16_ONE = np.uint16(0x3F80)
+
+
+def _stored(rows, cols, trans):
+    """Stored shape of op(X) (rows x cols) for the trans flag."""
+    return (cols, rows) if trans else (rows, cols)
+
+
+def _int_bf16(shape, seed, lo=-4, hi=4, pad=0):
+    vals = gen.integers(seed, shape[0] * shape[1], lo, hi).reshape(shape)
+    bits = gen.f32_to_bf16_bits(vals)
+    if pad:
+        bits = gen.pad_ld(bits, shape[1] + pad, gen.BF16_NAN)
+    return bits, vals
+
+
+def _op(vals, trans):
+    return vals.T if trans else vals
+
+
+# --- brute force in exact arithmetic --------------------------------------------
+def pin_gemm_bruteforce_exact(o):
+    shapes = [(1, 1, 1), (3, 5, 4), (7, 2, 9), (4, 6, 1)]
+    alphas = [Fraction(1), Fraction(-2), Fraction(1, 2)]
+    betas = [Fraction(0), Fraction(1), Fraction(-1, 2)]
+    seed = 100
+    for (m, n, k), tA, tB in itertools.product(shapes, (0, 1), (0, 1)):
+        seed += 3
+        A, Av = _int_bf16(_stored(m, k, tA), seed, pad=3)
+        B, Bv = _int_bf16(_stored(k, n, tB), seed + 1, pad=2)
+        opA, opB = _op(Av, tA), _op(Bv, tB)
+        prod = [[sum(Fraction(int(opA[i, p])) * Fraction(int(opB[p, j])) for p in range(k))
+                 for j in range(n)] for i in range(m)]
+        mag = [[sum(abs(int(opA[i, p]) * int(opB[p, j])) for p in range(k))
+                for j in range(n)] for i in range(m)]
+        for alpha, beta, cbf in itertools.product(alphas, betas, (False, True)):
+            Cv = gen.integers(seed + 2, m * n, -8, 8).reshape(m, n)
+            C = gen.f32_to_bf16_bits(Cv) if cbf else Cv.astype(np.float32)
+            ref, bound = o.gemm(m, n, k, tA, tB, float(alpha), A, B, float(beta), C)
+            for i in range(m):
+                for j in range(n):
+                    want = alpha * prod[i][j] + beta * Fraction(int(Cv[i, j]))
+                    assert Fraction(ref[i, j]) == want, (m, n, k, tA, tB, alpha, beta, cbf, i, j)
+                    assert bound[i, j] == mag[i][j], (m, n, k, tA, tB, i, j)
+
+
+def pin_syrk_bruteforce_exact(o):
+    for (n, k), uplo, trans in itertools.product([(1, 1), (5, 3), (6, 8)], (0, 1), (0, 1)):
+        A, Av = _int_bf16(_stored(n, k, trans), 7 + n + 10 * k + 100 * uplo + 1000 * trans, pad=1)
+        opA = _op(Av, trans)
+        Cv = gen.integers(55, n * n, -8, 8).reshape(n, n)
+        C = Cv.astype(np.float32)
+        for alpha, beta in [(Fraction(1), Fraction(1)), (Fraction(-1, 2), Fraction(0)),
+                            (Fraction(2), Fraction(-3, 2))]:
+            ref, bound = o.syrk(uplo, trans, n, k, float(alpha), A, float(beta), C)
+            for i in range(n):
+                for j in range(n):
+                    inside = (i >= j) if uplo == 0 else (i <= j)
+                    if not inside:
+                        assert np.isnan(ref[i, j]) and np.isnan(bound[i, j]), (n, k, uplo, trans, i, j)
+                        continue
+                    s = sum(Fraction(int(opA[i, p])) * Fraction(int(opA[j, p])) for p in range(k))
+                    want = alpha * s + beta * Fraction(int(Cv[i, j]))
+                    assert Fraction(ref[i, j]) == want, (n, k, uplo, trans, i, j)
+                    assert bound[i, j] == sum(abs(int(opA[i, p]) * int(opA[j, p])) for p in range(k))
+
+
+# --- NumPy float64 matmul ------------------------------------------------------
+def pin_gemm_matches_numpy(o):
+    m, n, k = 37, 29, 53
+    for tA, tB in itertools.product((0, 1), (0, 1)):
+        A = gen.matrix_bf16(*_stored(m, k, tA), "normal", seed=11 + tA)
+        B = gen.matrix_bf16(*_stored(k, n, tB), "normal", seed=21 + tB)
+        C = gen.matrix_f32(m, n, "normal", seed=31)
+        a = _op(gen.bf16_bits_to_f32(A).astype(np.float64), tA)
+        b = _op(gen.bf16_bits_to_f32(B).astype(np.float64), tB)
+        alpha, beta = 0.75, -1.25
+        want = alpha * (a @ b) + beta * C.astype(np.float64)
+        ref, bound = o.gemm(m, n, k, tA, tB, alpha, A, B, beta, C)
+        scale = abs(alpha) * (np.abs(a) @ np.abs(b)) + abs(beta) * np.abs(C)
+        assert np.all(np.abs(ref - want) <= 1e-13 * scale + 1e-300), (tA, tB)
+        assert np.allclose(bound, np.abs(a) @ np.abs(b), rtol=1e-13, atol=0), (tA, tB)
+
+
+def pin_syrk_matches_numpy(o):
+    n, k = 23, 31
+    for uplo, trans in itertools.product((0, 1), (0, 1)):
+        A = gen.matrix_bf16(*_stored(n, k, trans), "normal", seed=41 + trans)
+        C = gen.symmetric_f32(n, seed=43)
+        a = _op(gen.bf16_bits_to_f32(A).astype(np.float64), trans)
+        want = 1.5 * (a @ a.T) + 0.5 * C.astype(np.float64)
+        ref, _ = o.syrk(uplo, trans, n, k, 1.5, A, 0.5, C)
+        mask = np.tril(np.ones((n, n), bool)) if uplo == 0 else np.triu(np.ones((n, n), bool))
+        scale = 1.5 * (np.abs(a) @ np.abs(a).T) + 0.5 * np.abs(C)
+        assert np.all(np.abs(ref[mask] - want[mask]) <= 1e-13 * scale[mask]), (uplo, trans)
+        assert np.all(np.isnan(ref[~mask])), (uplo, trans)
+
+
+# --- closed forms -----------------------------------------------------------------
+def pin_identity(o):
+    n = 19
+    eye = np.zeros((n, n), np.uint16)
+    eye[np.arange(n), np.arange(n)] = BF16_ONE
+    B = gen.matrix_bf16(n, 13, "normal", seed=5)
+    ref, _ = o.gemm(n, 13, n, 0, 0, 1.0, eye, B)
+    assert np.array_equal(ref, gen.bf16_bits_to_f32(B).astype(np.float64))
+    A = gen.matrix_bf16(11, n, "normal", seed=6)
+    ref, _ = o.gemm(11, n, n, 0, 0, 1.0, A, eye)
+    assert np.array_equal(ref, gen.bf16_bits_to_f32(A).astype(np.float64))
+
+
+def pin_closed_forms(o):
+    m, n, k = 9, 12, 40
+    ones_a = np.full((m, k), BF16_ONE, np.uint16)
+    ones_b = np.full((k, n), BF16_ONE, np.uint16)
+    ref, bound = o.gemm(m, n, k, 0, 0, 1.0, ones_a, ones_b)
+    assert np.all(ref == k) and np.all(bound == k)
+    # rank one: op(A)[i][p] = i - 2, op(B)[p][j] = j - 1  ->  C = k (i - 2)(j - 1)
+    x = np.arange(m, dtype=np.float64) - 2
+    y = np.arange(n, dtype=np.float64) - 1
+    A = gen.f32_to_bf16_bits(np.repeat(x[:, None], k, axis=1))
+    B = gen.f32_to_bf16_bits(np.repeat(y[None, :], k, axis=0))
+    ref, bound = o.gemm(m, n, k, 0, 0, -3.0, A, B)
+    assert np.array_equal(ref, -3.0 * k * np.outer(x, y))
+    assert np.array_equal(bound, k * np.abs(np.outer(x, y)))
+    # SYRK of rows of constant value v_i: C = k v_i v_j
+    v = np.arange(n, dtype=np.float64) - 5
+    Asy = gen.f32_to_bf16_bits(np.repeat(v[:, None], k, axis=1))
+    ref, _ = o.syrk(0, 0, n, k, 1.0, Asy)
+    low = np.tril(np.ones((n, n), bool))
+    assert np.array_equal(ref[low], (k * np.outer(v, v))[low])
+
+
+# --- invariants ---------------------------------------------------------------------
+def pin_transpose_identity(o):
+    m, n, k = 21, 17, 26
+    for tA, tB in itertools.product((0, 1), (0, 1)):
+        A = gen.matrix_bf16(*_stored(m, k, tA), "normal", seed=61)
+        B = gen.matrix_bf16(*_stored(k, n, tB), "normal", seed=62)
+        c1, b1 = o.gemm(m, n, k, tA, tB, 1.0, A, B)
+        c2, b2 = o.gemm(n, m, k, 1 - tB, 1 - tA, 1.0, B, A)
+        assert np.array_equal(c1, c2.T) and np.array_equal(b1, b2.T), (tA, tB)
+
+
+def pin_syrk_is_gemm_triangle(o):
+    n, k = 27, 35
+    low = np.tril(np.ones((n, n), bool))
+    for trans in (0, 1):
+        A = gen.matrix_bf16(*_stored(n, k, trans), "normal", seed=71)
+        g, gb = o.gemm(n, n, k, trans, 1 - trans, 1.0, A, A)
+        for uplo, mask in ((0, low), (1, low.T)):
+            s, sb = o.syrk(uplo, trans, n, k, 1.0, A)
+            assert np.array_equal(s[mask], g[mask]) and np.array_equal(sb[mask], gb[mask]), (uplo, trans)
+
+
+def pin_beta_accumulation(o):
+    m, n, k = 14, 22, 18
+    A, _ = _int_bf16((m, k), 81, -8, 8)
+    B, _ = _int_bf16((k, n), 82, -8, 8)
+    C0 = gen.integers(83, m * n, -100, 100).reshape(m, n).astype(np.float32)
+    acc, _ = o.gemm(m, n, k, 0, 0, 1.0, A, B, 1.0, C0)
+    plain, _ = o.gemm(m, n, k, 0, 0, 1.0, A, B)
+    assert np.array_equal(acc, C0.astype(np.float64) + plain)
+    C0b = gen.f32_to_bf16_bits(C0)
+    acc_b, _ = o.gemm(m, n, k, 0, 0, 1.0, A, B, 1.0, C0b)
+    assert np.array_equal(acc_b, gen.bf16_bits_to_f32(C0b).astype(np.float64) + plain)
+
+
+def pin_alpha_scaling(o):
+    m, n, k = 10, 8, 33
+    A = gen.matrix_bf16(m, k, "normal", seed=91)
+    B = gen.matrix_bf16(k, n, "normal", seed=92)
+    one, b1 = o.gemm(m, n, k, 0, 0, 1.0, A, B)
+    two, b2 = o.gemm(m, n, k, 0, 0, 2.0, A, B)
+    neg, _ = o.gemm(m, n, k, 0, 0, -0.25, A, B)
+    assert np.array_equal(two, 2.0 * one) and np.array_equal(neg, -0.25 * one)
+    assert np.array_equal(b1, b2)
+
+
+# --- BLAS conventions ---------------------------------------------------------------------
+def pin_special_values(o):
+    m, n, k = 6, 7, 5
+    nanA = np.full((m, k), gen.BF16_NAN, np.uint16)
+    nanB = np.full((k, n), gen.BF16_NAN, np.uint16)
+    C = gen.matrix_f32(m, n, "normal", seed=101)
+    ref, bound = o.gemm(m, n, k, 0, 0, 0.0, nanA, nanB, 2.0, C)      # alpha = 0: A, B unread
+    assert np.array_equal(ref, 2.0 * C.astype(np.float64)) and np.all(bound == 0)
+    A = gen.matrix_bf16(m, k, "normal", seed=102)
+    B = gen.matrix_bf16(k, n, "normal", seed=103)
+    nanC = np.full((m, n), np.nan, np.float32)
+    ref, _ = o.gemm(m, n, k, 0, 0, 1.0, A, B, 0.0, nanC)              # beta = 0: C unread
+    assert np.all(np.isfinite(ref))
+    ref, bound = o.gemm(m, n, 0, 0, 0, 1.0, A, B, -1.0, C)            # k = 0: beta * C
+    assert np.array_equal(ref, -C.astype(np.float64)) and np.all(bound == 0)
+    s, _ = o.syrk(0, 0, m, k, 0.0, nanA, 1.0, C[:, :m].copy())
+    assert np.array_equal(s[np.tril(np.ones((m, m), bool))],
+                          C[:, :m].astype(np.float64)[np.tril(np.ones((m, m), bool))])
+
+
+def pin_entries_agree(o):
+    m, n, k = 33, 41, 27
+    rng = np.random.default_rng(5)
+    rows = rng.integers(0, m, 200)
+    cols = rng.integers(0, n, 200)
+    for tA, tB in itertools.product((0, 1), (0, 1)):
+        A = gen.matrix_bf16(*_stored(m, k, tA), "normal", seed=111)
+        B = gen.matrix_bf16(*_stored(k, n, tB), "normal", seed=112)
+        C = gen.f32_to_bf16_bits(gen.matrix_f32(m, n, "normal", seed=113))
+        full, fb = o.gemm(m, n, k, tA, tB, 0.5, A, B, 1.0, C)
+        e, eb = o.gemm_entries(k, tA, tB, 0.5, A, B, rows, cols, 1.0, C)
+        assert np.array_equal(e, full[rows, cols]) and np.array_equal(eb, fb[rows, cols])
+    As = gen.matrix_bf16(m, k, "normal", seed=114)
+    Cs = gen.symmetric_f32(m, seed=115)
+    r2 = rng.integers(0, m, 200)
+    for uplo in (0, 1):
+        full, _ = o.syrk(uplo, 0, m, k, 1.0, As, 1.0, Cs)
+        e, _ = o.syrk_entries(uplo, 0, k, 1.0, As, rows, r2, 1.0, Cs)
+        assert np.array_equal(e, full[rows, r2], equal_nan=True)
+
+
+PINS = [
+    pin_gemm_bruteforce_exact,
+    pin_syrk_bruteforce_exact,
+    pin_gemm_matches_numpy,
+    pin_syrk_matches_numpy,
+    pin_identity,
+    pin_closed_forms,
+    pin_transpose_identity,
+    pin_syrk_is_gemm_triangle,
+    pin_beta_accumulation,
+    pin_alpha_scaling,
+    pin_special_values,
+    pin_entries_agree,
+]

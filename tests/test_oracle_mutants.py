@@ -1,0 +1,66 @@
+"""Plant plausible mistakes in copies of the oracle's C source; each must fail a pin.
+
+This shows the pins are strong enough to catch a dropped term, a wrong sign, a
+transposed operand or index, a wrong triangle or a broken BLAS convention
+anywhere in the oracle. The mutants are compiled into a temporary directory;
+the committed oracle is never modified.
+"""
+
+import os
+
+import pytest
+
+import oracle
+from oracle_pins import PINS
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "bm_oracle.c")
+
+# (name, text to replace, replacement, which occurrence: 0 = first)
+MUTANTS = [
+    ("gemm_sign", "acc += prod;", "acc -= prod;", 0),
+    ("syrk_sign", "acc += prod;", "acc -= prod;", 1),
+    ("gemm_drop_alpha", "double value = alpha * acc;", "double value = acc;", 0),
+    ("syrk_drop_alpha", "double value = alpha * acc;", "double value = acc;", 1),
+    ("gemm_drop_beta", "value += beta * c_input", "value += c_input", 0),
+    ("syrk_drop_beta_term", "value += beta * c_input", "value += 0.0 * c_input", 1),
+    ("ignore_transpose", "return bf16_value(X[c * ld + r]);", "return bf16_value(X[r * ld + c]);", 0),
+    ("transposed_c_input", "((const float *)C)[i * ldc + j]", "((const float *)C)[j * ldc + i]", 0),
+    ("gemm_drop_first_term", "for (int64_t p = 0; p < k; ++p) {", "for (int64_t p = 1; p < k; ++p) {", 0),
+    ("syrk_drop_last_term", "for (int64_t p = 0; p < k; ++p) {", "for (int64_t p = 0; p + 1 < k; ++p) {", 1),
+    ("gemm_signed_bound", "mag += fabs(prod);", "mag += prod;", 0),
+    ("lower_strict", "return uplo == 0 ? (i >= j) : (i <= j);", "return uplo == 0 ? (i > j) : (i <= j);", 0),
+    ("upper_as_lower", "return uplo == 0 ? (i >= j) : (i <= j);", "return (i >= j);", 0),
+    ("syrk_same_row_twice", "op_at(A, lda, trans, j, p)", "op_at(A, lda, trans, i, p)", 0),
+    ("negative_beta_dropped", "if (beta != 0.0)\n        value += beta", "if (beta > 0.0)\n        value += beta", 0),
+    ("alpha_zero_reads_a", "if (alpha != 0.0) {\n        for", "{\n        for", 0),
+    ("bf16_c_misread", "return bf16_value(((const uint16_t *)C)[i * ldc + j]);",
+     "return (double)((const float *)C)[i * ldc + j];", 0),
+    ("gemm_last_column_skipped", "for (int64_t j = 0; j < n; ++j)\n            gemm_element",
+     "for (int64_t j = 0; j + 1 < n; ++j)\n            gemm_element", 0),
+]
+
+
+def _mutate(text, old, new, occurrence):
+    start = -1
+    for _ in range(occurrence + 1):
+        start = text.find(old, start + 1)
+        assert start >= 0, f"mutation anchor not found: {old!r}"
+    return text[:start] + new + text[start + len(old):]
+
+
+@pytest.mark.parametrize("name,old,new,occ", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(tmp_path, name, old, new, occ):
+    src = open(SRC).read()
+    mutated = _mutate(src, old, new, occ)
+    assert mutated != src
+    path = tmp_path / f"{name}.c"
+    path.write_text(mutated)
+    lib = oracle.compile_oracle(str(path), str(tmp_path / f"lib{name}.so"))
+    o = oracle.Oracle(lib)
+    failures = []
+    for pin in PINS:
+        try:
+            pin(o)
+        except Exception:  # any failure of a pin counts as catching the mutant
+            failures.append(pin.__name__)
+    assert failures, f"mutant {name} passed every pin"
