@@ -1,0 +1,435 @@
+// bm_api.cu -- host side of the C ABI declared in include/bm.h: argument checks,
+// launch planning, TMA tensor-map encoding (128-byte swizzle), launches and the
+// device status word.
+//
+// The tensor map is the host-built descriptor of "cp.async / ldmatrix ablation
+// plan", section 1.2 (a rank-2 tiled map: global extents and strides, box
+// extents, no interleave, hardware swizzle, zero fill out of bounds), with the
+// constraints of section 1.3 (16-byte aligned global address, 128-byte box rows
+// in 128-byte swizzle mode, whole-tile copies).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "bm.h"
+#include "bm_gemm_kernel.cuh"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kStagesBN256 = 4;
+constexpr int kStagesBN128 = 6;
+constexpr int kGroupM = 16;
+
+struct DeviceState {
+    bool ready = false;
+    int sm_count = 0;
+    int cc_major = 0, cc_minor = 0;
+    int *status = nullptr;  // one int, allocated on first use
+    bool attrs_set = false;
+};
+
+std::mutex g_mutex;
+DeviceState g_devices[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::atomic<uint32_t> g_timeout_ms{2000};
+std::atomic<int> g_debug_stall{0};
+
+using Kern = void (*)(CUtensorMap, CUtensorMap, bm::GemmParams);
+
+template <int BN, int STAGES>
+void *kernel_ptr()
+{
+    return reinterpret_cast<void *>(&bm::bm_gemm_tcgen05_kernel<BN, STAGES>);
+}
+
+bool fits_int32(int64_t v) { return v >= 0 && v <= 0x7FFFFFFFLL; }
+
+// Current device, checked for compute capability 10.3; status word allocated.
+bm_status device_state(DeviceState **out)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return BM_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState &st = g_devices[dev];
+    if (!st.ready) {
+        cudaDeviceProp prop;
+        if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return BM_ERR_CUDA;
+        st.sm_count = prop.multiProcessorCount;
+        st.cc_major = prop.major;
+        st.cc_minor = prop.minor;
+        st.ready = true;
+    }
+    if (st.cc_major != 10 || st.cc_minor != 3) return BM_ERR_ARCH;
+    if (g_encode == nullptr) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || fn == nullptr)
+            return BM_ERR_CUDA;
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    if (st.status == nullptr) {
+        if (cudaMalloc(&st.status, sizeof(int)) != cudaSuccess) return BM_ERR_CUDA;
+        if (cudaMemset(st.status, 0, sizeof(int)) != cudaSuccess) return BM_ERR_CUDA;
+    }
+    if (!st.attrs_set) {
+        const void *kerns[2] = {kernel_ptr<256, kStagesBN256>(), kernel_ptr<128, kStagesBN128>()};
+        const int bytes[2] = {bm::KernelCfg<256, kStagesBN256>::SMEM_BYTES,
+                              bm::KernelCfg<128, kStagesBN128>::SMEM_BYTES};
+        for (int i = 0; i < 2; ++i)
+            if (cudaFuncSetAttribute(kerns[i], cudaFuncAttributeMaxDynamicSharedMemorySize, bytes[i]) !=
+                cudaSuccess)
+                return BM_ERR_CUDA;
+        st.attrs_set = true;
+    }
+    *out = &st;
+    return BM_OK;
+}
+
+int sm_count_or_default()
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kMaxDevices) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0) return n;
+    }
+    cudaGetLastError();
+    return 152;  // GB300
+}
+
+// rank-2 bf16 tensor map: inner (contiguous) extent, outer extent, row pitch in elements
+bool encode_bf16_2d(CUtensorMap *map, const void *base, int64_t inner, int64_t outer, int64_t ld,
+                    uint32_t box_inner, uint32_t box_outer)
+{
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(std::max<int64_t>(inner, 1)),
+                          static_cast<cuuint64_t>(std::max<int64_t>(outer, 1))};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2u};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// Operand tile maps. K-major: box 64 (k) x rows; M/N-major: box 64 (m or n) x 64 (k).
+bool encode_operand(CUtensorMap *map, const void *base, bool mn_major, int64_t rows, int64_t k, int64_t ld,
+                    uint32_t tile_rows)
+{
+    if (mn_major) return encode_bf16_2d(map, base, rows, k, ld, 64, 64);
+    return encode_bf16_2d(map, base, k, rows, ld, 64, tile_rows);
+}
+
+struct Plan {
+    int bn = 256, stages = kStagesBN256;
+    int64_t tiles_m = 0, tiles_n = 0, num_tiles = 0;
+    int k_splits = 1, kb_per_split = 0, kb_total = 0;
+    int ctas = 0;
+    int64_t ldp = 0;
+    size_t ws_bytes = 0;
+};
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int64_t syrk_tile_count(int mode, int64_t tiles_m, int64_t tiles_n)
+{
+    int64_t total = 0;
+    for (int64_t tm = 0; tm < tiles_m; ++tm) {
+        int64_t lo, hi;
+        bm::syrk_row_tiles<256>(mode, tm, tiles_n, lo, hi);
+        total += hi - lo + 1;
+    }
+    return total;
+}
+
+Plan plan_gemm(int64_t m, int64_t n, int64_t k, size_t ws_bytes, int sms)
+{
+    Plan pl;
+    pl.bn = (n <= 128) ? 128 : 256;
+    pl.stages = pl.bn == 256 ? kStagesBN256 : kStagesBN128;
+    pl.tiles_m = ceil_div(m, bm::TILE_M);
+    pl.tiles_n = ceil_div(n, pl.bn);
+    pl.num_tiles = pl.tiles_m * pl.tiles_n;
+    pl.kb_total = static_cast<int>(ceil_div(std::max<int64_t>(k, 1), bm::TILE_K));
+    pl.kb_per_split = pl.kb_total;
+    pl.ldp = ceil_div(n, 4) * 4;
+    // Split K only when the tiles cannot fill half the GPU and each split keeps >= 4 k-blocks.
+    if (pl.num_tiles * 2 <= sms && pl.kb_total >= 8) {
+        int64_t want = std::min<int64_t>(ceil_div(sms, pl.num_tiles), pl.kb_total / 4);
+        while (want > 1) {
+            const int per = static_cast<int>(ceil_div(pl.kb_total, want));
+            const int splits = static_cast<int>(ceil_div(pl.kb_total, per));
+            const size_t need = static_cast<size_t>(splits) * static_cast<size_t>(m) * pl.ldp * sizeof(float);
+            if (need <= ws_bytes) {
+                pl.k_splits = splits;
+                pl.kb_per_split = per;
+                pl.ws_bytes = need;
+                break;
+            }
+            --want;
+        }
+    }
+    pl.ctas = static_cast<int>(std::min<int64_t>(pl.num_tiles * pl.k_splits, sms));
+    return pl;
+}
+
+Plan plan_syrk(int mode, int64_t n, int64_t k, int sms)
+{
+    Plan pl;
+    pl.bn = 256;
+    pl.stages = kStagesBN256;
+    pl.tiles_m = ceil_div(n, bm::TILE_M);
+    pl.tiles_n = ceil_div(n, 256);
+    pl.num_tiles = syrk_tile_count(mode, pl.tiles_m, pl.tiles_n);
+    pl.kb_total = static_cast<int>(ceil_div(std::max<int64_t>(k, 1), bm::TILE_K));
+    pl.kb_per_split = pl.kb_total;
+    pl.ctas = static_cast<int>(std::min<int64_t>(pl.num_tiles, sms));
+    return pl;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bm_status launch(const Plan &pl, const CUtensorMap &ta, const CUtensorMap &tb, bm::GemmParams &prm,
+                 cudaStream_t stream)
+{
+    if (pl.bn == 256) {
+        bm::bm_gemm_tcgen05_kernel<256, kStagesBN256>
+            <<<pl.ctas, bm::NUM_THREADS, bm::KernelCfg<256, kStagesBN256>::SMEM_BYTES, stream>>>(ta, tb, prm);
+    } else {
+        bm::bm_gemm_tcgen05_kernel<128, kStagesBN128>
+            <<<pl.ctas, bm::NUM_THREADS, bm::KernelCfg<128, kStagesBN128>::SMEM_BYTES, stream>>>(ta, tb, prm);
+    }
+    if (cudaGetLastError() != cudaSuccess) return BM_ERR_CUDA;
+    if (prm.k_splits > 1) {
+        const int64_t work = prm.m * ceil_div(prm.n, 4);
+        const int blocks = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(ceil_div(work, 256), 8 * 152)));
+        bm::bm_splitk_reduce_kernel<<<blocks, 256, 0, stream>>>(prm);
+        if (cudaGetLastError() != cudaSuccess) return BM_ERR_CUDA;
+    }
+    return BM_OK;
+}
+
+bm_status launch_scale(bm::GemmParams &prm, cudaStream_t stream)
+{
+    const int64_t work = prm.m * ceil_div(prm.n, 4);
+    const int blocks = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(ceil_div(work, 256), 8 * 152)));
+    bm::bm_scale_kernel<<<blocks, 256, 0, stream>>>(prm);
+    return cudaGetLastError() == cudaSuccess ? BM_OK : BM_ERR_CUDA;
+}
+
+bm::GemmParams base_params(int64_t m, int64_t n, int64_t k, float alpha, float beta, void *C, int64_t ldc,
+                           bm_ctype ct, DeviceState *st)
+{
+    bm::GemmParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.m = m;
+    p.n = n;
+    p.k = k;
+    p.C = C;
+    p.ldc = ldc;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.c_bf16 = ct == BM_C_BF16 ? 1 : 0;
+    p.k_splits = 1;
+    p.group_m = kGroupM;
+    p.status = st != nullptr ? st->status : nullptr;
+    p.timeout_ns = static_cast<uint64_t>(g_timeout_ms.load()) * 1000000ull;
+    p.debug_stall = g_debug_stall.load();
+    return p;
+}
+
+bm_status check_gemm_args(int64_t m, int64_t n, int64_t k, int transA, int transB, int64_t lda, int64_t ldb,
+                          int64_t ldc, int ct)
+{
+    if (m < 0 || n < 0 || k < 0) return BM_ERR_INVALID_VALUE;
+    if (!fits_int32(m) || !fits_int32(n) || !fits_int32(k)) return BM_ERR_INVALID_VALUE;
+    if ((transA != BM_OP_N && transA != BM_OP_T) || (transB != BM_OP_N && transB != BM_OP_T))
+        return BM_ERR_INVALID_VALUE;
+    if (ct != BM_C_F32 && ct != BM_C_BF16) return BM_ERR_INVALID_VALUE;
+    const int64_t need_a = transA == BM_OP_N ? k : m;
+    const int64_t need_b = transB == BM_OP_N ? n : k;
+    if (lda < std::max<int64_t>(1, need_a) || ldb < std::max<int64_t>(1, need_b) || ldc < std::max<int64_t>(1, n))
+        return BM_ERR_INVALID_VALUE;
+    return BM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+bm_status bm_gemm_bf16(int64_t m, int64_t n, int64_t k, bm_op transA, bm_op transB, float alpha, const void *A,
+                       int64_t lda, const void *B, int64_t ldb, float beta, void *C, int64_t ldc, bm_ctype c_type,
+                       void *workspace, size_t workspace_bytes, bm_stream_t stream)
+{
+    bm_status s = check_gemm_args(m, n, k, transA, transB, lda, ldb, ldc, c_type);
+    if (s != BM_OK) return s;
+    if (workspace_bytes > 0 && (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
+        return BM_ERR_WORKSPACE;
+    if (m == 0 || n == 0) return BM_OK;
+    const bool products = alpha != 0.0f && k > 0;
+    if (C == nullptr || (products && (A == nullptr || B == nullptr))) return BM_ERR_INVALID_VALUE;
+    const int64_t esz = c_type == BM_C_BF16 ? 2 : 4;
+    if (!aligned16(C) || (ldc * esz) % 16 != 0) return BM_ERR_MISALIGNED;
+    if (products && (!aligned16(A) || !aligned16(B) || (lda * 2) % 16 != 0 || (ldb * 2) % 16 != 0))
+        return BM_ERR_MISALIGNED;
+    DeviceState *st = nullptr;
+    s = device_state(&st);
+    if (s != BM_OK) return s;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    bm::GemmParams prm = base_params(m, n, k, alpha, beta, C, ldc, c_type, st);
+    prm.mode = bm::MODE_GEMM;
+    if (!products) return launch_scale(prm, cs);
+
+    const Plan pl = plan_gemm(m, n, k, workspace != nullptr ? workspace_bytes : 0, st->sm_count);
+    CUtensorMap ta, tb;
+    const bool a_mn = transA == BM_OP_T, b_mn = transB == BM_OP_N;
+    if (!encode_operand(&ta, A, a_mn, m, k, lda, bm::TILE_M)) return BM_ERR_CUDA;
+    if (!encode_operand(&tb, B, b_mn, n, k, ldb, static_cast<uint32_t>(pl.bn))) return BM_ERR_CUDA;
+    prm.a_mn_major = a_mn;
+    prm.b_mn_major = b_mn;
+    prm.tiles_m = pl.tiles_m;
+    prm.tiles_n = pl.tiles_n;
+    prm.num_tiles = pl.num_tiles;
+    prm.k_splits = pl.k_splits;
+    prm.kb_per_split = pl.kb_per_split;
+    prm.kb_total = pl.kb_total;
+    prm.partial = pl.k_splits > 1 ? static_cast<float *>(workspace) : nullptr;
+    prm.ldp = pl.ldp;
+    return launch(pl, ta, tb, prm, cs);
+}
+
+size_t bm_gemm_bf16_workspace_size(int64_t m, int64_t n, int64_t k)
+{
+    if (m <= 0 || n <= 0 || k <= 0) return 0;
+    const Plan pl = plan_gemm(m, n, k, SIZE_MAX, sm_count_or_default());
+    return pl.k_splits > 1 ? pl.ws_bytes : 0;
+}
+
+bm_status bm_syrk_bf16(bm_uplo uplo, bm_op trans, int64_t n, int64_t k, float alpha, const void *A, int64_t lda,
+                       float beta, void *C, int64_t ldc, bm_ctype c_type, bm_stream_t stream)
+{
+    if (uplo != BM_LOWER && uplo != BM_UPPER) return BM_ERR_INVALID_VALUE;
+    if (n < 0 || k < 0 || !fits_int32(n) || !fits_int32(k)) return BM_ERR_INVALID_VALUE;
+    if (trans != BM_OP_N && trans != BM_OP_T) return BM_ERR_INVALID_VALUE;
+    if (c_type != BM_C_F32 && c_type != BM_C_BF16) return BM_ERR_INVALID_VALUE;
+    const int64_t need_a = trans == BM_OP_N ? k : n;
+    if (lda < std::max<int64_t>(1, need_a) || ldc < std::max<int64_t>(1, n)) return BM_ERR_INVALID_VALUE;
+    if (n == 0) return BM_OK;
+    const bool products = alpha != 0.0f && k > 0;
+    if (C == nullptr || (products && A == nullptr)) return BM_ERR_INVALID_VALUE;
+    const int64_t esz = c_type == BM_C_BF16 ? 2 : 4;
+    if (!aligned16(C) || (ldc * esz) % 16 != 0) return BM_ERR_MISALIGNED;
+    if (products && (!aligned16(A) || (lda * 2) % 16 != 0)) return BM_ERR_MISALIGNED;
+    DeviceState *st = nullptr;
+    bm_status s = device_state(&st);
+    if (s != BM_OK) return s;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    bm::GemmParams prm = base_params(n, n, k, alpha, beta, C, ldc, c_type, st);
+    prm.mode = uplo == BM_LOWER ? bm::MODE_SYRK_LOWER : bm::MODE_SYRK_UPPER;
+    if (!products) return launch_scale(prm, cs);
+
+    const Plan pl = plan_syrk(prm.mode, n, k, st->sm_count);
+    CUtensorMap ta, tb;
+    const bool mn = trans == BM_OP_T;  // A stored [k][n]: both operands are M/N-major
+    if (!encode_operand(&ta, A, mn, n, k, lda, bm::TILE_M)) return BM_ERR_CUDA;
+    if (!encode_operand(&tb, A, mn, n, k, lda, static_cast<uint32_t>(pl.bn))) return BM_ERR_CUDA;
+    prm.a_mn_major = mn;
+    prm.b_mn_major = mn;
+    prm.tiles_m = pl.tiles_m;
+    prm.tiles_n = pl.tiles_n;
+    prm.num_tiles = pl.num_tiles;
+    prm.kb_per_split = pl.kb_per_split;
+    prm.kb_total = pl.kb_total;
+    return launch(pl, ta, tb, prm, cs);
+}
+
+bm_status bm_gemm_bf16_plan(int64_t m, int64_t n, int64_t k, size_t workspace_bytes, bm_plan *plan)
+{
+    if (plan == nullptr) return BM_ERR_INVALID_VALUE;
+    if (m < 0 || n < 0 || k < 0 || !fits_int32(m) || !fits_int32(n) || !fits_int32(k)) return BM_ERR_INVALID_VALUE;
+    std::memset(plan, 0, sizeof(*plan));
+    if (m == 0 || n == 0) return BM_OK;
+    if (k == 0) {
+        plan->kernels = 1;
+        return BM_OK;
+    }
+    const Plan pl = plan_gemm(m, n, k, workspace_bytes, sm_count_or_default());
+    plan->tile_m = bm::TILE_M;
+    plan->tile_n = pl.bn;
+    plan->tile_k = bm::TILE_K;
+    plan->stages = pl.stages;
+    plan->tiles = pl.num_tiles;
+    plan->k_splits = pl.k_splits;
+    plan->ctas = pl.ctas;
+    plan->kernels = pl.k_splits > 1 ? 2 : 1;
+    plan->workspace_bytes = pl.k_splits > 1 ? pl.ws_bytes : 0;
+    return BM_OK;
+}
+
+bm_status bm_syrk_bf16_plan(bm_uplo uplo, int64_t n, int64_t k, bm_plan *plan)
+{
+    if (plan == nullptr || (uplo != BM_LOWER && uplo != BM_UPPER)) return BM_ERR_INVALID_VALUE;
+    if (n < 0 || k < 0 || !fits_int32(n) || !fits_int32(k)) return BM_ERR_INVALID_VALUE;
+    std::memset(plan, 0, sizeof(*plan));
+    if (n == 0) return BM_OK;
+    if (k == 0) {
+        plan->kernels = 1;
+        return BM_OK;
+    }
+    const Plan pl = plan_syrk(uplo == BM_LOWER ? bm::MODE_SYRK_LOWER : bm::MODE_SYRK_UPPER, n, k,
+                              sm_count_or_default());
+    plan->tile_m = bm::TILE_M;
+    plan->tile_n = pl.bn;
+    plan->tile_k = bm::TILE_K;
+    plan->stages = pl.stages;
+    plan->tiles = pl.num_tiles;
+    plan->k_splits = 1;
+    plan->ctas = pl.ctas;
+    plan->kernels = 1;
+    return BM_OK;
+}
+
+bm_status bm_get_last_device_error(bm_stream_t stream)
+{
+    DeviceState *st = nullptr;
+    bm_status s = device_state(&st);
+    if (s != BM_OK) return s;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return BM_ERR_CUDA;
+    int code = 0;
+    if (cudaMemcpy(&code, st->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return BM_ERR_CUDA;
+    if (code != 0 && cudaMemset(st->status, 0, sizeof(int)) != cudaSuccess) return BM_ERR_CUDA;
+    return static_cast<bm_status>(code);
+}
+
+void bm_set_wait_timeout_ms(uint32_t ms) { g_timeout_ms.store(ms == 0 ? 1 : ms); }
+
+void bm_debug_inject_stall(int enable) { g_debug_stall.store(enable ? 1 : 0); }
+
+const char *bm_status_string(bm_status status)
+{
+    switch (status) {
+    case BM_OK: return "BM_OK";
+    case BM_ERR_INVALID_VALUE: return "BM_ERR_INVALID_VALUE";
+    case BM_ERR_MISALIGNED: return "BM_ERR_MISALIGNED";
+    case BM_ERR_ARCH: return "BM_ERR_ARCH";
+    case BM_ERR_CUDA: return "BM_ERR_CUDA";
+    case BM_ERR_TIMEOUT: return "BM_ERR_TIMEOUT";
+    case BM_ERR_WORKSPACE: return "BM_ERR_WORKSPACE";
+    }
+    return "BM_ERR_UNKNOWN";
+}
+
+int bm_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,541 @@
+// bm_gemm_kernel.cuh -- persistent, warp-specialised BF16 GEMM / SYRK kernel for
+// sm_103a (one CTA per SM).
+//
+//   C = alpha * op(A) * op(B) + beta * C      (GEMM)
+//   C = alpha * op(A) * op(A)^T + beta * C    (SYRK, one triangle)
+//
+// This is the BLAS3 local compute of "BLASMp development notes" (section 1;
+// stage B: SYRK's main compute is a GEMM), done with the staging ladder's last
+// rung from "cp.async / ldmatrix ablation plan" (section 2.3: TMA with a
+// multi-stage buffer, hardware 128-byte swizzle) and with the producer / MMA /
+// accumulator-slot / epilogue roles that "fused A2A/GEMM Perfetto profile
+// protocol" lists for its SM100/SM103 mainloop (MXFP8 hot-path table: load
+// empty-stage acquire, TMA submission, MMA input-stage wait, reusable TMEM
+// slot, MMA issue and stage release, epilogue).
+//
+// Roles (192 threads):
+//   warp 0, one lane  TMA producer: fills a STAGES-deep ring of shared-memory
+//                     stages (A tile 128 x 64, B tile BN x 64, bf16) guarded by
+//                     full/empty mbarriers.
+//   warp 1, one lane  MMA issuer: 4 x tcgen05.mma (K = 16 each) per stage into
+//                     one of two TMEM accumulators (128 lanes x BN fp32
+//                     columns); tcgen05.commit releases the stage, and at the
+//                     end of a tile signals the accumulator full. Warp 1 also
+//                     allocates and frees the tensor memory.
+//   warps 2-5         epilogue: TMEM -> registers (tcgen05.ld 32x32b), alpha,
+//                     transpose through shared memory, then coalesced 16-byte
+//                     loads of C (beta != 0) and stores of C; the SYRK
+//                     triangle and the ragged edges are masked per element.
+// Tiles are handed out persistently (CTA b takes units b, b + grid, ...), in
+// grouped-raster order for GEMM and row by row over the referenced triangle for
+// SYRK (tiles strictly on the other side of the diagonal are never visited).
+//
+// Every barrier wait is bounded: after the wait limit the thread records
+// BM_ERR_TIMEOUT in the device status word, raises a shared abort flag that
+// the other roles poll, waits (bounded) for its own copies / MMAs in flight,
+// and the CTA frees its tensor memory and exits.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "bm_ptx.cuh"
+
+namespace bm {
+
+enum : int { MODE_GEMM = 0, MODE_SYRK_LOWER = 1, MODE_SYRK_UPPER = 2 };
+enum : int { DEV_ERR_TIMEOUT = 5 };
+
+constexpr int TILE_M = 128;
+constexpr int TILE_K = 64;  // bf16 elements = 128 bytes = one swizzle row
+constexpr int UMMA_K = 16;
+constexpr int NUM_EPI_WARPS = 4;
+constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
+constexpr int EPI_WARP_FLOATS = 32 * 32;  // one 32 x 32 fp32 staging block per epilogue warp
+
+struct GemmParams {
+    int64_t m, n, k;   // output rows / columns (SYRK: m == n), reduction length
+    void *C;
+    int64_t ldc;
+    float alpha, beta;
+    int c_bf16;        // C element: 0 = fp32, 1 = bf16
+    int a_mn_major;    // operand tiles in shared memory: 0 = K-major, 1 = M/N-major
+    int b_mn_major;
+    int mode;          // MODE_*
+    int64_t tiles_m, tiles_n;
+    int64_t num_tiles; // GEMM: tiles_m * tiles_n; SYRK: tiles touching the triangle
+    int k_splits;      // > 1: each split writes an fp32 partial, a second kernel sums them
+    int kb_per_split;  // k-blocks (of TILE_K) per split
+    int kb_total;      // ceil(k / TILE_K)
+    int group_m;       // grouped raster: tile rows per group
+    float *partial;    // [k_splits][m][ldp] when k_splits > 1
+    int64_t ldp;
+    int *status;       // device status word (first error wins)
+    uint64_t timeout_ns;
+    int debug_stall;   // test hook: the first stage's copy is never issued
+};
+
+template <int BN, int STAGES>
+struct KernelCfg {
+    static constexpr int A_BYTES = TILE_M * TILE_K * 2;
+    static constexpr int B_BYTES = BN * TILE_K * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
+    static constexpr int EPI_BYTES = NUM_EPI_WARPS * EPI_WARP_FLOATS * 4;
+    static constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, acc full x2, acc empty x2, drain
+    static constexpr int BAR_BYTES = 8 * NUM_BARS + 16;
+    static constexpr int SMEM_BYTES = 1024 + RING_BYTES + EPI_BYTES + BAR_BYTES;
+    static constexpr int TMEM_COLS = 2 * BN;  // two accumulators
+    static_assert(BN == 128 || BN == 256, "BN");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+};
+
+// ---------------------------------------------------------------- scheduling
+struct Unit {
+    int64_t tm, tn;
+    int split;
+};
+
+// Range of tile columns [lo, hi] of tile row tm that touch the SYRK triangle.
+template <int BN>
+__host__ __device__ inline void syrk_row_tiles(int mode, int64_t tm, int64_t tiles_n, int64_t &lo,
+                                               int64_t &hi)
+{
+    if (mode == MODE_SYRK_LOWER) {  // some row >= some column
+        lo = 0;
+        const int64_t last = (TILE_M * tm + TILE_M - 1) / BN;
+        hi = last < tiles_n - 1 ? last : tiles_n - 1;
+    } else {  // some row <= some column
+        lo = (TILE_M * tm) / BN;
+        hi = tiles_n - 1;
+    }
+}
+
+template <int BN>
+__device__ __forceinline__ Unit map_unit(const GemmParams &p, int64_t u)
+{
+    Unit r;
+    const int64_t t = u / p.k_splits;
+    r.split = static_cast<int>(u - t * p.k_splits);
+    r.tm = 0;
+    r.tn = 0;
+    if (p.mode == MODE_GEMM) {
+        const int64_t per_group = static_cast<int64_t>(p.group_m) * p.tiles_n;
+        const int64_t g = t / per_group;
+        const int64_t first = g * p.group_m;
+        const int64_t rows = (p.tiles_m - first) < p.group_m ? (p.tiles_m - first) : p.group_m;
+        const int64_t local = t - g * per_group;
+        r.tm = first + local % rows;
+        r.tn = local / rows;
+    } else {
+        int64_t rem = t;
+        for (int64_t tm = 0; tm < p.tiles_m; ++tm) {
+            int64_t lo, hi;
+            syrk_row_tiles<BN>(p.mode, tm, p.tiles_n, lo, hi);
+            const int64_t cnt = hi - lo + 1;
+            if (rem < cnt) {
+                r.tm = tm;
+                r.tn = lo + rem;
+                break;
+            }
+            rem -= cnt;
+        }
+    }
+    return r;
+}
+
+// ---------------------------------------------------------------- bounded waits
+__device__ __noinline__ void signal_timeout(const GemmParams &p, volatile int *abort_flag)
+{
+    *abort_flag = 1;
+    if (p.status != nullptr) atomicCAS(p.status, 0, DEV_ERR_TIMEOUT);
+}
+
+// Single-thread wait: false when the limit passes or another role aborted.
+__device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                         uint64_t limit_ns)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 16; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (abort_flag != nullptr && *abort_flag) return false;
+        if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// Warp-uniform wait: every lane observes the phase (acquire) before any lane
+// proceeds, and all lanes take the same exit.
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                          uint64_t limit_ns)
+{
+    uint64_t t0 = 0;
+    for (int it = 0;; ++it) {
+        const bool ok = mbar_try_wait(bar, parity);
+        if (__all_sync(0xffffffffu, ok)) return true;
+        if (it == 0) t0 = global_timer_ns();
+        if ((it & 15) == 15) {
+            const bool stop = *abort_flag != 0 || (global_timer_ns() - t0 > limit_ns);
+            if (__any_sync(0xffffffffu, stop)) return false;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- output
+__device__ __forceinline__ bool in_output(const GemmParams &p, int64_t i, int64_t j)
+{
+    if (i >= p.m || j >= p.n) return false;
+    if (p.mode == MODE_SYRK_LOWER) return i >= j;
+    if (p.mode == MODE_SYRK_UPPER) return i <= j;
+    return true;
+}
+
+// C[i, j..j+3] = v + beta * C (C read only when beta != 0), masked per element.
+// j is a multiple of 4; C and ldc satisfy the 16-byte rule, so the vector
+// accesses are aligned.
+__device__ __forceinline__ void write_c4(const GemmParams &p, int64_t i, int64_t j, float v[4])
+{
+    bool all = (i < p.m) && (j + 3 < p.n);
+    if (p.mode == MODE_SYRK_LOWER) all = all && (i >= j + 3);
+    if (p.mode == MODE_SYRK_UPPER) all = all && (i <= j);
+    const bool use_beta = p.beta != 0.0f;
+    if (p.c_bf16) {
+        __nv_bfloat16 *row = reinterpret_cast<__nv_bfloat16 *>(p.C) + i * p.ldc;
+        if (all) {
+            if (use_beta) {
+                const uint2 old = *reinterpret_cast<const uint2 *>(row + j);
+                const __nv_bfloat162 o01 = *reinterpret_cast<const __nv_bfloat162 *>(&old.x);
+                const __nv_bfloat162 o23 = *reinterpret_cast<const __nv_bfloat162 *>(&old.y);
+                v[0] = fmaf(p.beta, __low2float(o01), v[0]);
+                v[1] = fmaf(p.beta, __high2float(o01), v[1]);
+                v[2] = fmaf(p.beta, __low2float(o23), v[2]);
+                v[3] = fmaf(p.beta, __high2float(o23), v[3]);
+            }
+            const __nv_bfloat162 r01 = __floats2bfloat162_rn(v[0], v[1]);
+            const __nv_bfloat162 r23 = __floats2bfloat162_rn(v[2], v[3]);
+            uint2 out;
+            out.x = *reinterpret_cast<const uint32_t *>(&r01);
+            out.y = *reinterpret_cast<const uint32_t *>(&r23);
+            *reinterpret_cast<uint2 *>(row + j) = out;
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                if (!in_output(p, i, j + e)) continue;
+                float x = v[e];
+                if (use_beta) x = fmaf(p.beta, __bfloat162float(row[j + e]), x);
+                row[j + e] = __float2bfloat16_rn(x);
+            }
+        }
+    } else {
+        float *row = reinterpret_cast<float *>(p.C) + i * p.ldc;
+        if (all) {
+            if (use_beta) {
+                const float4 old = *reinterpret_cast<const float4 *>(row + j);
+                v[0] = fmaf(p.beta, old.x, v[0]);
+                v[1] = fmaf(p.beta, old.y, v[1]);
+                v[2] = fmaf(p.beta, old.z, v[2]);
+                v[3] = fmaf(p.beta, old.w, v[3]);
+            }
+            *reinterpret_cast<float4 *>(row + j) = make_float4(v[0], v[1], v[2], v[3]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                if (!in_output(p, i, j + e)) continue;
+                float x = v[e];
+                if (use_beta) x = fmaf(p.beta, row[j + e], x);
+                row[j + e] = x;
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- roles
+template <int BN, int STAGES>
+__device__ __forceinline__ void run_producer(const CUtensorMap *tmA, const CUtensorMap *tmB,
+                                             const GemmParams &p, uint32_t ring, uint32_t bar0,
+                                             volatile int *abort_flag)
+{
+    using Cfg = KernelCfg<BN, STAGES>;
+    const int64_t units = p.num_tiles * p.k_splits;
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t issued = 0, issued_parity = 0;  // per stage: filled at least once / parity of last fill
+    bool ok = true, first = true;
+    for (int64_t u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        const Unit w = map_unit<BN>(p, u);
+        const int kb0 = w.split * p.kb_per_split;
+        const int kb1 = min(p.kb_total, kb0 + p.kb_per_split);
+        const int32_t row_a = static_cast<int32_t>(w.tm * TILE_M);
+        const int32_t row_b = static_cast<int32_t>(w.tn * BN);
+        for (int kb = kb0; kb < kb1; ++kb) {
+            const uint32_t empty = bar0 + 8u * (STAGES + stage);
+            if (!wait_one(empty, phase ^ 1u, abort_flag, p.timeout_ns)) {
+                ok = false;
+                break;
+            }
+            const uint32_t full = bar0 + 8u * stage;
+            mbar_arrive_expect_tx(full, Cfg::STAGE_BYTES);
+            issued |= 1u << stage;
+            issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+            const uint32_t sa = ring + stage * Cfg::STAGE_BYTES;
+            const uint32_t sb = sa + Cfg::A_BYTES;
+            const int32_t kx = kb * TILE_K;
+            if (!(p.debug_stall && first)) {
+                if (p.a_mn_major) {  // A stored [k][m]: two 64-wide chunks along M
+                    tma_load_2d(sa, tmA, full, row_a, kx);
+                    tma_load_2d(sa + 8192, tmA, full, row_a + 64, kx);
+                } else {             // A stored [m][k]: one 64 x 128 box
+                    tma_load_2d(sa, tmA, full, kx, row_a);
+                }
+                if (p.b_mn_major) {  // B stored [k][n]: BN/64 chunks along N
+#pragma unroll
+                    for (int c = 0; c < BN / 64; ++c) tma_load_2d(sb + 8192 * c, tmB, full, row_b + 64 * c, kx);
+                } else {             // B stored [n][k]: one 64 x BN box
+                    tma_load_2d(sb, tmB, full, kx, row_b);
+                }
+            }
+            first = false;
+            if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+    if (!ok) {
+        signal_timeout(p, abort_flag);
+        // Let every copy this thread started land before shared memory is released.
+        for (int s = 0; s < STAGES; ++s)
+            if ((issued >> s) & 1u) wait_one(bar0 + 8u * s, (issued_parity >> s) & 1u, nullptr, p.timeout_ns);
+    }
+}
+
+template <int BN, int STAGES>
+__device__ __forceinline__ void run_mma(const GemmParams &p, uint32_t ring, uint32_t bar0,
+                                        uint32_t tmem_base, volatile int *abort_flag)
+{
+    using Cfg = KernelCfg<BN, STAGES>;
+    const int64_t units = p.num_tiles * p.k_splits;
+    const uint32_t idesc = idesc_bf16_f32(TILE_M, BN, p.a_mn_major, p.b_mn_major);
+    int stage = 0, acc = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    bool ok = true, issued_any = false;
+    for (int64_t u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        const Unit w = map_unit<BN>(p, u);
+        const int kb0 = w.split * p.kb_per_split;
+        const int kb1 = min(p.kb_total, kb0 + p.kb_per_split);
+        const uint32_t acc_empty = bar0 + 8u * (2 * STAGES + 2 + acc);
+        if (!wait_one(acc_empty, acc_phase ^ 1u, abort_flag, p.timeout_ns)) {
+            ok = false;
+            break;
+        }
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = kb0; kb < kb1; ++kb) {
+            if (!wait_one(bar0 + 8u * stage, phase, abort_flag, p.timeout_ns)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+            const uint32_t sa = ring + stage * Cfg::STAGE_BYTES;
+            const uint32_t sb = sa + Cfg::A_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < TILE_K / UMMA_K; ++kk) {
+                // K-major: the next 16 k sit 32 bytes further along the swizzled row.
+                // M/N-major: the next 16 k are the next two 1024-byte row groups.
+                const uint64_t ad = p.a_mn_major ? smem_desc_sw128(sa + 2048u * kk, 8192u, 1024u)
+                                                 : smem_desc_sw128(sa + 32u * kk, 16u, 1024u);
+                const uint64_t bd = p.b_mn_major ? smem_desc_sw128(sb + 2048u * kk, 8192u, 1024u)
+                                                 : smem_desc_sw128(sb + 32u * kk, 16u, 1024u);
+                umma_bf16(d_tmem, ad, bd, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+            }
+            issued_any = true;
+            umma_commit(bar0 + 8u * (STAGES + stage));  // stage free once these MMAs finish
+            if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        if (!ok) break;
+        umma_commit(bar0 + 8u * (2 * STAGES + acc));  // accumulator ready for the epilogue
+        if (++acc == 2) {
+            acc = 0;
+            acc_phase ^= 1u;
+        }
+    }
+    if (!ok) {
+        signal_timeout(p, abort_flag);
+        if (issued_any) {  // drain: MMAs in flight must finish before TMEM is freed
+            const uint32_t drain = bar0 + 8u * (2 * STAGES + 4);
+            umma_commit(drain);
+            wait_one(drain, 0u, nullptr, p.timeout_ns);
+        }
+    }
+}
+
+template <int BN, int STAGES>
+__device__ __forceinline__ void run_epilogue(const GemmParams &p, uint32_t bar0, uint32_t tmem_base,
+                                             float *stage_buf, volatile int *abort_flag, int warp,
+                                             int lane)
+{
+    const int64_t units = p.num_tiles * p.k_splits;
+    const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31 are this warp's rows
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+        const Unit w = map_unit<BN>(p, u);
+        if (!wait_warp(bar0 + 8u * (2 * STAGES + acc), acc_phase, abort_flag, p.timeout_ns)) {
+            if (lane == 0) signal_timeout(p, abort_flag);
+            break;
+        }
+        tc_fence_after_sync();
+        const int64_t row0 = w.tm * TILE_M + quad * 32;
+        const int64_t col0 = w.tn * BN;
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN);
+#pragma unroll 1
+        for (int ch = 0; ch < BN / 32; ++ch) {
+            uint32_t r[32];
+            tmem_load_32cols(taddr + 32u * ch, r);
+            if (ch == BN / 32 - 1) {  // accumulator fully read: hand it back to the MMA warp
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar0 + 8u * (2 * STAGES + 2 + acc));
+            }
+            // Row `lane` of this 32 x 32 block into shared memory; 16-byte chunk c of
+            // row r goes to slot c ^ (r & 7) so that both passes are conflict-free.
+            float4 *srow = reinterpret_cast<float4 *>(stage_buf + lane * 32);
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                srow[c ^ (lane & 7)] =
+                    make_float4(p.alpha * __uint_as_float(r[4 * c + 0]), p.alpha * __uint_as_float(r[4 * c + 1]),
+                                p.alpha * __uint_as_float(r[4 * c + 2]), p.alpha * __uint_as_float(r[4 * c + 3]));
+            __syncwarp();
+            // Coalesced pass: 8 lanes cover one 32-column row segment, 4 rows per step.
+#pragma unroll
+            for (int step = 0; step < 8; ++step) {
+                const int rr = step * 4 + (lane >> 3);
+                const int cc = lane & 7;
+                const float4 v4 = reinterpret_cast<const float4 *>(stage_buf + rr * 32)[cc ^ (rr & 7)];
+                const int64_t gi = row0 + rr;
+                const int64_t gj = col0 + ch * 32 + cc * 4;
+                if (gi >= p.m || gj >= p.n) continue;
+                float v[4] = {v4.x, v4.y, v4.z, v4.w};
+                if (p.k_splits > 1) {
+                    float *dst = p.partial + (static_cast<int64_t>(w.split) * p.m + gi) * p.ldp + gj;
+                    *reinterpret_cast<float4 *>(dst) = v4;
+                } else {
+                    write_c4(p, gi, gj, v);
+                }
+            }
+            __syncwarp();
+        }
+        if (++acc == 2) {
+            acc = 0;
+            acc_phase ^= 1u;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- kernels
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    bm_gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                           const GemmParams p)
+{
+    using Cfg = KernelCfg<BN, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
+    uint8_t *smem = smem_raw + pad;
+    const uint32_t ring = raw + pad;
+    float *epi = reinterpret_cast<float *>(smem + Cfg::RING_BYTES);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::RING_BYTES + Cfg::EPI_BYTES);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Cfg::NUM_BARS);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    const uint32_t bar0 = smem_addr(bars);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(bar0 + 8u * s, 1);             // full: the producer's expect_tx arrival
+            mbar_init(bar0 + 8u * (STAGES + s), 1);  // empty: one tcgen05.commit
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar0 + 8u * (2 * STAGES + b), 1);                  // accumulator full
+            mbar_init(bar0 + 8u * (2 * STAGES + 2 + b), NUM_EPI_WARPS);  // accumulator empty
+        }
+        mbar_init(bar0 + 8u * (2 * STAGES + 4), 1);  // drain (abort path only)
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&tmA);
+        tma_prefetch_map(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(tmem_slot), Cfg::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) run_producer<BN, STAGES>(&tmA, &tmB, p, ring, bar0, abort_flag);
+    } else if (warp == 1) {
+        if (lane == 0) run_mma<BN, STAGES>(p, ring, bar0, tmem_base, abort_flag);
+    } else {
+        run_epilogue<BN, STAGES>(p, bar0, tmem_base, epi + (warp - 2) * EPI_WARP_FLOATS, abort_flag, warp, lane);
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    }
+}
+
+// Sum of the K-split partials in split order, then beta * C, cast and masked store.
+__global__ void __launch_bounds__(256) bm_splitk_reduce_kernel(const GemmParams p)
+{
+    const int64_t cols4 = (p.n + 3) / 4;
+    const int64_t total = p.m * cols4;
+    const int64_t plane = p.m * p.ldp;
+    for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
+         idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t i = idx / cols4;
+        const int64_t j = (idx - i * cols4) * 4;
+        const float *src = p.partial + i * p.ldp + j;
+        float4 s = *reinterpret_cast<const float4 *>(src);
+        for (int sp = 1; sp < p.k_splits; ++sp) {
+            const float4 t = *reinterpret_cast<const float4 *>(src + sp * plane);
+            s.x += t.x;
+            s.y += t.y;
+            s.z += t.z;
+            s.w += t.w;
+        }
+        float v[4] = {s.x, s.y, s.z, s.w};
+        write_c4(p, i, j, v);
+    }
+}
+
+// alpha == 0 or k == 0: C = beta * C on the output region (C unread when beta == 0).
+__global__ void __launch_bounds__(256) bm_scale_kernel(const GemmParams p)
+{
+    const int64_t cols4 = (p.n + 3) / 4;
+    const int64_t total = p.m * cols4;
+    for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
+         idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t i = idx / cols4;
+        const int64_t j = (idx - i * cols4) * 4;
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
+        write_c4(p, i, j, v);
+    }
+}
+
+}  // namespace bm

@@ -1,0 +1,164 @@
+/*
+ * bm.h -- C ABI of the GB300 (sm_103a) BF16 BLAS3 library: GEMM and SYRK.
+ *
+ * The operations are the BLAS3 local compute that the distributed framework in
+ * "BLASMp development notes" rests on (section 1: GEMM is the long-term base
+ * and performance yardstick; stage B: SYRK's main compute is a GEMM), carried
+ * out by the tensor-core GEMM mainloop that the "cp.async / ldmatrix ablation
+ * plan" dissects (section 2, fixed baseline: BF16 GEMM, FP32 accumulate), and
+ * the beta = 0 / beta = 1 weight-gradient GEMMs of "fused A2A/GEMM Perfetto
+ * profile protocol" (official timing rules: ZeroBubble W accumulates into a
+ * BF16 gradient with beta = 1).
+ *
+ * Conventions shared by every entry point
+ *   - Storage is row-major: element (r, c) of a matrix X with leading
+ *     dimension ldx sits at X[r * ldx + c]. Column-major callers use
+ *     C^T = op(B)^T op(A)^T, i.e. swap A and B and the transpose flags.
+ *   - A and B hold bfloat16; products accumulate in FP32 on the tensor cores;
+ *     alpha and beta are applied in FP32; C is FP32 or BF16 (round to nearest
+ *     even on store).
+ *   - BLAS rules: when beta == 0 the input C is not read (NaN/Inf in C do not
+ *     propagate); when alpha == 0 or k == 0 the result is beta * C and A, B
+ *     are not read; m == 0 or n == 0 is a no-op returning BM_OK. C must not
+ *     overlap A or B.
+ *   - Ownership: every pointer is a DEVICE pointer owned by the caller and
+ *     must stay valid until the work queued on `stream` has finished. The
+ *     library allocates nothing per call; it keeps one small device status
+ *     word per device, allocated on first use.
+ *   - Alignment (the tensor-memory-accelerator rules quoted in the ablation
+ *     plan, section 1.3: 16-byte aligned global addresses): A, B and C must be
+ *     16-byte aligned and lda*2, ldb*2, ldc*sizeof(C element) multiples of 16
+ *     bytes; otherwise BM_ERR_MISALIGNED and nothing is launched.
+ *   - Calls are asynchronous on `stream` (NULL = the legacy default stream).
+ *     Argument errors are returned synchronously before anything is queued;
+ *     a failed launch returns BM_ERR_CUDA. A device-side wait that runs out
+ *     of time (see bm_set_wait_timeout_ms) is reported later by
+ *     bm_get_last_device_error.
+ *   - The device must be compute capability 10.3 (GB300, sm_103a); any other
+ *     device gives BM_ERR_ARCH. There is no other code path.
+ */
+#ifndef BM_H
+#define BM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define BM_API __attribute__((visibility("default")))
+#else
+#define BM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same handle as cudaStream_t / CUstream. */
+typedef struct CUstream_st *bm_stream_t;
+
+typedef enum {
+    BM_OK = 0,
+    BM_ERR_INVALID_VALUE = 1, /* negative size, ld too small, bad enum           */
+    BM_ERR_MISALIGNED = 2,    /* pointer or leading dimension breaks the 16-B rule */
+    BM_ERR_ARCH = 3,          /* current device is not compute capability 10.3   */
+    BM_ERR_CUDA = 4,          /* a CUDA runtime/driver call or launch failed      */
+    BM_ERR_TIMEOUT = 5,       /* a device-side bounded wait ran out of time       */
+    BM_ERR_WORKSPACE = 6      /* workspace pointer misaligned or NULL with bytes>0 */
+} bm_status;
+
+typedef enum { BM_OP_N = 0, BM_OP_T = 1 } bm_op;
+typedef enum { BM_C_F32 = 0, BM_C_BF16 = 1 } bm_ctype;
+typedef enum { BM_LOWER = 0, BM_UPPER = 1 } bm_uplo;
+
+/*
+ * GEMM:  C[m x n] = alpha * op(A) * op(B) + beta * C
+ *
+ *   op(A) is m x k: A is stored [m, k] (lda >= k) when transA == BM_OP_N and
+ *   [k, m] (lda >= m) when transA == BM_OP_T. op(B) is k x n: B is stored
+ *   [k, n] (ldb >= n) for BM_OP_N and [n, k] (ldb >= k) for BM_OP_T.
+ *   C is [m, n] with ldc >= n, element type c_type; elements of C beyond
+ *   column n within ldc are never touched.
+ *
+ *   workspace / workspace_bytes: optional caller-owned device scratch for
+ *   splitting K across CTAs when m*n is too small to fill the GPU. NULL/0
+ *   disables the split; the result is correct either way. The size the
+ *   planner would like is bm_gemm_bf16_workspace_size(); less is accepted
+ *   (fewer splits). The workspace must be 256-byte aligned.
+ *
+ *   Returns BM_OK once the work is queued on `stream`.
+ */
+BM_API bm_status bm_gemm_bf16(int64_t m, int64_t n, int64_t k, bm_op transA, bm_op transB,
+                              float alpha, const void *A, int64_t lda, const void *B, int64_t ldb,
+                              float beta, void *C, int64_t ldc, bm_ctype c_type,
+                              void *workspace, size_t workspace_bytes, bm_stream_t stream);
+
+/* Bytes of workspace that bm_gemm_bf16 would use for this shape (0 = none). */
+BM_API size_t bm_gemm_bf16_workspace_size(int64_t m, int64_t n, int64_t k);
+
+/*
+ * SYRK:  C = alpha * op(A) * op(A)^T + beta * C   on one triangle of C[n x n]
+ *
+ *   op(A) is n x k: A is stored [n, k] (lda >= k) when trans == BM_OP_N
+ *   (C = A A^T) and [k, n] (lda >= n) when trans == BM_OP_T (C = A^T A).
+ *   uplo == BM_LOWER updates the elements with row >= column, BM_UPPER those
+ *   with row <= column. The other triangle is neither read nor written.
+ *   Tiles of C that lie entirely in the other triangle are not computed.
+ *   C is [n, n] with ldc >= n.
+ *
+ *   Returns BM_OK once the work is queued on `stream`.
+ */
+BM_API bm_status bm_syrk_bf16(bm_uplo uplo, bm_op trans, int64_t n, int64_t k, float alpha,
+                              const void *A, int64_t lda, float beta, void *C, int64_t ldc,
+                              bm_ctype c_type, bm_stream_t stream);
+
+/*
+ * Device-side errors. Every wait inside the kernels (on a shared-memory
+ * barrier) gives up after the wait limit, records BM_ERR_TIMEOUT in the
+ * device status word, frees its tensor memory and returns, so that the CUDA
+ * context stays usable. This call synchronises `stream`, reads and clears
+ * the status word of the current device and returns it (BM_OK if none).
+ */
+BM_API bm_status bm_get_last_device_error(bm_stream_t stream);
+
+/* Wait limit of the device-side barrier waits in milliseconds (default 2000). */
+BM_API void bm_set_wait_timeout_ms(uint32_t ms);
+
+/*
+ * Test hook for the bounded waits (off by default). While enabled, every CTA
+ * of the next GEMM/SYRK launches leaves its first operand copy unissued, so
+ * the MMA warp's wait on that stage runs out: the kernel records
+ * BM_ERR_TIMEOUT, frees its tensor memory and exits, and the context stays
+ * usable. Pair it with a short bm_set_wait_timeout_ms.
+ */
+BM_API void bm_debug_inject_stall(int enable);
+
+/* Human-readable name of a status code (static storage). */
+BM_API const char *bm_status_string(bm_status status);
+
+/*
+ * Resolved launch plan of a GEMM, for reports and tests: output tile
+ * (tile_m x tile_n), number of output tiles, K splits, CTAs launched and the
+ * number of kernels one call launches. Performs the same argument checks as
+ * bm_gemm_bf16 (except pointer alignment, since no pointers are given).
+ */
+typedef struct {
+    int32_t tile_m, tile_n, tile_k;
+    int32_t stages;
+    int64_t tiles;
+    int32_t k_splits;
+    int32_t ctas;
+    int32_t kernels;
+    size_t workspace_bytes;
+} bm_plan;
+
+BM_API bm_status bm_gemm_bf16_plan(int64_t m, int64_t n, int64_t k, size_t workspace_bytes, bm_plan *plan);
+BM_API bm_status bm_syrk_bf16_plan(bm_uplo uplo, int64_t n, int64_t k, bm_plan *plan);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+BM_API int bm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BM_H */

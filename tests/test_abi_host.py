@@ -1,0 +1,157 @@
+"""C-ABI library: loads, exports every declared symbol, validates arguments (CPU only).
+
+No compute call reaches a GPU here: every call either fails argument checks
+before any CUDA call, is a no-op (m == 0 or n == 0), or (on a machine without
+a GPU) stops at the device query.
+"""
+
+import os
+import re
+
+import pytest
+
+import blas3_tensor_core_gb300 as bm
+from blas3_tensor_core_gb300 import build as bm_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    bm_build.build()
+    return bm.library()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "bm.h")).read()
+    return sorted(set(re.findall(r"BM_API\s+[\w\s\*]*?\b(bm_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_symbols()
+    for required in ("bm_gemm_bf16", "bm_syrk_bf16", "bm_get_last_device_error", "bm_status_string"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    assert bm.bm_status_string(0) == "BM_OK"
+    assert bm.bm_status_string(5) == "BM_ERR_TIMEOUT"
+    assert bm.bm_status_string(99) == "BM_ERR_UNKNOWN"
+    assert bm.bm_version() >= 100
+
+
+def _gemm(m=64, n=64, k=64, ta=0, tb=0, A=0x1000, lda=None, B=0x2000, ldb=None, C=0x3000, ldc=None,
+          ct=0, ws=None, wsb=0, alpha=1.0, beta=0.0):
+    lda = lda if lda is not None else (m if ta else k)
+    ldb = ldb if ldb is not None else (k if tb else n)
+    ldc = ldc if ldc is not None else n
+    return bm.bm_gemm_bf16(m, n, k, ta, tb, alpha, A, lda, B, ldb, beta, C, ldc, ct, ws, wsb, None)
+
+
+def test_gemm_argument_errors(lib):
+    assert _gemm(m=-1) == bm.BM_ERR_INVALID_VALUE
+    assert _gemm(k=-5) == bm.BM_ERR_INVALID_VALUE
+    assert _gemm(m=2 ** 31) == bm.BM_ERR_INVALID_VALUE
+    assert _gemm(ta=2) == bm.BM_ERR_INVALID_VALUE
+    assert _gemm(ct=7) == bm.BM_ERR_INVALID_VALUE
+    assert _gemm(lda=63) == bm.BM_ERR_INVALID_VALUE              # lda < k
+    assert _gemm(ta=1, lda=63) == bm.BM_ERR_INVALID_VALUE        # lda < m for op T
+    assert _gemm(ldb=32) == bm.BM_ERR_INVALID_VALUE
+    assert _gemm(ldc=60) == bm.BM_ERR_INVALID_VALUE
+    assert _gemm(C=0) == bm.BM_ERR_INVALID_VALUE
+    assert _gemm(A=0) == bm.BM_ERR_INVALID_VALUE
+    assert _gemm(ws=None, wsb=1024) == bm.BM_ERR_WORKSPACE
+    assert _gemm(ws=0x4010, wsb=1024) == bm.BM_ERR_WORKSPACE      # not 256-byte aligned
+
+
+def test_gemm_alignment_errors(lib):
+    assert _gemm(A=0x1008) == bm.BM_ERR_MISALIGNED
+    assert _gemm(C=0x3004) == bm.BM_ERR_MISALIGNED
+    assert _gemm(m=8, k=12, lda=12) == bm.BM_ERR_MISALIGNED       # 24-byte rows
+    assert _gemm(n=10, ldc=10) == bm.BM_ERR_MISALIGNED            # fp32 C, 40-byte rows
+    assert _gemm(n=12, ldc=12, ldb=16, ct=bm.BM_C_BF16) == bm.BM_ERR_MISALIGNED
+
+
+def test_gemm_noops_touch_nothing(lib):
+    assert _gemm(m=0) == bm.BM_OK
+    assert _gemm(n=0, ldc=1, ldb=1) == bm.BM_OK
+
+
+def test_alpha_zero_skips_operand_checks(lib):
+    # A and B are not read when alpha == 0: their pointers may be null or misaligned.
+    st = _gemm(alpha=0.0, A=0, B=0x2001)
+    assert st != bm.BM_ERR_INVALID_VALUE and st != bm.BM_ERR_MISALIGNED
+
+
+def test_syrk_argument_errors(lib):
+    def s(uplo=0, trans=0, n=64, k=64, A=0x1000, lda=None, C=0x3000, ldc=None, ct=0):
+        lda = lda if lda is not None else (n if trans else k)
+        ldc = ldc if ldc is not None else n
+        return bm.bm_syrk_bf16(uplo, trans, n, k, 1.0, A, lda, 1.0, C, ldc, ct, None)
+    assert s(uplo=3) == bm.BM_ERR_INVALID_VALUE
+    assert s(trans=5) == bm.BM_ERR_INVALID_VALUE
+    assert s(n=-1) == bm.BM_ERR_INVALID_VALUE
+    assert s(lda=10) == bm.BM_ERR_INVALID_VALUE
+    assert s(trans=1, lda=32) == bm.BM_ERR_INVALID_VALUE
+    assert s(ldc=32) == bm.BM_ERR_INVALID_VALUE
+    assert s(A=0x1002) == bm.BM_ERR_MISALIGNED
+    assert s(n=0, ldc=1) == bm.BM_OK
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(), reason="expects a machine without a GPU")
+def test_valid_call_without_gpu_reports_cuda_error(lib):
+    assert _gemm() == bm.BM_ERR_CUDA
+
+
+def test_gemm_plans(lib):
+    st, p = bm.bm_gemm_bf16_plan(4096, 4096, 4096, 0)
+    assert st == 0 and (p.tile_m, p.tile_n, p.tile_k) == (128, 256, 64)
+    assert p.tiles == 32 * 16 and p.k_splits == 1 and p.kernels == 1
+    st, p = bm.bm_gemm_bf16_plan(2048, 5120, 5120, 0)
+    assert p.tiles == 16 * 20
+    st, p = bm.bm_gemm_bf16_plan(100, 100, 100, 0)
+    assert p.tile_n == 128 and p.tiles == 1
+    # a 512 x 512 output with K = 8192 fills the GPU only when K is split
+    st, p = bm.bm_gemm_bf16_plan(512, 512, 8192, 0)
+    assert p.k_splits == 1 and p.workspace_bytes == 0
+    need = bm.bm_gemm_bf16_workspace_size(512, 512, 8192)
+    assert need > 0
+    st, p = bm.bm_gemm_bf16_plan(512, 512, 8192, need)
+    assert p.k_splits > 1 and p.kernels == 2 and p.workspace_bytes == need
+    assert p.workspace_bytes == p.k_splits * 512 * 512 * 4
+    st, p = bm.bm_gemm_bf16_plan(512, 512, 8192, need // 2)      # less workspace: fewer splits
+    assert 1 <= p.k_splits < bm.bm_gemm_bf16_plan(512, 512, 8192, need)[1].k_splits
+    assert p.workspace_bytes <= need // 2
+    st, p = bm.bm_gemm_bf16_plan(64, 64, 0, 0)
+    assert st == 0 and p.kernels == 1 and p.tiles == 0
+    assert bm.bm_gemm_bf16_plan(-1, 4, 4, 0)[0] == bm.BM_ERR_INVALID_VALUE
+
+
+def _syrk_tiles_bruteforce(n, lower, bm_=128, bn=256):
+    tiles = 0
+    for tm in range((n + bm_ - 1) // bm_):
+        for tn in range((n + bn - 1) // bn):
+            rows = range(tm * bm_, min(n, tm * bm_ + bm_))
+            cols = range(tn * bn, min(n, tn * bn + bn))
+            # does the tile hold an element of the triangle (nominal tile extents)?
+            r_lo, r_hi, c_lo, c_hi = tm * bm_, tm * bm_ + bm_ - 1, tn * bn, tn * bn + bn - 1
+            if (lower and r_hi >= c_lo) or (not lower and r_lo <= c_hi):
+                tiles += 1
+                assert rows and cols
+    return tiles
+
+
+@pytest.mark.parametrize("n", [1, 100, 128, 129, 256, 300, 1000, 8192])
+def test_syrk_plans_visit_only_triangle_tiles(lib, n):
+    for uplo in (bm.BM_LOWER, bm.BM_UPPER):
+        st, p = bm.bm_syrk_bf16_plan(uplo, n, 64)
+        assert st == 0
+        assert p.tiles == _syrk_tiles_bruteforce(n, uplo == bm.BM_LOWER)
+    if n == 8192:
+        # 64 tile rows of 128, 32 tile columns of 256: row t holds floor(t/2)+1 lower tiles
+        assert bm.bm_syrk_bf16_plan(bm.BM_LOWER, n, 64)[1].tiles == 1056

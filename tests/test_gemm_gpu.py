@@ -1,0 +1,231 @@
+"""GEMM parity: the CUDA path (through the C ABI) against the CPU oracle, on a GB300.
+
+Small and ragged shapes are compared element by element on the whole output
+(several tiles, ragged edges in m, n and k); the workloads at full size are
+compared on sampled positions covering every output tile, in the launch
+configuration the bench times. Exact-integer inputs pin the descriptors and
+the tensor-memory layout bit for bit; Gaussian inputs use the tolerance
+1e-3 * |alpha| * sum|a*b| (+ 2^-8 |ref| for BF16 output).
+"""
+
+import itertools
+
+import numpy as np
+import pytest
+
+import bm_inputs as gen
+import oracle
+from gpu_helpers import (CBuffer, assert_parity, c_input_values, operand, run_gemm, tile_samples, torch)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from blas3_tensor_core_gb300 import build
+    build.build()
+    assert torch().cuda.is_available()
+
+
+def _stored(rows, cols, trans):
+    return (cols, rows) if trans else (rows, cols)
+
+
+def _pad_for(cols, elem_bytes):
+    per = 16 // elem_bytes
+    return (-cols) % per + per  # always pad: the gap must never be read
+
+
+def _operands(m, n, k, ta, tb, dist, seed, std=1.0, lo=-1.0, hi=1.0):
+    ra, ca = _stored(m, k, ta)
+    rb, cb = _stored(k, n, tb)
+    A = operand(ra, ca, dist, seed, std, lo, hi, pad=_pad_for(ca, 2))
+    B = operand(rb, cb, dist, seed + 1, std, lo, hi, pad=_pad_for(cb, 2))
+    return A, B
+
+
+def _ldc(n, bf16):
+    per = 8 if bf16 else 4
+    return n + (-n) % per + per
+
+
+ORC = None
+
+
+def orc():
+    global ORC
+    if ORC is None:
+        ORC = oracle.default()
+    return ORC
+
+
+# ----------------------------------------------------------------------------- exact
+@pytest.mark.parametrize("ta,tb", list(itertools.product((0, 1), (0, 1))))
+@pytest.mark.parametrize("shape", [(256, 256, 256), (200, 300, 136), (129, 520, 64), (1, 8, 8)])
+def test_exact_integer_inputs_bitwise(shape, ta, tb):
+    m, n, k = shape
+    A, B = _operands(m, n, k, ta, tb, "int", seed=11, lo=-8, hi=8)
+    cbuf = CBuffer(m, n, _ldc(n, False), False, init=np.full((m, n), np.nan, np.float32))  # beta = 0: unread
+    got, raw = run_gemm(m, n, k, ta, tb, 1.0, A, B, 0.0, cbuf)
+    ref, _ = orc().gemm(m, n, k, ta, tb, 1.0, A, B)
+    assert np.array_equal(got, ref), f"max |diff| {np.max(np.abs(got - ref))}"
+    cbuf.assert_guard_intact(raw)
+
+
+def test_exact_integer_beta_accumulate_bitwise():
+    m, n, k = 384, 264, 200
+    A, B = _operands(m, n, k, 0, 0, "int", seed=21, lo=-8, hi=8)
+    c0 = gen.integers(23, m * n, -100, 100).reshape(m, n).astype(np.float32)
+    cbuf = CBuffer(m, n, _ldc(n, False), False, init=c0)
+    got, raw = run_gemm(m, n, k, 0, 0, 2.0, A, B, -1.0, cbuf)
+    ref, _ = orc().gemm(m, n, k, 0, 0, 2.0, A, B, -1.0, c0)
+    assert np.array_equal(got, ref)
+    cbuf.assert_guard_intact(raw)
+
+
+# ----------------------------------------------------------------------------- tolerance
+def test_config_256_uniform_fp32():
+    """256^3, A and B uniform in [-1, 1] rounded to bf16, FP32 C, alpha = 1, beta = 0."""
+    m = n = k = 256
+    A = operand(m, k, "uniform", seed=1)
+    B = operand(k, n, "uniform", seed=2)
+    cbuf = CBuffer(m, n, n, False, init=np.full((m, n), np.nan, np.float32))
+    got, raw = run_gemm(m, n, k, 0, 0, 1.0, A, B, 0.0, cbuf)
+    ref, bound = orc().gemm(m, n, k, 0, 0, 1.0, A, B)
+    assert_parity(got, ref, bound, 1.0, 0.0, None, False, "256^3 fp32")
+    cbuf.assert_guard_intact(raw)
+
+
+@pytest.mark.parametrize("ta,tb", list(itertools.product((0, 1), (0, 1))))
+@pytest.mark.parametrize("bf16_out,beta", [(False, 0.0), (False, 1.5), (True, 0.0), (True, -0.5)])
+def test_gaussian_ragged_multi_tile(ta, tb, bf16_out, beta):
+    m, n, k = 640, 520, 328
+    alpha = -0.75
+    A, B = _operands(m, n, k, ta, tb, "normal", seed=31)
+    c0 = gen.matrix_f32(m, n, "normal", seed=33)
+    c_init = gen.f32_to_bf16_bits(c0) if bf16_out else c0
+    cbuf = CBuffer(m, n, _ldc(n, bf16_out), bf16_out, init=c_init)
+    got, raw = run_gemm(m, n, k, ta, tb, alpha, A, B, beta, cbuf)
+    ref, bound = orc().gemm(m, n, k, ta, tb, alpha, A, B, beta, c_init if beta != 0 else None)
+    assert_parity(got, ref, bound, alpha, beta, c_input_values(c_init, bf16_out), bf16_out, "ragged")
+    cbuf.assert_guard_intact(raw)
+
+
+def test_backward_shaped_small_transA_beta1_bf16():
+    """dW += dY^T X in miniature: transA, K small, beta = 1 into an existing bf16 C, N(0, 0.02)."""
+    m, n, k = 384, 640, 256
+    A, B = _operands(m, n, k, 1, 0, "normal", seed=41, std=0.02)
+    c_init = gen.matrix_bf16(m, n, "normal", seed=43, std=0.02)
+    cbuf = CBuffer(m, n, _ldc(n, True), True, init=c_init)
+    got, raw = run_gemm(m, n, k, 1, 0, 1.0, A, B, 1.0, cbuf)
+    ref, bound = orc().gemm(m, n, k, 1, 0, 1.0, A, B, 1.0, c_init)
+    assert_parity(got, ref, bound, 1.0, 1.0, c_input_values(c_init, True), True, "dW small")
+    cbuf.assert_guard_intact(raw)
+
+
+# ----------------------------------------------------------------------------- BLAS conventions
+def test_alpha_zero_does_not_read_a_or_b():
+    m, n, k = 130, 260, 70
+    A = np.full((m, 72), gen.BF16_NAN, np.uint16)
+    B = np.full((k, 264), gen.BF16_NAN, np.uint16)
+    c0 = gen.matrix_f32(m, n, "normal", seed=51)
+    cbuf = CBuffer(m, n, 264, False, init=c0)
+    got, raw = run_gemm(m, n, k, 0, 0, 0.0, A, B, -2.0, cbuf)
+    assert np.array_equal(got, (-2.0 * c0).astype(np.float32).astype(np.float64))
+    cbuf.assert_guard_intact(raw)
+
+
+def test_k_zero_gives_beta_c_and_beta_zero_gives_zero():
+    m, n = 70, 36
+    A = np.zeros((m, 8), np.uint16)
+    B = np.zeros((8, 40), np.uint16)
+    c0 = gen.matrix_bf16(m, n, "normal", seed=52)
+    cbuf = CBuffer(m, n, 40, True, init=c0)
+    got, raw = run_gemm(m, n, 0, 0, 0, 1.0, A, B, 0.5, cbuf)
+    assert np.array_equal(got, 0.5 * gen.bf16_bits_to_f32(c0).astype(np.float64))
+    cbuf.assert_guard_intact(raw)
+    cbuf2 = CBuffer(m, n, 40, False, init=np.full((m, n), np.nan, np.float32))
+    got, raw = run_gemm(m, n, 0, 0, 0, 1.0, A, B, 0.0, cbuf2)
+    assert np.all(got == 0.0)
+    cbuf2.assert_guard_intact(raw)
+
+
+# ----------------------------------------------------------------------------- split K
+def test_split_k_matches_oracle_and_is_deterministic():
+    import blas3_tensor_core_gb300 as bm
+    t = torch()
+    m, n, k = 512, 512, 8192
+    A, B = _operands(m, n, k, 0, 0, "normal", seed=61)
+    need = bm.bm_gemm_bf16_workspace_size(m, n, k)
+    st, plan = bm.bm_gemm_bf16_plan(m, n, k, need)
+    assert plan.k_splits > 1
+    ws = t.empty(need // 4 + 64, dtype=t.float32, device="cuda")
+    outs = []
+    for _ in range(2):
+        cbuf = CBuffer(m, n, n, False, init=np.full((m, n), np.nan, np.float32))
+        got, raw = run_gemm(m, n, k, 0, 0, 1.0, A, B, 0.0, cbuf, workspace=ws)
+        cbuf.assert_guard_intact(raw)
+        outs.append(got)
+    assert np.array_equal(outs[0], outs[1])
+    rows, cols = tile_samples(m, n, per_tile=64, seed=3)
+    ref, bound = orc().gemm_entries(k, 0, 0, 1.0, A, B, rows, cols)
+    assert_parity(outs[0][rows, cols], ref, bound, 1.0, 0.0, None, False, "split-K")
+    cbuf = CBuffer(m, n, n, False)
+    plain, _ = run_gemm(m, n, k, 0, 0, 1.0, A, B, 0.0, cbuf)  # no workspace: one split
+    assert_parity(plain[rows, cols], ref, bound, 1.0, 0.0, None, False, "no split")
+
+
+# ----------------------------------------------------------------------------- persistence
+def test_persistent_many_tiles_exact():
+    """More tiles than SMs (each CTA loops over several tiles and both accumulators)."""
+    m, n, k = 4096, 2048, 192
+    A, B = _operands(m, n, k, 0, 0, "int", seed=71, lo=-8, hi=8)
+    cbuf = CBuffer(m, n, n, False)
+    got, raw = run_gemm(m, n, k, 0, 0, 1.0, A, B, 0.0, cbuf)
+    rows, cols = tile_samples(m, n, per_tile=16, seed=4)
+    ref, _ = orc().gemm_entries(k, 0, 0, 1.0, A, B, rows, cols)
+    assert np.array_equal(got[rows, cols], ref)
+    # whole rows, one per tile row, exactly
+    rr = np.arange(0, m, 128) + 37
+    full_rows = np.repeat(rr, n)
+    full_cols = np.tile(np.arange(n), len(rr))
+    ref_rows, _ = orc().gemm_entries(k, 0, 0, 1.0, A, B, full_rows, full_cols)
+    assert np.array_equal(got[full_rows, full_cols], ref_rows)
+    cbuf.assert_guard_intact(raw)
+
+
+# ----------------------------------------------------------------------------- full-size workloads
+FULL = [
+    # name, m, n, k, transA, transB, std, beta, bf16 C
+    ("gemm_4096_cube_bf16", 4096, 4096, 4096, 0, 0, 1.0, 0.0, True),
+    ("sweep_512_k256", 512, 512, 256, 0, 0, 1.0, 0.0, True),
+    ("sweep_512_k512", 512, 512, 512, 0, 0, 1.0, 0.0, True),
+    ("sweep_512_k1024", 512, 512, 1024, 0, 0, 1.0, 0.0, True),
+    ("sweep_512_k4096", 512, 512, 4096, 0, 0, 1.0, 0.0, True),
+    ("sweep_512_k8192", 512, 512, 8192, 0, 0, 1.0, 0.0, True),
+    ("sweep_4096_k256", 4096, 4096, 256, 0, 0, 1.0, 0.0, True),
+    ("sweep_4096_k512", 4096, 4096, 512, 0, 0, 1.0, 0.0, True),
+    ("sweep_4096_k1024", 4096, 4096, 1024, 0, 0, 1.0, 0.0, True),
+    ("sweep_4096_k8192", 4096, 4096, 8192, 0, 0, 1.0, 0.0, True),
+    ("bwd_dX_2048x5120x5120", 2048, 5120, 5120, 0, 0, 0.02, 0.0, True),
+    ("bwd_dW_5120x5120x2048_transA_beta1", 5120, 5120, 2048, 1, 0, 0.02, 1.0, True),
+]
+
+
+@pytest.mark.parametrize("name,m,n,k,ta,tb,std,beta,cbf", FULL, ids=[f[0] for f in FULL])
+def test_full_size_workload_sampled(name, m, n, k, ta, tb, std, beta, cbf):
+    import blas3_tensor_core_gb300 as bm
+    t = torch()
+    A = operand(*_stored(m, k, ta), "normal", 1, std)
+    B = operand(*_stored(k, n, tb), "normal", 2, std)
+    c_init = gen.matrix_bf16(m, n, "normal", 3, std) if beta != 0 else None
+    cbuf = CBuffer(m, n, n, cbf, init=c_init, extra_rows=1)
+    need = bm.bm_gemm_bf16_workspace_size(m, n, k)
+    ws = t.empty(max(need // 4, 1), dtype=t.float32, device="cuda") if need else None
+    got, raw = run_gemm(m, n, k, ta, tb, 1.0, A, B, beta, cbuf, workspace=ws)
+    assert np.all(np.isfinite(got))
+    rows, cols = tile_samples(m, n, per_tile=4, seed=5)
+    ref, bound = orc().gemm_entries(k, ta, tb, 1.0, A, B, rows, cols, beta, c_init)
+    c_in = c_input_values(c_init, cbf)
+    assert_parity(got[rows, cols], ref, bound, 1.0, beta, None if c_in is None else c_in[rows, cols], cbf, name)
+    cbuf.assert_guard_intact(raw)
