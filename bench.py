@@ -1,0 +1,611 @@
+#!/usr/bin/env python3
+"""Bench: BF16 GEMM TFLOP/s on one GB300 (replicas on N GPUs), plus the K-sweep.
+
+One step is one call of the C-ABI GEMM (tensor-map encode, persistent tcgen05
+kernel: tile scheduling, TMA producer, MMA, epilogue) on the 4096^3 workload:
+A[4096, 4096] and B[4096, 4096] row-major with N(0, 1) entries rounded to
+bf16, FP32 accumulate, bf16 C, alpha = 1, beta = 0 (the square BF16 GEMM that
+"cp.async / ldmatrix ablation plan" section 0.3 times at 4096^3). The K-sweep
+of its section 2.3 (K in {256, 512, 1024, 4096, 8192} x M = N in {512, 4096})
+is timed the same way and reported in the "sweep" field.
+
+Timing: W warm-up steps, then exactly K steps between two CUDA events on the
+launching stream, bracketed by a barrier and a device synchronisation on both
+sides; the max over ranks is taken. Inputs are resident in HBM; every step
+uses the next of several input sets whose total is larger than twice the L2,
+so no step finds its operands in L2. Clocks and throttle reasons are sampled
+through NVML during the timed region. `e2e` repeats the measurement through
+the same C-ABI call with the inputs in pinned host memory: each step copies
+A and B to the device and C back inside the timed region.
+
+`--impl reference` times the CPU oracle (plain double-precision triple loop)
+on a bounded sample of the same workload; it is the comparison arm, not a
+target.
+
+Prints ONE JSON line on rank 0.
+"""
+
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "BF16 GEMM TFLOP/s (4096³ + K-sweep) and % of GB300 dense BF16 tensor peak"
+UNIT = "TFLOP/s"
+# Best 4096^3 BF16 figure printed by the pages (TMA multistage kernel, 4.006 ms,
+# on an sm_120-class card): context, not the target.
+PAGES_4096_TFLOPS = 34.31
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+MAIN = dict(name="gemm_bf16_4096x4096x4096_nn_bf16c", m=4096, n=4096, k=4096, ta=0, tb=0, std=1.0,
+            beta=0.0, cbf=True)
+SWEEP = [dict(name=f"sweep_{mn}x{mn}x{k}", m=mn, n=mn, k=k, ta=0, tb=0, std=1.0, beta=0.0, cbf=True)
+         for mn in (512, 4096) for k in (256, 512, 1024, 4096, 8192)]
+EXTRA = [
+    dict(name="bwd_dX_2048x5120x5120", m=2048, n=5120, k=5120, ta=0, tb=0, std=0.02, beta=0.0, cbf=True),
+    dict(name="bwd_dW_5120x5120x2048_transA_beta1", m=5120, n=5120, k=2048, ta=1, tb=0, std=0.02,
+         beta=1.0, cbf=True),
+    dict(name="gemm_256x256x256_uniform_f32c", m=256, n=256, k=256, ta=0, tb=0, std=None, beta=0.0,
+         cbf=False),
+]
+SYRK_CFG = dict(name="syrk_lower_8192x4096_f32c_beta1", n=8192, k=4096, beta=1.0)
+
+
+# ----------------------------------------------------------------------------- work accounting
+def gemm_flops(m, n, k):
+    """2*M*N*K, the convention of the pages' 4096^3 tables (e.g. 2*4096^3 / 4.259 ms = 32.27 TFLOP/s)."""
+    return 2 * m * n * k
+
+
+def syrk_flops(n, k):
+    """Products of the referenced triangle incl. the diagonal: n(n+1)/2 outputs x 2k."""
+    return n * (n + 1) * k
+
+
+def gemm_bytes(m, n, k, c_bytes, beta):
+    """Each operand read once, C written once (and read once when beta != 0)."""
+    return 2 * (m * k + k * n) + c_bytes * m * n * (2 if beta != 0 else 1)
+
+
+def syrk_bytes(n, k, c_bytes, beta):
+    tri = n * (n + 1) // 2
+    return 2 * n * k + c_bytes * tri * (2 if beta != 0 else 1)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS, source="fallback")
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "blas3_tensor_core_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary, if it matches the current kernel source."""
+    path = os.path.join(ROOT, "profiles", f"{workload}.ncu.txt")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None, None
+    fields = {}
+    for line in text.splitlines():
+        if ":" in line and not line.startswith(" "):
+            key, _, val = line.partition(":")
+            fields[key.strip()] = val.strip()
+    if fields.get("kernel_source_sha256") != kernel_source_hash():
+        return None, "stale"
+    try:
+        return float(fields["dram_bytes_per_launch"]), os.path.relpath(path, ROOT)
+    except (KeyError, ValueError):
+        return None, None
+
+
+# ----------------------------------------------------------------------------- clocks (NVML via ctypes)
+class ClockSampler:
+    """Samples SM clock, power and clock-event reasons every few ms on a host thread."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, torch_device, period_s=0.005):
+        self.period = period_s
+        self.samples = []
+        self.window = None
+        self.max_mhz = None
+        self.ok = False
+        self._stop = threading.Event()
+        self._thread = None
+        try:
+            self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nvml.nvmlInit_v2() != 0:
+                return
+            self.handle = ctypes.c_void_p()
+            got = False
+            try:
+                import torch
+                props = torch.cuda.get_device_properties(torch_device)
+                bus = f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0"
+                got = self.nvml.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(self.handle)) == 0
+            except Exception:
+                got = False
+            if not got and self.nvml.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(self.handle)) != 0:
+                return
+            mx = ctypes.c_uint()
+            if self.nvml.nvmlDeviceGetMaxClockInfo(self.handle, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            self._reasons_fn = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(self.nvml, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            self.ok = True
+        except (OSError, AttributeError):
+            self.ok = False
+
+    def _sample(self):
+        clk, pw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(clk))
+        self.nvml.nvmlDeviceGetPowerUsage(self.handle, ctypes.byref(pw))
+        self._reasons_fn(self.handle, ctypes.byref(rs))
+        return (time.perf_counter(), clk.value, pw.value / 1000.0, rs.value)
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                self.samples.append(self._sample())
+            except Exception:
+                pass
+            time.sleep(self.period)
+
+    def start(self):
+        if self.ok:
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
+
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
+
+    def stop(self):
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join()
+
+    def summary(self):
+        if not self.ok:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "source": "unavailable"}
+        t0, t1 = self.window if self.window else (float("-inf"), float("inf"))
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        reasons = set()
+        for s in inside:
+            for bit, name in self.REASONS.items():
+                if s[3] & bit:
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median([s[1] for s in inside]) if inside else None,
+                "sm_max_mhz": self.max_mhz,
+                "power_w_max": max((s[2] for s in inside), default=None),
+                "reasons": sorted(reasons), "samples": len(inside), "source": "nvml"}
+
+
+# ----------------------------------------------------------------------------- distributed plumbing
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = False
+        if self.world > 1:
+            import torch.distributed as dist
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            dist.init_process_group("gloo", rank=self.rank, world_size=self.world)
+            self.pg = True
+
+    def barrier(self):
+        if self.pg:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def max(self, value: float) -> float:
+        if not self.pg:
+            return value
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([value], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- GPU workload
+def host_inputs(cfg):
+    import bm_inputs as gen
+    m, n, k, ta, tb = cfg["m"], cfg["n"], cfg["k"], cfg["ta"], cfg["tb"]
+    ra, ca = (k, m) if ta else (m, k)
+    rb, cb = (n, k) if tb else (k, n)
+    if cfg["std"] is None:
+        A = gen.matrix_bf16(ra, ca, "uniform", seed=1)
+        B = gen.matrix_bf16(rb, cb, "uniform", seed=2)
+    else:
+        A = gen.matrix_bf16(ra, ca, "normal", seed=1, std=cfg["std"])
+        B = gen.matrix_bf16(rb, cb, "normal", seed=2, std=cfg["std"])
+    C0 = None
+    if cfg["beta"] != 0:
+        C0 = gen.matrix_bf16(m, n, "normal", seed=3, std=cfg["std"] or 1.0)
+    return A, B, C0
+
+
+class GemmWorkload:
+    """Device-resident input sets for one GEMM shape, rotated so that no step hits L2."""
+
+    def __init__(self, cfg, torch_mod, min_total=2 * L2_BYTES, max_sets=1024):
+        import numpy as np
+        t = torch_mod
+        self.cfg = cfg
+        self.t = t
+        A, B, C0 = host_inputs(cfg)
+        self.A_host, self.B_host, self.C0_host = A, B, C0
+        dA = t.from_numpy(A.view(np.int16)).view(t.bfloat16).cuda()
+        dB = t.from_numpy(B.view(np.int16)).view(t.bfloat16).cuda()
+        cdt = t.bfloat16 if cfg["cbf"] else t.float32
+        m, n = cfg["m"], cfg["n"]
+        dC = t.empty((m, n), dtype=cdt, device="cuda")
+        if C0 is not None:
+            dC.copy_(t.from_numpy(C0.view(np.int16)).view(t.bfloat16).to(cdt))
+        per_set = dA.numel() * 2 + dB.numel() * 2 + dC.numel() * dC.element_size()
+        nsets = max(2, min(max_sets, -(-min_total // per_set)))
+        self.sets = [(dA, dB, dC)] + [(dA.clone(), dB.clone(), dC.clone()) for _ in range(nsets - 1)]
+        self.set_bytes = per_set
+        import blas3_tensor_core_gb300 as bm
+        self.bm = bm
+        need = bm.bm_gemm_bf16_workspace_size(m, n, cfg["k"])
+        self.ws = t.empty(max(need // 4, 1), dtype=t.float32, device="cuda") if need else None
+        self.ws_bytes = need
+        st, self.plan = bm.bm_gemm_bf16_plan(m, n, cfg["k"], need)
+        assert st == 0
+        self.lda = A.shape[1]
+        self.ldb = B.shape[1]
+
+    def call(self, i, stream_handle):
+        c = self.cfg
+        dA, dB, dC = self.sets[i % len(self.sets)]
+        st = self.bm.bm_gemm_bf16(c["m"], c["n"], c["k"], c["ta"], c["tb"], 1.0, dA.data_ptr(), self.lda,
+                                  dB.data_ptr(), self.ldb, c["beta"], dC.data_ptr(), c["n"],
+                                  self.bm.BM_C_BF16 if c["cbf"] else self.bm.BM_C_F32,
+                                  None if self.ws is None else self.ws.data_ptr(), self.ws_bytes, stream_handle)
+        if st != 0:
+            raise RuntimeError(f"bm_gemm_bf16: {self.bm.bm_status_string(st)}")
+
+    def flops(self):
+        c = self.cfg
+        return gemm_flops(c["m"], c["n"], c["k"])
+
+    def bytes(self):
+        c = self.cfg
+        return gemm_bytes(c["m"], c["n"], c["k"], 2 if c["cbf"] else 4, c["beta"])
+
+
+def timed_steps(wl, steps, warmup, dist, sampler=None):
+    """Device time (ms) of exactly `steps` calls, max over ranks."""
+    t = wl.t
+    stream = t.cuda.current_stream()
+    h = stream.cuda_stream
+    for i in range(warmup):
+        wl.call(i, h)
+    t.cuda.synchronize()
+    dist.barrier()
+    t.cuda.synchronize()
+    ev0, ev1 = t.cuda.Event(enable_timing=True), t.cuda.Event(enable_timing=True)
+    host0 = time.perf_counter()
+    ev0.record(stream)
+    for i in range(steps):
+        wl.call(warmup + i, h)
+    ev1.record(stream)
+    t.cuda.synchronize()
+    host1 = time.perf_counter()
+    if sampler is not None:
+        sampler.mark(host0, host1)
+    dist.barrier()
+    t.cuda.synchronize()
+    st = wl.bm.bm_get_last_device_error(h)
+    if st != 0:
+        raise RuntimeError(f"device error: {wl.bm.bm_status_string(st)}")
+    return dist.max(ev0.elapsed_time(ev1))
+
+
+def e2e_steps(wl, steps, warmup, dist):
+    """Same call with pinned host inputs: H2D of A and B and D2H of C inside the timed region."""
+    import numpy as np
+    t = wl.t
+    stream = t.cuda.current_stream()
+    h = stream.cuda_stream
+    hA = t.from_numpy(wl.A_host.view(np.int16)).view(t.bfloat16).pin_memory()
+    hB = t.from_numpy(wl.B_host.view(np.int16)).view(t.bfloat16).pin_memory()
+    dA, dB, dC = wl.sets[0]
+    hC = t.empty(dC.shape, dtype=dC.dtype).pin_memory()
+    hC0 = None
+    if wl.C0_host is not None:  # beta != 0: the step's input C travels too
+        hC0 = t.from_numpy(wl.C0_host.view(np.int16)).view(t.bfloat16).to(dC.dtype).pin_memory()
+
+    def step():
+        dA.copy_(hA, non_blocking=True)
+        dB.copy_(hB, non_blocking=True)
+        if hC0 is not None:
+            dC.copy_(hC0, non_blocking=True)
+        wl.call(0, h)
+        hC.copy_(dC, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    t.cuda.synchronize()
+    dist.barrier()
+    t.cuda.synchronize()
+    ev0, ev1 = t.cuda.Event(enable_timing=True), t.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(steps):
+        step()
+    ev1.record(stream)
+    t.cuda.synchronize()
+    dist.barrier()
+    ms = dist.max(ev0.elapsed_time(ev1))
+    h2d = hA.numel() * 2 + hB.numel() * 2 + (0 if hC0 is None else hC0.numel() * hC0.element_size())
+    d2h = hC.numel() * hC.element_size()
+    return ms, h2d, d2h, hC
+
+
+# ----------------------------------------------------------------------------- CPU oracle legs
+def oracle_rows_rate(A, B, cfg, budget_s):
+    """Oracle TFLOP/s on the first R rows of the workload, R sized to about budget_s of CPU work."""
+    import oracle
+    o = oracle.default()
+    m, n, k = cfg["m"], cfg["n"], cfg["k"]
+    rows = 4
+    t0 = time.perf_counter()
+    o.gemm(rows, n, k, 0, 0, 1.0, A[:rows], B)
+    dt = max(time.perf_counter() - t0, 1e-6)
+    R = int(max(4, min(m, rows * budget_s / dt)))
+    t0 = time.perf_counter()
+    ref, bound = o.gemm(R, n, k, 0, 0, 1.0, A[:R], B)
+    dt = time.perf_counter() - t0
+    return {"rows": R, "seconds": dt, "tflops": gemm_flops(R, n, k) / dt / 1e12, "cores": o.num_threads(),
+            "ref": ref, "bound": bound}
+
+
+def cpu_baseline_leg(wl, budget_s):
+    """The oracle timed on a bounded sample (the first rows of C); also checks those rows of the GPU C."""
+    import numpy as np
+    import oracle
+    cfg = wl.cfg
+    res = oracle_rows_rate(wl.A_host, wl.B_host, cfg, budget_s)
+    dC = wl.sets[0][2]
+    t = wl.t
+    got = dC[:res["rows"]].float().cpu().numpy().astype(np.float64)
+    ok, worst, _ = oracle.compare(got, res["ref"], res["bound"], 1.0, 0.0, None, cfg["cbf"])
+    return {"value": round(res["tflops"], 6), "unit": UNIT, "cores": res["cores"], "kind": "oracle",
+            "sample": f"first {res['rows']} of {cfg['m']} rows of C for {cfg['name']} "
+                      f"({res['seconds']:.1f} s of CPU work; TFLOP/s scaled by 2*rows*n*k)",
+            "parity_rows_checked": res["rows"], "parity_ok": bool(ok), "worst_err_over_tol": round(worst, 6)}
+
+
+def reference_arm(args, dist):
+    """--impl reference: the CPU oracle, each step a bounded sample of the 4096^3 workload."""
+    if dist.rank != 0:
+        return None
+    import numpy as np
+    import oracle
+    cfg = MAIN
+    A, B, _ = host_inputs(cfg)
+    o = oracle.default()
+    n, k = cfg["n"], cfg["k"]
+    budget = float(args.reference_budget_s)
+    total_steps = args.steps + args.warmup
+    per_step_s = max(budget / max(total_steps, 1), 0.002)
+    rng = np.random.default_rng(0)
+    # calibrate entries per step
+    probe = 64
+    rows, cols = rng.integers(0, cfg["m"], probe), rng.integers(0, n, probe)
+    t0 = time.perf_counter()
+    o.gemm_entries(k, 0, 0, 1.0, A, B, rows, cols)
+    dt = max(time.perf_counter() - t0, 1e-6)
+    entries = int(max(1, min(cfg["m"] * n, probe * per_step_s / dt)))
+    samples = [(rng.integers(0, cfg["m"], entries), rng.integers(0, n, entries)) for _ in range(4)]
+    for i in range(args.warmup):
+        o.gemm_entries(k, 0, 0, 1.0, A, B, *samples[i % 4])
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        o.gemm_entries(k, 0, 0, 1.0, A, B, *samples[i % 4])
+    dt = time.perf_counter() - t0
+    flops = 2.0 * entries * k * args.steps
+    value = flops / dt / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / max(args.steps, 1) * 1e3, 6), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": main_config(None),
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": o.num_threads(), "kind": "oracle",
+                         "sample": f"{entries} random entries of C per step for {cfg['name']} "
+                                   f"(2*k flops each)"},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    return line
+
+
+def main_config(wl):
+    cfg = MAIN
+    c = {"workload": cfg["name"], "m": cfg["m"], "n": cfg["n"], "k": cfg["k"], "transA": "N", "transB": "N",
+         "A": "row-major [4096,4096] N(0,1) rounded to bf16 (seed 1)",
+         "B": "row-major [4096,4096] N(0,1) rounded to bf16 (seed 2)",
+         "C": "bf16 [4096,4096], alpha=1, beta=0", "accumulate": "fp32",
+         "parallelism": "replicas (one independent GEMM per GPU, no collective)"}
+    if wl is not None:
+        c["l2"] = (f"inputs larger than L2: {len(wl.sets)} rotating input sets of {wl.set_bytes / 2**20:.0f} MiB "
+                   f"(> 2 x 129 MB L2)")
+        c["plan"] = wl.plan.as_dict()
+    return c
+
+
+# ----------------------------------------------------------------------------- main
+def run_gpu_arm(args, dist):
+    import torch
+    torch.cuda.set_device(dist.local)
+    import blas3_tensor_core_gb300 as bm
+    if not os.path.exists(bm.library_path):
+        from blas3_tensor_core_gb300 import build
+        build.build()
+    peaks = load_peaks()
+    wl = GemmWorkload(MAIN, torch)
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    ms = timed_steps(wl, args.steps, args.warmup, dist, sampler)
+    sampler.stop()
+    clocks = sampler.summary()
+    per_step = ms / args.steps
+    value = dist.world * wl.flops() * args.steps / (ms * 1e-3) / 1e12
+    achieved = wl.flops() / (per_step * 1e-3) / 1e12
+    traffic, traffic_src = profiled_traffic(MAIN["name"])
+    roofline = {"bound": "tensor", "achieved": round(achieved, 3), "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+                "traffic": traffic,
+                "peak_kind": f"burst bf16 dense ({peaks['source']}, MEASURED_PEAKS.json bf16_tflops)",
+                "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4),
+                "algorithmic_flops_per_launch": wl.flops(),
+                "algorithmic_bytes_per_launch": wl.bytes(),
+                "kernel": "bm_gemm_tcgen05_kernel<256,4>",
+                "traffic_source": traffic_src}
+    e2e_ms, h2d, d2h, _ = e2e_steps(wl, args.e2e_steps, max(3, args.warmup // 10), dist)
+    e2e = {"value": round(dist.world * wl.flops() * args.e2e_steps / (e2e_ms * 1e-3) / 1e12, 3), "unit": UNIT,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+           "ms_per_step": round(e2e_ms / args.e2e_steps, 4)}
+    sweep = []
+    if not args.no_sweep:
+        for cfg in SWEEP + (EXTRA if args.all_configs else []):
+            sw = GemmWorkload(cfg, torch)
+            sms = timed_steps(sw, args.sweep_steps, max(3, args.sweep_steps // 10), dist)
+            t_launch = sms / args.sweep_steps * 1e-3
+            tf = sw.flops() / t_launch / 1e12
+            gbs = sw.bytes() / t_launch / 1e9
+            bound = "tensor" if sw.flops() / (peaks["bf16_tflops"] * 1e12) >= sw.bytes() / (peaks["hbm_gbs"] * 1e9) \
+                else "hbm"
+            sweep.append({"workload": cfg["name"], "us_per_step": round(t_launch * 1e6, 3),
+                          "tflops": round(tf, 2), "gbs": round(gbs, 1),
+                          "frac_tensor": round(tf / peaks["bf16_tflops"], 4),
+                          "frac_hbm": round(gbs / peaks["hbm_gbs"], 4), "bound": bound,
+                          "k_splits": sw.plan.k_splits, "tiles": sw.plan.tiles})
+            del sw
+            torch.cuda.empty_cache()
+        if args.all_configs:
+            sweep.append(syrk_point(args, dist, peaks))
+    cpu = None
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_leg(wl, args.cpu_budget_s)
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(per_step, 6), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": round(value / dist.world / PAGES_4096_TFLOPS, 2),
+        "vs_baseline_ref": f"{PAGES_4096_TFLOPS} TFLOP/s per GPU: the pages' best 4096^3 BF16 figure "
+                           "(TMA multistage, sm_120-class card, other hardware)",
+        "dtype": "bf16", "data": "synthetic", "config": main_config(wl),
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": args.steps * wl.plan.kernels, "clocks": clocks,
+        "frac_of_peak": round(achieved / peaks["bf16_tflops"], 4), "sweep": sweep,
+    }
+    return line
+
+
+def syrk_point(args, dist, peaks):
+    import numpy as np
+    import torch
+    import bm_inputs as gen
+    import blas3_tensor_core_gb300 as bm
+    n, k = SYRK_CFG["n"], SYRK_CFG["k"]
+    A = gen.matrix_bf16(n, k, "normal", seed=1)
+    C0 = gen.symmetric_f32(n, seed=3)
+    dA = torch.from_numpy(A.view(np.int16)).view(torch.bfloat16).cuda()
+    dCs = [torch.from_numpy(C0).cuda() for _ in range(2)]
+    h = torch.cuda.current_stream().cuda_stream
+
+    class W:
+        t = torch
+        bm = None
+
+        def call(self, i, hh):
+            st = bm.bm_syrk_bf16(0, 0, n, k, 1.0, dA.data_ptr(), k, 1.0, dCs[i % 2].data_ptr(), n, 0, hh)
+            if st != 0:
+                raise RuntimeError(bm.bm_status_string(st))
+    w = W()
+    w.bm = bm
+    ms = timed_steps(w, args.sweep_steps // 4 + 1, 3, dist)
+    t_launch = ms / (args.sweep_steps // 4 + 1) * 1e-3
+    fl, by = syrk_flops(n, k), syrk_bytes(n, k, 4, 1.0)
+    return {"workload": SYRK_CFG["name"], "us_per_step": round(t_launch * 1e6, 3),
+            "tflops": round(fl / t_launch / 1e12, 2), "gbs": round(by / t_launch / 1e9, 1),
+            "frac_tensor": round(fl / t_launch / 1e12 / peaks["bf16_tflops"], 4),
+            "frac_hbm": round(by / t_launch / 1e9 / peaks["hbm_gbs"], 4), "bound": "tensor",
+            "flops_convention": "n(n+1)k (lower triangle incl. diagonal)"}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=100)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--sweep-steps", type=int, default=200)
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--all-configs", action="store_true", help="also time the backward pair, 256^3 and SYRK")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    ap.add_argument("--reference-budget-s", type=float, default=120.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.steps < 1:
+        ap.error("--steps must be >= 1")
+    return args
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    dist = Dist()
+    try:
+        if args.impl == "reference":
+            line = reference_arm(args, dist)
+        else:
+            line = run_gpu_arm(args, dist)
+        if dist.rank == 0 and line is not None:
+            print(json.dumps(line), flush=True)
+    finally:
+        dist.close()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -21,7 +21,7 @@ __all__ = [
     "BM_LOWER", "BM_UPPER", "Plan",
     "bm_gemm_bf16", "bm_syrk_bf16", "bm_gemm_bf16_workspace_size", "bm_get_last_device_error",
     "bm_set_wait_timeout_ms", "bm_debug_inject_stall", "bm_status_string", "bm_gemm_bf16_plan",
-    "bm_syrk_bf16_plan", "bm_version", "gemm", "syrk", "workspace_size",
+    "bm_syrk_bf16_plan", "bm_set_tile_override", "bm_version", "gemm", "syrk", "workspace_size",
 ]
 
 BM_OK, BM_ERR_INVALID_VALUE, BM_ERR_MISALIGNED, BM_ERR_ARCH, BM_ERR_CUDA, BM_ERR_TIMEOUT, BM_ERR_WORKSPACE = range(7)
@@ -41,7 +41,8 @@ _i64, _i32, _u32, _f32, _vp, _sz = (ctypes.c_int64, ctypes.c_int, ctypes.c_uint3
 class Plan(ctypes.Structure):
     _fields_ = [("tile_m", ctypes.c_int32), ("tile_n", ctypes.c_int32), ("tile_k", ctypes.c_int32),
                 ("stages", ctypes.c_int32), ("tiles", ctypes.c_int64), ("k_splits", ctypes.c_int32),
-                ("ctas", ctypes.c_int32), ("kernels", ctypes.c_int32), ("workspace_bytes", ctypes.c_size_t)]
+                ("ctas", ctypes.c_int32), ("cta_pair", ctypes.c_int32), ("kernels", ctypes.c_int32),
+                ("workspace_bytes", ctypes.c_size_t)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}
@@ -84,6 +85,8 @@ def library():
                 lib.bm_gemm_bf16_plan.restype = _i32
                 lib.bm_syrk_bf16_plan.argtypes = [_i32, _i64, _i64, ctypes.POINTER(Plan)]
                 lib.bm_syrk_bf16_plan.restype = _i32
+                lib.bm_set_tile_override.argtypes = [_i32]
+                lib.bm_set_tile_override.restype = _i32
                 lib.bm_version.argtypes = []
                 lib.bm_version.restype = _i32
                 _lib = lib
@@ -131,6 +134,13 @@ def bm_syrk_bf16_plan(uplo, n, k):
     plan = Plan()
     st = library().bm_syrk_bf16_plan(uplo, n, k, ctypes.byref(plan))
     return st, plan
+
+
+TILE_AUTO, TILE_SINGLE_128x256, TILE_SINGLE_128x128, TILE_PAIR_256x256 = range(4)
+
+
+def bm_set_tile_override(variant: int) -> int:
+    return library().bm_set_tile_override(variant)
 
 
 def bm_version() -> int:

@@ -23,9 +23,16 @@
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kStagesBN256 = 4;
-constexpr int kStagesBN128 = 6;
 constexpr int kGroupM = 16;
+
+// Kernel variants: output tile (rows x BN), ring depth, CTAs per tile.
+//   kSingle256: 128 x 256 per CTA, 4 stages of 48 KB
+//   kSingle128: 128 x 128 per CTA, 6 stages of 32 KB (narrow outputs)
+//   kPair256:   256 x 256 per CTA pair (cta_group::2), 6 stages of 32 KB per CTA
+enum Variant { kSingle256 = 0, kSingle128 = 1, kPair256 = 2, kNumVariants = 3 };
+constexpr int kVariantBN[kNumVariants] = {256, 128, 256};
+constexpr int kVariantStages[kNumVariants] = {4, 6, 6};
+constexpr int kVariantPair[kNumVariants] = {1, 1, 2};
 
 struct DeviceState {
     bool ready = false;
@@ -33,6 +40,7 @@ struct DeviceState {
     int cc_major = 0, cc_minor = 0;
     int *status = nullptr;  // one int, allocated on first use
     bool attrs_set = false;
+    int max_pair_clusters = 0;  // co-resident clusters of the pair kernel
 };
 
 std::mutex g_mutex;
@@ -40,13 +48,24 @@ DeviceState g_devices[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::atomic<uint32_t> g_timeout_ms{2000};
 std::atomic<int> g_debug_stall{0};
+std::atomic<int> g_tile_override{0};  // 0 = automatic, else 1 + Variant
 
-using Kern = void (*)(CUtensorMap, CUtensorMap, bm::GemmParams);
-
-template <int BN, int STAGES>
-void *kernel_ptr()
+const void *variant_kernel(int v)
 {
-    return reinterpret_cast<void *>(&bm::bm_gemm_tcgen05_kernel<BN, STAGES>);
+    switch (v) {
+    case kSingle256: return reinterpret_cast<const void *>(&bm::bm_gemm_tcgen05_kernel<256, 4, 1>);
+    case kSingle128: return reinterpret_cast<const void *>(&bm::bm_gemm_tcgen05_kernel<128, 6, 1>);
+    default: return reinterpret_cast<const void *>(&bm::bm_gemm_tcgen05_kernel<256, 6, 2>);
+    }
+}
+
+int variant_smem(int v)
+{
+    switch (v) {
+    case kSingle256: return bm::KernelCfg<256, 4, 1>::SMEM_BYTES;
+    case kSingle128: return bm::KernelCfg<128, 6, 1>::SMEM_BYTES;
+    default: return bm::KernelCfg<256, 6, 2>::SMEM_BYTES;
+    }
 }
 
 bool fits_int32(int64_t v) { return v >= 0 && v <= 0x7FFFFFFFLL; }
@@ -84,13 +103,28 @@ bm_status device_state(DeviceState **out)
         if (cudaMemset(st.status, 0, sizeof(int)) != cudaSuccess) return BM_ERR_CUDA;
     }
     if (!st.attrs_set) {
-        const void *kerns[2] = {kernel_ptr<256, kStagesBN256>(), kernel_ptr<128, kStagesBN128>()};
-        const int bytes[2] = {bm::KernelCfg<256, kStagesBN256>::SMEM_BYTES,
-                              bm::KernelCfg<128, kStagesBN128>::SMEM_BYTES};
-        for (int i = 0; i < 2; ++i)
-            if (cudaFuncSetAttribute(kerns[i], cudaFuncAttributeMaxDynamicSharedMemorySize, bytes[i]) !=
-                cudaSuccess)
+        for (int v = 0; v < kNumVariants; ++v)
+            if (cudaFuncSetAttribute(variant_kernel(v), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     variant_smem(v)) != cudaSuccess)
                 return BM_ERR_CUDA;
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(2 * (st.sm_count / 2), 1, 1);
+        cfg.blockDim = dim3(bm::NUM_THREADS, 1, 1);
+        cfg.dynamicSmemBytes = variant_smem(kPair256);
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, variant_kernel(kPair256), &cfg) != cudaSuccess ||
+            clusters <= 0) {
+            cudaGetLastError();
+            clusters = 0;  // pair kernel unavailable: single-CTA tiles only
+        }
+        st.max_pair_clusters = clusters;
         st.attrs_set = true;
     }
     *out = &st;
@@ -132,7 +166,8 @@ bool encode_operand(CUtensorMap *map, const void *base, bool mn_major, int64_t r
 }
 
 struct Plan {
-    int bn = 256, stages = kStagesBN256;
+    int variant = kSingle256;
+    int tile_m = bm::CTA_M, bn = 256, stages = 4, pair = 1;
     int64_t tiles_m = 0, tiles_n = 0, num_tiles = 0;
     int k_splits = 1, kb_per_split = 0, kb_total = 0;
     int ctas = 0;
@@ -142,31 +177,56 @@ struct Plan {
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-int64_t syrk_tile_count(int mode, int64_t tiles_m, int64_t tiles_n)
+void set_variant(Plan &pl, int v)
+{
+    pl.variant = v;
+    pl.bn = kVariantBN[v];
+    pl.stages = kVariantStages[v];
+    pl.pair = kVariantPair[v];
+    pl.tile_m = bm::CTA_M * pl.pair;
+}
+
+int64_t syrk_tile_count(int mode, int64_t tiles_m, int64_t tiles_n, int tile_m, int bn)
 {
     int64_t total = 0;
     for (int64_t tm = 0; tm < tiles_m; ++tm) {
         int64_t lo, hi;
-        bm::syrk_row_tiles<256>(mode, tm, tiles_n, lo, hi);
+        if (tile_m == 256) bm::syrk_row_tiles<256, 256>(mode, tm, tiles_n, lo, hi);
+        else if (bn == 128) bm::syrk_row_tiles<128, 128>(mode, tm, tiles_n, lo, hi);
+        else bm::syrk_row_tiles<128, 256>(mode, tm, tiles_n, lo, hi);
         total += hi - lo + 1;
     }
     return total;
 }
 
-Plan plan_gemm(int64_t m, int64_t n, int64_t k, size_t ws_bytes, int sms)
+// Persistent grid: one CTA (or CTA pair) per SM (pair of SMs), never more than the work units.
+void size_grid(Plan &pl, int sms, int pair_clusters)
+{
+    const int64_t units = pl.num_tiles * pl.k_splits;
+    if (pl.pair == 2) pl.ctas = static_cast<int>(2 * std::min<int64_t>(units, pair_clusters));
+    else pl.ctas = static_cast<int>(std::min<int64_t>(units, sms));
+}
+
+// Pair tiles (256 x 256 on two SMs) whenever they alone can occupy at least half
+// of the SM pairs; otherwise 128-row tiles on single SMs (more, smaller tiles).
+Plan plan_gemm(int64_t m, int64_t n, int64_t k, size_t ws_bytes, int sms, int pair_clusters)
 {
     Plan pl;
-    pl.bn = (n <= 128) ? 128 : 256;
-    pl.stages = pl.bn == 256 ? kStagesBN256 : kStagesBN128;
-    pl.tiles_m = ceil_div(m, bm::TILE_M);
+    const int64_t pair_tiles = ceil_div(m, 256) * ceil_div(n, 256);
+    const int forced = g_tile_override.load() - 1;
+    if (forced >= 0 && (forced != kPair256 || pair_clusters > 0)) set_variant(pl, forced);
+    else if (pair_clusters > 0 && m > bm::CTA_M && n > 128 && pair_tiles * 2 >= pair_clusters) set_variant(pl, kPair256);
+    else set_variant(pl, n <= 128 ? kSingle128 : kSingle256);
+    pl.tiles_m = ceil_div(m, pl.tile_m);
     pl.tiles_n = ceil_div(n, pl.bn);
     pl.num_tiles = pl.tiles_m * pl.tiles_n;
     pl.kb_total = static_cast<int>(ceil_div(std::max<int64_t>(k, 1), bm::TILE_K));
     pl.kb_per_split = pl.kb_total;
     pl.ldp = ceil_div(n, 4) * 4;
     // Split K only when the tiles cannot fill half the GPU and each split keeps >= 4 k-blocks.
-    if (pl.num_tiles * 2 <= sms && pl.kb_total >= 8) {
-        int64_t want = std::min<int64_t>(ceil_div(sms, pl.num_tiles), pl.kb_total / 4);
+    const int64_t slots = pl.pair == 2 ? pair_clusters : sms;
+    if (pl.num_tiles * 2 <= slots && pl.kb_total >= 8) {
+        int64_t want = std::min<int64_t>(ceil_div(slots, pl.num_tiles), pl.kb_total / 4);
         while (want > 1) {
             const int per = static_cast<int>(ceil_div(pl.kb_total, want));
             const int splits = static_cast<int>(ceil_div(pl.kb_total, per));
@@ -180,21 +240,23 @@ Plan plan_gemm(int64_t m, int64_t n, int64_t k, size_t ws_bytes, int sms)
             --want;
         }
     }
-    pl.ctas = static_cast<int>(std::min<int64_t>(pl.num_tiles * pl.k_splits, sms));
+    size_grid(pl, sms, pair_clusters);
     return pl;
 }
 
-Plan plan_syrk(int mode, int64_t n, int64_t k, int sms)
+Plan plan_syrk(int mode, int64_t n, int64_t k, int sms, int pair_clusters)
 {
     Plan pl;
-    pl.bn = 256;
-    pl.stages = kStagesBN256;
-    pl.tiles_m = ceil_div(n, bm::TILE_M);
-    pl.tiles_n = ceil_div(n, 256);
-    pl.num_tiles = syrk_tile_count(mode, pl.tiles_m, pl.tiles_n);
+    const int64_t tiles = ceil_div(n, 256);
+    const int forced = g_tile_override.load() - 1;
+    if (forced >= 0 && (forced != kPair256 || pair_clusters > 0)) set_variant(pl, forced);
+    else set_variant(pl, (pair_clusters > 0 && tiles * (tiles + 1) / 2 * 2 >= pair_clusters) ? kPair256 : kSingle256);
+    pl.tiles_m = ceil_div(n, pl.tile_m);
+    pl.tiles_n = ceil_div(n, pl.bn);
+    pl.num_tiles = syrk_tile_count(mode, pl.tiles_m, pl.tiles_n, pl.tile_m, pl.bn);
     pl.kb_total = static_cast<int>(ceil_div(std::max<int64_t>(k, 1), bm::TILE_K));
     pl.kb_per_split = pl.kb_total;
-    pl.ctas = static_cast<int>(std::min<int64_t>(pl.num_tiles, sms));
+    size_grid(pl, sms, pair_clusters);
     return pl;
 }
 
@@ -203,14 +265,31 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bm_status launch(const Plan &pl, const CUtensorMap &ta, const CUtensorMap &tb, bm::GemmParams &prm,
                  cudaStream_t stream)
 {
-    if (pl.bn == 256) {
-        bm::bm_gemm_tcgen05_kernel<256, kStagesBN256>
-            <<<pl.ctas, bm::NUM_THREADS, bm::KernelCfg<256, kStagesBN256>::SMEM_BYTES, stream>>>(ta, tb, prm);
-    } else {
-        bm::bm_gemm_tcgen05_kernel<128, kStagesBN128>
-            <<<pl.ctas, bm::NUM_THREADS, bm::KernelCfg<128, kStagesBN128>::SMEM_BYTES, stream>>>(ta, tb, prm);
+    if (pl.ctas <= 0) return BM_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3(static_cast<unsigned>(pl.ctas), 1, 1);
+    cfg.blockDim = dim3(bm::NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(variant_smem(pl.variant));
+    cfg.stream = stream;
+    if (pl.pair == 2) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
     }
-    if (cudaGetLastError() != cudaSuccess) return BM_ERR_CUDA;
+    cudaError_t err;
+    switch (pl.variant) {
+    case kSingle256: err = cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<256, 4, 1>, ta, tb, prm); break;
+    case kSingle128: err = cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<128, 6, 1>, ta, tb, prm); break;
+    default: err = cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<256, 6, 2>, ta, tb, prm); break;
+    }
+    if (err != cudaSuccess) {
+        cudaGetLastError();
+        return BM_ERR_CUDA;
+    }
     if (prm.k_splits > 1) {
         const int64_t work = prm.m * ceil_div(prm.n, 4);
         const int blocks = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(ceil_div(work, 256), 8 * 152)));
@@ -226,6 +305,43 @@ bm_status launch_scale(bm::GemmParams &prm, cudaStream_t stream)
     const int blocks = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(ceil_div(work, 256), 8 * 152)));
     bm::bm_scale_kernel<<<blocks, 256, 0, stream>>>(prm);
     return cudaGetLastError() == cudaSuccess ? BM_OK : BM_ERR_CUDA;
+}
+
+void fill_params(bm::GemmParams &prm, const Plan &pl)
+{
+    prm.tiles_m = pl.tiles_m;
+    prm.tiles_n = pl.tiles_n;
+    prm.num_tiles = pl.num_tiles;
+    prm.k_splits = pl.k_splits;
+    prm.kb_per_split = pl.kb_per_split;
+    prm.kb_total = pl.kb_total;
+    prm.ldp = pl.ldp;
+}
+
+void export_plan(const Plan &pl, bm_plan *plan)
+{
+    plan->tile_m = pl.tile_m;
+    plan->tile_n = pl.bn;
+    plan->tile_k = bm::TILE_K;
+    plan->stages = pl.stages;
+    plan->tiles = pl.num_tiles;
+    plan->k_splits = pl.k_splits;
+    plan->ctas = pl.ctas;
+    plan->cta_pair = pl.pair;
+    plan->kernels = pl.k_splits > 1 ? 2 : 1;
+    plan->workspace_bytes = pl.k_splits > 1 ? pl.ws_bytes : 0;
+}
+
+// Pair-cluster capacity for planning without a device (host-only planning): one per SM pair.
+int pair_clusters_or_default(int sms)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kMaxDevices) {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        if (g_devices[dev].attrs_set) return g_devices[dev].max_pair_clusters;
+    }
+    cudaGetLastError();
+    return sms / 2;
 }
 
 bm::GemmParams base_params(int64_t m, int64_t n, int64_t k, float alpha, float beta, void *C, int64_t ldc,
@@ -291,28 +407,25 @@ bm_status bm_gemm_bf16(int64_t m, int64_t n, int64_t k, bm_op transA, bm_op tran
     prm.mode = bm::MODE_GEMM;
     if (!products) return launch_scale(prm, cs);
 
-    const Plan pl = plan_gemm(m, n, k, workspace != nullptr ? workspace_bytes : 0, st->sm_count);
+    const Plan pl = plan_gemm(m, n, k, workspace != nullptr ? workspace_bytes : 0, st->sm_count,
+                              st->max_pair_clusters);
     CUtensorMap ta, tb;
     const bool a_mn = transA == BM_OP_T, b_mn = transB == BM_OP_N;
-    if (!encode_operand(&ta, A, a_mn, m, k, lda, bm::TILE_M)) return BM_ERR_CUDA;
-    if (!encode_operand(&tb, B, b_mn, n, k, ldb, static_cast<uint32_t>(pl.bn))) return BM_ERR_CUDA;
+    // each CTA stages 128 rows of op(A) and bn / pair rows of op(B)^T
+    if (!encode_operand(&ta, A, a_mn, m, k, lda, bm::CTA_M)) return BM_ERR_CUDA;
+    if (!encode_operand(&tb, B, b_mn, n, k, ldb, static_cast<uint32_t>(pl.bn / pl.pair))) return BM_ERR_CUDA;
     prm.a_mn_major = a_mn;
     prm.b_mn_major = b_mn;
-    prm.tiles_m = pl.tiles_m;
-    prm.tiles_n = pl.tiles_n;
-    prm.num_tiles = pl.num_tiles;
-    prm.k_splits = pl.k_splits;
-    prm.kb_per_split = pl.kb_per_split;
-    prm.kb_total = pl.kb_total;
+    fill_params(prm, pl);
     prm.partial = pl.k_splits > 1 ? static_cast<float *>(workspace) : nullptr;
-    prm.ldp = pl.ldp;
     return launch(pl, ta, tb, prm, cs);
 }
 
 size_t bm_gemm_bf16_workspace_size(int64_t m, int64_t n, int64_t k)
 {
     if (m <= 0 || n <= 0 || k <= 0) return 0;
-    const Plan pl = plan_gemm(m, n, k, SIZE_MAX, sm_count_or_default());
+    const int sms = sm_count_or_default();
+    const Plan pl = plan_gemm(m, n, k, SIZE_MAX, sms, pair_clusters_or_default(sms));
     return pl.k_splits > 1 ? pl.ws_bytes : 0;
 }
 
@@ -339,18 +452,14 @@ bm_status bm_syrk_bf16(bm_uplo uplo, bm_op trans, int64_t n, int64_t k, float al
     prm.mode = uplo == BM_LOWER ? bm::MODE_SYRK_LOWER : bm::MODE_SYRK_UPPER;
     if (!products) return launch_scale(prm, cs);
 
-    const Plan pl = plan_syrk(prm.mode, n, k, st->sm_count);
+    const Plan pl = plan_syrk(prm.mode, n, k, st->sm_count, st->max_pair_clusters);
     CUtensorMap ta, tb;
     const bool mn = trans == BM_OP_T;  // A stored [k][n]: both operands are M/N-major
-    if (!encode_operand(&ta, A, mn, n, k, lda, bm::TILE_M)) return BM_ERR_CUDA;
-    if (!encode_operand(&tb, A, mn, n, k, lda, static_cast<uint32_t>(pl.bn))) return BM_ERR_CUDA;
+    if (!encode_operand(&ta, A, mn, n, k, lda, bm::CTA_M)) return BM_ERR_CUDA;
+    if (!encode_operand(&tb, A, mn, n, k, lda, static_cast<uint32_t>(pl.bn / pl.pair))) return BM_ERR_CUDA;
     prm.a_mn_major = mn;
     prm.b_mn_major = mn;
-    prm.tiles_m = pl.tiles_m;
-    prm.tiles_n = pl.tiles_n;
-    prm.num_tiles = pl.num_tiles;
-    prm.kb_per_split = pl.kb_per_split;
-    prm.kb_total = pl.kb_total;
+    fill_params(prm, pl);
     return launch(pl, ta, tb, prm, cs);
 }
 
@@ -364,16 +473,8 @@ bm_status bm_gemm_bf16_plan(int64_t m, int64_t n, int64_t k, size_t workspace_by
         plan->kernels = 1;
         return BM_OK;
     }
-    const Plan pl = plan_gemm(m, n, k, workspace_bytes, sm_count_or_default());
-    plan->tile_m = bm::TILE_M;
-    plan->tile_n = pl.bn;
-    plan->tile_k = bm::TILE_K;
-    plan->stages = pl.stages;
-    plan->tiles = pl.num_tiles;
-    plan->k_splits = pl.k_splits;
-    plan->ctas = pl.ctas;
-    plan->kernels = pl.k_splits > 1 ? 2 : 1;
-    plan->workspace_bytes = pl.k_splits > 1 ? pl.ws_bytes : 0;
+    const int sms = sm_count_or_default();
+    export_plan(plan_gemm(m, n, k, workspace_bytes, sms, pair_clusters_or_default(sms)), plan);
     return BM_OK;
 }
 
@@ -387,16 +488,10 @@ bm_status bm_syrk_bf16_plan(bm_uplo uplo, int64_t n, int64_t k, bm_plan *plan)
         plan->kernels = 1;
         return BM_OK;
     }
-    const Plan pl = plan_syrk(uplo == BM_LOWER ? bm::MODE_SYRK_LOWER : bm::MODE_SYRK_UPPER, n, k,
-                              sm_count_or_default());
-    plan->tile_m = bm::TILE_M;
-    plan->tile_n = pl.bn;
-    plan->tile_k = bm::TILE_K;
-    plan->stages = pl.stages;
-    plan->tiles = pl.num_tiles;
-    plan->k_splits = 1;
-    plan->ctas = pl.ctas;
-    plan->kernels = 1;
+    const int sms = sm_count_or_default();
+    export_plan(plan_syrk(uplo == BM_LOWER ? bm::MODE_SYRK_LOWER : bm::MODE_SYRK_UPPER, n, k, sms,
+                          pair_clusters_or_default(sms)),
+                plan);
     return BM_OK;
 }
 
@@ -415,6 +510,13 @@ bm_status bm_get_last_device_error(bm_stream_t stream)
 void bm_set_wait_timeout_ms(uint32_t ms) { g_timeout_ms.store(ms == 0 ? 1 : ms); }
 
 void bm_debug_inject_stall(int enable) { g_debug_stall.store(enable ? 1 : 0); }
+
+bm_status bm_set_tile_override(int variant)
+{
+    if (variant < 0 || variant > kNumVariants) return BM_ERR_INVALID_VALUE;
+    g_tile_override.store(variant);
+    return BM_OK;
+}
 
 const char *bm_status_string(bm_status status)
 {

@@ -1,5 +1,5 @@
 // bm_gemm_kernel.cuh -- persistent, warp-specialised BF16 GEMM / SYRK kernel for
-// sm_103a (one CTA per SM).
+// sm_103a (one CTA per SM; optionally a CTA pair per output tile).
 //
 //   C = alpha * op(A) * op(B) + beta * C      (GEMM)
 //   C = alpha * op(A) * op(A)^T + beta * C    (SYRK, one triangle)
@@ -13,27 +13,36 @@
 // empty-stage acquire, TMA submission, MMA input-stage wait, reusable TMEM
 // slot, MMA issue and stage release, epilogue).
 //
-// Roles (192 threads):
+// PAIR = 1: each CTA owns a 128 x BN output tile.
+// PAIR = 2: a cluster of two CTAs on two SMs owns a 256 x BN tile. Each CTA
+//   stages its own 128 rows of A and its own BN/2 rows of B; one
+//   tcgen05.mma.cta_group::2 issued by CTA 0 reads both CTAs' shared memory and
+//   writes 128 accumulator rows into each CTA's tensor memory. Per SM this
+//   halves the B operand bytes that the tensor core reads from shared memory
+//   per MMA (8 KB instead of 12 KB for a K = 16 step).
+//
+// Roles (192 threads per CTA):
 //   warp 0, one lane  TMA producer: fills a STAGES-deep ring of shared-memory
-//                     stages (A tile 128 x 64, B tile BN x 64, bf16) guarded by
-//                     full/empty mbarriers.
-//   warp 1, one lane  MMA issuer: 4 x tcgen05.mma (K = 16 each) per stage into
-//                     one of two TMEM accumulators (128 lanes x BN fp32
-//                     columns); tcgen05.commit releases the stage, and at the
-//                     end of a tile signals the accumulator full. Warp 1 also
-//                     allocates and frees the tensor memory.
+//                     stages guarded by full/empty mbarriers (PAIR = 2: both
+//                     CTAs' copies complete bytes on CTA 0's full barrier).
+//   warp 1, one lane  MMA issuer (CTA 0 only): 4 x tcgen05.mma (K = 16 each)
+//                     per stage into one of two TMEM accumulators (128 lanes
+//                     x BN fp32 columns per CTA); tcgen05.commit releases the
+//                     stage (in both CTAs) and, at the end of a tile, signals
+//                     the accumulator full. Warp 1 allocates and frees TMEM.
 //   warps 2-5         epilogue: TMEM -> registers (tcgen05.ld 32x32b), alpha,
 //                     transpose through shared memory, then coalesced 16-byte
 //                     loads of C (beta != 0) and stores of C; the SYRK
 //                     triangle and the ragged edges are masked per element.
-// Tiles are handed out persistently (CTA b takes units b, b + grid, ...), in
-// grouped-raster order for GEMM and row by row over the referenced triangle for
-// SYRK (tiles strictly on the other side of the diagonal are never visited).
+// Tiles are handed out persistently (cluster c takes units c, c + clusters,
+// ...), in grouped-raster order for GEMM and row by row over the referenced
+// triangle for SYRK (tiles strictly on the other side of the diagonal are never
+// visited).
 //
 // Every barrier wait is bounded: after the wait limit the thread records
-// BM_ERR_TIMEOUT in the device status word, raises a shared abort flag that
-// the other roles poll, waits (bounded) for its own copies / MMAs in flight,
-// and the CTA frees its tensor memory and exits.
+// BM_ERR_TIMEOUT in the device status word and raises a shared abort flag that
+// the other roles of its CTA poll; copies and MMAs in flight are waited for
+// (again with a limit) and the CTA frees its tensor memory and exits.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -46,7 +55,7 @@ namespace bm {
 enum : int { MODE_GEMM = 0, MODE_SYRK_LOWER = 1, MODE_SYRK_UPPER = 2 };
 enum : int { DEV_ERR_TIMEOUT = 5 };
 
-constexpr int TILE_M = 128;
+constexpr int CTA_M = 128;  // accumulator rows (TMEM lanes) per CTA
 constexpr int TILE_K = 64;  // bf16 elements = 128 bytes = one swizzle row
 constexpr int UMMA_K = 16;
 constexpr int NUM_EPI_WARPS = 4;
@@ -75,11 +84,14 @@ struct GemmParams {
     int debug_stall;   // test hook: the first stage's copy is never issued
 };
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int PAIR>
 struct KernelCfg {
-    static constexpr int A_BYTES = TILE_M * TILE_K * 2;
-    static constexpr int B_BYTES = BN * TILE_K * 2;
+    static constexpr int TILE_M = CTA_M * PAIR;  // output rows per tile
+    static constexpr int B_ROWS = BN / PAIR;     // rows of op(B)^T staged by each CTA
+    static constexpr int A_BYTES = CTA_M * TILE_K * 2;
+    static constexpr int B_BYTES = B_ROWS * TILE_K * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int TX_BYTES = STAGE_BYTES * PAIR;  // bytes that complete one full barrier
     static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
     static constexpr int EPI_BYTES = NUM_EPI_WARPS * EPI_WARP_FLOATS * 4;
     static constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, acc full x2, acc empty x2, drain
@@ -87,6 +99,8 @@ struct KernelCfg {
     static constexpr int SMEM_BYTES = 1024 + RING_BYTES + EPI_BYTES + BAR_BYTES;
     static constexpr int TMEM_COLS = 2 * BN;  // two accumulators
     static_assert(BN == 128 || BN == 256, "BN");
+    static_assert(PAIR == 1 || PAIR == 2, "PAIR");
+    static_assert(B_ROWS % 64 == 0, "B rows per CTA");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 };
 
@@ -96,22 +110,22 @@ struct Unit {
     int split;
 };
 
-// Range of tile columns [lo, hi] of tile row tm that touch the SYRK triangle.
-template <int BN>
-__host__ __device__ inline void syrk_row_tiles(int mode, int64_t tm, int64_t tiles_n, int64_t &lo,
-                                               int64_t &hi)
+// Range of tile columns [lo, hi] of tile row tm (tiles TM x BN) that touch the
+// SYRK triangle.
+template <int TM, int BN>
+__host__ __device__ inline void syrk_row_tiles(int mode, int64_t tm, int64_t tiles_n, int64_t &lo, int64_t &hi)
 {
     if (mode == MODE_SYRK_LOWER) {  // some row >= some column
         lo = 0;
-        const int64_t last = (TILE_M * tm + TILE_M - 1) / BN;
+        const int64_t last = (TM * tm + TM - 1) / BN;
         hi = last < tiles_n - 1 ? last : tiles_n - 1;
     } else {  // some row <= some column
-        lo = (TILE_M * tm) / BN;
+        lo = (TM * tm) / BN;
         hi = tiles_n - 1;
     }
 }
 
-template <int BN>
+template <int TM, int BN>
 __device__ __forceinline__ Unit map_unit(const GemmParams &p, int64_t u)
 {
     Unit r;
@@ -131,7 +145,7 @@ __device__ __forceinline__ Unit map_unit(const GemmParams &p, int64_t u)
         int64_t rem = t;
         for (int64_t tm = 0; tm < p.tiles_m; ++tm) {
             int64_t lo, hi;
-            syrk_row_tiles<BN>(p.mode, tm, p.tiles_n, lo, hi);
+            syrk_row_tiles<TM, BN>(p.mode, tm, p.tiles_n, lo, hi);
             const int64_t cnt = hi - lo + 1;
             if (rem < cnt) {
                 r.tm = tm;
@@ -144,6 +158,20 @@ __device__ __forceinline__ Unit map_unit(const GemmParams &p, int64_t u)
     return r;
 }
 
+template <int PAIR>
+__device__ __forceinline__ int64_t first_unit()
+{
+    if constexpr (PAIR == 1) return blockIdx.x;
+    else return cluster_index();
+}
+
+template <int PAIR>
+__device__ __forceinline__ int64_t unit_stride()
+{
+    if constexpr (PAIR == 1) return gridDim.x;
+    else return cluster_count();
+}
+
 // ---------------------------------------------------------------- bounded waits
 __device__ __noinline__ void signal_timeout(const GemmParams &p, volatile int *abort_flag)
 {
@@ -151,16 +179,23 @@ __device__ __noinline__ void signal_timeout(const GemmParams &p, volatile int *a
     if (p.status != nullptr) atomicCAS(p.status, 0, DEV_ERR_TIMEOUT);
 }
 
-// Single-thread wait: false when the limit passes or another role aborted.
-__device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                         uint64_t limit_ns)
+template <bool CLUSTER>
+__device__ __forceinline__ bool try_wait(uint32_t bar, uint32_t parity)
 {
-    if (mbar_try_wait(bar, parity)) return true;
+    if constexpr (CLUSTER) return mbar_try_wait_cluster(bar, parity);
+    else return mbar_try_wait(bar, parity);
+}
+
+// Single-thread wait: false when the limit passes or another role aborted.
+template <bool CLUSTER = false>
+__device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity, volatile int *abort_flag, uint64_t limit_ns)
+{
+    if (try_wait<CLUSTER>(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (;;) {
 #pragma unroll 1
         for (int i = 0; i < 16; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+            if (try_wait<CLUSTER>(bar, parity)) return true;
         if (abort_flag != nullptr && *abort_flag) return false;
         if (global_timer_ns() - t0 > limit_ns) return false;
     }
@@ -168,18 +203,25 @@ __device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity, volatile
 
 // Warp-uniform wait: every lane observes the phase (acquire) before any lane
 // proceeds, and all lanes take the same exit.
-__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                          uint64_t limit_ns)
+template <bool CLUSTER = false>
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int *abort_flag, uint64_t limit_ns)
 {
     uint64_t t0 = 0;
     for (int it = 0;; ++it) {
-        const bool ok = mbar_try_wait(bar, parity);
+        const bool ok = try_wait<CLUSTER>(bar, parity);
         if (__all_sync(0xffffffffu, ok)) return true;
         if (it == 0) t0 = global_timer_ns();
         if ((it & 15) == 15) {
             const bool stop = *abort_flag != 0 || (global_timer_ns() - t0 > limit_ns);
             if (__any_sync(0xffffffffu, stop)) return false;
         }
+    }
+}
+
+__device__ __forceinline__ void spin_ns(uint64_t ns)
+{
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < ns) {
     }
 }
 
@@ -252,48 +294,68 @@ __device__ __forceinline__ void write_c4(const GemmParams &p, int64_t i, int64_t
 }
 
 // ---------------------------------------------------------------- roles
-template <int BN, int STAGES>
-__device__ __forceinline__ void run_producer(const CUtensorMap *tmA, const CUtensorMap *tmB,
-                                             const GemmParams &p, uint32_t ring, uint32_t bar0,
-                                             volatile int *abort_flag)
+template <int BN, int STAGES, int PAIR>
+__device__ __forceinline__ void run_producer(const CUtensorMap *tmA, const CUtensorMap *tmB, const GemmParams &p,
+                                             uint32_t ring, uint32_t bar0, uint32_t rank, volatile int *abort_flag)
 {
-    using Cfg = KernelCfg<BN, STAGES>;
+    using Cfg = KernelCfg<BN, STAGES, PAIR>;
     const int64_t units = p.num_tiles * p.k_splits;
     int stage = 0;
     uint32_t phase = 0;
-    uint32_t issued = 0, issued_parity = 0;  // per stage: filled at least once / parity of last fill
-    bool ok = true, first = true;
-    for (int64_t u = blockIdx.x; u < units && ok; u += gridDim.x) {
-        const Unit w = map_unit<BN>(p, u);
+    uint32_t armed = 0, armed_parity = 0;  // per stage: armed at least once / parity of last arming
+    bool ok = true, first = true, issued_any = false;
+    for (int64_t u = first_unit<PAIR>(); u < units && ok; u += unit_stride<PAIR>()) {
+        const Unit w = map_unit<Cfg::TILE_M, BN>(p, u);
         const int kb0 = w.split * p.kb_per_split;
         const int kb1 = min(p.kb_total, kb0 + p.kb_per_split);
-        const int32_t row_a = static_cast<int32_t>(w.tm * TILE_M);
-        const int32_t row_b = static_cast<int32_t>(w.tn * BN);
+        const int32_t row_a = static_cast<int32_t>(w.tm * Cfg::TILE_M + rank * CTA_M);
+        const int32_t row_b = static_cast<int32_t>(w.tn * BN + rank * Cfg::B_ROWS);
         for (int kb = kb0; kb < kb1; ++kb) {
             const uint32_t empty = bar0 + 8u * (STAGES + stage);
-            if (!wait_one(empty, phase ^ 1u, abort_flag, p.timeout_ns)) {
+            if (!wait_one<PAIR == 2>(empty, phase ^ 1u, abort_flag, p.timeout_ns)) {
                 ok = false;
                 break;
             }
             const uint32_t full = bar0 + 8u * stage;
-            mbar_arrive_expect_tx(full, Cfg::STAGE_BYTES);
-            issued |= 1u << stage;
-            issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+            if (rank == 0) {
+                mbar_arrive_expect_tx(full, Cfg::TX_BYTES);
+                armed |= 1u << stage;
+                armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+            }
             const uint32_t sa = ring + stage * Cfg::STAGE_BYTES;
             const uint32_t sb = sa + Cfg::A_BYTES;
             const int32_t kx = kb * TILE_K;
             if (!(p.debug_stall && first)) {
-                if (p.a_mn_major) {  // A stored [k][m]: two 64-wide chunks along M
-                    tma_load_2d(sa, tmA, full, row_a, kx);
-                    tma_load_2d(sa + 8192, tmA, full, row_a + 64, kx);
-                } else {             // A stored [m][k]: one 64 x 128 box
-                    tma_load_2d(sa, tmA, full, kx, row_a);
-                }
-                if (p.b_mn_major) {  // B stored [k][n]: BN/64 chunks along N
+                issued_any = true;
+                if constexpr (PAIR == 1) {
+                    if (p.a_mn_major) {  // A stored [k][m]: two 64-wide chunks along M
+                        tma_load_2d(sa, tmA, full, row_a, kx);
+                        tma_load_2d(sa + 8192, tmA, full, row_a + 64, kx);
+                    } else {  // A stored [m][k]: one 64 x 128 box
+                        tma_load_2d(sa, tmA, full, kx, row_a);
+                    }
+                    if (p.b_mn_major) {  // B stored [k][n]: chunks of 64 along N
 #pragma unroll
-                    for (int c = 0; c < BN / 64; ++c) tma_load_2d(sb + 8192 * c, tmB, full, row_b + 64 * c, kx);
-                } else {             // B stored [n][k]: one 64 x BN box
-                    tma_load_2d(sb, tmB, full, kx, row_b);
+                        for (int c = 0; c < Cfg::B_ROWS / 64; ++c)
+                            tma_load_2d(sb + 8192 * c, tmB, full, row_b + 64 * c, kx);
+                    } else {  // B stored [n][k]: one 64 x B_ROWS box
+                        tma_load_2d(sb, tmB, full, kx, row_b);
+                    }
+                } else {
+                    const uint32_t full0 = map_shared_to_rank(full, 0);  // CTA 0 counts both CTAs' bytes
+                    if (p.a_mn_major) {
+                        tma_load_2d_pair(sa, tmA, full0, row_a, kx);
+                        tma_load_2d_pair(sa + 8192, tmA, full0, row_a + 64, kx);
+                    } else {
+                        tma_load_2d_pair(sa, tmA, full0, kx, row_a);
+                    }
+                    if (p.b_mn_major) {
+#pragma unroll
+                        for (int c = 0; c < Cfg::B_ROWS / 64; ++c)
+                            tma_load_2d_pair(sb + 8192 * c, tmB, full0, row_b + 64 * c, kx);
+                    } else {
+                        tma_load_2d_pair(sb, tmB, full0, kx, row_b);
+                    }
                 }
             }
             first = false;
@@ -307,26 +369,27 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmA, const CUten
         signal_timeout(p, abort_flag);
         // Let every copy this thread started land before shared memory is released.
         for (int s = 0; s < STAGES; ++s)
-            if ((issued >> s) & 1u) wait_one(bar0 + 8u * s, (issued_parity >> s) & 1u, nullptr, p.timeout_ns);
+            if ((armed >> s) & 1u) wait_one(bar0 + 8u * s, (armed_parity >> s) & 1u, nullptr, p.timeout_ns);
+        if (PAIR == 2 && issued_any) spin_ns(100000);  // copies counted on the other CTA's barrier
     }
 }
 
-template <int BN, int STAGES>
-__device__ __forceinline__ void run_mma(const GemmParams &p, uint32_t ring, uint32_t bar0,
-                                        uint32_t tmem_base, volatile int *abort_flag)
+template <int BN, int STAGES, int PAIR>
+__device__ __forceinline__ void run_mma(const GemmParams &p, uint32_t ring, uint32_t bar0, uint32_t tmem_base,
+                                        volatile int *abort_flag)
 {
-    using Cfg = KernelCfg<BN, STAGES>;
+    using Cfg = KernelCfg<BN, STAGES, PAIR>;
     const int64_t units = p.num_tiles * p.k_splits;
-    const uint32_t idesc = idesc_bf16_f32(TILE_M, BN, p.a_mn_major, p.b_mn_major);
+    const uint32_t idesc = idesc_bf16_f32(Cfg::TILE_M, BN, p.a_mn_major, p.b_mn_major);
     int stage = 0, acc = 0;
     uint32_t phase = 0, acc_phase = 0;
     bool ok = true, issued_any = false;
-    for (int64_t u = blockIdx.x; u < units && ok; u += gridDim.x) {
-        const Unit w = map_unit<BN>(p, u);
+    for (int64_t u = first_unit<PAIR>(); u < units && ok; u += unit_stride<PAIR>()) {
+        const Unit w = map_unit<Cfg::TILE_M, BN>(p, u);
         const int kb0 = w.split * p.kb_per_split;
         const int kb1 = min(p.kb_total, kb0 + p.kb_per_split);
         const uint32_t acc_empty = bar0 + 8u * (2 * STAGES + 2 + acc);
-        if (!wait_one(acc_empty, acc_phase ^ 1u, abort_flag, p.timeout_ns)) {
+        if (!wait_one<PAIR == 2>(acc_empty, acc_phase ^ 1u, abort_flag, p.timeout_ns)) {
             ok = false;
             break;
         }
@@ -348,17 +411,23 @@ __device__ __forceinline__ void run_mma(const GemmParams &p, uint32_t ring, uint
                                                  : smem_desc_sw128(sa + 32u * kk, 16u, 1024u);
                 const uint64_t bd = p.b_mn_major ? smem_desc_sw128(sb + 2048u * kk, 8192u, 1024u)
                                                  : smem_desc_sw128(sb + 32u * kk, 16u, 1024u);
-                umma_bf16(d_tmem, ad, bd, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+                const uint32_t accumulate = (kb > kb0 || kk > 0) ? 1u : 0u;
+                if constexpr (PAIR == 1) umma_bf16(d_tmem, ad, bd, idesc, accumulate);
+                else umma_bf16_pair(d_tmem, ad, bd, idesc, accumulate);
             }
             issued_any = true;
-            umma_commit(bar0 + 8u * (STAGES + stage));  // stage free once these MMAs finish
+            // the stage is free (in both CTAs) once these MMAs finish
+            if constexpr (PAIR == 1) umma_commit(bar0 + 8u * (STAGES + stage));
+            else umma_commit_pair(bar0 + 8u * (STAGES + stage), 0x3);
             if (++stage == STAGES) {
                 stage = 0;
                 phase ^= 1u;
             }
         }
         if (!ok) break;
-        umma_commit(bar0 + 8u * (2 * STAGES + acc));  // accumulator ready for the epilogue
+        // accumulator ready for the epilogue (of both CTAs)
+        if constexpr (PAIR == 1) umma_commit(bar0 + 8u * (2 * STAGES + acc));
+        else umma_commit_pair(bar0 + 8u * (2 * STAGES + acc), 0x3);
         if (++acc == 2) {
             acc = 0;
             acc_phase ^= 1u;
@@ -368,29 +437,30 @@ __device__ __forceinline__ void run_mma(const GemmParams &p, uint32_t ring, uint
         signal_timeout(p, abort_flag);
         if (issued_any) {  // drain: MMAs in flight must finish before TMEM is freed
             const uint32_t drain = bar0 + 8u * (2 * STAGES + 4);
-            umma_commit(drain);
+            if constexpr (PAIR == 1) umma_commit(drain);
+            else umma_commit_pair(drain, 0x1);
             wait_one(drain, 0u, nullptr, p.timeout_ns);
         }
     }
 }
 
-template <int BN, int STAGES>
-__device__ __forceinline__ void run_epilogue(const GemmParams &p, uint32_t bar0, uint32_t tmem_base,
-                                             float *stage_buf, volatile int *abort_flag, int warp,
-                                             int lane)
+template <int BN, int STAGES, int PAIR>
+__device__ __forceinline__ void run_epilogue(const GemmParams &p, uint32_t bar0, uint32_t tmem_base, float *stage_buf,
+                                             uint32_t rank, volatile int *abort_flag, int warp, int lane)
 {
+    using Cfg = KernelCfg<BN, STAGES, PAIR>;
     const int64_t units = p.num_tiles * p.k_splits;
     const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31 are this warp's rows
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
-        const Unit w = map_unit<BN>(p, u);
-        if (!wait_warp(bar0 + 8u * (2 * STAGES + acc), acc_phase, abort_flag, p.timeout_ns)) {
+    for (int64_t u = first_unit<PAIR>(); u < units; u += unit_stride<PAIR>()) {
+        const Unit w = map_unit<Cfg::TILE_M, BN>(p, u);
+        if (!wait_warp<PAIR == 2>(bar0 + 8u * (2 * STAGES + acc), acc_phase, abort_flag, p.timeout_ns)) {
             if (lane == 0) signal_timeout(p, abort_flag);
             break;
         }
         tc_fence_after_sync();
-        const int64_t row0 = w.tm * TILE_M + quad * 32;
+        const int64_t row0 = w.tm * Cfg::TILE_M + rank * CTA_M + quad * 32;
         const int64_t col0 = w.tn * BN;
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN);
 #pragma unroll 1
@@ -400,7 +470,11 @@ __device__ __forceinline__ void run_epilogue(const GemmParams &p, uint32_t bar0,
             if (ch == BN / 32 - 1) {  // accumulator fully read: hand it back to the MMA warp
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar0 + 8u * (2 * STAGES + 2 + acc));
+                if (lane == 0) {
+                    const uint32_t acc_empty = bar0 + 8u * (2 * STAGES + 2 + acc);
+                    if constexpr (PAIR == 1) mbar_arrive(acc_empty);
+                    else mbar_arrive_remote(map_shared_to_rank(acc_empty, 0));
+                }
             }
             // Row `lane` of this 32 x 32 block into shared memory; 16-byte chunk c of
             // row r goes to slot c ^ (r & 7) so that both passes are conflict-free.
@@ -438,17 +512,17 @@ __device__ __forceinline__ void run_epilogue(const GemmParams &p, uint32_t bar0,
 }
 
 // ---------------------------------------------------------------- kernels
-template <int BN, int STAGES>
+template <int BN, int STAGES, int PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     bm_gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                            const GemmParams p)
 {
-    using Cfg = KernelCfg<BN, STAGES>;
+    using Cfg = KernelCfg<BN, STAGES, PAIR>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
     uint8_t *smem = smem_raw + pad;
-    const uint32_t ring = raw + pad;
+    const uint32_t ring = raw + pad;  // identical offset in both CTAs of a pair
     float *epi = reinterpret_cast<float *>(smem + Cfg::RING_BYTES);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::RING_BYTES + Cfg::EPI_BYTES);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Cfg::NUM_BARS);
@@ -456,15 +530,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t bar0 = smem_addr(bars);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = PAIR == 2 ? cluster_cta_rank() : 0u;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(bar0 + 8u * s, 1);             // full: the producer's expect_tx arrival
+            mbar_init(bar0 + 8u * s, 1);             // full: CTA 0's expect_tx arrival (+ bytes)
             mbar_init(bar0 + 8u * (STAGES + s), 1);  // empty: one tcgen05.commit
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(bar0 + 8u * (2 * STAGES + b), 1);                  // accumulator full
-            mbar_init(bar0 + 8u * (2 * STAGES + 2 + b), NUM_EPI_WARPS);  // accumulator empty
+            mbar_init(bar0 + 8u * (2 * STAGES + b), 1);                         // accumulator full
+            mbar_init(bar0 + 8u * (2 * STAGES + 2 + b), NUM_EPI_WARPS * PAIR);  // accumulator empty
         }
         mbar_init(bar0 + 8u * (2 * STAGES + 4), 1);  // drain (abort path only)
         *abort_flag = 0;
@@ -475,28 +550,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tma_prefetch_map(&tmB);
     }
     if (warp == 1) {
-        tmem_alloc(smem_addr(tmem_slot), Cfg::TMEM_COLS);
-        tmem_relinquish();
+        if constexpr (PAIR == 1) {
+            tmem_alloc(smem_addr(tmem_slot), Cfg::TMEM_COLS);
+            tmem_relinquish();
+        } else {
+            tmem_alloc_pair(smem_addr(tmem_slot), Cfg::TMEM_COLS);
+            tmem_relinquish_pair();
+        }
     }
     tc_fence_before_sync();
     __syncthreads();
+    if constexpr (PAIR == 2) cluster_sync();  // peer barriers initialised before any remote arrival
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
 
     if (warp == 0) {
-        if (lane == 0) run_producer<BN, STAGES>(&tmA, &tmB, p, ring, bar0, abort_flag);
+        if (lane == 0) run_producer<BN, STAGES, PAIR>(&tmA, &tmB, p, ring, bar0, rank, abort_flag);
     } else if (warp == 1) {
-        if (lane == 0) run_mma<BN, STAGES>(p, ring, bar0, tmem_base, abort_flag);
+        if (lane == 0 && rank == 0) run_mma<BN, STAGES, PAIR>(p, ring, bar0, tmem_base, abort_flag);
     } else {
-        run_epilogue<BN, STAGES>(p, bar0, tmem_base, epi + (warp - 2) * EPI_WARP_FLOATS, abort_flag, warp, lane);
+        run_epilogue<BN, STAGES, PAIR>(p, bar0, tmem_base, epi + (warp - 2) * EPI_WARP_FLOATS, rank, abort_flag,
+                                       warp, lane);
     }
 
     tc_fence_before_sync();
     __syncthreads();
+    if constexpr (PAIR == 2) cluster_sync();  // no CTA leaves while its peer may still touch it
     if (warp == 1) {
         __syncwarp();
         tc_fence_after_sync();
-        tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+        if constexpr (PAIR == 1) tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+        else tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
     }
 }
 

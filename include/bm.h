@@ -132,14 +132,25 @@ BM_API void bm_set_wait_timeout_ms(uint32_t ms);
  */
 BM_API void bm_debug_inject_stall(int enable);
 
+/*
+ * Tile override for ablations and tests (process-wide; 0 = automatic choice,
+ * the default). 1: 128 x 256 tiles on single SMs; 2: 128 x 128 tiles on single
+ * SMs; 3: 256 x 256 tiles on SM pairs. Results are identical up to FP32
+ * summation order; only speed changes. Returns BM_ERR_INVALID_VALUE for other
+ * values.
+ */
+BM_API bm_status bm_set_tile_override(int variant);
+
 /* Human-readable name of a status code (static storage). */
 BM_API const char *bm_status_string(bm_status status);
 
 /*
- * Resolved launch plan of a GEMM, for reports and tests: output tile
- * (tile_m x tile_n), number of output tiles, K splits, CTAs launched and the
- * number of kernels one call launches. Performs the same argument checks as
- * bm_gemm_bf16 (except pointer alignment, since no pointers are given).
+ * Resolved launch plan of a GEMM or SYRK, for reports and tests: output tile
+ * (tile_m x tile_n, k-block tile_k), ring stages, number of output tiles
+ * visited, K splits, CTAs launched, CTAs per output tile (2 = an SM pair
+ * working on one tile), and the number of kernels one call launches.
+ * Performs the same size checks as the call (no pointers are given). On a
+ * machine without a usable GPU the plan assumes 152 SMs.
  */
 typedef struct {
     int32_t tile_m, tile_n, tile_k;
@@ -147,6 +158,7 @@ typedef struct {
     int64_t tiles;
     int32_t k_splits;
     int32_t ctas;
+    int32_t cta_pair;
     int32_t kernels;
     size_t workspace_bytes;
 } bm_plan;

@@ -3,6 +3,7 @@ through the C ABI, and comparison against the CPU oracle."""
 
 from __future__ import annotations
 
+import contextlib
 import functools
 
 import numpy as np
@@ -159,3 +160,18 @@ def tile_samples(m, n, tile_m=128, tile_n=256, per_tile=4, seed=0, extra=None):
         rows.append(extra[0])
         cols.append(extra[1])
     return np.concatenate(rows).astype(np.int64), np.concatenate(cols).astype(np.int64)
+
+
+VARIANTS = [0, 1, 2, 3]          # automatic, 128x256 single SM, 128x128 single SM, 256x256 SM pair
+VARIANT_IDS = ["auto", "single128x256", "single128x128", "pair256x256"]
+
+
+@contextlib.contextmanager
+def tile_variant(v):
+    """Force one kernel variant for the calls inside the block (0 = automatic)."""
+    import blas3_tensor_core_gb300 as bm
+    assert bm.bm_set_tile_override(v) == bm.BM_OK
+    try:
+        yield
+    finally:
+        bm.bm_set_tile_override(0)

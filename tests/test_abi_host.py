@@ -109,13 +109,18 @@ def test_valid_call_without_gpu_reports_cuda_error(lib):
 
 
 def test_gemm_plans(lib):
+    # large outputs: 256 x 256 tiles on SM pairs, one CTA pair per SM pair
     st, p = bm.bm_gemm_bf16_plan(4096, 4096, 4096, 0)
-    assert st == 0 and (p.tile_m, p.tile_n, p.tile_k) == (128, 256, 64)
-    assert p.tiles == 32 * 16 and p.k_splits == 1 and p.kernels == 1
+    assert st == 0 and (p.tile_m, p.tile_n, p.tile_k, p.cta_pair) == (256, 256, 64, 2)
+    assert p.tiles == 16 * 16 and p.k_splits == 1 and p.kernels == 1
+    assert p.ctas == 152 and p.stages == 6
     st, p = bm.bm_gemm_bf16_plan(2048, 5120, 5120, 0)
-    assert p.tiles == 16 * 20
+    assert p.tiles == 8 * 20 and p.cta_pair == 2
+    # small outputs: 128-row tiles on single SMs
     st, p = bm.bm_gemm_bf16_plan(100, 100, 100, 0)
-    assert p.tile_n == 128 and p.tiles == 1
+    assert p.tile_n == 128 and p.tiles == 1 and p.cta_pair == 1 and p.ctas == 1
+    st, p = bm.bm_gemm_bf16_plan(512, 512, 256, 0)
+    assert (p.tile_m, p.tile_n, p.cta_pair, p.tiles) == (128, 256, 1, 8)
     # a 512 x 512 output with K = 8192 fills the GPU only when K is split
     st, p = bm.bm_gemm_bf16_plan(512, 512, 8192, 0)
     assert p.k_splits == 1 and p.workspace_bytes == 0
@@ -151,7 +156,25 @@ def test_syrk_plans_visit_only_triangle_tiles(lib, n):
     for uplo in (bm.BM_LOWER, bm.BM_UPPER):
         st, p = bm.bm_syrk_bf16_plan(uplo, n, 64)
         assert st == 0
-        assert p.tiles == _syrk_tiles_bruteforce(n, uplo == bm.BM_LOWER)
+        assert p.tiles == _syrk_tiles_bruteforce(n, uplo == bm.BM_LOWER, p.tile_m, p.tile_n)
     if n == 8192:
-        # 64 tile rows of 128, 32 tile columns of 256: row t holds floor(t/2)+1 lower tiles
-        assert bm.bm_syrk_bf16_plan(bm.BM_LOWER, n, 64)[1].tiles == 1056
+        # 32 x 32 square tiles of 256 on SM pairs: 32 * 33 / 2 on or below the diagonal
+        p = bm.bm_syrk_bf16_plan(bm.BM_LOWER, n, 64)[1]
+        assert (p.tile_m, p.tile_n, p.cta_pair, p.tiles) == (256, 256, 2, 528)
+    if n <= 256:
+        assert bm.bm_syrk_bf16_plan(bm.BM_LOWER, n, 64)[1].cta_pair == 1
+
+
+def test_tile_override_values(lib):
+    assert bm.bm_set_tile_override(5) == bm.BM_ERR_INVALID_VALUE
+    assert bm.bm_set_tile_override(-1) == bm.BM_ERR_INVALID_VALUE
+    try:
+        for v, want in [(1, (128, 256, 1)), (2, (128, 128, 1)), (3, (256, 256, 2))]:
+            assert bm.bm_set_tile_override(v) == bm.BM_OK
+            p = bm.bm_gemm_bf16_plan(1000, 1000, 64, 0)[1]
+            assert (p.tile_m, p.tile_n, p.cta_pair) == want
+            s = bm.bm_syrk_bf16_plan(bm.BM_LOWER, 1000, 64)[1]
+            assert (s.tile_m, s.tile_n, s.cta_pair) == want
+            assert s.tiles == _syrk_tiles_bruteforce(1000, True, s.tile_m, s.tile_n)
+    finally:
+        assert bm.bm_set_tile_override(0) == bm.BM_OK

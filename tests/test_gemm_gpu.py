@@ -15,7 +15,8 @@ import pytest
 
 import bm_inputs as gen
 import oracle
-from gpu_helpers import (CBuffer, assert_parity, c_input_values, operand, run_gemm, tile_samples, torch)
+from gpu_helpers import (VARIANT_IDS, VARIANTS, CBuffer, assert_parity, c_input_values, operand, run_gemm,
+                         tile_samples, tile_variant, torch)
 
 pytestmark = pytest.mark.gpu
 
@@ -60,24 +61,28 @@ def orc():
 
 
 # ----------------------------------------------------------------------------- exact
+@pytest.mark.parametrize("variant", VARIANTS, ids=VARIANT_IDS)
 @pytest.mark.parametrize("ta,tb", list(itertools.product((0, 1), (0, 1))))
-@pytest.mark.parametrize("shape", [(256, 256, 256), (200, 300, 136), (129, 520, 64), (1, 8, 8)])
-def test_exact_integer_inputs_bitwise(shape, ta, tb):
+@pytest.mark.parametrize("shape", [(256, 256, 256), (200, 300, 136), (129, 520, 64), (1, 8, 8), (520, 264, 72)])
+def test_exact_integer_inputs_bitwise(shape, ta, tb, variant):
     m, n, k = shape
     A, B = _operands(m, n, k, ta, tb, "int", seed=11, lo=-8, hi=8)
     cbuf = CBuffer(m, n, _ldc(n, False), False, init=np.full((m, n), np.nan, np.float32))  # beta = 0: unread
-    got, raw = run_gemm(m, n, k, ta, tb, 1.0, A, B, 0.0, cbuf)
+    with tile_variant(variant):
+        got, raw = run_gemm(m, n, k, ta, tb, 1.0, A, B, 0.0, cbuf)
     ref, _ = orc().gemm(m, n, k, ta, tb, 1.0, A, B)
     assert np.array_equal(got, ref), f"max |diff| {np.max(np.abs(got - ref))}"
     cbuf.assert_guard_intact(raw)
 
 
-def test_exact_integer_beta_accumulate_bitwise():
+@pytest.mark.parametrize("variant", VARIANTS, ids=VARIANT_IDS)
+def test_exact_integer_beta_accumulate_bitwise(variant):
     m, n, k = 384, 264, 200
     A, B = _operands(m, n, k, 0, 0, "int", seed=21, lo=-8, hi=8)
     c0 = gen.integers(23, m * n, -100, 100).reshape(m, n).astype(np.float32)
     cbuf = CBuffer(m, n, _ldc(n, False), False, init=c0)
-    got, raw = run_gemm(m, n, k, 0, 0, 2.0, A, B, -1.0, cbuf)
+    with tile_variant(variant):
+        got, raw = run_gemm(m, n, k, 0, 0, 2.0, A, B, -1.0, cbuf)
     ref, _ = orc().gemm(m, n, k, 0, 0, 2.0, A, B, -1.0, c0)
     assert np.array_equal(got, ref)
     cbuf.assert_guard_intact(raw)
@@ -96,16 +101,18 @@ def test_config_256_uniform_fp32():
     cbuf.assert_guard_intact(raw)
 
 
+@pytest.mark.parametrize("variant", [0, 3], ids=["auto", "pair256x256"])
 @pytest.mark.parametrize("ta,tb", list(itertools.product((0, 1), (0, 1))))
 @pytest.mark.parametrize("bf16_out,beta", [(False, 0.0), (False, 1.5), (True, 0.0), (True, -0.5)])
-def test_gaussian_ragged_multi_tile(ta, tb, bf16_out, beta):
+def test_gaussian_ragged_multi_tile(ta, tb, bf16_out, beta, variant):
     m, n, k = 640, 520, 328
     alpha = -0.75
     A, B = _operands(m, n, k, ta, tb, "normal", seed=31)
     c0 = gen.matrix_f32(m, n, "normal", seed=33)
     c_init = gen.f32_to_bf16_bits(c0) if bf16_out else c0
     cbuf = CBuffer(m, n, _ldc(n, bf16_out), bf16_out, init=c_init)
-    got, raw = run_gemm(m, n, k, ta, tb, alpha, A, B, beta, cbuf)
+    with tile_variant(variant):
+        got, raw = run_gemm(m, n, k, ta, tb, alpha, A, B, beta, cbuf)
     ref, bound = orc().gemm(m, n, k, ta, tb, alpha, A, B, beta, c_init if beta != 0 else None)
     assert_parity(got, ref, bound, alpha, beta, c_input_values(c_init, bf16_out), bf16_out, "ragged")
     cbuf.assert_guard_intact(raw)
@@ -151,37 +158,41 @@ def test_k_zero_gives_beta_c_and_beta_zero_gives_zero():
 
 
 # ----------------------------------------------------------------------------- split K
-def test_split_k_matches_oracle_and_is_deterministic():
+@pytest.mark.parametrize("variant", [0, 3], ids=["auto", "pair256x256"])
+def test_split_k_matches_oracle_and_is_deterministic(variant):
     import blas3_tensor_core_gb300 as bm
     t = torch()
-    m, n, k = 512, 512, 8192
+    m, n, k = 512, 520, 8192
     A, B = _operands(m, n, k, 0, 0, "normal", seed=61)
-    need = bm.bm_gemm_bf16_workspace_size(m, n, k)
-    st, plan = bm.bm_gemm_bf16_plan(m, n, k, need)
-    assert plan.k_splits > 1
-    ws = t.empty(need // 4 + 64, dtype=t.float32, device="cuda")
     outs = []
-    for _ in range(2):
-        cbuf = CBuffer(m, n, n, False, init=np.full((m, n), np.nan, np.float32))
-        got, raw = run_gemm(m, n, k, 0, 0, 1.0, A, B, 0.0, cbuf, workspace=ws)
-        cbuf.assert_guard_intact(raw)
-        outs.append(got)
+    with tile_variant(variant):
+        need = bm.bm_gemm_bf16_workspace_size(m, n, k)
+        st, plan = bm.bm_gemm_bf16_plan(m, n, k, need)
+        assert plan.k_splits > 1 and plan.cta_pair == (2 if variant == 3 else 1)
+        ws = t.empty(need // 4 + 64, dtype=t.float32, device="cuda")
+        for _ in range(2):
+            cbuf = CBuffer(m, n, _ldc(n, False), False, init=np.full((m, n), np.nan, np.float32))
+            got, raw = run_gemm(m, n, k, 0, 0, 1.0, A, B, 0.0, cbuf, workspace=ws)
+            cbuf.assert_guard_intact(raw)
+            outs.append(got)
     assert np.array_equal(outs[0], outs[1])
     rows, cols = tile_samples(m, n, per_tile=64, seed=3)
     ref, bound = orc().gemm_entries(k, 0, 0, 1.0, A, B, rows, cols)
     assert_parity(outs[0][rows, cols], ref, bound, 1.0, 0.0, None, False, "split-K")
-    cbuf = CBuffer(m, n, n, False)
+    cbuf = CBuffer(m, n, _ldc(n, False), False)
     plain, _ = run_gemm(m, n, k, 0, 0, 1.0, A, B, 0.0, cbuf)  # no workspace: one split
     assert_parity(plain[rows, cols], ref, bound, 1.0, 0.0, None, False, "no split")
 
 
 # ----------------------------------------------------------------------------- persistence
-def test_persistent_many_tiles_exact():
+@pytest.mark.parametrize("variant", [0, 1], ids=["auto", "single128x256"])
+def test_persistent_many_tiles_exact(variant):
     """More tiles than SMs (each CTA loops over several tiles and both accumulators)."""
     m, n, k = 4096, 2048, 192
     A, B = _operands(m, n, k, 0, 0, "int", seed=71, lo=-8, hi=8)
     cbuf = CBuffer(m, n, n, False)
-    got, raw = run_gemm(m, n, k, 0, 0, 1.0, A, B, 0.0, cbuf)
+    with tile_variant(variant):
+        got, raw = run_gemm(m, n, k, 0, 0, 1.0, A, B, 0.0, cbuf)
     rows, cols = tile_samples(m, n, per_tile=16, seed=4)
     ref, _ = orc().gemm_entries(k, 0, 0, 1.0, A, B, rows, cols)
     assert np.array_equal(got[rows, cols], ref)

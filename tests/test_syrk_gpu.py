@@ -12,7 +12,8 @@ import pytest
 
 import bm_inputs as gen
 import oracle
-from gpu_helpers import CBuffer, assert_parity, c_input_values, operand, run_syrk, tile_samples, torch
+from gpu_helpers import (VARIANT_IDS, VARIANTS, CBuffer, assert_parity, c_input_values, operand, run_syrk,
+                         tile_samples, tile_variant, torch)
 
 pytestmark = pytest.mark.gpu
 
@@ -34,24 +35,27 @@ def _a(n, k, trans, dist, seed, std=1.0, lo=-1.0, hi=1.0):
     return operand(rows, cols, dist, seed, std, lo, hi, pad=(-cols) % 8 + 8)
 
 
+@pytest.mark.parametrize("variant", VARIANTS, ids=VARIANT_IDS)
 @pytest.mark.parametrize("uplo,trans", list(itertools.product((0, 1), (0, 1))))
 @pytest.mark.parametrize("n,k", [(300, 136), (256, 64), (520, 200)])
-def test_syrk_exact_integer(uplo, trans, n, k):
+def test_syrk_exact_integer(uplo, trans, n, k, variant):
     A = _a(n, k, trans, "int", seed=5, lo=-8, hi=8)
     c0 = gen.integers(6, n * n, -50, 50).reshape(n, n).astype(np.float32)
     c0 = np.tril(c0) + np.tril(c0, -1).T
     ldc = n + (-n) % 4 + 4
     cbuf = CBuffer(n, n, ldc, False, init=c0)
-    got, raw = run_syrk(uplo, trans, n, k, 1.0, A, 1.0, cbuf)
+    with tile_variant(variant):
+        got, raw = run_syrk(uplo, trans, n, k, 1.0, A, 1.0, cbuf)
     ref, _ = oracle.default().syrk(uplo, trans, n, k, 1.0, A, 1.0, c0)
     mask = _mask(n, uplo)
     assert np.array_equal(got[mask], ref[mask])
     cbuf.assert_guard_intact(raw, mask_written=mask)
 
 
+@pytest.mark.parametrize("variant", [0, 3], ids=["auto", "pair256x256"])
 @pytest.mark.parametrize("uplo,trans", list(itertools.product((0, 1), (0, 1))))
 @pytest.mark.parametrize("bf16_out", [False, True])
-def test_syrk_gaussian(uplo, trans, bf16_out):
+def test_syrk_gaussian(uplo, trans, bf16_out, variant):
     n, k = 400, 264
     A = _a(n, k, trans, "normal", seed=7)
     c0 = gen.symmetric_f32(n, seed=8)
@@ -59,7 +63,8 @@ def test_syrk_gaussian(uplo, trans, bf16_out):
     ldc = n + 8
     cbuf = CBuffer(n, n, ldc, bf16_out, init=c_init)
     alpha, beta = 0.5, -0.5
-    got, raw = run_syrk(uplo, trans, n, k, alpha, A, beta, cbuf)
+    with tile_variant(variant):
+        got, raw = run_syrk(uplo, trans, n, k, alpha, A, beta, cbuf)
     ref, bound = oracle.default().syrk(uplo, trans, n, k, alpha, A, beta, c_init)
     mask = _mask(n, uplo)
     assert_parity(got[mask], ref[mask], bound[mask], alpha, beta, c_input_values(c_init, bf16_out)[mask],
