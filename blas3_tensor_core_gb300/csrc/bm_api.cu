@@ -380,6 +380,85 @@ bm_status check_gemm_args(int64_t m, int64_t n, int64_t k, int transA, int trans
     return BM_OK;
 }
 
+// ---------------------------------------------------------------- allocation-free GEMM
+// Scratch for bm_gemm_bf16_noalloc: the split-K partials live in this file-scope
+// device array instead of a caller or library allocation. Every GPU that loads
+// the library holds it until the process exits. In host code the symbol is only
+// a host-side stand-in; the device address comes from cudaGetSymbolAddress.
+static __device__ __align__(256) float g_noalloc_scratch[BM_NOALLOC_SCRATCH_BYTES / sizeof(float)];
+
+float *g_noalloc_scratch_addr[kMaxDevices] = {};
+
+// Set-up for the allocation-free entry point on the current device: the same
+// device checks and one-time attributes as the other entry points, but no
+// cudaMalloc (the status word is used only if another entry point already
+// created it), and the device address of the scratch array (looked up once per
+// device, with that device current).
+bm_status noalloc_device_setup(DeviceState **out, float **scratch)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return BM_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState &st = g_devices[dev];
+    if (!st.ready) {
+        cudaDeviceProp prop;
+        if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return BM_ERR_CUDA;
+        st.sm_count = prop.multiProcessorCount;
+        st.cc_major = prop.major;
+        st.cc_minor = prop.minor;
+        st.ready = true;
+    }
+    if (st.cc_major != 10 || st.cc_minor != 3) return BM_ERR_ARCH;
+    if (g_encode == nullptr) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || fn == nullptr)
+            return BM_ERR_CUDA;
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    if (!st.attrs_set) {
+        for (int v = 0; v < kNumVariants; ++v)
+            if (cudaFuncSetAttribute(variant_kernel(v), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     variant_smem(v)) != cudaSuccess)
+                return BM_ERR_CUDA;
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(2 * (st.sm_count / 2), 1, 1);
+        cfg.blockDim = dim3(bm::NUM_THREADS, 1, 1);
+        cfg.dynamicSmemBytes = variant_smem(kPair256);
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, variant_kernel(kPair256), &cfg) != cudaSuccess ||
+            clusters <= 0) {
+            cudaGetLastError();
+            clusters = 0;
+        }
+        st.max_pair_clusters = clusters;
+        st.attrs_set = true;
+    }
+    if (g_noalloc_scratch_addr[dev] == nullptr) {
+        void *addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || addr == nullptr) {
+            cudaGetLastError();
+            return BM_ERR_CUDA;
+        }
+        g_noalloc_scratch_addr[dev] = static_cast<float *>(addr);
+    }
+    *scratch = g_noalloc_scratch_addr[dev];
+    *out = &st;
+    return BM_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -427,6 +506,43 @@ size_t bm_gemm_bf16_workspace_size(int64_t m, int64_t n, int64_t k)
     const int sms = sm_count_or_default();
     const Plan pl = plan_gemm(m, n, k, SIZE_MAX, sms, pair_clusters_or_default(sms));
     return pl.k_splits > 1 ? pl.ws_bytes : 0;
+}
+
+bm_status bm_gemm_bf16_noalloc(int64_t m, int64_t n, int64_t k, bm_op transA, bm_op transB, float alpha,
+                               const void *A, int64_t lda, const void *B, int64_t ldb, float beta, void *C,
+                               int64_t ldc, bm_ctype c_type, bm_stream_t stream)
+{
+    bm_status s = check_gemm_args(m, n, k, transA, transB, lda, ldb, ldc, c_type);
+    if (s != BM_OK) return s;
+    if (m == 0 || n == 0) return BM_OK;
+    const bool products = alpha != 0.0f && k > 0;
+    if (C == nullptr || (products && (A == nullptr || B == nullptr))) return BM_ERR_INVALID_VALUE;
+    const int64_t esz = c_type == BM_C_BF16 ? 2 : 4;
+    if (!aligned16(C) || (ldc * esz) % 16 != 0) return BM_ERR_MISALIGNED;
+    if (products && (!aligned16(A) || !aligned16(B) || (lda * 2) % 16 != 0 || (ldb * 2) % 16 != 0))
+        return BM_ERR_MISALIGNED;
+    DeviceState *st = nullptr;
+    float *scratch = nullptr;
+    s = noalloc_device_setup(&st, &scratch);
+    if (s != BM_OK) return s;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    bm::GemmParams prm = base_params(m, n, k, alpha, beta, C, ldc, c_type, st);
+    prm.mode = bm::MODE_GEMM;
+    if (!products) return launch_scale(prm, cs);
+
+    // The plan bm_gemm_bf16 makes with the workspace it asks for; its partials
+    // must fit the static scratch array.
+    const Plan pl = plan_gemm(m, n, k, SIZE_MAX, st->sm_count, st->max_pair_clusters);
+    if (pl.k_splits > 1 && pl.ws_bytes > BM_NOALLOC_SCRATCH_BYTES) return BM_ERR_WORKSPACE;
+    CUtensorMap ta, tb;
+    const bool a_mn = transA == BM_OP_T, b_mn = transB == BM_OP_N;
+    if (!encode_operand(&ta, A, a_mn, m, k, lda, bm::CTA_M)) return BM_ERR_CUDA;
+    if (!encode_operand(&tb, B, b_mn, n, k, ldb, static_cast<uint32_t>(pl.bn / pl.pair))) return BM_ERR_CUDA;
+    prm.a_mn_major = a_mn;
+    prm.b_mn_major = b_mn;
+    fill_params(prm, pl);
+    prm.partial = pl.k_splits > 1 ? scratch : nullptr;
+    return launch(pl, ta, tb, prm, cs);
 }
 
 bm_status bm_syrk_bf16(bm_uplo uplo, bm_op trans, int64_t n, int64_t k, float alpha, const void *A, int64_t lda,

@@ -95,6 +95,45 @@ BM_API bm_status bm_gemm_bf16(int64_t m, int64_t n, int64_t k, bm_op transA, bm_
 /* Bytes of workspace that bm_gemm_bf16 would use for this shape (0 = none). */
 BM_API size_t bm_gemm_bf16_workspace_size(int64_t m, int64_t n, int64_t k);
 
+/* Size of the device scratch array that bm_gemm_bf16_noalloc uses (16 MiB). */
+#define BM_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/*
+ * GEMM that allocates nothing. The paper has no counterpart: this entry
+ * point exists for callers that cannot call cudaMalloc, such as code that
+ * runs inside a framework which owns all device memory through its own pool,
+ * a plug-in called back by another library that gives it no allocator, or a
+ * latency-critical path where the implicit synchronisation of cudaMalloc is
+ * not acceptable.
+ *
+ * Same operation, arguments, layout rules and errors as bm_gemm_bf16, except
+ * that there is no workspace argument. When the launch plan splits K (small
+ * m * n, long k), the partial sums go to one file-scope device array of
+ * BM_NOALLOC_SCRATCH_BYTES that the library holds on every GPU it is loaded
+ * on, until the process exits. The plan is the one bm_gemm_bf16 uses with a
+ * workspace of bm_gemm_bf16_workspace_size(m, n, k) bytes; if that is more than
+ * BM_NOALLOC_SCRATCH_BYTES the call returns BM_ERR_WORKSPACE and launches
+ * nothing. The caller still owns and passes A, B and C.
+ *
+ *   - The first call on a device looks up the device address of the array
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - All calls on a device share the one array, and it keeps the last
+ *     call's contents. Nothing in it needs to start at zero (every partial
+ *     that is read was written by the same call). Calls whose kernels
+ *     overlap on the GPU (different streams, no ordering between them) race
+ *     on it and give wrong results; order them on one stream or with events.
+ *   - No cudaMalloc, cudaFree or other allocating routine is called. A
+ *     device-side wait that runs out is recorded in the status word read by
+ *     bm_get_last_device_error only if another entry point of this library
+ *     has already created that word on the device (this call never creates
+ *     it).
+ */
+BM_API bm_status bm_gemm_bf16_noalloc(int64_t m, int64_t n, int64_t k, bm_op transA, bm_op transB,
+                                      float alpha, const void *A, int64_t lda, const void *B,
+                                      int64_t ldb, float beta, void *C, int64_t ldc, bm_ctype c_type,
+                                      bm_stream_t stream);
+
 /*
  * SYRK:  C = alpha * op(A) * op(A)^T + beta * C   on one triangle of C[n x n]
  *
