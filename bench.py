@@ -497,7 +497,8 @@ def run_gpu_arm(args, dist):
                 "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4),
                 "algorithmic_flops_per_launch": wl.flops(),
                 "algorithmic_bytes_per_launch": wl.bytes(),
-                "kernel": "bm_gemm_tcgen05_kernel<256,4>",
+                "kernel": (f"bm_gemm_tcgen05_kernel<{wl.plan.tile_n},{wl.plan.stages},{wl.plan.cta_pair}>"
+                           + (" + bm_splitk_reduce_kernel" if wl.plan.kernels > 1 else "")),
                 "traffic_source": traffic_src}
     e2e_ms, h2d, d2h, _ = e2e_steps(wl, args.e2e_steps, max(3, args.warmup // 10), dist)
     e2e = {"value": round(dist.world * wl.flops() * args.e2e_steps / (e2e_ms * 1e-3) / 1e12, 3), "unit": UNIT,

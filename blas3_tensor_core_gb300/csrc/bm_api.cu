@@ -157,6 +157,50 @@ bool encode_bf16_2d(CUtensorMap *map, const void *base, int64_t inner, int64_t o
     return r == CUDA_SUCCESS;
 }
 
+// Map of C used only to prefetch each CTA's output rows into L2 (box: tile
+// columns x 128 rows, no swizzle).
+bool encode_c_prefetch(CUtensorMap *map, void *C, bm_ctype ct, int64_t m, int64_t n, int64_t ldc, uint32_t cols)
+{
+    const cuuint64_t esz = ct == BM_C_BF16 ? 2u : 4u;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(m)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldc) * esz};
+    cuuint32_t box[2] = {cols, static_cast<cuuint32_t>(bm::CTA_M)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, ct == BM_C_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                          2, C, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// Map of C for the epilogue's TMA stores: box of 128 bytes (64 bf16 or 32 fp32
+// columns) x 32 rows, 128-byte swizzle (the staging layout the epilogue writes).
+bool encode_c_store(CUtensorMap *map, void *C, bm_ctype ct, int64_t m, int64_t n, int64_t ldc)
+{
+    const cuuint64_t esz = ct == BM_C_BF16 ? 2u : 4u;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(m)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldc) * esz};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esz), 32u};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, ct == BM_C_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                          2, C, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// Map of the fp32 partial slots [slots * tile rows][tile columns] for the
+// epilogue's TMA stores: box 32 x 32, 128-byte swizzle.
+bool encode_slots(CUtensorMap *map, void *partial, int64_t rows, int64_t cols)
+{
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 4u};
+    cuuint32_t box[2] = {32u, 32u};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, partial, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // Operand tile maps. K-major: box 64 (k) x rows; M/N-major: box 64 (m or n) x 64 (k).
 bool encode_operand(CUtensorMap *map, const void *base, bool mn_major, int64_t rows, int64_t k, int64_t ld,
                     uint32_t tile_rows)
@@ -169,11 +213,15 @@ struct Plan {
     int variant = kSingle256;
     int tile_m = bm::CTA_M, bn = 256, stages = 4, pair = 1;
     int64_t tiles_m = 0, tiles_n = 0, num_tiles = 0;
+    int64_t full_tiles = 0, num_units = 0;  // whole tiles first; the rest are split k_splits ways
     int k_splits = 1, kb_per_split = 0, kb_total = 0;
     int ctas = 0;
-    int64_t ldp = 0;
     size_t ws_bytes = 0;
 };
+
+// Largest workspace a tail split may ask for (the full-GPU split of small
+// outputs is not capped).
+constexpr size_t kTailSplitMaxBytes = 16u << 20;
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -202,9 +250,37 @@ int64_t syrk_tile_count(int mode, int64_t tiles_m, int64_t tiles_n, int tile_m, 
 // Persistent grid: one CTA (or CTA pair) per SM (pair of SMs), never more than the work units.
 void size_grid(Plan &pl, int sms, int pair_clusters)
 {
-    const int64_t units = pl.num_tiles * pl.k_splits;
-    if (pl.pair == 2) pl.ctas = static_cast<int>(2 * std::min<int64_t>(units, pair_clusters));
-    else pl.ctas = static_cast<int>(std::min<int64_t>(units, sms));
+    pl.num_units = pl.full_tiles + (pl.num_tiles - pl.full_tiles) * pl.k_splits;
+    if (pl.pair == 2) pl.ctas = static_cast<int>(2 * std::min<int64_t>(pl.num_units, pair_clusters));
+    else pl.ctas = static_cast<int>(std::min<int64_t>(pl.num_units, sms));
+}
+
+// Split the last `split_tiles` tiles of the unit order `want` ways (or fewer)
+// along K, if each part keeps >= 4 k-blocks, the partial slots fit `budget`,
+// and the mainloop time it saves beats the cost of the extra reduce kernel.
+// One 64-deep k-block of a tile takes 4 MMAs of 128 tensor-core cycles, about
+// 0.26 us at 2 GHz; the reduce launch and its traffic cost a few us.
+constexpr double kKBlockUs = 0.256;
+constexpr double kSplitMinGainUs = 6.0;
+
+void try_split(Plan &pl, int64_t split_tiles, int64_t want, size_t budget)
+{
+    const size_t slot_bytes = static_cast<size_t>(pl.tile_m) * pl.bn * sizeof(float);
+    want = std::min<int64_t>(want, pl.kb_total / 4);
+    while (want > 1) {
+        const int per = static_cast<int>(ceil_div(pl.kb_total, want));
+        const int splits = static_cast<int>(ceil_div(pl.kb_total, per));
+        const size_t need = static_cast<size_t>(splits) * static_cast<size_t>(split_tiles) * slot_bytes;
+        const double gain_us = kKBlockUs * (pl.kb_total - per);
+        if (splits > 1 && need <= budget && gain_us >= kSplitMinGainUs) {
+            pl.k_splits = splits;
+            pl.kb_per_split = per;
+            pl.full_tiles = pl.num_tiles - split_tiles;
+            pl.ws_bytes = need;
+            return;
+        }
+        --want;
+    }
 }
 
 // Pair tiles (256 x 256 on two SMs) whenever they alone can occupy at least half
@@ -220,24 +296,18 @@ Plan plan_gemm(int64_t m, int64_t n, int64_t k, size_t ws_bytes, int sms, int pa
     pl.tiles_m = ceil_div(m, pl.tile_m);
     pl.tiles_n = ceil_div(n, pl.bn);
     pl.num_tiles = pl.tiles_m * pl.tiles_n;
+    pl.full_tiles = pl.num_tiles;
     pl.kb_total = static_cast<int>(ceil_div(std::max<int64_t>(k, 1), bm::TILE_K));
     pl.kb_per_split = pl.kb_total;
-    pl.ldp = ceil_div(n, 4) * 4;
-    // Split K only when the tiles cannot fill half the GPU and each split keeps >= 4 k-blocks.
     const int64_t slots = pl.pair == 2 ? pair_clusters : sms;
-    if (pl.num_tiles * 2 <= slots && pl.kb_total >= 8) {
-        int64_t want = std::min<int64_t>(ceil_div(slots, pl.num_tiles), pl.kb_total / 4);
-        while (want > 1) {
-            const int per = static_cast<int>(ceil_div(pl.kb_total, want));
-            const int splits = static_cast<int>(ceil_div(pl.kb_total, per));
-            const size_t need = static_cast<size_t>(splits) * static_cast<size_t>(m) * pl.ldp * sizeof(float);
-            if (need <= ws_bytes) {
-                pl.k_splits = splits;
-                pl.kb_per_split = per;
-                pl.ws_bytes = need;
-                break;
-            }
-            --want;
+    if (slots > 0 && pl.kb_total >= 8) {
+        if (pl.num_tiles * 2 <= slots) {
+            // Too few tiles to fill half the GPU: split every tile along K.
+            try_split(pl, pl.num_tiles, ceil_div(slots, pl.num_tiles), ws_bytes);
+        } else {
+            // The last wave is at most half full: split its tiles along K over the idle slots.
+            const int64_t tail = pl.num_tiles % slots;
+            if (tail > 0 && tail * 2 <= slots) try_split(pl, tail, slots / tail, std::min(ws_bytes, kTailSplitMaxBytes));
         }
     }
     size_grid(pl, sms, pair_clusters);
@@ -254,6 +324,7 @@ Plan plan_syrk(int mode, int64_t n, int64_t k, int sms, int pair_clusters)
     pl.tiles_m = ceil_div(n, pl.tile_m);
     pl.tiles_n = ceil_div(n, pl.bn);
     pl.num_tiles = syrk_tile_count(mode, pl.tiles_m, pl.tiles_n, pl.tile_m, pl.bn);
+    pl.full_tiles = pl.num_tiles;
     pl.kb_total = static_cast<int>(ceil_div(std::max<int64_t>(k, 1), bm::TILE_K));
     pl.kb_per_split = pl.kb_total;
     size_grid(pl, sms, pair_clusters);
@@ -265,6 +336,25 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bm_status launch(const Plan &pl, const CUtensorMap &ta, const CUtensorMap &tb, bm::GemmParams &prm,
                  cudaStream_t stream)
 {
+    // beta != 0: the epilogue reads C, so each whole tile's C is prefetched into L2.
+    // beta == 0 (GEMM): the epilogue stores C with TMA through a swizzled map instead.
+    CUtensorMap tc;
+    std::memset(&tc, 0, sizeof(tc));
+    prm.prefetch_c = 0;
+    prm.store_c_tma = 0;
+    const bm_ctype ct = prm.c_bf16 ? BM_C_BF16 : BM_C_F32;
+    if (prm.beta != 0.0f) {
+        if (encode_c_prefetch(&tc, prm.C, ct, prm.m, prm.n, prm.ldc, static_cast<uint32_t>(pl.bn)))
+            prm.prefetch_c = 1;
+    } else if (prm.mode == bm::MODE_GEMM) {
+        if (encode_c_store(&tc, prm.C, ct, prm.m, prm.n, prm.ldc)) prm.store_c_tma = 1;
+    }
+    CUtensorMap tp;
+    std::memset(&tp, 0, sizeof(tp));
+    prm.store_p_tma = 0;
+    if (prm.k_splits > 1 && prm.partial != nullptr &&
+        encode_slots(&tp, prm.partial, (prm.num_tiles - prm.full_tiles) * prm.k_splits * pl.tile_m, pl.bn))
+        prm.store_p_tma = 1;
     if (pl.ctas <= 0) return BM_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -282,18 +372,26 @@ bm_status launch(const Plan &pl, const CUtensorMap &ta, const CUtensorMap &tb, b
     }
     cudaError_t err;
     switch (pl.variant) {
-    case kSingle256: err = cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<256, 4, 1>, ta, tb, prm); break;
-    case kSingle128: err = cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<128, 6, 1>, ta, tb, prm); break;
-    default: err = cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<256, 6, 2>, ta, tb, prm); break;
+    case kSingle256:
+        err = cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<256, 4, 1>, ta, tb, tc, tp, prm);
+        break;
+    case kSingle128:
+        err = cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<128, 6, 1>, ta, tb, tc, tp, prm);
+        break;
+    default: err = cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<256, 6, 2>, ta, tb, tc, tp, prm); break;
     }
     if (err != cudaSuccess) {
         cudaGetLastError();
         return BM_ERR_CUDA;
     }
     if (prm.k_splits > 1) {
-        const int64_t work = prm.m * ceil_div(prm.n, 4);
+        const int64_t work = (prm.num_tiles - prm.full_tiles) * pl.tile_m * (pl.bn / 4);
         const int blocks = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(ceil_div(work, 256), 8 * 152)));
-        bm::bm_splitk_reduce_kernel<<<blocks, 256, 0, stream>>>(prm);
+        switch (pl.variant) {
+        case kSingle256: bm::bm_splitk_reduce_kernel<128, 256><<<blocks, 256, 0, stream>>>(prm); break;
+        case kSingle128: bm::bm_splitk_reduce_kernel<128, 128><<<blocks, 256, 0, stream>>>(prm); break;
+        default: bm::bm_splitk_reduce_kernel<256, 256><<<blocks, 256, 0, stream>>>(prm); break;
+        }
         if (cudaGetLastError() != cudaSuccess) return BM_ERR_CUDA;
     }
     return BM_OK;
@@ -312,10 +410,11 @@ void fill_params(bm::GemmParams &prm, const Plan &pl)
     prm.tiles_m = pl.tiles_m;
     prm.tiles_n = pl.tiles_n;
     prm.num_tiles = pl.num_tiles;
+    prm.full_tiles = pl.full_tiles;
+    prm.num_units = pl.num_units;
     prm.k_splits = pl.k_splits;
     prm.kb_per_split = pl.kb_per_split;
     prm.kb_total = pl.kb_total;
-    prm.ldp = pl.ldp;
 }
 
 void export_plan(const Plan &pl, bm_plan *plan)
@@ -326,6 +425,7 @@ void export_plan(const Plan &pl, bm_plan *plan)
     plan->stages = pl.stages;
     plan->tiles = pl.num_tiles;
     plan->k_splits = pl.k_splits;
+    plan->split_tiles = pl.num_tiles - pl.full_tiles;
     plan->ctas = pl.ctas;
     plan->cta_pair = pl.pair;
     plan->kernels = pl.k_splits > 1 ? 2 : 1;

@@ -58,7 +58,9 @@ enum : int { DEV_ERR_TIMEOUT = 5 };
 constexpr int CTA_M = 128;  // accumulator rows (TMEM lanes) per CTA
 constexpr int TILE_K = 64;  // bf16 elements = 128 bytes = one swizzle row
 constexpr int UMMA_K = 16;
-constexpr int NUM_EPI_WARPS = 4;
+// Two epilogue warps per TMEM lane quadrant: warps w and w + 4 read the same 32
+// accumulator rows and split the column chunks between them.
+constexpr int NUM_EPI_WARPS = 8;
 constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
 constexpr int EPI_WARP_FLOATS = 32 * 32;  // one 32 x 32 fp32 staging block per epilogue warp
 
@@ -72,16 +74,20 @@ struct GemmParams {
     int b_mn_major;
     int mode;          // MODE_*
     int64_t tiles_m, tiles_n;
-    int64_t num_tiles; // GEMM: tiles_m * tiles_n; SYRK: tiles touching the triangle
-    int k_splits;      // > 1: each split writes an fp32 partial, a second kernel sums them
-    int kb_per_split;  // k-blocks (of TILE_K) per split
-    int kb_total;      // ceil(k / TILE_K)
-    int group_m;       // grouped raster: tile rows per group
-    float *partial;    // [k_splits][m][ldp] when k_splits > 1
-    int64_t ldp;
+    int64_t num_tiles;  // GEMM: tiles_m * tiles_n; SYRK: tiles touching the triangle
+    int64_t full_tiles; // units [0, full_tiles) are whole tiles; each later tile is split k_splits ways
+    int64_t num_units;  // full_tiles + (num_tiles - full_tiles) * k_splits
+    int k_splits;       // > 1: split units write fp32 partials that a second kernel sums
+    int kb_per_split;   // k-blocks (of TILE_K) per split
+    int kb_total;       // ceil(k / TILE_K)
+    int group_m;        // grouped raster: tile rows per group
+    float *partial;     // [split tile][split][tile rows][tile columns] fp32 when k_splits > 1
     int *status;       // device status word (first error wins)
     uint64_t timeout_ns;
     int debug_stall;   // test hook: the first stage's copy is never issued
+    int prefetch_c;    // beta != 0: tmC maps C for L2 prefetch (box tile columns x 128 rows)
+    int store_c_tma;   // beta == 0, GEMM: tmC maps C for TMA stores (box 128 bytes x 32 rows, 128B swizzle)
+    int store_p_tma;   // split units: tmP maps the partial slots for TMA stores (fp32, box 32 x 32, 128B swizzle)
 };
 
 template <int BN, int STAGES, int PAIR>
@@ -107,7 +113,8 @@ struct KernelCfg {
 // ---------------------------------------------------------------- scheduling
 struct Unit {
     int64_t tm, tn;
-    int split;
+    int kb0, kb1;     // k-blocks of this unit
+    int64_t slot;     // partial-sum slot (split units only), -1 for a whole tile
 };
 
 // Range of tile columns [lo, hi] of tile row tm (tiles TM x BN) that touch the
@@ -125,36 +132,60 @@ __host__ __device__ inline void syrk_row_tiles(int mode, int64_t tm, int64_t til
     }
 }
 
+// Tile t -> (tile row, tile column): grouped raster for GEMM, row by row over
+// the triangle for SYRK.
 template <int TM, int BN>
-__device__ __forceinline__ Unit map_unit(const GemmParams &p, int64_t u)
+__device__ __forceinline__ void tile_coords(const GemmParams &p, int64_t t, int64_t &tm, int64_t &tn)
 {
-    Unit r;
-    const int64_t t = u / p.k_splits;
-    r.split = static_cast<int>(u - t * p.k_splits);
-    r.tm = 0;
-    r.tn = 0;
+    tm = 0;
+    tn = 0;
     if (p.mode == MODE_GEMM) {
         const int64_t per_group = static_cast<int64_t>(p.group_m) * p.tiles_n;
         const int64_t g = t / per_group;
         const int64_t first = g * p.group_m;
         const int64_t rows = (p.tiles_m - first) < p.group_m ? (p.tiles_m - first) : p.group_m;
         const int64_t local = t - g * per_group;
-        r.tm = first + local % rows;
-        r.tn = local / rows;
+        tm = first + local % rows;
+        tn = local / rows;
     } else {
         int64_t rem = t;
-        for (int64_t tm = 0; tm < p.tiles_m; ++tm) {
+        for (int64_t r = 0; r < p.tiles_m; ++r) {
             int64_t lo, hi;
-            syrk_row_tiles<TM, BN>(p.mode, tm, p.tiles_n, lo, hi);
+            syrk_row_tiles<TM, BN>(p.mode, r, p.tiles_n, lo, hi);
             const int64_t cnt = hi - lo + 1;
             if (rem < cnt) {
-                r.tm = tm;
-                r.tn = lo + rem;
+                tm = r;
+                tn = lo + rem;
                 break;
             }
             rem -= cnt;
         }
     }
+}
+
+// Work unit u: a whole tile (u < full_tiles), or one K range of a split tile.
+// Split tiles come last, so with units handed out round-robin they fill the
+// otherwise partly idle last wave.
+template <int TM, int BN>
+__device__ __forceinline__ Unit map_unit(const GemmParams &p, int64_t u)
+{
+    Unit r;
+    int64_t t;
+    if (u < p.full_tiles) {
+        t = u;
+        r.kb0 = 0;
+        r.kb1 = p.kb_total;
+        r.slot = -1;
+    } else {
+        const int64_t v = u - p.full_tiles;
+        const int64_t local = v / p.k_splits;
+        const int split = static_cast<int>(v - local * p.k_splits);
+        t = p.full_tiles + local;
+        r.kb0 = split * p.kb_per_split;
+        r.kb1 = min(p.kb_total, r.kb0 + p.kb_per_split);
+        r.slot = p.k_splits > 1 ? v : -1;
+    }
+    tile_coords<TM, BN>(p, t, r.tm, r.tn);
     return r;
 }
 
@@ -293,23 +324,71 @@ __device__ __forceinline__ void write_c4(const GemmParams &p, int64_t i, int64_t
     }
 }
 
+// Out-of-line masked store for vectors on a ragged edge or the SYRK diagonal;
+// keeps the epilogue's unrolled fast path small.
+__device__ __noinline__ void write_c4_edge(const GemmParams &p, int64_t i, int64_t j, float4 v4)
+{
+    float v[4] = {v4.x, v4.y, v4.z, v4.w};
+    write_c4(p, i, j, v);
+}
+
+// write_c4 for a full, unmasked 4-vector whose old C value was loaded earlier
+// (raw bits: fp32 -> 4 words; bf16 -> words x, y hold 4 values).
+__device__ __forceinline__ void write_c4_preloaded(const GemmParams &p, int64_t i, int64_t j, float v[4],
+                                                   uint4 old)
+{
+    if (p.c_bf16) {
+        const __nv_bfloat162 o01 = *reinterpret_cast<const __nv_bfloat162 *>(&old.x);
+        const __nv_bfloat162 o23 = *reinterpret_cast<const __nv_bfloat162 *>(&old.y);
+        v[0] = fmaf(p.beta, __low2float(o01), v[0]);
+        v[1] = fmaf(p.beta, __high2float(o01), v[1]);
+        v[2] = fmaf(p.beta, __low2float(o23), v[2]);
+        v[3] = fmaf(p.beta, __high2float(o23), v[3]);
+        const __nv_bfloat162 r01 = __floats2bfloat162_rn(v[0], v[1]);
+        const __nv_bfloat162 r23 = __floats2bfloat162_rn(v[2], v[3]);
+        uint2 out;
+        out.x = *reinterpret_cast<const uint32_t *>(&r01);
+        out.y = *reinterpret_cast<const uint32_t *>(&r23);
+        *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(p.C) + i * p.ldc + j) = out;
+    } else {
+        v[0] = fmaf(p.beta, __uint_as_float(old.x), v[0]);
+        v[1] = fmaf(p.beta, __uint_as_float(old.y), v[1]);
+        v[2] = fmaf(p.beta, __uint_as_float(old.z), v[2]);
+        v[3] = fmaf(p.beta, __uint_as_float(old.w), v[3]);
+        *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.C) + i * p.ldc + j) =
+            make_float4(v[0], v[1], v[2], v[3]);
+    }
+}
+
+// Is C[i, j..j+3] a full vector inside the output (no edge, no triangle mask)?
+__device__ __forceinline__ bool full_vector(const GemmParams &p, int64_t i, int64_t j)
+{
+    bool all = (i < p.m) && (j + 3 < p.n);
+    if (p.mode == MODE_SYRK_LOWER) all = all && (i >= j + 3);
+    if (p.mode == MODE_SYRK_UPPER) all = all && (i <= j);
+    return all;
+}
+
 // ---------------------------------------------------------------- roles
 template <int BN, int STAGES, int PAIR>
-__device__ __forceinline__ void run_producer(const CUtensorMap *tmA, const CUtensorMap *tmB, const GemmParams &p,
-                                             uint32_t ring, uint32_t bar0, uint32_t rank, volatile int *abort_flag)
+__device__ __forceinline__ void run_producer(const CUtensorMap *tmA, const CUtensorMap *tmB, const CUtensorMap *tmC,
+                                             const GemmParams &p, uint32_t ring, uint32_t bar0, uint32_t rank,
+                                             volatile int *abort_flag)
 {
     using Cfg = KernelCfg<BN, STAGES, PAIR>;
-    const int64_t units = p.num_tiles * p.k_splits;
+    const int64_t units = p.num_units;
     int stage = 0;
     uint32_t phase = 0;
     uint32_t armed = 0, armed_parity = 0;  // per stage: armed at least once / parity of last arming
     bool ok = true, first = true, issued_any = false;
     for (int64_t u = first_unit<PAIR>(); u < units && ok; u += unit_stride<PAIR>()) {
         const Unit w = map_unit<Cfg::TILE_M, BN>(p, u);
-        const int kb0 = w.split * p.kb_per_split;
-        const int kb1 = min(p.kb_total, kb0 + p.kb_per_split);
+        const int kb0 = w.kb0;
+        const int kb1 = w.kb1;
         const int32_t row_a = static_cast<int32_t>(w.tm * Cfg::TILE_M + rank * CTA_M);
         const int32_t row_b = static_cast<int32_t>(w.tn * BN + rank * Cfg::B_ROWS);
+        // The epilogue of this tile will read this CTA's 128 rows of C: start pulling them into L2.
+        if (p.prefetch_c && w.slot < 0) tma_prefetch_l2_2d(tmC, static_cast<int32_t>(w.tn * BN), row_a);
         for (int kb = kb0; kb < kb1; ++kb) {
             const uint32_t empty = bar0 + 8u * (STAGES + stage);
             if (!wait_one<PAIR == 2>(empty, phase ^ 1u, abort_flag, p.timeout_ns)) {
@@ -379,15 +458,15 @@ __device__ __forceinline__ void run_mma(const GemmParams &p, uint32_t ring, uint
                                         volatile int *abort_flag)
 {
     using Cfg = KernelCfg<BN, STAGES, PAIR>;
-    const int64_t units = p.num_tiles * p.k_splits;
+    const int64_t units = p.num_units;
     const uint32_t idesc = idesc_bf16_f32(Cfg::TILE_M, BN, p.a_mn_major, p.b_mn_major);
     int stage = 0, acc = 0;
     uint32_t phase = 0, acc_phase = 0;
     bool ok = true, issued_any = false;
     for (int64_t u = first_unit<PAIR>(); u < units && ok; u += unit_stride<PAIR>()) {
         const Unit w = map_unit<Cfg::TILE_M, BN>(p, u);
-        const int kb0 = w.split * p.kb_per_split;
-        const int kb1 = min(p.kb_total, kb0 + p.kb_per_split);
+        const int kb0 = w.kb0;
+        const int kb1 = w.kb1;
         const uint32_t acc_empty = bar0 + 8u * (2 * STAGES + 2 + acc);
         if (!wait_one<PAIR == 2>(acc_empty, acc_phase ^ 1u, abort_flag, p.timeout_ns)) {
             ok = false;
@@ -445,12 +524,16 @@ __device__ __forceinline__ void run_mma(const GemmParams &p, uint32_t ring, uint
 }
 
 template <int BN, int STAGES, int PAIR>
-__device__ __forceinline__ void run_epilogue(const GemmParams &p, uint32_t bar0, uint32_t tmem_base, float *stage_buf,
-                                             uint32_t rank, volatile int *abort_flag, int warp, int lane)
+__device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUtensorMap *tmP, const GemmParams &p,
+                                             uint32_t bar0,
+                                             uint32_t tmem_base, float *stage_buf, uint32_t rank,
+                                             volatile int *abort_flag, int warp, int lane)
 {
     using Cfg = KernelCfg<BN, STAGES, PAIR>;
-    const int64_t units = p.num_tiles * p.k_splits;
+    const int64_t units = p.num_units;
     const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31 are this warp's rows
+    const int half = (warp - 2) >> 2;  // which of the two warps on this quadrant: even or odd chunks
+    const bool beta_nonzero = p.beta != 0.0f;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int64_t u = first_unit<PAIR>(); u < units; u += unit_stride<PAIR>()) {
@@ -460,14 +543,83 @@ __device__ __forceinline__ void run_epilogue(const GemmParams &p, uint32_t bar0,
             break;
         }
         tc_fence_after_sync();
+        const bool use_beta_fast = beta_nonzero && w.slot < 0;
+        // split units: this CTA's rows of the tile's fp32 partial slot
+        float *slot_rows = w.slot < 0 ? nullptr
+                                      : p.partial + w.slot * static_cast<int64_t>(Cfg::TILE_M * BN) +
+                                            static_cast<int64_t>(rank * CTA_M + quad * 32) * BN;
         const int64_t row0 = w.tm * Cfg::TILE_M + rank * CTA_M + quad * 32;
         const int64_t col0 = w.tn * BN;
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN);
+        const bool to_slot = w.slot >= 0;
+        if (to_slot ? p.store_p_tma : p.store_c_tma) {
+            // Chunks of 128 bytes per row (64 bf16 or 32 fp32 columns), 32 rows: each lane
+            // converts its row into a 128B-swizzled staging block, one lane stores it with
+            // TMA, into C (the map clips rows >= m and columns >= n) or into the unit's
+            // fp32 partial slot.
+            const CUtensorMap *map = to_slot ? tmP : tmC;
+            const bool bf16_out = !to_slot && p.c_bf16;
+            const int cw = bf16_out ? 64 : 32;
+            const int nchunks = BN / cw;
+            const uint32_t stage_addr = smem_addr(stage_buf);
+            const int64_t slot_row = to_slot ? w.slot * Cfg::TILE_M + rank * CTA_M + quad * 32 : 0;
+            for (int c = half; c < nchunks; c += 2) {
+                uint32_t r[64];
+                tmem_load_32cols(taddr + static_cast<uint32_t>(c * cw), *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+                if (bf16_out)
+                    tmem_load_32cols(taddr + static_cast<uint32_t>(c * cw + 32),
+                                     *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+                if (c + 2 >= nchunks) {  // this warp's last chunk of the tile: release the accumulator
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) {
+                        const uint32_t acc_empty = bar0 + 8u * (2 * STAGES + 2 + acc);
+                        if constexpr (PAIR == 1) mbar_arrive(acc_empty);
+                        else mbar_arrive_remote(map_shared_to_rank(acc_empty, 0));
+                    }
+                }
+                if (lane == 0) bulk_wait_group_read0();  // the previous store has read the staging block
+                __syncwarp();
+                uint4 *srow = reinterpret_cast<uint4 *>(stage_buf) + lane * 8;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    uint4 q;
+                    if (bf16_out) {
+                        __nv_bfloat162 h[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            h[e] = __floats2bfloat162_rn(p.alpha * __uint_as_float(r[8 * j + 2 * e]),
+                                                         p.alpha * __uint_as_float(r[8 * j + 2 * e + 1]));
+                        q = *reinterpret_cast<const uint4 *>(h);
+                    } else {
+                        q = make_uint4(__float_as_uint(p.alpha * __uint_as_float(r[4 * j + 0])),
+                                       __float_as_uint(p.alpha * __uint_as_float(r[4 * j + 1])),
+                                       __float_as_uint(p.alpha * __uint_as_float(r[4 * j + 2])),
+                                       __float_as_uint(p.alpha * __uint_as_float(r[4 * j + 3])));
+                    }
+                    srow[j ^ (lane & 7)] = q;
+                }
+                fence_proxy_async_shared();
+                __syncwarp();
+                if (lane == 0) {
+                    if (to_slot) {
+                        tma_store_2d(map, stage_addr, c * cw, static_cast<int32_t>(slot_row));
+                        bulk_commit_group();
+                    } else {
+                        const int64_t cx = col0 + static_cast<int64_t>(c) * cw;
+                        if (row0 < p.m && cx < p.n) {
+                            tma_store_2d(map, stage_addr, static_cast<int32_t>(cx), static_cast<int32_t>(row0));
+                            bulk_commit_group();
+                        }
+                    }
+                }
+            }
+        } else {
 #pragma unroll 1
-        for (int ch = 0; ch < BN / 32; ++ch) {
+        for (int ch = half; ch < BN / 32; ch += 2) {
             uint32_t r[32];
             tmem_load_32cols(taddr + 32u * ch, r);
-            if (ch == BN / 32 - 1) {  // accumulator fully read: hand it back to the MMA warp
+            if (ch >= BN / 32 - 2) {  // this warp's last chunk: its part of the accumulator is read
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) {
@@ -486,35 +638,69 @@ __device__ __forceinline__ void run_epilogue(const GemmParams &p, uint32_t bar0,
                                 p.alpha * __uint_as_float(r[4 * c + 2]), p.alpha * __uint_as_float(r[4 * c + 3]));
             __syncwarp();
             // Coalesced pass: 8 lanes cover one 32-column row segment, 4 rows per step.
+            // With beta != 0 the old C values of all 8 steps are loaded first, so the
+            // loads are in flight together instead of one load latency per step.
+            const int cc = lane & 7;
+            const int64_t gj0 = col0 + ch * 32 + cc * 4;
+            uint4 old[8];
+            if (use_beta_fast) {
+#pragma unroll
+                for (int step = 0; step < 8; ++step) {
+                    const int64_t gi = row0 + step * 4 + (lane >> 3);
+                    old[step] = make_uint4(0u, 0u, 0u, 0u);
+                    if (!full_vector(p, gi, gj0)) continue;
+                    if (p.c_bf16) {
+                        const uint2 o = *reinterpret_cast<const uint2 *>(
+                            reinterpret_cast<const __nv_bfloat16 *>(p.C) + gi * p.ldc + gj0);
+                        old[step].x = o.x;
+                        old[step].y = o.y;
+                    } else {
+                        old[step] = *reinterpret_cast<const uint4 *>(reinterpret_cast<const float *>(p.C) +
+                                                                      gi * p.ldc + gj0);
+                    }
+                }
+            }
 #pragma unroll
             for (int step = 0; step < 8; ++step) {
                 const int rr = step * 4 + (lane >> 3);
-                const int cc = lane & 7;
                 const float4 v4 = reinterpret_cast<const float4 *>(stage_buf + rr * 32)[cc ^ (rr & 7)];
                 const int64_t gi = row0 + rr;
-                const int64_t gj = col0 + ch * 32 + cc * 4;
-                if (gi >= p.m || gj >= p.n) continue;
-                float v[4] = {v4.x, v4.y, v4.z, v4.w};
-                if (p.k_splits > 1) {
-                    float *dst = p.partial + (static_cast<int64_t>(w.split) * p.m + gi) * p.ldp + gj;
-                    *reinterpret_cast<float4 *>(dst) = v4;
-                } else {
-                    write_c4(p, gi, gj, v);
+                if (slot_rows != nullptr) {  // whole tile row segment, edges included
+                    *reinterpret_cast<float4 *>(slot_rows + rr * BN + ch * 32 + cc * 4) = v4;
+                } else if (full_vector(p, gi, gj0)) {
+                    float v[4] = {v4.x, v4.y, v4.z, v4.w};
+                    if (use_beta_fast) {
+                        write_c4_preloaded(p, gi, gj0, v, old[step]);
+                    } else if (p.c_bf16) {
+                        const __nv_bfloat162 r01 = __floats2bfloat162_rn(v[0], v[1]);
+                        const __nv_bfloat162 r23 = __floats2bfloat162_rn(v[2], v[3]);
+                        uint2 out;
+                        out.x = *reinterpret_cast<const uint32_t *>(&r01);
+                        out.y = *reinterpret_cast<const uint32_t *>(&r23);
+                        *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(p.C) + gi * p.ldc + gj0) = out;
+                    } else {
+                        *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.C) + gi * p.ldc + gj0) = v4;
+                    }
+                } else if (gi < p.m && gj0 < p.n) {
+                    write_c4_edge(p, gi, gj0, v4);
                 }
             }
             __syncwarp();
+        }
         }
         if (++acc == 2) {
             acc = 0;
             acc_phase ^= 1u;
         }
     }
+    if ((p.store_c_tma || p.store_p_tma) && lane == 0) bulk_wait_group0();  // stores done before exit
 }
 
 // ---------------------------------------------------------------- kernels
 template <int BN, int STAGES, int PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     bm_gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                           const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmP,
                            const GemmParams p)
 {
     using Cfg = KernelCfg<BN, STAGES, PAIR>;
@@ -548,6 +734,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_map(&tmA);
         tma_prefetch_map(&tmB);
+        if (p.prefetch_c || p.store_c_tma) tma_prefetch_map(&tmC);
+        if (p.store_p_tma) tma_prefetch_map(&tmP);
     }
     if (warp == 1) {
         if constexpr (PAIR == 1) {
@@ -565,11 +753,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t tmem_base = *tmem_slot;
 
     if (warp == 0) {
-        if (lane == 0) run_producer<BN, STAGES, PAIR>(&tmA, &tmB, p, ring, bar0, rank, abort_flag);
+        if (lane == 0) run_producer<BN, STAGES, PAIR>(&tmA, &tmB, &tmC, p, ring, bar0, rank, abort_flag);
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) run_mma<BN, STAGES, PAIR>(p, ring, bar0, tmem_base, abort_flag);
     } else {
-        run_epilogue<BN, STAGES, PAIR>(p, bar0, tmem_base, epi + (warp - 2) * EPI_WARP_FLOATS, rank, abort_flag,
+        run_epilogue<BN, STAGES, PAIR>(&tmC, &tmP, p, bar0, tmem_base, epi + (warp - 2) * EPI_WARP_FLOATS, rank,
+                                       abort_flag,
                                        warp, lane);
     }
 
@@ -584,20 +773,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
 }
 
-// Sum of the K-split partials in split order, then beta * C, cast and masked store.
+// Split tiles: sum of the K-split partial slots in split order, then beta * C,
+// cast and masked store. TM x BN is the tile of the kernel that wrote them.
+template <int TM, int BN>
 __global__ void __launch_bounds__(256) bm_splitk_reduce_kernel(const GemmParams p)
 {
-    const int64_t cols4 = (p.n + 3) / 4;
-    const int64_t total = p.m * cols4;
-    const int64_t plane = p.m * p.ldp;
+    const int64_t split_tiles = p.num_tiles - p.full_tiles;
+    const int64_t per_tile = static_cast<int64_t>(TM) * (BN / 4);
+    const int64_t total = split_tiles * per_tile;
+    const int64_t slot_elems = static_cast<int64_t>(TM) * BN;
     for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
          idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t i = idx / cols4;
-        const int64_t j = (idx - i * cols4) * 4;
-        const float *src = p.partial + i * p.ldp + j;
+        const int64_t local = idx / per_tile;
+        const int64_t rem = idx - local * per_tile;
+        const int r = static_cast<int>(rem / (BN / 4));
+        const int c = static_cast<int>(rem - static_cast<int64_t>(r) * (BN / 4)) * 4;
+        int64_t tm, tn;
+        tile_coords<TM, BN>(p, p.full_tiles + local, tm, tn);
+        const int64_t i = tm * TM + r;
+        const int64_t j = tn * BN + c;
+        if (i >= p.m || j >= p.n) continue;
+        const float *src = p.partial + local * p.k_splits * slot_elems + static_cast<int64_t>(r) * BN + c;
         float4 s = *reinterpret_cast<const float4 *>(src);
         for (int sp = 1; sp < p.k_splits; ++sp) {
-            const float4 t = *reinterpret_cast<const float4 *>(src + sp * plane);
+            const float4 t = *reinterpret_cast<const float4 *>(src + sp * slot_elems);
             s.x += t.x;
             s.y += t.y;
             s.z += t.z;

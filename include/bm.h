@@ -80,10 +80,13 @@ typedef enum { BM_LOWER = 0, BM_UPPER = 1 } bm_uplo;
  *   column n within ldc are never touched.
  *
  *   workspace / workspace_bytes: optional caller-owned device scratch for
- *   splitting K across CTAs when m*n is too small to fill the GPU. NULL/0
- *   disables the split; the result is correct either way. The size the
- *   planner would like is bm_gemm_bf16_workspace_size(); less is accepted
- *   (fewer splits). The workspace must be 256-byte aligned.
+ *   FP32 partial sums when tiles are split along K: all tiles when m*n is too
+ *   small to fill the GPU, or the tiles of a last, partly filled wave of the
+ *   persistent schedule (then the idle SMs share them). NULL/0 disables the
+ *   split; the result is correct either way. The size the planner would like
+ *   is bm_gemm_bf16_workspace_size(); less is accepted (fewer or no splits).
+ *   The workspace must be 256-byte aligned; its contents need not be
+ *   initialised and are overwritten.
  *
  *   Returns BM_OK once the work is queued on `stream`.
  */
@@ -186,10 +189,12 @@ BM_API const char *bm_status_string(bm_status status);
 /*
  * Resolved launch plan of a GEMM or SYRK, for reports and tests: output tile
  * (tile_m x tile_n, k-block tile_k), ring stages, number of output tiles
- * visited, K splits, CTAs launched, CTAs per output tile (2 = an SM pair
- * working on one tile), and the number of kernels one call launches.
- * Performs the same size checks as the call (no pointers are given). On a
- * machine without a usable GPU the plan assumes 152 SMs.
+ * visited, K splits and how many tiles are split (the tiles of a last, partly
+ * filled wave, or all tiles when there are too few to fill the GPU), CTAs
+ * launched, CTAs per output tile (2 = an SM pair working on one tile), and
+ * the number of kernels one call launches. Performs the same size checks as
+ * the call (no pointers are given). On a machine without a usable GPU the
+ * plan assumes 152 SMs.
  */
 typedef struct {
     int32_t tile_m, tile_n, tile_k;
@@ -200,6 +205,7 @@ typedef struct {
     int32_t cta_pair;
     int32_t kernels;
     size_t workspace_bytes;
+    int64_t split_tiles;
 } bm_plan;
 
 BM_API bm_status bm_gemm_bf16_plan(int64_t m, int64_t n, int64_t k, size_t workspace_bytes, bm_plan *plan);

@@ -132,8 +132,36 @@ def test_gemm_plans(lib):
     st, p = bm.bm_gemm_bf16_plan(512, 512, 8192, need // 2)      # less workspace: fewer splits
     assert 1 <= p.k_splits < bm.bm_gemm_bf16_plan(512, 512, 8192, need)[1].k_splits
     assert p.workspace_bytes <= need // 2
+    # short K: not worth a second kernel
+    assert bm.bm_gemm_bf16_workspace_size(512, 512, 1024) == 0
     st, p = bm.bm_gemm_bf16_plan(64, 64, 0, 0)
     assert st == 0 and p.kernels == 1 and p.tiles == 0
+
+
+def test_tail_split_plans(lib):
+    # 4096^3 on SM pairs: 256 tiles = 3 full waves of 76 + 28; the 28 are split in two along K
+    need = bm.bm_gemm_bf16_workspace_size(4096, 4096, 4096)
+    assert need == 2 * 28 * 256 * 256 * 4
+    p = bm.bm_gemm_bf16_plan(4096, 4096, 4096, need)[1]
+    assert (p.split_tiles, p.k_splits, p.kernels, p.ctas) == (28, 2, 2, 152)
+    # no workspace: whole tiles only
+    p = bm.bm_gemm_bf16_plan(4096, 4096, 4096, 0)[1]
+    assert (p.split_tiles, p.k_splits, p.kernels) == (0, 1, 1)
+    # dX 2048x5120x5120: 160 tiles = 2 waves + 8; split 8 ways within the 16 MiB tail budget
+    p = bm.bm_gemm_bf16_plan(2048, 5120, 5120, 1 << 30)[1]
+    assert (p.split_tiles, p.k_splits) == (8, 8) and p.workspace_bytes <= 16 << 20
+    # a short K saves too little mainloop time to pay for the extra reduce
+    p = bm.bm_gemm_bf16_plan(5120, 5120, 2048, 1 << 30)[1]     # 400 tiles = 5 waves + 20
+    assert p.split_tiles == 0 and p.k_splits == 1
+    p = bm.bm_gemm_bf16_plan(5120, 5120, 4096, 1 << 30)[1]
+    assert p.split_tiles == 20 and p.k_splits == 3
+    p = bm.bm_gemm_bf16_plan(4096, 4096, 1024, 1 << 30)[1]
+    assert p.split_tiles == 0
+    # a last wave more than half full is not split
+    p = bm.bm_gemm_bf16_plan(8192, 8192 - 1024, 4096, 1 << 30)[1]  # 32 x 28 = 896 tiles = 11 waves + 60
+    assert p.split_tiles == 0 and p.k_splits == 1
+    # SYRK never splits
+    assert bm.bm_syrk_bf16_plan(bm.BM_LOWER, 8192, 4096)[1].k_splits == 1
     assert bm.bm_gemm_bf16_plan(-1, 4, 4, 0)[0] == bm.BM_ERR_INVALID_VALUE
 
 

@@ -184,6 +184,30 @@ def test_split_k_matches_oracle_and_is_deterministic(variant):
     assert_parity(plain[rows, cols], ref, bound, 1.0, 0.0, None, False, "no split")
 
 
+@pytest.mark.parametrize("variant", [0, 1], ids=["auto", "single128x256"])
+def test_tail_split_exact_and_deterministic(variant):
+    """The tiles of a partly filled last wave are split along K over the idle SMs."""
+    import blas3_tensor_core_gb300 as bm
+    t = torch()
+    m, n, k = 2560, 2048, 3072  # SM pairs: 80 tiles = 76 + 4; single SMs: 160 tiles = 152 + 8
+    A, B = _operands(m, n, k, 0, 0, "int", seed=81, lo=-8, hi=8)
+    c0 = gen.integers(83, m * n, -100, 100).reshape(m, n).astype(np.float32)
+    with tile_variant(variant):
+        need = bm.bm_gemm_bf16_workspace_size(m, n, k)
+        plan = bm.bm_gemm_bf16_plan(m, n, k, need)[1]
+        assert plan.split_tiles > 0 and plan.k_splits > 1 and plan.kernels == 2
+        ws = t.empty(need // 4, dtype=t.float32, device="cuda")
+        outs = []
+        for _ in range(2):
+            cbuf = CBuffer(m, n, n, False, init=c0)
+            got, raw = run_gemm(m, n, k, 0, 0, 1.0, A, B, -1.0, cbuf, workspace=ws)
+            cbuf.assert_guard_intact(raw)
+            outs.append(got)
+    assert np.array_equal(outs[0], outs[1])
+    ref, _ = orc().gemm(m, n, k, 0, 0, 1.0, A, B, -1.0, c0)
+    assert np.array_equal(outs[0], ref)
+
+
 # ----------------------------------------------------------------------------- persistence
 @pytest.mark.parametrize("variant", [0, 1], ids=["auto", "single128x256"])
 def test_persistent_many_tiles_exact(variant):

@@ -66,7 +66,7 @@ def _noalloc(m, n, k, dA, dB, lda, ldb, alpha, beta, c_init, bf16):
 
 def test_split_k_without_allocation_matches_workspace_path_twice():
     import blas3_tensor_core_gb300 as bm
-    m, n, k = 512, 520, 8192
+    m, n, k = 512, 520, 2048
     st, plan = bm.bm_gemm_bf16_plan(m, n, k, bm.bm_gemm_bf16_workspace_size(m, n, k))
     assert plan.k_splits > 1 and plan.workspace_bytes <= bm.BM_NOALLOC_SCRATCH_BYTES
     # two calls in a row, on different inputs: the second must not see the first's partials
