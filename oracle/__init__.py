@@ -11,7 +11,8 @@ Acceptance rule (per output element):
                + 2^-8 * |ref|                     (BF16 output: one rounding)
                + 2^-20 * |beta * C_in|            (FP32 combine of beta * C)
 
-``bound = sum_p |op(A)[i][p] * op(B)[p][j]|``. The first term is the stated
+``bound = sum_p |op(A)[i][p] * op(B)[p][j]|`` (for SYR2K the sum runs over both
+products). The first term is the stated
 tolerance for a k-term FP32 accumulation; the second is the unit roundoff of a
 round-to-nearest-even cast to bfloat16; the third covers the few FP32
 operations of the alpha/beta combine (unit roundoff 2^-24 each), which the
@@ -20,8 +21,9 @@ first term omits when alpha*bound is small next to beta*C.
 Parity unpinned: none. Every function here is pinned by the tests in
 ``tests/test_oracle_pins.py`` (brute force in exact integer arithmetic,
 closed forms, NumPy float64 matmul, and the invariants A*I = A,
-(A*B)^T = B^T*A^T, SYRK = one triangle of GEMM(A, A^T), beta-accumulation
-= sum of two beta=0 calls).
+(A*B)^T = B^T*A^T, SYRK = one triangle of GEMM(A, A^T), SYR2K = one triangle of
+GEMM(A, B^T) + GEMM(B, A^T), SYR2K(A, A) = 2 SYRK(A), beta-accumulation = sum of
+two beta=0 calls).
 """
 
 from __future__ import annotations
@@ -81,7 +83,13 @@ class Oracle:
         lib.oracle_syrk_entries.argtypes = [_c_int, _c_int, _c_i64, _c_dbl, _c_vp, _c_i64,
                                             _c_dbl, _c_vp, _c_i64, _c_int, _c_i64, _c_vp,
                                             _c_vp, _c_vp, _c_vp]
-        for fn in ("oracle_gemm", "oracle_gemm_entries", "oracle_syrk", "oracle_syrk_entries"):
+        lib.oracle_syr2k.argtypes = [_c_int, _c_int, _c_i64, _c_i64, _c_dbl, _c_vp, _c_i64, _c_vp, _c_i64,
+                                     _c_dbl, _c_vp, _c_i64, _c_int, _c_vp, _c_vp, _c_i64]
+        lib.oracle_syr2k_entries.argtypes = [_c_int, _c_int, _c_i64, _c_dbl, _c_vp, _c_i64, _c_vp, _c_i64,
+                                             _c_dbl, _c_vp, _c_i64, _c_int, _c_i64, _c_vp, _c_vp, _c_vp,
+                                             _c_vp]
+        for fn in ("oracle_gemm", "oracle_gemm_entries", "oracle_syrk", "oracle_syrk_entries",
+                   "oracle_syr2k", "oracle_syr2k_entries"):
             getattr(lib, fn).restype = None
         self._lib = lib
 
@@ -171,6 +179,34 @@ class Oracle:
                                       A.shape[1], float(beta), self._ptr(Cin), ldc, cbf,
                                       rows.shape[0], rows.ctypes.data, cols.ctypes.data,
                                       ref.ctypes.data, bound.ctypes.data)
+        return ref, bound
+
+
+    # -- SYR2K ---------------------------------------------------------------
+    def syr2k(self, uplo, trans, n, k, alpha, A, B, beta=0.0, C=None):
+        """Full n x n result of alpha*(op(A) op(B)^T + op(B) op(A)^T) + beta*C; NaN off the triangle."""
+        A = self._bf16(A)
+        B = self._bf16(B)
+        Cin, ldc, cbf = self._cin(C, beta)
+        ref = np.empty((n, n), dtype=np.float64)
+        bound = np.empty((n, n), dtype=np.float64)
+        self._lib.oracle_syr2k(int(uplo), int(trans), n, k, float(alpha), A.ctypes.data, A.shape[1],
+                               B.ctypes.data, B.shape[1], float(beta), self._ptr(Cin), ldc, cbf,
+                               ref.ctypes.data, bound.ctypes.data, n)
+        return ref, bound
+
+    def syr2k_entries(self, uplo, trans, k, alpha, A, B, rows, cols, beta=0.0, C=None):
+        A = self._bf16(A)
+        B = self._bf16(B)
+        Cin, ldc, cbf = self._cin(C, beta)
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        cols = np.ascontiguousarray(cols, dtype=np.int64)
+        ref = np.empty(rows.shape[0], dtype=np.float64)
+        bound = np.empty(rows.shape[0], dtype=np.float64)
+        self._lib.oracle_syr2k_entries(int(uplo), int(trans), k, float(alpha), A.ctypes.data, A.shape[1],
+                                       B.ctypes.data, B.shape[1], float(beta), self._ptr(Cin), ldc, cbf,
+                                       rows.shape[0], rows.ctypes.data, cols.ctypes.data,
+                                       ref.ctypes.data, bound.ctypes.data)
         return ref, bound
 
 

@@ -15,6 +15,10 @@
  *   SYRK:  C[i][j] = alpha * sum_p op(A)[i][p] * op(A)[j][p] + beta * C[i][j]
  *          for (i, j) in one triangle of the n x n matrix C; op(A) is n x k
  *          ("SYRK main compute done with a GEMM", BLASMp notes, stage B).
+ *   SYR2K: C[i][j] = alpha * (sum_p op(A)[i][p] * op(B)[j][p]
+ *                             + sum_p op(B)[i][p] * op(A)[j][p]) + beta * C[i][j]
+ *          on one triangle; op(A), op(B) are n x k (the SYR2K operator of
+ *          BLASMp notes, stage D; the BLAS rank-2k update).
  *
  * Alongside each value the oracle returns bound[i][j] = sum_p |product|, the
  * scale against which the tolerance max|C - C_ref| <= 1e-3 * |alpha| * bound
@@ -102,6 +106,28 @@ static void syrk_element(int64_t i, int64_t j, int64_t k, int trans, double alph
     *bound = mag;
 }
 
+/* One output element of SYR2K: the two products of rows i and j of op(A), op(B). */
+static void syr2k_element(int64_t i, int64_t j, int64_t k, int trans, double alpha, const uint16_t *A,
+                          int64_t lda, const uint16_t *B, int64_t ldb, double beta, const void *C,
+                          int64_t ldc, int c_is_bf16, double *ref, double *bound)
+{
+    double ab = 0.0, ba = 0.0, mag = 0.0;
+    if (alpha != 0.0) {
+        for (int64_t p = 0; p < k; ++p) {
+            double x = op_at(A, lda, trans, i, p) * op_at(B, ldb, trans, j, p);
+            double y = op_at(B, ldb, trans, i, p) * op_at(A, lda, trans, j, p);
+            ab += x;
+            ba += y;
+            mag += fabs(x) + fabs(y);
+        }
+    }
+    double value = alpha * (ab + ba);
+    if (beta != 0.0)
+        value += beta * c_input(C, ldc, c_is_bf16, i, j);
+    *ref = value;
+    *bound = mag;
+}
+
 /* Is (i, j) in the referenced triangle? uplo 0 = lower (i >= j), 1 = upper (i <= j). */
 static int in_triangle(int uplo, int64_t i, int64_t j)
 {
@@ -171,6 +197,42 @@ void oracle_syrk_entries(int uplo, int trans, int64_t k, double alpha, const uin
         if (in_triangle(uplo, rows[t], cols[t])) {
             syrk_element(rows[t], cols[t], k, trans, alpha, A, lda, beta, C, ldc, c_is_bf16,
                          &ref[t], &bound[t]);
+        } else {
+            ref[t] = NAN;
+            bound[t] = NAN;
+        }
+    }
+}
+
+/* Full SYR2K: entries outside the triangle are set to NaN (not referenced). */
+void oracle_syr2k(int uplo, int trans, int64_t n, int64_t k, double alpha, const uint16_t *A,
+                  int64_t lda, const uint16_t *B, int64_t ldb, double beta, const void *C,
+                  int64_t ldc, int c_is_bf16, double *ref, double *bound, int64_t ldr)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < n; ++i)
+        for (int64_t j = 0; j < n; ++j) {
+            if (in_triangle(uplo, i, j)) {
+                syr2k_element(i, j, k, trans, alpha, A, lda, B, ldb, beta, C, ldc, c_is_bf16,
+                              &ref[i * ldr + j], &bound[i * ldr + j]);
+            } else {
+                ref[i * ldr + j] = NAN;
+                bound[i * ldr + j] = NAN;
+            }
+        }
+}
+
+/* SYR2K at chosen positions; positions outside the triangle give NaN. */
+void oracle_syr2k_entries(int uplo, int trans, int64_t k, double alpha, const uint16_t *A,
+                          int64_t lda, const uint16_t *B, int64_t ldb, double beta, const void *C,
+                          int64_t ldc, int c_is_bf16, int64_t count, const int64_t *rows,
+                          const int64_t *cols, double *ref, double *bound)
+{
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t t = 0; t < count; ++t) {
+        if (in_triangle(uplo, rows[t], cols[t])) {
+            syr2k_element(rows[t], cols[t], k, trans, alpha, A, lda, B, ldb, beta, C, ldc,
+                          c_is_bf16, &ref[t], &bound[t]);
         } else {
             ref[t] = NAN;
             bound[t] = NAN;

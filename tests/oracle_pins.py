@@ -7,6 +7,8 @@ oracle disagrees with
 * NumPy's float64 matmul on the decoded operands (a library routine),
 * closed forms (ones, rank one, identity),
 * the invariants (A*B)^T = B^T*A^T, SYRK = one triangle of GEMM(A, A^T),
+  SYR2K = one triangle of GEMM(A, B^T) + GEMM(B, A^T), SYR2K(A, A) = 2 SYRK(A),
+  SYR2K(A, B) = SYR2K(B, A),
   beta=1 accumulation = C0 + a beta=0 call, exact power-of-two alpha scaling,
 * the BLAS conventions for alpha = 0, beta = 0 and k = 0.
 
@@ -90,6 +92,27 @@ def pin_syrk_bruteforce_exact(o):
                     assert bound[i, j] == sum(abs(int(opA[i, p]) * int(opA[j, p])) for p in range(k))
 
 
+def pin_syr2k_bruteforce_exact(o):
+    for (n, k), uplo, trans in itertools.product([(1, 1), (5, 3), (6, 7)], (0, 1), (0, 1)):
+        A, Av = _int_bf16(_stored(n, k, trans), 300 + n + 10 * k + 100 * uplo + 1000 * trans, pad=2)
+        B, Bv = _int_bf16(_stored(n, k, trans), 301 + n + 10 * k + 100 * uplo + 1000 * trans, pad=1)
+        opA, opB = _op(Av, trans), _op(Bv, trans)
+        Cv = gen.integers(57, n * n, -8, 8).reshape(n, n)
+        for alpha, beta in [(Fraction(1), Fraction(0)), (Fraction(-1, 2), Fraction(1)), (Fraction(3), Fraction(-2))]:
+            ref, bound = o.syr2k(uplo, trans, n, k, float(alpha), A, B, float(beta), Cv.astype(np.float32))
+            for i in range(n):
+                for j in range(n):
+                    inside = (i >= j) if uplo == 0 else (i <= j)
+                    if not inside:
+                        assert np.isnan(ref[i, j]) and np.isnan(bound[i, j])
+                        continue
+                    s2 = sum(Fraction(int(opA[i, p])) * int(opB[j, p]) + Fraction(int(opB[i, p])) * int(opA[j, p])
+                             for p in range(k))
+                    assert Fraction(ref[i, j]) == alpha * s2 + beta * int(Cv[i, j]), (n, k, uplo, trans, i, j)
+                    assert bound[i, j] == sum(abs(int(opA[i, p]) * int(opB[j, p])) + abs(int(opB[i, p]) * int(opA[j, p]))
+                                              for p in range(k))
+
+
 # --- NumPy float64 matmul ------------------------------------------------------
 def pin_gemm_matches_numpy(o):
     m, n, k = 37, 29, 53
@@ -119,6 +142,23 @@ def pin_syrk_matches_numpy(o):
         scale = 1.5 * (np.abs(a) @ np.abs(a).T) + 0.5 * np.abs(C)
         assert np.all(np.abs(ref[mask] - want[mask]) <= 1e-13 * scale[mask]), (uplo, trans)
         assert np.all(np.isnan(ref[~mask])), (uplo, trans)
+
+
+def pin_syr2k_matches_numpy(o):
+    n, k = 21, 33
+    for uplo, trans in itertools.product((0, 1), (0, 1)):
+        A = gen.matrix_bf16(*_stored(n, k, trans), "normal", seed=141 + trans)
+        B = gen.matrix_bf16(*_stored(n, k, trans), "normal", seed=151 + trans)
+        C = gen.symmetric_f32(n, seed=161)
+        a = _op(gen.bf16_bits_to_f32(A).astype(np.float64), trans)
+        b = _op(gen.bf16_bits_to_f32(B).astype(np.float64), trans)
+        want = -0.5 * (a @ b.T + b @ a.T) + 2.0 * C.astype(np.float64)
+        ref, bound = o.syr2k(uplo, trans, n, k, -0.5, A, B, 2.0, C)
+        mask = np.tril(np.ones((n, n), bool)) if uplo == 0 else np.triu(np.ones((n, n), bool))
+        mag = np.abs(a) @ np.abs(b).T + np.abs(b) @ np.abs(a).T
+        assert np.all(np.abs(ref[mask] - want[mask]) <= 1e-13 * (0.5 * mag[mask] + 2.0 * np.abs(C[mask])))
+        assert np.allclose(bound[mask], mag[mask], rtol=1e-13, atol=0)
+        assert np.all(np.isnan(ref[~mask]))
 
 
 # --- closed forms -----------------------------------------------------------------
@@ -176,6 +216,27 @@ def pin_syrk_is_gemm_triangle(o):
         for uplo, mask in ((0, low), (1, low.T)):
             s, sb = o.syrk(uplo, trans, n, k, 1.0, A)
             assert np.array_equal(s[mask], g[mask]) and np.array_equal(sb[mask], gb[mask]), (uplo, trans)
+
+
+def pin_syr2k_invariants(o):
+    n, k = 19, 24
+    low = np.tril(np.ones((n, n), bool))
+    for trans in (0, 1):
+        A = gen.matrix_bf16(*_stored(n, k, trans), "normal", seed=171)
+        B = gen.matrix_bf16(*_stored(n, k, trans), "normal", seed=172)
+        s2, b2 = o.syr2k(0, trans, n, k, 1.0, A, B)
+        # one triangle of GEMM(A, B^T) + GEMM(B, A^T)
+        g1, gb1 = o.gemm(n, n, k, trans, 1 - trans, 1.0, A, B)
+        g2, gb2 = o.gemm(n, n, k, trans, 1 - trans, 1.0, B, A)
+        assert np.array_equal(s2[low], (g1 + g2)[low]) and np.array_equal(b2[low], (gb1 + gb2)[low])
+        # swapping the operands changes nothing
+        t2, _ = o.syr2k(0, trans, n, k, 1.0, B, A)
+        assert np.array_equal(s2[low], t2[low])
+        # SYR2K(A, A) = 2 SYRK(A)
+        d2, db = o.syr2k(1, trans, n, k, 0.75, A, A)
+        sy, sb = o.syrk(1, trans, n, k, 0.75, A)
+        up = low.T
+        assert np.array_equal(d2[up], 2.0 * sy[up]) and np.array_equal(db[up], 2.0 * sb[up])
 
 
 def pin_beta_accumulation(o):
@@ -241,6 +302,11 @@ def pin_entries_agree(o):
         full, _ = o.syrk(uplo, 0, m, k, 1.0, As, 1.0, Cs)
         e, _ = o.syrk_entries(uplo, 0, k, 1.0, As, rows, r2, 1.0, Cs)
         assert np.array_equal(e, full[rows, r2], equal_nan=True)
+        Bs = gen.matrix_bf16(m, k, "normal", seed=116)
+        full2, fb2 = o.syr2k(uplo, 0, m, k, 0.5, As, Bs, 1.0, Cs)
+        e2, eb2 = o.syr2k_entries(uplo, 0, k, 0.5, As, Bs, rows, r2, 1.0, Cs)
+        assert np.array_equal(e2, full2[rows, r2], equal_nan=True)
+        assert np.array_equal(eb2, fb2[rows, r2], equal_nan=True)
 
 
 PINS = [
@@ -248,6 +314,9 @@ PINS = [
     pin_syrk_bruteforce_exact,
     pin_gemm_matches_numpy,
     pin_syrk_matches_numpy,
+    pin_syr2k_bruteforce_exact,
+    pin_syr2k_matches_numpy,
+    pin_syr2k_invariants,
     pin_identity,
     pin_closed_forms,
     pin_transpose_identity,

@@ -35,6 +35,13 @@ MUTANTS = [
     ("alpha_zero_reads_a", "if (alpha != 0.0) {\n        for", "{\n        for", 0),
     ("bf16_c_misread", "return bf16_value(((const uint16_t *)C)[i * ldc + j]);",
      "return (double)((const float *)C)[i * ldc + j];", 0),
+    ("syr2k_drop_second_product", "ba += y;", "ba += 0.0 * y;", 0),
+    ("syr2k_same_operand_twice", "op_at(A, lda, trans, i, p) * op_at(B, ldb, trans, j, p)",
+     "op_at(A, lda, trans, i, p) * op_at(A, lda, trans, j, p)", 0),
+    ("syr2k_mirrored_second_product", "op_at(B, ldb, trans, i, p) * op_at(A, lda, trans, j, p)",
+     "op_at(A, lda, trans, i, p) * op_at(B, ldb, trans, j, p)", 0),
+    ("syr2k_drop_beta", "value += beta * c_input", "value += 0.0 * c_input", 2),
+    ("syr2k_signed_bound", "mag += fabs(x) + fabs(y);", "mag += fabs(x) + y;", 0),
     ("gemm_last_column_skipped", "for (int64_t j = 0; j < n; ++j)\n            gemm_element",
      "for (int64_t j = 0; j + 1 < n; ++j)\n            gemm_element", 0),
 ]
