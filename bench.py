@@ -339,6 +339,36 @@ def timed_steps(wl, steps, warmup, dist, sampler=None):
     return dist.max(ev0.elapsed_time(ev1))
 
 
+def graph_steps(wl, steps):
+    """Device time (ms) per call when `steps` calls are captured in one CUDA graph and replayed."""
+    t = wl.t
+    side = t.cuda.Stream()
+    side.wait_stream(t.cuda.current_stream())
+    with t.cuda.stream(side):  # first-call set-up (device state, attributes) happens outside capture
+        wl.call(0, side.cuda_stream)
+    t.cuda.current_stream().wait_stream(side)
+    t.cuda.synchronize()
+    g = t.cuda.CUDAGraph()
+    with t.cuda.graph(g):
+        h = t.cuda.current_stream().cuda_stream
+        for i in range(steps):
+            wl.call(i, h)
+    g.replay()
+    t.cuda.synchronize()
+    ev0, ev1 = t.cuda.Event(enable_timing=True), t.cuda.Event(enable_timing=True)
+    stream = t.cuda.current_stream()
+    ev0.record(stream)
+    g.replay()
+    ev1.record(stream)
+    t.cuda.synchronize()
+    st = wl.bm.bm_get_last_device_error(stream.cuda_stream)
+    if st != 0:
+        raise RuntimeError(f"device error: {wl.bm.bm_status_string(st)}")
+    ms = ev0.elapsed_time(ev1) / steps
+    del g
+    return ms
+
+
 def e2e_steps(wl, steps, warmup, dist):
     """Same call with pinned host inputs: H2D of A and B and D2H of C inside the timed region."""
     import numpy as np
@@ -500,6 +530,7 @@ def run_gpu_arm(args, dist):
                 "kernel": (f"bm_gemm_tcgen05_kernel<{wl.plan.tile_n},{wl.plan.stages},{wl.plan.cta_pair}>"
                            + (" + bm_splitk_reduce_kernel" if wl.plan.kernels > 1 else "")),
                 "traffic_source": traffic_src}
+    graph_ms = graph_steps(wl, min(args.steps, 200))
     e2e_ms, h2d, d2h, _ = e2e_steps(wl, args.e2e_steps, max(3, args.warmup // 10), dist)
     e2e = {"value": round(dist.world * wl.flops() * args.e2e_steps / (e2e_ms * 1e-3) / 1e12, 3), "unit": UNIT,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
@@ -514,15 +545,20 @@ def run_gpu_arm(args, dist):
             gbs = sw.bytes() / t_launch / 1e9
             bound = "tensor" if sw.flops() / (peaks["bf16_tflops"] * 1e12) >= sw.bytes() / (peaks["hbm_gbs"] * 1e9) \
                 else "hbm"
+            g_launch = graph_steps(sw, min(args.sweep_steps, 100)) * 1e-3
             sweep.append({"workload": cfg["name"], "us_per_step": round(t_launch * 1e6, 3),
                           "tflops": round(tf, 2), "gbs": round(gbs, 1),
                           "frac_tensor": round(tf / peaks["bf16_tflops"], 4),
                           "frac_hbm": round(gbs / peaks["hbm_gbs"], 4), "bound": bound,
-                          "k_splits": sw.plan.k_splits, "tiles": sw.plan.tiles})
+                          "us_per_step_graph": round(g_launch * 1e6, 3),
+                          "tflops_graph": round(sw.flops() / g_launch / 1e12, 2),
+                          "k_splits": sw.plan.k_splits, "tiles": sw.plan.tiles,
+                          "tile": f"{sw.plan.tile_m}x{sw.plan.tile_n}"})
             del sw
             torch.cuda.empty_cache()
         if args.all_configs:
             sweep.append(syrk_point(args, dist, peaks))
+            sweep.append(syrk_point(args, dist, peaks, two_products=True))
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline_leg(wl, args.cpu_budget_s)
@@ -535,12 +571,17 @@ def run_gpu_arm(args, dist):
         "dtype": "bf16", "data": "synthetic", "config": main_config(wl),
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": args.steps * wl.plan.kernels, "clocks": clocks,
-        "frac_of_peak": round(achieved / peaks["bf16_tflops"], 4), "sweep": sweep,
+        "frac_of_peak": round(achieved / peaks["bf16_tflops"], 4),
+        "graph": {"us_per_step": round(graph_ms * 1e3, 3),
+                  "value": round(dist.world * wl.flops() / (graph_ms * 1e-3) / 1e12, 3), "unit": UNIT,
+                  "note": f"{min(args.steps, 200)} calls captured in one CUDA graph, one replay timed"},
+        "sweep": sweep,
     }
     return line
 
 
-def syrk_point(args, dist, peaks):
+def syrk_point(args, dist, peaks, two_products=False):
+    """SYRK lower 8192 x 4096 (fp32 C, beta = 1), or SYR2K of the same size with a second operand."""
     import numpy as np
     import torch
     import bm_inputs as gen
@@ -549,27 +590,34 @@ def syrk_point(args, dist, peaks):
     A = gen.matrix_bf16(n, k, "normal", seed=1)
     C0 = gen.symmetric_f32(n, seed=3)
     dA = torch.from_numpy(A.view(np.int16)).view(torch.bfloat16).cuda()
+    dB = torch.from_numpy(gen.matrix_bf16(n, k, "normal", seed=2).view(np.int16)).view(torch.bfloat16).cuda() \
+        if two_products else dA
     dCs = [torch.from_numpy(C0).cuda() for _ in range(2)]
-    h = torch.cuda.current_stream().cuda_stream
 
     class W:
         t = torch
-        bm = None
 
         def call(self, i, hh):
-            st = bm.bm_syrk_bf16(0, 0, n, k, 1.0, dA.data_ptr(), k, 1.0, dCs[i % 2].data_ptr(), n, 0, hh)
+            if two_products:
+                st = bm.bm_syr2k_bf16(0, 0, n, k, 1.0, dA.data_ptr(), k, dB.data_ptr(), k, 1.0, dCs[i % 2].data_ptr(),
+                                      n, 0, hh)
+            else:
+                st = bm.bm_syrk_bf16(0, 0, n, k, 1.0, dA.data_ptr(), k, 1.0, dCs[i % 2].data_ptr(), n, 0, hh)
             if st != 0:
                 raise RuntimeError(bm.bm_status_string(st))
     w = W()
     w.bm = bm
-    ms = timed_steps(w, args.sweep_steps // 4 + 1, 3, dist)
-    t_launch = ms / (args.sweep_steps // 4 + 1) * 1e-3
-    fl, by = syrk_flops(n, k), syrk_bytes(n, k, 4, 1.0)
-    return {"workload": SYRK_CFG["name"], "us_per_step": round(t_launch * 1e6, 3),
+    steps = args.sweep_steps // 4 + 1
+    ms = timed_steps(w, steps, 3, dist)
+    t_launch = ms / steps * 1e-3
+    mult = 2 if two_products else 1
+    fl, by = mult * syrk_flops(n, k), syrk_bytes(n, k, 4, 1.0) + (2 * n * k if two_products else 0)
+    name = SYRK_CFG["name"] if not two_products else "syr2k_lower_8192x4096_f32c_beta1"
+    return {"workload": name, "us_per_step": round(t_launch * 1e6, 3),
             "tflops": round(fl / t_launch / 1e12, 2), "gbs": round(by / t_launch / 1e9, 1),
             "frac_tensor": round(fl / t_launch / 1e12 / peaks["bf16_tflops"], 4),
             "frac_hbm": round(by / t_launch / 1e9 / peaks["hbm_gbs"], 4), "bound": "tensor",
-            "flops_convention": "n(n+1)k (lower triangle incl. diagonal)"}
+            "flops_convention": f"{mult} n(n+1)k (lower triangle incl. diagonal)"}
 
 
 def parse_args(argv=None):

@@ -19,9 +19,9 @@ __all__ = [
     "BM_OK", "BM_ERR_INVALID_VALUE", "BM_ERR_MISALIGNED", "BM_ERR_ARCH", "BM_ERR_CUDA",
     "BM_ERR_TIMEOUT", "BM_ERR_WORKSPACE", "BM_OP_N", "BM_OP_T", "BM_C_F32", "BM_C_BF16",
     "BM_LOWER", "BM_UPPER", "Plan",
-    "bm_gemm_bf16", "bm_gemm_bf16_noalloc", "BM_NOALLOC_SCRATCH_BYTES", "bm_syrk_bf16", "bm_gemm_bf16_workspace_size", "bm_get_last_device_error",
+    "bm_gemm_bf16", "bm_gemm_bf16_noalloc", "BM_NOALLOC_SCRATCH_BYTES", "bm_syrk_bf16", "bm_syr2k_bf16", "bm_gemm_bf16_workspace_size", "bm_get_last_device_error",
     "bm_set_wait_timeout_ms", "bm_debug_inject_stall", "bm_status_string", "bm_gemm_bf16_plan",
-    "bm_syrk_bf16_plan", "bm_set_tile_override", "bm_version", "gemm", "syrk", "workspace_size",
+    "bm_syrk_bf16_plan", "bm_set_tile_override", "bm_version", "gemm", "syrk", "syr2k", "workspace_size",
 ]
 
 BM_OK, BM_ERR_INVALID_VALUE, BM_ERR_MISALIGNED, BM_ERR_ARCH, BM_ERR_CUDA, BM_ERR_TIMEOUT, BM_ERR_WORKSPACE = range(7)
@@ -74,6 +74,9 @@ def library():
                 lib.bm_syrk_bf16.argtypes = [_i32, _i32, _i64, _i64, _f32, _vp, _i64, _f32, _vp, _i64,
                                              _i32, _vp]
                 lib.bm_syrk_bf16.restype = _i32
+                lib.bm_syr2k_bf16.argtypes = [_i32, _i32, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp,
+                                              _i64, _i32, _vp]
+                lib.bm_syr2k_bf16.restype = _i32
                 lib.bm_gemm_bf16_workspace_size.argtypes = [_i64, _i64, _i64]
                 lib.bm_gemm_bf16_workspace_size.restype = _sz
                 lib.bm_get_last_device_error.argtypes = [_vp]
@@ -116,6 +119,10 @@ def bm_gemm_bf16_noalloc(m, n, k, transA, transB, alpha, A, lda, B, ldb, beta, C
 
 def bm_syrk_bf16(uplo, trans, n, k, alpha, A, lda, beta, C, ldc, c_type, stream=None) -> int:
     return library().bm_syrk_bf16(uplo, trans, n, k, alpha, A, lda, beta, C, ldc, c_type, stream)
+
+
+def bm_syr2k_bf16(uplo, trans, n, k, alpha, A, lda, B, ldb, beta, C, ldc, c_type, stream=None) -> int:
+    return library().bm_syr2k_bf16(uplo, trans, n, k, alpha, A, lda, B, ldb, beta, C, ldc, c_type, stream)
 
 
 def bm_gemm_bf16_workspace_size(m, n, k) -> int:
@@ -209,6 +216,27 @@ def gemm(A, B, C, alpha=1.0, beta=0.0, transA=False, transB=False, workspace=Non
                       float(beta), C.data_ptr(), _rowmajor_ld(C, "C"), _ctype(C),
                       ws_ptr, ws_bytes, _stream_handle(stream))
     _check(st, "bm_gemm_bf16")
+    return C
+
+
+def syr2k(A, B, C, alpha=1.0, beta=0.0, uplo="L", trans=False, stream=None):
+    """One triangle of C = alpha * (op(A) op(B)^T + op(B) op(A)^T) + beta * C (row-major, bf16 A, B)."""
+    import torch
+    if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16:
+        raise TypeError("A and B must be bfloat16")
+    if A.shape != B.shape:
+        raise ValueError("A and B must have the same shape")
+    n = C.shape[0]
+    if C.shape[1] != n:
+        raise ValueError("C must be square")
+    k = A.shape[0] if trans else A.shape[1]
+    if (A.shape[1] if trans else A.shape[0]) != n:
+        raise ValueError("inconsistent shapes")
+    lo = BM_LOWER if str(uplo).upper().startswith("L") else BM_UPPER
+    st = bm_syr2k_bf16(lo, int(bool(trans)), n, k, float(alpha), A.data_ptr(), _rowmajor_ld(A, "A"),
+                       B.data_ptr(), _rowmajor_ld(B, "B"), float(beta), C.data_ptr(), _rowmajor_ld(C, "C"),
+                       _ctype(C), _stream_handle(stream))
+    _check(st, "bm_syr2k_bf16")
     return C
 
 

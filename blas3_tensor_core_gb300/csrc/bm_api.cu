@@ -314,18 +314,23 @@ Plan plan_gemm(int64_t m, int64_t n, int64_t k, size_t ws_bytes, int sms, int pa
     return pl;
 }
 
-Plan plan_syrk(int mode, int64_t n, int64_t k, int sms, int pair_clusters)
+// SYRK / SYR2K: tiles touching the triangle. SYR2K runs both products through
+// one accumulator, and its A and B maps serve in both operand roles, so it
+// needs the variants whose A and B tiles have the same 128 rows.
+Plan plan_syrk(int mode, int64_t n, int64_t k, int sms, int pair_clusters, bool two_products = false)
 {
     Plan pl;
     const int64_t tiles = ceil_div(n, 256);
-    const int forced = g_tile_override.load() - 1;
+    const int single = two_products ? kSingle128 : kSingle256;
+    int forced = g_tile_override.load() - 1;
+    if (two_products && forced == kSingle256) forced = kSingle128;
     if (forced >= 0 && (forced != kPair256 || pair_clusters > 0)) set_variant(pl, forced);
-    else set_variant(pl, (pair_clusters > 0 && tiles * (tiles + 1) / 2 * 2 >= pair_clusters) ? kPair256 : kSingle256);
+    else set_variant(pl, (pair_clusters > 0 && tiles * (tiles + 1) / 2 * 2 >= pair_clusters) ? kPair256 : single);
     pl.tiles_m = ceil_div(n, pl.tile_m);
     pl.tiles_n = ceil_div(n, pl.bn);
     pl.num_tiles = syrk_tile_count(mode, pl.tiles_m, pl.tiles_n, pl.tile_m, pl.bn);
     pl.full_tiles = pl.num_tiles;
-    pl.kb_total = static_cast<int>(ceil_div(std::max<int64_t>(k, 1), bm::TILE_K));
+    pl.kb_total = static_cast<int>(ceil_div(std::max<int64_t>(k, 1), bm::TILE_K)) * (two_products ? 2 : 1);
     pl.kb_per_split = pl.kb_total;
     size_grid(pl, sms, pair_clusters);
     return pl;
@@ -357,18 +362,22 @@ bm_status launch(const Plan &pl, const CUtensorMap &ta, const CUtensorMap &tb, b
         prm.store_p_tma = 1;
     if (pl.ctas <= 0) return BM_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cfg.gridDim = dim3(static_cast<unsigned>(pl.ctas), 1, 1);
     cfg.blockDim = dim3(bm::NUM_THREADS, 1, 1);
     cfg.dynamicSmemBytes = static_cast<size_t>(variant_smem(pl.variant));
     cfg.stream = stream;
+    cfg.attrs = attr;
+    // programmatic dependent launch: the kernel's set-up may overlap the previous kernel's tail
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 1;
     if (pl.pair == 2) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = 2;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
     }
     cudaError_t err;
     switch (pl.variant) {
@@ -387,10 +396,24 @@ bm_status launch(const Plan &pl, const CUtensorMap &ta, const CUtensorMap &tb, b
     if (prm.k_splits > 1) {
         const int64_t work = (prm.num_tiles - prm.full_tiles) * pl.tile_m * (pl.bn / 4);
         const int blocks = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(ceil_div(work, 256), 8 * 152)));
+        cudaLaunchConfig_t rc = {};
+        cudaLaunchAttribute ra[1];
+        ra[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        ra[0].val.programmaticStreamSerializationAllowed = 1;
+        rc.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+        rc.blockDim = dim3(256, 1, 1);
+        rc.stream = stream;
+        rc.attrs = ra;
+        rc.numAttrs = 1;
+        cudaError_t re;
         switch (pl.variant) {
-        case kSingle256: bm::bm_splitk_reduce_kernel<128, 256><<<blocks, 256, 0, stream>>>(prm); break;
-        case kSingle128: bm::bm_splitk_reduce_kernel<128, 128><<<blocks, 256, 0, stream>>>(prm); break;
-        default: bm::bm_splitk_reduce_kernel<256, 256><<<blocks, 256, 0, stream>>>(prm); break;
+        case kSingle256: re = cudaLaunchKernelEx(&rc, bm::bm_splitk_reduce_kernel<128, 256>, prm); break;
+        case kSingle128: re = cudaLaunchKernelEx(&rc, bm::bm_splitk_reduce_kernel<128, 128>, prm); break;
+        default: re = cudaLaunchKernelEx(&rc, bm::bm_splitk_reduce_kernel<256, 256>, prm); break;
+        }
+        if (re != cudaSuccess) {
+            cudaGetLastError();
+            return BM_ERR_CUDA;
         }
         if (cudaGetLastError() != cudaSuccess) return BM_ERR_CUDA;
     }
@@ -401,8 +424,20 @@ bm_status launch_scale(bm::GemmParams &prm, cudaStream_t stream)
 {
     const int64_t work = prm.m * ceil_div(prm.n, 4);
     const int blocks = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(ceil_div(work, 256), 8 * 152)));
-    bm::bm_scale_kernel<<<blocks, 256, 0, stream>>>(prm);
-    return cudaGetLastError() == cudaSuccess ? BM_OK : BM_ERR_CUDA;
+    cudaLaunchConfig_t rc = {};
+    cudaLaunchAttribute ra[1];
+    ra[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    ra[0].val.programmaticStreamSerializationAllowed = 1;
+    rc.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+    rc.blockDim = dim3(256, 1, 1);
+    rc.stream = stream;
+    rc.attrs = ra;
+    rc.numAttrs = 1;
+    if (cudaLaunchKernelEx(&rc, bm::bm_scale_kernel, prm) != cudaSuccess) {
+        cudaGetLastError();
+        return BM_ERR_CUDA;
+    }
+    return BM_OK;
 }
 
 void fill_params(bm::GemmParams &prm, const Plan &pl)
@@ -676,6 +711,45 @@ bm_status bm_syrk_bf16(bm_uplo uplo, bm_op trans, int64_t n, int64_t k, float al
     prm.a_mn_major = mn;
     prm.b_mn_major = mn;
     fill_params(prm, pl);
+    return launch(pl, ta, tb, prm, cs);
+}
+
+bm_status bm_syr2k_bf16(bm_uplo uplo, bm_op trans, int64_t n, int64_t k, float alpha, const void *A, int64_t lda,
+                        const void *B, int64_t ldb, float beta, void *C, int64_t ldc, bm_ctype c_type,
+                        bm_stream_t stream)
+{
+    if (uplo != BM_LOWER && uplo != BM_UPPER) return BM_ERR_INVALID_VALUE;
+    if (n < 0 || k < 0 || !fits_int32(n) || !fits_int32(k)) return BM_ERR_INVALID_VALUE;
+    if (trans != BM_OP_N && trans != BM_OP_T) return BM_ERR_INVALID_VALUE;
+    if (c_type != BM_C_F32 && c_type != BM_C_BF16) return BM_ERR_INVALID_VALUE;
+    const int64_t need = trans == BM_OP_N ? k : n;
+    if (lda < std::max<int64_t>(1, need) || ldb < std::max<int64_t>(1, need) || ldc < std::max<int64_t>(1, n))
+        return BM_ERR_INVALID_VALUE;
+    if (n == 0) return BM_OK;
+    const bool products = alpha != 0.0f && k > 0;
+    if (C == nullptr || (products && (A == nullptr || B == nullptr))) return BM_ERR_INVALID_VALUE;
+    const int64_t esz = c_type == BM_C_BF16 ? 2 : 4;
+    if (!aligned16(C) || (ldc * esz) % 16 != 0) return BM_ERR_MISALIGNED;
+    if (products && (!aligned16(A) || !aligned16(B) || (lda * 2) % 16 != 0 || (ldb * 2) % 16 != 0))
+        return BM_ERR_MISALIGNED;
+    DeviceState *st = nullptr;
+    bm_status s = device_state(&st);
+    if (s != BM_OK) return s;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    bm::GemmParams prm = base_params(n, n, k, alpha, beta, C, ldc, c_type, st);
+    prm.mode = uplo == BM_LOWER ? bm::MODE_SYRK_LOWER : bm::MODE_SYRK_UPPER;
+    if (!products) return launch_scale(prm, cs);
+
+    const Plan pl = plan_syrk(prm.mode, n, k, st->sm_count, st->max_pair_clusters, true);
+    CUtensorMap ta, tb;
+    const bool mn = trans == BM_OP_T;  // A, B stored [k][n]: both operands are M/N-major
+    // Both maps serve as the A operand (128 rows) and the B operand (bn / pair = 128 rows).
+    if (!encode_operand(&ta, A, mn, n, k, lda, bm::CTA_M)) return BM_ERR_CUDA;
+    if (!encode_operand(&tb, B, mn, n, k, ldb, bm::CTA_M)) return BM_ERR_CUDA;
+    prm.a_mn_major = mn;
+    prm.b_mn_major = mn;
+    fill_params(prm, pl);
+    prm.syr2k_kb = pl.kb_total / 2;
     return launch(pl, ta, tb, prm, cs);
 }
 

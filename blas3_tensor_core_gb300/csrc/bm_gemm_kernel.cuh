@@ -87,6 +87,7 @@ struct GemmParams {
     int debug_stall;   // test hook: the first stage's copy is never issued
     int prefetch_c;    // beta != 0: tmC maps C for L2 prefetch (box tile columns x 128 rows)
     int store_c_tma;   // beta == 0, GEMM: tmC maps C for TMA stores (box 128 bytes x 32 rows, 128B swizzle)
+    int syr2k_kb;      // SYR2K: k-blocks of one product; later k-blocks swap the roles of tmA and tmB
     int store_p_tma;   // split units: tmP maps the partial slots for TMA stores (fp32, box 32 x 32, 128B swizzle)
 };
 
@@ -403,37 +404,41 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmA, const CUten
             }
             const uint32_t sa = ring + stage * Cfg::STAGE_BYTES;
             const uint32_t sb = sa + Cfg::A_BYTES;
-            const int32_t kx = kb * TILE_K;
+            // SYR2K: the first syr2k_kb k-blocks accumulate op(A) op(B)^T, the rest op(B) op(A)^T
+            const bool swap = p.syr2k_kb > 0 && kb >= p.syr2k_kb;
+            const CUtensorMap *mapA = swap ? tmB : tmA;
+            const CUtensorMap *mapB = swap ? tmA : tmB;
+            const int32_t kx = (swap ? kb - p.syr2k_kb : kb) * TILE_K;
             if (!(p.debug_stall && first)) {
                 issued_any = true;
                 if constexpr (PAIR == 1) {
                     if (p.a_mn_major) {  // A stored [k][m]: two 64-wide chunks along M
-                        tma_load_2d(sa, tmA, full, row_a, kx);
-                        tma_load_2d(sa + 8192, tmA, full, row_a + 64, kx);
+                        tma_load_2d(sa, mapA, full, row_a, kx);
+                        tma_load_2d(sa + 8192, mapA, full, row_a + 64, kx);
                     } else {  // A stored [m][k]: one 64 x 128 box
-                        tma_load_2d(sa, tmA, full, kx, row_a);
+                        tma_load_2d(sa, mapA, full, kx, row_a);
                     }
                     if (p.b_mn_major) {  // B stored [k][n]: chunks of 64 along N
 #pragma unroll
                         for (int c = 0; c < Cfg::B_ROWS / 64; ++c)
-                            tma_load_2d(sb + 8192 * c, tmB, full, row_b + 64 * c, kx);
+                            tma_load_2d(sb + 8192 * c, mapB, full, row_b + 64 * c, kx);
                     } else {  // B stored [n][k]: one 64 x B_ROWS box
-                        tma_load_2d(sb, tmB, full, kx, row_b);
+                        tma_load_2d(sb, mapB, full, kx, row_b);
                     }
                 } else {
                     const uint32_t full0 = map_shared_to_rank(full, 0);  // CTA 0 counts both CTAs' bytes
                     if (p.a_mn_major) {
-                        tma_load_2d_pair(sa, tmA, full0, row_a, kx);
-                        tma_load_2d_pair(sa + 8192, tmA, full0, row_a + 64, kx);
+                        tma_load_2d_pair(sa, mapA, full0, row_a, kx);
+                        tma_load_2d_pair(sa + 8192, mapA, full0, row_a + 64, kx);
                     } else {
-                        tma_load_2d_pair(sa, tmA, full0, kx, row_a);
+                        tma_load_2d_pair(sa, mapA, full0, kx, row_a);
                     }
                     if (p.b_mn_major) {
 #pragma unroll
                         for (int c = 0; c < Cfg::B_ROWS / 64; ++c)
-                            tma_load_2d_pair(sb + 8192 * c, tmB, full0, row_b + 64 * c, kx);
+                            tma_load_2d_pair(sb + 8192 * c, mapB, full0, row_b + 64 * c, kx);
                     } else {
-                        tma_load_2d_pair(sb, tmB, full0, kx, row_b);
+                        tma_load_2d_pair(sb, mapB, full0, kx, row_b);
                     }
                 }
             }
@@ -751,6 +756,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if constexpr (PAIR == 2) cluster_sync();  // peer barriers initialised before any remote arrival
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    // The set-up above overlaps the end of the previous kernel on the stream; no
+    // global memory (A, B, C, workspace) is touched before that kernel is complete.
+    griddep_launch_dependents();
+    griddep_wait();
 
     if (warp == 0) {
         if (lane == 0) run_producer<BN, STAGES, PAIR>(&tmA, &tmB, &tmC, p, ring, bar0, rank, abort_flag);
@@ -778,6 +787,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 template <int TM, int BN>
 __global__ void __launch_bounds__(256) bm_splitk_reduce_kernel(const GemmParams p)
 {
+    griddep_launch_dependents();
+    griddep_wait();  // the partial slots come from the previous kernel
     const int64_t split_tiles = p.num_tiles - p.full_tiles;
     const int64_t per_tile = static_cast<int64_t>(TM) * (BN / 4);
     const int64_t total = split_tiles * per_tile;
@@ -810,6 +821,8 @@ __global__ void __launch_bounds__(256) bm_splitk_reduce_kernel(const GemmParams 
 // alpha == 0 or k == 0: C = beta * C on the output region (C unread when beta == 0).
 __global__ void __launch_bounds__(256) bm_scale_kernel(const GemmParams p)
 {
+    griddep_launch_dependents();
+    griddep_wait();
     const int64_t cols4 = (p.n + 3) / 4;
     const int64_t total = p.m * cols4;
     for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;

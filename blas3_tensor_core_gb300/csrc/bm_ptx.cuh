@@ -62,6 +62,18 @@ __device__ __forceinline__ uint32_t map_shared_to_rank(uint32_t addr, uint32_t r
     return r;
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// Lets the next kernel on the stream (launched with programmatic stream
+// serialisation) be scheduled onto SMs as this grid's CTAs finish.
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Waits until the preceding grid on the stream has completed and its memory
+// operations are visible (returns at once when there is no such dependency).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
 {

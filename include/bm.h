@@ -154,6 +154,23 @@ BM_API bm_status bm_syrk_bf16(bm_uplo uplo, bm_op trans, int64_t n, int64_t k, f
                               bm_ctype c_type, bm_stream_t stream);
 
 /*
+ * SYR2K:  C = alpha * (op(A) * op(B)^T + op(B) * op(A)^T) + beta * C
+ *         on one triangle of C[n x n]
+ *
+ *   The rank-2k update among the BLAS3 operators of "BLASMp development
+ *   notes" (stage D adds SYR2K; stage F restructures it like SYRK). op(A) and
+ *   op(B) are n x k: A, B are stored [n, k] (lda, ldb >= k) when trans ==
+ *   BM_OP_N and [k, n] (lda, ldb >= n) when trans == BM_OP_T. Both products go
+ *   through one FP32 accumulator per tile; uplo, the untouched other
+ *   triangle, C and the error behaviour are as for bm_syrk_bf16.
+ *
+ *   Returns BM_OK once the work is queued on `stream`.
+ */
+BM_API bm_status bm_syr2k_bf16(bm_uplo uplo, bm_op trans, int64_t n, int64_t k, float alpha,
+                               const void *A, int64_t lda, const void *B, int64_t ldb, float beta,
+                               void *C, int64_t ldc, bm_ctype c_type, bm_stream_t stream);
+
+/*
  * Device-side errors. Every wait inside the kernels (on a shared-memory
  * barrier) gives up after the wait limit, records BM_ERR_TIMEOUT in the
  * device status word, frees its tensor memory and returns, so that the CUDA

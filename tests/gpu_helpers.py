@@ -11,7 +11,7 @@ import numpy as np
 import bm_inputs as gen
 import oracle
 
-F32_CANARY = np.uint32(0x7FBADBAD)   # a NaN payload that no computation produces
+F32_CANARY = np.uint32(0x7FFADBAD)   # a quiet-NaN payload that no computation produces
 BF16_CANARY = np.uint16(0x7FBD)
 
 
@@ -128,6 +128,20 @@ def run_syrk(uplo, trans, n, k, alpha, A, beta, cbuf: CBuffer):
     dA = bf16_to_device(A)
     st = bm.bm_syrk_bf16(uplo, trans, n, k, alpha, dA.data_ptr(), A.shape[1], beta, cbuf.ptr, cbuf.ldc,
                          bm.BM_C_BF16 if cbuf.bf16 else bm.BM_C_F32, t.cuda.current_stream().cuda_stream)
+    assert st == bm.BM_OK, bm.bm_status_string(st)
+    t.cuda.synchronize()
+    check_no_device_error()
+    return cbuf.result()
+
+
+def run_syr2k(uplo, trans, n, k, alpha, A, B, beta, cbuf: CBuffer):
+    import blas3_tensor_core_gb300 as bm
+    t = torch()
+    dA = bf16_to_device(A)
+    dB = bf16_to_device(B)
+    st = bm.bm_syr2k_bf16(uplo, trans, n, k, alpha, dA.data_ptr(), A.shape[1], dB.data_ptr(), B.shape[1], beta,
+                          cbuf.ptr, cbuf.ldc, bm.BM_C_BF16 if cbuf.bf16 else bm.BM_C_F32,
+                          t.cuda.current_stream().cuda_stream)
     assert st == bm.BM_OK, bm.bm_status_string(st)
     t.cuda.synchronize()
     check_no_device_error()

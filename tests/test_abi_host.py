@@ -103,6 +103,22 @@ def test_syrk_argument_errors(lib):
     assert s(n=0, ldc=1) == bm.BM_OK
 
 
+def test_syr2k_argument_errors(lib):
+    def s2(uplo=0, trans=0, n=64, k=64, A=0x1000, lda=None, B=0x2000, ldb=None, C=0x3000, ldc=None, ct=0):
+        lda = lda if lda is not None else (n if trans else k)
+        ldb = ldb if ldb is not None else (n if trans else k)
+        ldc = ldc if ldc is not None else n
+        return bm.bm_syr2k_bf16(uplo, trans, n, k, 1.0, A, lda, B, ldb, 1.0, C, ldc, ct, None)
+    assert s2(uplo=2) == bm.BM_ERR_INVALID_VALUE
+    assert s2(trans=3) == bm.BM_ERR_INVALID_VALUE
+    assert s2(k=-1) == bm.BM_ERR_INVALID_VALUE
+    assert s2(ldb=10) == bm.BM_ERR_INVALID_VALUE
+    assert s2(trans=1, lda=16) == bm.BM_ERR_INVALID_VALUE
+    assert s2(B=0) == bm.BM_ERR_INVALID_VALUE
+    assert s2(B=0x2004) == bm.BM_ERR_MISALIGNED
+    assert s2(n=0, ldc=1) == bm.BM_OK
+
+
 @pytest.mark.skipif(__import__("torch").cuda.is_available(), reason="expects a machine without a GPU")
 def test_valid_call_without_gpu_reports_cuda_error(lib):
     assert _gemm() == bm.BM_ERR_CUDA

@@ -208,6 +208,47 @@ def test_tail_split_exact_and_deterministic(variant):
     assert np.array_equal(outs[0], ref)
 
 
+# ----------------------------------------------------------------------------- stream ordering
+@pytest.mark.parametrize("m,n,k", [(2048, 2048, 1024), (512, 512, 8192)], ids=["pair_tiles", "split_k"])
+def test_dependent_calls_back_to_back(m, n, k):
+    """D = A B; D = 2 D (alpha = 0 path); E = D B2 -- queued with no host synchronisation.
+
+    Each kernel starts its set-up while the previous one finishes (programmatic
+    dependent launch) and must still see the previous kernel's complete output.
+    """
+    import blas3_tensor_core_gb300 as bm
+    from gpu_helpers import bf16_to_device, device_to_numpy
+    t = torch()
+    A = operand(m, k, "int", 91, lo=-4, hi=4)
+    B = operand(k, n, "int", 92, lo=-4, hi=4)
+    B2 = operand(n, n, "int", 93, lo=-2, hi=2)
+    dA, dB, dB2 = bf16_to_device(A), bf16_to_device(B), bf16_to_device(B2)
+    dD = t.empty((m, n), dtype=t.float32, device="cuda")
+    dE = t.empty((m, n), dtype=t.float32, device="cuda")
+    need = max(bm.bm_gemm_bf16_workspace_size(m, n, k), bm.bm_gemm_bf16_workspace_size(m, n, n))
+    ws = t.empty(max(need // 4, 64), dtype=t.float32, device="cuda")
+    dDb = t.empty((m, n), dtype=t.bfloat16, device="cuda")
+    h = t.cuda.current_stream().cuda_stream
+    assert bm.bm_gemm_bf16(m, n, k, 0, 0, 1.0, dA.data_ptr(), k, dB.data_ptr(), n, 0.0, dD.data_ptr(), n,
+                           bm.BM_C_F32, ws.data_ptr(), need, h) == bm.BM_OK
+    assert bm.bm_gemm_bf16(m, n, k, 0, 0, 0.0, None, k, None, n, 2.0, dD.data_ptr(), n,
+                           bm.BM_C_F32, None, 0, h) == bm.BM_OK
+    # bf16 copy of D on the same stream (a torch kernel between two of ours)
+    dDb.copy_(dD)
+    assert bm.bm_gemm_bf16(m, n, n, 0, 0, 1.0, dDb.data_ptr(), n, dB2.data_ptr(), n, 0.0, dE.data_ptr(), n,
+                           bm.BM_C_F32, ws.data_ptr(), need, h) == bm.BM_OK
+    t.cuda.synchronize()
+    assert bm.bm_get_last_device_error(h) == bm.BM_OK
+    D = dD.cpu().numpy().astype(np.float64)
+    Db = device_to_numpy(dDb)
+    E = dE.cpu().numpy().astype(np.float64)
+    rows, cols = tile_samples(m, n, per_tile=8, seed=9)
+    refD, _ = orc().gemm_entries(k, 0, 0, 2.0, A, B, rows, cols)
+    assert np.array_equal(D[rows, cols], refD)  # small integers: exact
+    refE, boundE = orc().gemm_entries(n, 0, 0, 1.0, Db, B2, rows, cols)
+    assert_parity(E[rows, cols], refE, boundE, 1.0, 0.0, None, False, "E = D B2")
+
+
 # ----------------------------------------------------------------------------- persistence
 @pytest.mark.parametrize("variant", [0, 1], ids=["auto", "single128x256"])
 def test_persistent_many_tiles_exact(variant):
