@@ -9,7 +9,9 @@ bench. It holds none of the GEMM/SYRK arithmetic: only
 * its mapping to uniform deviates in [0, 1) (top 53 bits) and to normal
   deviates by the Box-Muller transform (cosine branch, element ``i`` uses
   uniforms ``2i`` and ``2i+1``);
-* IEEE round-to-nearest-even from float32 to bfloat16, and back.
+* IEEE round-to-nearest-even from float32 to bfloat16, and back;
+* rounding from float32 to FP8 E4M3 (nearest, ties to even, saturating at
+  448), and back, through the table of the format's 127 finite magnitudes.
 
 The workloads are those of the BF16 GEMM shapes the pages study (square
 4096^3, the K-sweep, the backward dX/dW pair and a lower SYRK): entries are
@@ -35,6 +37,10 @@ __all__ = [
     "symmetric_f32",
     "pad_ld",
     "BF16_NAN",
+    "E4M3_VALUES",
+    "f32_to_e4m3_bits",
+    "e4m3_bits_to_f32",
+    "matrix_e4m3",
 ]
 
 _GOLDEN = np.uint64(0x9E3779B97F4A7C15)
@@ -134,3 +140,49 @@ def pad_ld(mat: np.ndarray, ld: int, fill) -> np.ndarray:
     out[:, :cols] = mat
     out[:, cols:] = fill
     return out
+
+
+# --- FP8 E4M3 (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; no infinities;
+# S.1111.111 is NaN; largest finite magnitude 448) -----------------------------------
+def _e4m3_table() -> np.ndarray:
+    """Value of every non-negative finite code 0x00..0x7E, in code order (increasing)."""
+    vals = []
+    for c in range(0x7F):
+        e, m = c >> 3, c & 7
+        vals.append((m / 8.0) * 2.0 ** -6 if e == 0 else (1.0 + m / 8.0) * 2.0 ** (e - 7))
+    return np.array(vals, dtype=np.float64)
+
+
+E4M3_VALUES = _e4m3_table()
+E4M3_NAN = np.uint8(0x7F)
+
+
+def f32_to_e4m3_bits(x) -> np.ndarray:
+    """Round float32 values to E4M3: nearest representable value, ties to the even
+    code, magnitudes beyond 448 saturate to 448, NaN stays NaN."""
+    f = np.asarray(x, dtype=np.float32).astype(np.float64)
+    a = np.abs(f)
+    hi = np.clip(np.searchsorted(E4M3_VALUES, a, side="left"), 0, len(E4M3_VALUES) - 1)
+    lo = np.clip(hi - 1, 0, len(E4M3_VALUES) - 1)
+    d_hi = np.abs(E4M3_VALUES[hi] - a)
+    d_lo = np.abs(a - E4M3_VALUES[lo])
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & ((hi & 1) == 0))
+    code = np.where(pick_hi, hi, lo).astype(np.uint8)
+    code = np.where(a >= E4M3_VALUES[-1], np.uint8(0x7E), code)  # saturate
+    code = code | np.where(np.signbit(f), np.uint8(0x80), np.uint8(0))
+    return np.where(np.isnan(f), E4M3_NAN, code).astype(np.uint8)
+
+
+def e4m3_bits_to_f32(b) -> np.ndarray:
+    b = np.asarray(b, dtype=np.uint8)
+    mag = E4M3_VALUES[np.minimum(b & 0x7F, 0x7E)]
+    out = np.where((b & 0x80) != 0, -mag, mag)
+    return np.where((b & 0x7F) == 0x7F, np.nan, out).astype(np.float32)
+
+
+def matrix_e4m3(rows: int, cols: int, dist: str = "normal", seed: int = 1, std: float = 1.0,
+                lo: float = -1.0, hi: float = 1.0) -> np.ndarray:
+    """Row-major [rows, cols] E4M3 codes (uint8); the value is drawn in float64, rounded to
+    float32, then to E4M3 (nearest, ties to even, saturating)."""
+    vals = _draw(dist, seed, rows * cols, std, lo, hi)
+    return f32_to_e4m3_bits(vals.astype(np.float32)).reshape(rows, cols)

@@ -88,8 +88,14 @@ class Oracle:
         lib.oracle_syr2k_entries.argtypes = [_c_int, _c_int, _c_i64, _c_dbl, _c_vp, _c_i64, _c_vp, _c_i64,
                                              _c_dbl, _c_vp, _c_i64, _c_int, _c_i64, _c_vp, _c_vp, _c_vp,
                                              _c_vp]
+        lib.oracle_gemm_e4m3.argtypes = [_c_i64, _c_i64, _c_i64, _c_dbl, _c_vp, _c_i64, _c_vp, _c_i64,
+                                         _c_dbl, _c_vp, _c_i64, _c_int, _c_vp, _c_vp, _c_i64]
+        lib.oracle_gemm_e4m3_entries.argtypes = [_c_i64, _c_dbl, _c_vp, _c_i64, _c_vp, _c_i64, _c_dbl,
+                                                 _c_vp, _c_i64, _c_int, _c_i64, _c_vp, _c_vp, _c_vp,
+                                                 _c_vp]
         for fn in ("oracle_gemm", "oracle_gemm_entries", "oracle_syrk", "oracle_syrk_entries",
-                   "oracle_syr2k", "oracle_syr2k_entries"):
+                   "oracle_syr2k", "oracle_syr2k_entries", "oracle_gemm_e4m3",
+                   "oracle_gemm_e4m3_entries"):
             getattr(lib, fn).restype = None
         self._lib = lib
 
@@ -181,6 +187,40 @@ class Oracle:
                                       ref.ctypes.data, bound.ctypes.data)
         return ref, bound
 
+
+    # -- GEMM with FP8 E4M3 operands --------------------------------------------
+    @staticmethod
+    def _e4m3(x: np.ndarray) -> np.ndarray:
+        x = np.ascontiguousarray(x)
+        if x.dtype != np.uint8:
+            raise TypeError("operands must be E4M3 codes (uint8)")
+        return x
+
+    def gemm_e4m3(self, m, n, k, alpha, A, B, beta=0.0, C=None):
+        """Full m x n result of alpha * A B^T + beta * C; A [m, k], B [n, k] E4M3 codes."""
+        A = self._e4m3(A)
+        B = self._e4m3(B)
+        Cin, ldc, cbf = self._cin(C, beta)
+        ref = np.empty((m, n), dtype=np.float64)
+        bound = np.empty((m, n), dtype=np.float64)
+        self._lib.oracle_gemm_e4m3(m, n, k, float(alpha), A.ctypes.data, A.shape[1], B.ctypes.data,
+                                   B.shape[1], float(beta), self._ptr(Cin), ldc, cbf, ref.ctypes.data,
+                                   bound.ctypes.data, n)
+        return ref, bound
+
+    def gemm_e4m3_entries(self, k, alpha, A, B, rows, cols, beta=0.0, C=None):
+        A = self._e4m3(A)
+        B = self._e4m3(B)
+        Cin, ldc, cbf = self._cin(C, beta)
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        cols = np.ascontiguousarray(cols, dtype=np.int64)
+        ref = np.empty(rows.shape[0], dtype=np.float64)
+        bound = np.empty(rows.shape[0], dtype=np.float64)
+        self._lib.oracle_gemm_e4m3_entries(k, float(alpha), A.ctypes.data, A.shape[1], B.ctypes.data,
+                                           B.shape[1], float(beta), self._ptr(Cin), ldc, cbf, rows.shape[0],
+                                           rows.ctypes.data, cols.ctypes.data, ref.ctypes.data,
+                                           bound.ctypes.data)
+        return ref, bound
 
     # -- SYR2K ---------------------------------------------------------------
     def syr2k(self, uplo, trans, n, k, alpha, A, B, beta=0.0, C=None):

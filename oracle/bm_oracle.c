@@ -20,6 +20,11 @@
  *          on one triangle; op(A), op(B) are n x k (the SYR2K operator of
  *          BLASMp notes, stage D; the BLAS rank-2k update).
  *
+ *   GEMM, FP8 E4M3 operands: C[i][j] = alpha * sum_p A[i][p] * B[j][p] + beta * C[i][j]
+ *          with A [m, k] and B [n, k] holding E4M3 codes (the all-E4M3 inputs,
+ *          FP32-accumulated products of the FP8 paths in "fused A2A/GEMM
+ *          Perfetto profile protocol", FP8 section).
+ *
  * Alongside each value the oracle returns bound[i][j] = sum_p |product|, the
  * scale against which the tolerance max|C - C_ref| <= 1e-3 * |alpha| * bound
  * is stated.
@@ -47,6 +52,22 @@ static double bf16_value(uint16_t bits)
     float f;
     memcpy(&f, &word, sizeof f);
     return (double)f;
+}
+
+/* FP8 E4M3 code -> double, exact: 1 sign bit, 4 exponent bits (bias 7), 3
+ * mantissa bits; exponent field 0 is subnormal (m / 8 * 2^-6); S.1111.111 is NaN;
+ * there are no infinities. */
+static double e4m3_value(uint8_t code)
+{
+    int e = (code >> 3) & 0xF, m = code & 7;
+    double mag;
+    if (e == 0xF && m == 7)
+        return NAN;
+    if (e == 0)
+        mag = ldexp((double)m / 8.0, -6);
+    else
+        mag = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return (code & 0x80) ? -mag : mag;
 }
 
 /* Element (r, c) of op(X), X stored row-major with leading dimension ld. */
@@ -95,6 +116,27 @@ static void syrk_element(int64_t i, int64_t j, int64_t k, int trans, double alph
     if (alpha != 0.0) {
         for (int64_t p = 0; p < k; ++p) {
             double prod = op_at(A, lda, trans, i, p) * op_at(A, lda, trans, j, p);
+            acc += prod;
+            mag += fabs(prod);
+        }
+    }
+    double value = alpha * acc;
+    if (beta != 0.0)
+        value += beta * c_input(C, ldc, c_is_bf16, i, j);
+    *ref = value;
+    *bound = mag;
+}
+
+/* One output element of the E4M3 GEMM: row i of A against row j of B. */
+static void gemm_e4m3_element(int64_t i, int64_t j, int64_t k, double alpha, const uint8_t *A,
+                              int64_t lda, const uint8_t *B, int64_t ldb, double beta,
+                              const void *C, int64_t ldc, int c_is_bf16, double *ref,
+                              double *bound)
+{
+    double acc = 0.0, mag = 0.0;
+    if (alpha != 0.0) {
+        for (int64_t p = 0; p < k; ++p) {
+            double prod = e4m3_value(A[i * lda + p]) * e4m3_value(B[j * ldb + p]);
             acc += prod;
             mag += fabs(prod);
         }
@@ -238,4 +280,28 @@ void oracle_syr2k_entries(int uplo, int trans, int64_t k, double alpha, const ui
             bound[t] = NAN;
         }
     }
+}
+
+/* Full E4M3 GEMM C = alpha * A * B^T + beta * C; A [m, k], B [n, k]. */
+void oracle_gemm_e4m3(int64_t m, int64_t n, int64_t k, double alpha, const uint8_t *A, int64_t lda,
+                      const uint8_t *B, int64_t ldb, double beta, const void *C, int64_t ldc,
+                      int c_is_bf16, double *ref, double *bound, int64_t ldr)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < m; ++i)
+        for (int64_t j = 0; j < n; ++j)
+            gemm_e4m3_element(i, j, k, alpha, A, lda, B, ldb, beta, C, ldc, c_is_bf16,
+                              &ref[i * ldr + j], &bound[i * ldr + j]);
+}
+
+/* E4M3 GEMM at chosen positions. */
+void oracle_gemm_e4m3_entries(int64_t k, double alpha, const uint8_t *A, int64_t lda,
+                              const uint8_t *B, int64_t ldb, double beta, const void *C,
+                              int64_t ldc, int c_is_bf16, int64_t count, const int64_t *rows,
+                              const int64_t *cols, double *ref, double *bound)
+{
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t t = 0; t < count; ++t)
+        gemm_e4m3_element(rows[t], cols[t], k, alpha, A, lda, B, ldb, beta, C, ldc, c_is_bf16,
+                          &ref[t], &bound[t]);
 }

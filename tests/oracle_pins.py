@@ -309,6 +309,69 @@ def pin_entries_agree(o):
         assert np.array_equal(eb2, fb2[rows, r2], equal_nan=True)
 
 
+# --- FP8 E4M3 GEMM ---------------------------------------------------------------------
+def _int_e4m3(shape, seed, lo=-8, hi=8, pad=0):
+    vals = gen.integers(seed, shape[0] * shape[1], lo, hi).reshape(shape)
+    codes = gen.f32_to_e4m3_bits(vals)
+    if pad:
+        codes = gen.pad_ld(codes, shape[1] + pad, np.uint8(0x7F))  # NaN padding, never read
+    return codes, vals
+
+
+def pin_e4m3_decode_every_code(o):
+    # 1 x 1 x 1 products with B = 1.0 (code 0x38) decode each A code
+    one = np.full((1, 1), 0x38, np.uint8)
+    for c in range(256):
+        ref, _ = o.gemm_e4m3(1, 1, 1, 1.0, np.full((1, 1), c, np.uint8), one)
+        want = gen.e4m3_bits_to_f32(np.uint8([c]))[0]
+        if np.isnan(want):
+            assert np.isnan(ref[0, 0]), c
+        else:
+            assert ref[0, 0] == want, (hex(c), ref[0, 0], want)
+
+
+def pin_e4m3_bruteforce_exact(o):
+    for (m, n, k) in [(1, 1, 1), (3, 4, 5), (6, 2, 9)]:
+        A, Av = _int_e4m3((m, k), 200 + m, pad=5)
+        B, Bv = _int_e4m3((n, k), 201 + n, pad=3)
+        Cv = gen.integers(202, m * n, -9, 9).reshape(m, n)
+        for alpha, beta in [(Fraction(1), Fraction(0)), (Fraction(-1, 4), Fraction(2))]:
+            ref, bound = o.gemm_e4m3(m, n, k, float(alpha), A, B, float(beta), Cv.astype(np.float32))
+            for i in range(m):
+                for j in range(n):
+                    s2 = sum(int(Av[i, p]) * int(Bv[j, p]) for p in range(k))
+                    assert Fraction(ref[i, j]) == alpha * s2 + beta * int(Cv[i, j]), (m, n, k, i, j)
+                    assert bound[i, j] == sum(abs(int(Av[i, p]) * int(Bv[j, p])) for p in range(k))
+
+
+def pin_e4m3_equals_bf16_gemm_on_same_values(o):
+    # E4M3 values are exact in bf16: the FP8 GEMM must equal the (pinned) bf16 GEMM with op(B) = B^T
+    m, n, k = 23, 19, 41
+    A = gen.matrix_e4m3(m, k, "normal", seed=211, std=4.0)
+    B = gen.matrix_e4m3(n, k, "normal", seed=212, std=0.5)
+    Ab = gen.f32_to_bf16_bits(gen.e4m3_bits_to_f32(A))
+    Bb = gen.f32_to_bf16_bits(gen.e4m3_bits_to_f32(B))
+    C = gen.matrix_f32(m, n, "normal", seed=213)
+    r8, b8 = o.gemm_e4m3(m, n, k, 0.5, A, B, -1.5, C)
+    r16, b16 = o.gemm(m, n, k, 0, 1, 0.5, Ab, Bb, -1.5, C)
+    assert np.array_equal(r8, r16) and np.array_equal(b8, b16)
+    rows = np.arange(m) % m
+    cols = (np.arange(m) * 7) % n
+    e, eb = o.gemm_e4m3_entries(k, 0.5, A, B, rows, cols, -1.5, C)
+    assert np.array_equal(e, r8[rows, cols]) and np.array_equal(eb, b8[rows, cols])
+
+
+def pin_e4m3_matches_numpy(o):
+    m, n, k = 31, 17, 64
+    A = gen.matrix_e4m3(m, k, "normal", seed=221)
+    B = gen.matrix_e4m3(n, k, "uniform", seed=222, lo=-2, hi=2)
+    a = gen.e4m3_bits_to_f32(A).astype(np.float64)
+    b = gen.e4m3_bits_to_f32(B).astype(np.float64)
+    ref, bound = o.gemm_e4m3(m, n, k, 2.0, A, B)
+    assert np.all(np.abs(ref - 2.0 * a @ b.T) <= 1e-13 * 2.0 * (np.abs(a) @ np.abs(b).T))
+    assert np.allclose(bound, np.abs(a) @ np.abs(b).T, rtol=1e-13, atol=0)
+
+
 PINS = [
     pin_gemm_bruteforce_exact,
     pin_syrk_bruteforce_exact,
@@ -325,4 +388,8 @@ PINS = [
     pin_alpha_scaling,
     pin_special_values,
     pin_entries_agree,
+    pin_e4m3_decode_every_code,
+    pin_e4m3_bruteforce_exact,
+    pin_e4m3_equals_bf16_gemm_on_same_values,
+    pin_e4m3_matches_numpy,
 ]

@@ -46,3 +46,25 @@ def test_symmetric_and_padding():
     m = gen.matrix_bf16(4, 5, "uniform", seed=1)
     p = gen.pad_ld(m, 8, gen.BF16_NAN)
     assert p.shape == (4, 8) and np.array_equal(p[:, :5], m) and np.all(p[:, 5:] == gen.BF16_NAN)
+
+
+def test_e4m3_table_and_rounding():
+    v = gen.E4M3_VALUES
+    assert len(v) == 127 and v[0] == 0.0 and v[1] == 2.0 ** -9 and v[8] == 2.0 ** -6 and v[-1] == 448.0
+    assert np.all(np.diff(v) > 0)
+    # integers up to 16 are exact, 17 is a tie between 16 and 18 and goes to the even code (16)
+    ints = np.arange(-16, 17, dtype=np.float32)
+    assert np.array_equal(gen.e4m3_bits_to_f32(gen.f32_to_e4m3_bits(ints)), ints)
+    assert gen.e4m3_bits_to_f32(gen.f32_to_e4m3_bits(np.float32([17.0, 19.0, 1000.0, -1000.0]))).tolist() == \
+        [16.0, 20.0, 448.0, -448.0]
+    # every code decodes and re-encodes to itself (NaN excepted)
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+    back = gen.f32_to_e4m3_bits(gen.e4m3_bits_to_f32(codes))
+    assert np.array_equal(back[codes != 0x80], codes[codes != 0x80])  # -0 may come back as +0 or -0
+    assert np.isnan(gen.e4m3_bits_to_f32(np.uint8([0x7F, 0xFF]))).all()
+    # nearest: random values land on a neighbour within half a spacing
+    x = gen.normal(5, 20000, std=3.0).astype(np.float32)
+    y = gen.e4m3_bits_to_f32(gen.f32_to_e4m3_bits(x)).astype(np.float64)
+    idx = np.searchsorted(v, np.abs(x))
+    gap = v[np.minimum(idx, 126)] - v[np.maximum(idx - 1, 0)]
+    assert np.all(np.abs(np.abs(y) - np.abs(x)) <= gap / 2 + 1e-12)

@@ -42,6 +42,11 @@ MUTANTS = [
      "op_at(A, lda, trans, i, p) * op_at(B, ldb, trans, j, p)", 0),
     ("syr2k_drop_beta", "value += beta * c_input", "value += 0.0 * c_input", 2),
     ("syr2k_signed_bound", "mag += fabs(x) + fabs(y);", "mag += fabs(x) + y;", 0),
+    ("e4m3_bias_off_by_one", "mag = ldexp(1.0 + (double)m / 8.0, e - 7);", "mag = ldexp(1.0 + (double)m / 8.0, e - 8);", 0),
+    ("e4m3_no_subnormals", "mag = ldexp((double)m / 8.0, -6);", "mag = ldexp(1.0 + (double)m / 8.0, -7);", 0),
+    ("e4m3_mantissa_bits", "int e = (code >> 3) & 0xF, m = code & 7;", "int e = (code >> 3) & 0xF, m = code & 3;", 0),
+    ("e4m3_sign_dropped", "return (code & 0x80) ? -mag : mag;", "return mag;", 0),
+    ("e4m3_b_k_reversed", "e4m3_value(B[j * ldb + p])", "e4m3_value(B[j * ldb + (k - 1 - p)])", 0),
     ("gemm_last_column_skipped", "for (int64_t j = 0; j < n; ++j)\n            gemm_element",
      "for (int64_t j = 0; j + 1 < n; ++j)\n            gemm_element", 0),
 ]
