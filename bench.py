@@ -59,6 +59,8 @@ EXTRA = [
          beta=1.0, cbf=True),
     dict(name="gemm_256x256x256_uniform_f32c", m=256, n=256, k=256, ta=0, tb=0, std=None, beta=0.0,
          cbf=False),
+    dict(name="gemm_e4m3_4096x4096x4096_tn_bf16c", m=4096, n=4096, k=4096, ta=0, tb=1, std=1.0, beta=0.0,
+         cbf=True, e4m3=True),
 ]
 SYRK_CFG = dict(name="syrk_lower_8192x4096_f32c_beta1", n=8192, k=4096, beta=1.0)
 
@@ -247,6 +249,8 @@ class Dist:
 def host_inputs(cfg):
     import bm_inputs as gen
     m, n, k, ta, tb = cfg["m"], cfg["n"], cfg["k"], cfg["ta"], cfg["tb"]
+    if cfg.get("e4m3"):  # A [m, k], B [n, k] E4M3 codes, C = A B^T
+        return gen.matrix_e4m3(m, k, "normal", seed=1), gen.matrix_e4m3(n, k, "normal", seed=2), None
     ra, ca = (k, m) if ta else (m, k)
     rb, cb = (n, k) if tb else (k, n)
     if cfg["std"] is None:
@@ -271,23 +275,29 @@ class GemmWorkload:
         self.t = t
         A, B, C0 = host_inputs(cfg)
         self.A_host, self.B_host, self.C0_host = A, B, C0
-        dA = t.from_numpy(A.view(np.int16)).view(t.bfloat16).cuda()
-        dB = t.from_numpy(B.view(np.int16)).view(t.bfloat16).cuda()
+        self.e4m3 = bool(cfg.get("e4m3"))
+        if self.e4m3:
+            dA = t.from_numpy(A).cuda()
+            dB = t.from_numpy(B).cuda()
+        else:
+            dA = t.from_numpy(A.view(np.int16)).view(t.bfloat16).cuda()
+            dB = t.from_numpy(B.view(np.int16)).view(t.bfloat16).cuda()
         cdt = t.bfloat16 if cfg["cbf"] else t.float32
         m, n = cfg["m"], cfg["n"]
         dC = t.empty((m, n), dtype=cdt, device="cuda")
         if C0 is not None:
             dC.copy_(t.from_numpy(C0.view(np.int16)).view(t.bfloat16).to(cdt))
-        per_set = dA.numel() * 2 + dB.numel() * 2 + dC.numel() * dC.element_size()
+        per_set = dA.numel() * dA.element_size() + dB.numel() * dB.element_size() + dC.numel() * dC.element_size()
         nsets = max(2, min(max_sets, -(-min_total // per_set)))
         self.sets = [(dA, dB, dC)] + [(dA.clone(), dB.clone(), dC.clone()) for _ in range(nsets - 1)]
         self.set_bytes = per_set
         import blas3_tensor_core_gb300 as bm
         self.bm = bm
-        need = bm.bm_gemm_bf16_workspace_size(m, n, cfg["k"])
+        need = (bm.bm_gemm_e4m3_workspace_size if self.e4m3 else bm.bm_gemm_bf16_workspace_size)(m, n, cfg["k"])
         self.ws = t.empty(max(need // 4, 1), dtype=t.float32, device="cuda") if need else None
         self.ws_bytes = need
-        st, self.plan = bm.bm_gemm_bf16_plan(m, n, cfg["k"], need)
+        # the plan of an E4M3 GEMM equals that of a bf16 GEMM with half the K (same bytes per k-block)
+        st, self.plan = bm.bm_gemm_bf16_plan(m, n, cfg["k"] // 2 if self.e4m3 else cfg["k"], need)
         assert st == 0
         self.lda = A.shape[1]
         self.ldb = B.shape[1]
@@ -295,6 +305,14 @@ class GemmWorkload:
     def call(self, i, stream_handle):
         c = self.cfg
         dA, dB, dC = self.sets[i % len(self.sets)]
+        if self.e4m3:
+            st = self.bm.bm_gemm_e4m3(c["m"], c["n"], c["k"], 1.0, dA.data_ptr(), self.lda, dB.data_ptr(), self.ldb,
+                                      c["beta"], dC.data_ptr(), c["n"],
+                                      self.bm.BM_C_BF16 if c["cbf"] else self.bm.BM_C_F32,
+                                      None if self.ws is None else self.ws.data_ptr(), self.ws_bytes, stream_handle)
+            if st != 0:
+                raise RuntimeError(f"bm_gemm_e4m3: {self.bm.bm_status_string(st)}")
+            return
         st = self.bm.bm_gemm_bf16(c["m"], c["n"], c["k"], c["ta"], c["tb"], 1.0, dA.data_ptr(), self.lda,
                                   dB.data_ptr(), self.ldb, c["beta"], dC.data_ptr(), c["n"],
                                   self.bm.BM_C_BF16 if c["cbf"] else self.bm.BM_C_F32,
@@ -308,7 +326,8 @@ class GemmWorkload:
 
     def bytes(self):
         c = self.cfg
-        return gemm_bytes(c["m"], c["n"], c["k"], 2 if c["cbf"] else 4, c["beta"])
+        b = gemm_bytes(c["m"], c["n"], c["k"], 2 if c["cbf"] else 4, c["beta"])
+        return b - (c["m"] * c["k"] + c["k"] * c["n"]) if self.e4m3 else b  # 1-byte operands
 
 
 def timed_steps(wl, steps, warmup, dist, sampler=None):
@@ -543,12 +562,13 @@ def run_gpu_arm(args, dist):
             t_launch = sms / args.sweep_steps * 1e-3
             tf = sw.flops() / t_launch / 1e12
             gbs = sw.bytes() / t_launch / 1e9
-            bound = "tensor" if sw.flops() / (peaks["bf16_tflops"] * 1e12) >= sw.bytes() / (peaks["hbm_gbs"] * 1e9) \
-                else "hbm"
+            # FP8 tensor peak: the measured bf16 peak times the nominal FP8 / BF16 ratio (4.5 / 2.25 PF)
+            tpeak = peaks["bf16_tflops"] * (2.0 if sw.e4m3 else 1.0)
+            bound = "tensor" if sw.flops() / (tpeak * 1e12) >= sw.bytes() / (peaks["hbm_gbs"] * 1e9) else "hbm"
             g_launch = graph_steps(sw, min(args.sweep_steps, 100)) * 1e-3
             sweep.append({"workload": cfg["name"], "us_per_step": round(t_launch * 1e6, 3),
                           "tflops": round(tf, 2), "gbs": round(gbs, 1),
-                          "frac_tensor": round(tf / peaks["bf16_tflops"], 4),
+                          "frac_tensor": round(tf / tpeak, 4),
                           "frac_hbm": round(gbs / peaks["hbm_gbs"], 4), "bound": bound,
                           "us_per_step_graph": round(g_launch * 1e6, 3),
                           "tflops_graph": round(sw.flops() / g_launch / 1e12, 2),

@@ -19,7 +19,8 @@ __all__ = [
     "BM_OK", "BM_ERR_INVALID_VALUE", "BM_ERR_MISALIGNED", "BM_ERR_ARCH", "BM_ERR_CUDA",
     "BM_ERR_TIMEOUT", "BM_ERR_WORKSPACE", "BM_OP_N", "BM_OP_T", "BM_C_F32", "BM_C_BF16",
     "BM_LOWER", "BM_UPPER", "Plan",
-    "bm_gemm_bf16", "bm_gemm_bf16_noalloc", "BM_NOALLOC_SCRATCH_BYTES", "bm_syrk_bf16", "bm_syr2k_bf16", "bm_gemm_bf16_workspace_size", "bm_get_last_device_error",
+    "bm_gemm_bf16", "bm_gemm_bf16_noalloc", "BM_NOALLOC_SCRATCH_BYTES", "bm_syrk_bf16", "bm_syr2k_bf16",
+    "bm_gemm_e4m3", "bm_gemm_e4m3_workspace_size", "bm_gemm_bf16_workspace_size", "bm_get_last_device_error",
     "bm_set_wait_timeout_ms", "bm_debug_inject_stall", "bm_status_string", "bm_gemm_bf16_plan",
     "bm_syrk_bf16_plan", "bm_set_tile_override", "bm_version", "gemm", "syrk", "syr2k", "workspace_size",
 ]
@@ -71,6 +72,11 @@ def library():
                 lib.bm_gemm_bf16_noalloc.argtypes = [_i64, _i64, _i64, _i32, _i32, _f32, _vp, _i64, _vp, _i64,
                                                      _f32, _vp, _i64, _i32, _vp]
                 lib.bm_gemm_bf16_noalloc.restype = _i32
+                lib.bm_gemm_e4m3.argtypes = [_i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64, _i32,
+                                             _vp, _sz, _vp]
+                lib.bm_gemm_e4m3.restype = _i32
+                lib.bm_gemm_e4m3_workspace_size.argtypes = [_i64, _i64, _i64]
+                lib.bm_gemm_e4m3_workspace_size.restype = _sz
                 lib.bm_syrk_bf16.argtypes = [_i32, _i32, _i64, _i64, _f32, _vp, _i64, _f32, _vp, _i64,
                                              _i32, _vp]
                 lib.bm_syrk_bf16.restype = _i32
@@ -119,6 +125,16 @@ def bm_gemm_bf16_noalloc(m, n, k, transA, transB, alpha, A, lda, B, ldb, beta, C
 
 def bm_syrk_bf16(uplo, trans, n, k, alpha, A, lda, beta, C, ldc, c_type, stream=None) -> int:
     return library().bm_syrk_bf16(uplo, trans, n, k, alpha, A, lda, beta, C, ldc, c_type, stream)
+
+
+def bm_gemm_e4m3(m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, c_type, workspace=None, workspace_bytes=0,
+                 stream=None) -> int:
+    return library().bm_gemm_e4m3(m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, c_type, workspace,
+                                  workspace_bytes, stream)
+
+
+def bm_gemm_e4m3_workspace_size(m, n, k) -> int:
+    return library().bm_gemm_e4m3_workspace_size(m, n, k)
 
 
 def bm_syr2k_bf16(uplo, trans, n, k, alpha, A, lda, B, ldb, beta, C, ldc, c_type, stream=None) -> int:

@@ -50,21 +50,28 @@ std::atomic<uint32_t> g_timeout_ms{2000};
 std::atomic<int> g_debug_stall{0};
 std::atomic<int> g_tile_override{0};  // 0 = automatic, else 1 + Variant
 
-const void *variant_kernel(int v)
+template <int ELEM>
+const void *variant_kernel_t(int v)
 {
     switch (v) {
-    case kSingle256: return reinterpret_cast<const void *>(&bm::bm_gemm_tcgen05_kernel<256, 4, 1>);
-    case kSingle128: return reinterpret_cast<const void *>(&bm::bm_gemm_tcgen05_kernel<128, 6, 1>);
-    default: return reinterpret_cast<const void *>(&bm::bm_gemm_tcgen05_kernel<256, 6, 2>);
+    case kSingle256: return reinterpret_cast<const void *>(&bm::bm_gemm_tcgen05_kernel<256, 4, 1, ELEM>);
+    case kSingle128: return reinterpret_cast<const void *>(&bm::bm_gemm_tcgen05_kernel<128, 6, 1, ELEM>);
+    default: return reinterpret_cast<const void *>(&bm::bm_gemm_tcgen05_kernel<256, 6, 2, ELEM>);
     }
 }
 
+const void *variant_kernel(int v, int elem = bm::ELEM_BF16)
+{
+    return elem == bm::ELEM_E4M3 ? variant_kernel_t<bm::ELEM_E4M3>(v) : variant_kernel_t<bm::ELEM_BF16>(v);
+}
+
+// Shared memory does not depend on the element type (k-blocks are 128 bytes of K).
 int variant_smem(int v)
 {
     switch (v) {
-    case kSingle256: return bm::KernelCfg<256, 4, 1>::SMEM_BYTES;
-    case kSingle128: return bm::KernelCfg<128, 6, 1>::SMEM_BYTES;
-    default: return bm::KernelCfg<256, 6, 2>::SMEM_BYTES;
+    case kSingle256: return bm::KernelCfg<256, 4, 1, bm::ELEM_BF16>::SMEM_BYTES;
+    case kSingle128: return bm::KernelCfg<128, 6, 1, bm::ELEM_BF16>::SMEM_BYTES;
+    default: return bm::KernelCfg<256, 6, 2, bm::ELEM_BF16>::SMEM_BYTES;
     }
 }
 
@@ -103,10 +110,11 @@ bm_status device_state(DeviceState **out)
         if (cudaMemset(st.status, 0, sizeof(int)) != cudaSuccess) return BM_ERR_CUDA;
     }
     if (!st.attrs_set) {
-        for (int v = 0; v < kNumVariants; ++v)
-            if (cudaFuncSetAttribute(variant_kernel(v), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     variant_smem(v)) != cudaSuccess)
-                return BM_ERR_CUDA;
+        for (int e = 0; e < 2; ++e)
+            for (int v = 0; v < kNumVariants; ++v)
+                if (cudaFuncSetAttribute(variant_kernel(v, e), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         variant_smem(v)) != cudaSuccess)
+                    return BM_ERR_CUDA;
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -142,19 +150,28 @@ int sm_count_or_default()
     return 152;  // GB300
 }
 
-// rank-2 bf16 tensor map: inner (contiguous) extent, outer extent, row pitch in elements
+// rank-2 tensor map of 2-byte (bf16) or 1-byte (E4M3, copied as bytes)
+// elements: inner (contiguous) extent, outer extent, row pitch in elements.
+bool encode_operand_2d(CUtensorMap *map, const void *base, int elem, int64_t inner, int64_t outer, int64_t ld,
+                       uint32_t box_inner, uint32_t box_outer)
+{
+    const cuuint64_t esz = elem == bm::ELEM_E4M3 ? 1u : 2u;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(std::max<int64_t>(inner, 1)),
+                          static_cast<cuuint64_t>(std::max<int64_t>(outer, 1))};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * esz};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, elem == bm::ELEM_E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                          const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 bool encode_bf16_2d(CUtensorMap *map, const void *base, int64_t inner, int64_t outer, int64_t ld,
                     uint32_t box_inner, uint32_t box_outer)
 {
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(std::max<int64_t>(inner, 1)),
-                          static_cast<cuuint64_t>(std::max<int64_t>(outer, 1))};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2u};
-    cuuint32_t box[2] = {box_inner, box_outer};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
-                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    return encode_operand_2d(map, base, bm::ELEM_BF16, inner, outer, ld, box_inner, box_outer);
 }
 
 // Map of C used only to prefetch each CTA's output rows into L2 (box: tile
@@ -285,7 +302,8 @@ void try_split(Plan &pl, int64_t split_tiles, int64_t want, size_t budget)
 
 // Pair tiles (256 x 256 on two SMs) whenever they alone can occupy at least half
 // of the SM pairs; otherwise 128-row tiles on single SMs (more, smaller tiles).
-Plan plan_gemm(int64_t m, int64_t n, int64_t k, size_t ws_bytes, int sms, int pair_clusters)
+Plan plan_gemm(int64_t m, int64_t n, int64_t k, size_t ws_bytes, int sms, int pair_clusters,
+               int elem = bm::ELEM_BF16)
 {
     Plan pl;
     const int64_t pair_tiles = ceil_div(m, 256) * ceil_div(n, 256);
@@ -297,7 +315,7 @@ Plan plan_gemm(int64_t m, int64_t n, int64_t k, size_t ws_bytes, int sms, int pa
     pl.tiles_n = ceil_div(n, pl.bn);
     pl.num_tiles = pl.tiles_m * pl.tiles_n;
     pl.full_tiles = pl.num_tiles;
-    pl.kb_total = static_cast<int>(ceil_div(std::max<int64_t>(k, 1), bm::TILE_K));
+    pl.kb_total = static_cast<int>(ceil_div(std::max<int64_t>(k, 1), bm::kblock_elems(elem)));
     pl.kb_per_split = pl.kb_total;
     const int64_t slots = pl.pair == 2 ? pair_clusters : sms;
     if (slots > 0 && pl.kb_total >= 8) {
@@ -338,8 +356,19 @@ Plan plan_syrk(int mode, int64_t n, int64_t k, int sms, int pair_clusters, bool 
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+template <int ELEM>
+cudaError_t launch_main(const cudaLaunchConfig_t &cfg, int variant, const CUtensorMap &ta, const CUtensorMap &tb,
+                        const CUtensorMap &tc, const CUtensorMap &tp, const bm::GemmParams &prm)
+{
+    switch (variant) {
+    case kSingle256: return cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<256, 4, 1, ELEM>, ta, tb, tc, tp, prm);
+    case kSingle128: return cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<128, 6, 1, ELEM>, ta, tb, tc, tp, prm);
+    default: return cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<256, 6, 2, ELEM>, ta, tb, tc, tp, prm);
+    }
+}
+
 bm_status launch(const Plan &pl, const CUtensorMap &ta, const CUtensorMap &tb, bm::GemmParams &prm,
-                 cudaStream_t stream)
+                 cudaStream_t stream, int elem = bm::ELEM_BF16)
 {
     // beta != 0: the epilogue reads C, so each whole tile's C is prefetched into L2.
     // beta == 0 (GEMM): the epilogue stores C with TMA through a swizzled map instead.
@@ -379,16 +408,8 @@ bm_status launch(const Plan &pl, const CUtensorMap &ta, const CUtensorMap &tb, b
         attr[1].val.clusterDim.z = 1;
         cfg.numAttrs = 2;
     }
-    cudaError_t err;
-    switch (pl.variant) {
-    case kSingle256:
-        err = cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<256, 4, 1>, ta, tb, tc, tp, prm);
-        break;
-    case kSingle128:
-        err = cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<128, 6, 1>, ta, tb, tc, tp, prm);
-        break;
-    default: err = cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<256, 6, 2>, ta, tb, tc, tp, prm); break;
-    }
+    const cudaError_t err = elem == bm::ELEM_E4M3 ? launch_main<bm::ELEM_E4M3>(cfg, pl.variant, ta, tb, tc, tp, prm)
+                                                  : launch_main<bm::ELEM_BF16>(cfg, pl.variant, ta, tb, tc, tp, prm);
     if (err != cudaSuccess) {
         cudaGetLastError();
         return BM_ERR_CUDA;
@@ -557,10 +578,11 @@ bm_status noalloc_device_setup(DeviceState **out, float **scratch)
         g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
     if (!st.attrs_set) {
-        for (int v = 0; v < kNumVariants; ++v)
-            if (cudaFuncSetAttribute(variant_kernel(v), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     variant_smem(v)) != cudaSuccess)
-                return BM_ERR_CUDA;
+        for (int e = 0; e < 2; ++e)
+            for (int v = 0; v < kNumVariants; ++v)
+                if (cudaFuncSetAttribute(variant_kernel(v, e), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         variant_smem(v)) != cudaSuccess)
+                    return BM_ERR_CUDA;
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -751,6 +773,51 @@ bm_status bm_syr2k_bf16(bm_uplo uplo, bm_op trans, int64_t n, int64_t k, float a
     fill_params(prm, pl);
     prm.syr2k_kb = pl.kb_total / 2;
     return launch(pl, ta, tb, prm, cs);
+}
+
+bm_status bm_gemm_e4m3(int64_t m, int64_t n, int64_t k, float alpha, const void *A, int64_t lda, const void *B,
+                       int64_t ldb, float beta, void *C, int64_t ldc, bm_ctype c_type, void *workspace,
+                       size_t workspace_bytes, bm_stream_t stream)
+{
+    // A [m, k] and B [n, k] row-major: both operands K-major (op(B) = B^T)
+    bm_status s = check_gemm_args(m, n, k, BM_OP_N, BM_OP_T, lda, ldb, ldc, c_type);
+    if (s != BM_OK) return s;
+    if (workspace_bytes > 0 && (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
+        return BM_ERR_WORKSPACE;
+    if (m == 0 || n == 0) return BM_OK;
+    const bool products = alpha != 0.0f && k > 0;
+    if (C == nullptr || (products && (A == nullptr || B == nullptr))) return BM_ERR_INVALID_VALUE;
+    const int64_t esz = c_type == BM_C_BF16 ? 2 : 4;
+    if (!aligned16(C) || (ldc * esz) % 16 != 0) return BM_ERR_MISALIGNED;
+    if (products && (!aligned16(A) || !aligned16(B) || lda % 16 != 0 || ldb % 16 != 0)) return BM_ERR_MISALIGNED;
+    DeviceState *st = nullptr;
+    s = device_state(&st);
+    if (s != BM_OK) return s;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    bm::GemmParams prm = base_params(m, n, k, alpha, beta, C, ldc, c_type, st);
+    prm.mode = bm::MODE_GEMM;
+    if (!products) return launch_scale(prm, cs);
+
+    const Plan pl = plan_gemm(m, n, k, workspace != nullptr ? workspace_bytes : 0, st->sm_count,
+                              st->max_pair_clusters, bm::ELEM_E4M3);
+    CUtensorMap ta, tb;
+    const uint32_t kb = static_cast<uint32_t>(bm::kblock_elems(bm::ELEM_E4M3));
+    if (!encode_operand_2d(&ta, A, bm::ELEM_E4M3, k, m, lda, kb, bm::CTA_M)) return BM_ERR_CUDA;
+    if (!encode_operand_2d(&tb, B, bm::ELEM_E4M3, k, n, ldb, kb, static_cast<uint32_t>(pl.bn / pl.pair)))
+        return BM_ERR_CUDA;
+    prm.a_mn_major = 0;
+    prm.b_mn_major = 0;
+    fill_params(prm, pl);
+    prm.partial = pl.k_splits > 1 ? static_cast<float *>(workspace) : nullptr;
+    return launch(pl, ta, tb, prm, cs, bm::ELEM_E4M3);
+}
+
+size_t bm_gemm_e4m3_workspace_size(int64_t m, int64_t n, int64_t k)
+{
+    if (m <= 0 || n <= 0 || k <= 0) return 0;
+    const int sms = sm_count_or_default();
+    const Plan pl = plan_gemm(m, n, k, SIZE_MAX, sms, pair_clusters_or_default(sms), bm::ELEM_E4M3);
+    return pl.k_splits > 1 ? pl.ws_bytes : 0;
 }
 
 bm_status bm_gemm_bf16_plan(int64_t m, int64_t n, int64_t k, size_t workspace_bytes, bm_plan *plan)

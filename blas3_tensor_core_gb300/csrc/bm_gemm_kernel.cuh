@@ -56,8 +56,13 @@ enum : int { MODE_GEMM = 0, MODE_SYRK_LOWER = 1, MODE_SYRK_UPPER = 2 };
 enum : int { DEV_ERR_TIMEOUT = 5 };
 
 constexpr int CTA_M = 128;  // accumulator rows (TMEM lanes) per CTA
-constexpr int TILE_K = 64;  // bf16 elements = 128 bytes = one swizzle row
-constexpr int UMMA_K = 16;
+constexpr int TILE_K = 64;  // bf16 elements = 128 bytes = one swizzle row (a k-block)
+constexpr int UMMA_K = 16;  // bf16 elements of one MMA = 32 bytes
+// Operand element types: bf16 (kind::f16) or FP8 E4M3 (kind::f8f6f4). A k-block
+// is 128 bytes of K either way (64 bf16 or 128 E4M3) and one MMA consumes 32
+// bytes of K, so the shared-memory layout and descriptors are the same.
+enum : int { ELEM_BF16 = 0, ELEM_E4M3 = 1 };
+__host__ __device__ constexpr int kblock_elems(int elem) { return elem == ELEM_E4M3 ? 128 : 64; }
 // Two epilogue warps per TMEM lane quadrant: warps w and w + 4 read the same 32
 // accumulator rows and split the column chunks between them.
 constexpr int NUM_EPI_WARPS = 8;
@@ -78,8 +83,8 @@ struct GemmParams {
     int64_t full_tiles; // units [0, full_tiles) are whole tiles; each later tile is split k_splits ways
     int64_t num_units;  // full_tiles + (num_tiles - full_tiles) * k_splits
     int k_splits;       // > 1: split units write fp32 partials that a second kernel sums
-    int kb_per_split;   // k-blocks (of TILE_K) per split
-    int kb_total;       // ceil(k / TILE_K)
+    int kb_per_split;   // k-blocks (128 bytes of K each) per split
+    int kb_total;       // ceil(k / elements per k-block)
     int group_m;        // grouped raster: tile rows per group
     float *partial;     // [split tile][split][tile rows][tile columns] fp32 when k_splits > 1
     int *status;       // device status word (first error wins)
@@ -91,11 +96,12 @@ struct GemmParams {
     int store_p_tma;   // split units: tmP maps the partial slots for TMA stores (fp32, box 32 x 32, 128B swizzle)
 };
 
-template <int BN, int STAGES, int PAIR>
+template <int BN, int STAGES, int PAIR, int ELEM>
 struct KernelCfg {
     static constexpr int TILE_M = CTA_M * PAIR;  // output rows per tile
+    static constexpr int KB_ELEMS = kblock_elems(ELEM);  // K elements per k-block (128 bytes)
     static constexpr int B_ROWS = BN / PAIR;     // rows of op(B)^T staged by each CTA
-    static constexpr int A_BYTES = CTA_M * TILE_K * 2;
+    static constexpr int A_BYTES = CTA_M * TILE_K * 2;  // 128 rows x 128 bytes of K, any element type
     static constexpr int B_BYTES = B_ROWS * TILE_K * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int TX_BYTES = STAGE_BYTES * PAIR;  // bytes that complete one full barrier
@@ -371,12 +377,12 @@ __device__ __forceinline__ bool full_vector(const GemmParams &p, int64_t i, int6
 }
 
 // ---------------------------------------------------------------- roles
-template <int BN, int STAGES, int PAIR>
+template <int BN, int STAGES, int PAIR, int ELEM>
 __device__ __forceinline__ void run_producer(const CUtensorMap *tmA, const CUtensorMap *tmB, const CUtensorMap *tmC,
                                              const GemmParams &p, uint32_t ring, uint32_t bar0, uint32_t rank,
                                              volatile int *abort_flag)
 {
-    using Cfg = KernelCfg<BN, STAGES, PAIR>;
+    using Cfg = KernelCfg<BN, STAGES, PAIR, ELEM>;
     const int64_t units = p.num_units;
     int stage = 0;
     uint32_t phase = 0;
@@ -408,7 +414,7 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmA, const CUten
             const bool swap = p.syr2k_kb > 0 && kb >= p.syr2k_kb;
             const CUtensorMap *mapA = swap ? tmB : tmA;
             const CUtensorMap *mapB = swap ? tmA : tmB;
-            const int32_t kx = (swap ? kb - p.syr2k_kb : kb) * TILE_K;
+            const int32_t kx = (swap ? kb - p.syr2k_kb : kb) * Cfg::KB_ELEMS;
             if (!(p.debug_stall && first)) {
                 issued_any = true;
                 if constexpr (PAIR == 1) {
@@ -458,13 +464,13 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmA, const CUten
     }
 }
 
-template <int BN, int STAGES, int PAIR>
+template <int BN, int STAGES, int PAIR, int ELEM>
 __device__ __forceinline__ void run_mma(const GemmParams &p, uint32_t ring, uint32_t bar0, uint32_t tmem_base,
                                         volatile int *abort_flag)
 {
-    using Cfg = KernelCfg<BN, STAGES, PAIR>;
+    using Cfg = KernelCfg<BN, STAGES, PAIR, ELEM>;
     const int64_t units = p.num_units;
-    const uint32_t idesc = idesc_bf16_f32(Cfg::TILE_M, BN, p.a_mn_major, p.b_mn_major);
+    const uint32_t idesc = idesc_f32acc(Cfg::TILE_M, BN, ELEM == ELEM_E4M3 ? 0u : 1u, p.a_mn_major, p.b_mn_major);
     int stage = 0, acc = 0;
     uint32_t phase = 0, acc_phase = 0;
     bool ok = true, issued_any = false;
@@ -496,8 +502,13 @@ __device__ __forceinline__ void run_mma(const GemmParams &p, uint32_t ring, uint
                 const uint64_t bd = p.b_mn_major ? smem_desc_sw128(sb + 2048u * kk, 8192u, 1024u)
                                                  : smem_desc_sw128(sb + 32u * kk, 16u, 1024u);
                 const uint32_t accumulate = (kb > kb0 || kk > 0) ? 1u : 0u;
-                if constexpr (PAIR == 1) umma_bf16(d_tmem, ad, bd, idesc, accumulate);
-                else umma_bf16_pair(d_tmem, ad, bd, idesc, accumulate);
+                if constexpr (ELEM == ELEM_E4M3) {
+                    if constexpr (PAIR == 1) umma_f8(d_tmem, ad, bd, idesc, accumulate);
+                    else umma_f8_pair(d_tmem, ad, bd, idesc, accumulate);
+                } else {
+                    if constexpr (PAIR == 1) umma_bf16(d_tmem, ad, bd, idesc, accumulate);
+                    else umma_bf16_pair(d_tmem, ad, bd, idesc, accumulate);
+                }
             }
             issued_any = true;
             // the stage is free (in both CTAs) once these MMAs finish
@@ -528,13 +539,13 @@ __device__ __forceinline__ void run_mma(const GemmParams &p, uint32_t ring, uint
     }
 }
 
-template <int BN, int STAGES, int PAIR>
+template <int BN, int STAGES, int PAIR, int ELEM>
 __device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUtensorMap *tmP, const GemmParams &p,
                                              uint32_t bar0,
                                              uint32_t tmem_base, float *stage_buf, uint32_t rank,
                                              volatile int *abort_flag, int warp, int lane)
 {
-    using Cfg = KernelCfg<BN, STAGES, PAIR>;
+    using Cfg = KernelCfg<BN, STAGES, PAIR, ELEM>;
     const int64_t units = p.num_units;
     const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31 are this warp's rows
     const int half = (warp - 2) >> 2;  // which of the two warps on this quadrant: even or odd chunks
@@ -702,13 +713,13 @@ __device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUten
 }
 
 // ---------------------------------------------------------------- kernels
-template <int BN, int STAGES, int PAIR>
+template <int BN, int STAGES, int PAIR, int ELEM>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     bm_gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                            const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmP,
                            const GemmParams p)
 {
-    using Cfg = KernelCfg<BN, STAGES, PAIR>;
+    using Cfg = KernelCfg<BN, STAGES, PAIR, ELEM>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
@@ -762,11 +773,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     griddep_wait();
 
     if (warp == 0) {
-        if (lane == 0) run_producer<BN, STAGES, PAIR>(&tmA, &tmB, &tmC, p, ring, bar0, rank, abort_flag);
+        if (lane == 0) run_producer<BN, STAGES, PAIR, ELEM>(&tmA, &tmB, &tmC, p, ring, bar0, rank, abort_flag);
     } else if (warp == 1) {
-        if (lane == 0 && rank == 0) run_mma<BN, STAGES, PAIR>(p, ring, bar0, tmem_base, abort_flag);
+        if (lane == 0 && rank == 0) run_mma<BN, STAGES, PAIR, ELEM>(p, ring, bar0, tmem_base, abort_flag);
     } else {
-        run_epilogue<BN, STAGES, PAIR>(&tmC, &tmP, p, bar0, tmem_base, epi + (warp - 2) * EPI_WARP_FLOATS, rank,
+        run_epilogue<BN, STAGES, PAIR, ELEM>(&tmC, &tmP, p, bar0, tmem_base, epi + (warp - 2) * EPI_WARP_FLOATS, rank,
                                        abort_flag,
                                        warp, lane);
     }

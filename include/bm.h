@@ -138,6 +138,28 @@ BM_API bm_status bm_gemm_bf16_noalloc(int64_t m, int64_t n, int64_t k, bm_op tra
                                       bm_stream_t stream);
 
 /*
+ * GEMM with FP8 E4M3 operands:  C[m x n] = alpha * A * B^T + beta * C
+ *
+ *   The all-E4M3, FP32-accumulated matrix products of the FP8 paths in "fused
+ *   A2A/GEMM Perfetto profile protocol" (FP8 section). A is [m, k] (lda >= k)
+ *   and B is [n, k] (ldb >= k), both row-major with one E4M3 code per byte
+ *   (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; subnormals
+ *   honoured). Any per-tensor scaling of the FP8 data goes into alpha. C is
+ *   FP32 or BF16 as for bm_gemm_bf16, and the workspace, BLAS rules, errors and
+ *   stream behaviour are the same, except the alignment rule: lda and ldb
+ *   must be multiples of 16 (bytes = elements).
+ *
+ *   Returns BM_OK once the work is queued on `stream`.
+ */
+BM_API bm_status bm_gemm_e4m3(int64_t m, int64_t n, int64_t k, float alpha, const void *A, int64_t lda,
+                              const void *B, int64_t ldb, float beta, void *C, int64_t ldc,
+                              bm_ctype c_type, void *workspace, size_t workspace_bytes,
+                              bm_stream_t stream);
+
+/* Bytes of workspace that bm_gemm_e4m3 would use for this shape (0 = none). */
+BM_API size_t bm_gemm_e4m3_workspace_size(int64_t m, int64_t n, int64_t k);
+
+/*
  * SYRK:  C = alpha * op(A) * op(A)^T + beta * C   on one triangle of C[n x n]
  *
  *   op(A) is n x k: A is stored [n, k] (lda >= k) when trans == BM_OP_N

@@ -25,6 +25,11 @@ def bf16_to_device(bits: np.ndarray):
     return t.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(t.bfloat16).cuda()
 
 
+def u8_to_device(codes: np.ndarray):
+    t = torch()
+    return t.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8)).cuda()
+
+
 def f32_to_device(x: np.ndarray):
     t = torch()
     return t.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).cuda()
@@ -128,6 +133,24 @@ def run_syrk(uplo, trans, n, k, alpha, A, beta, cbuf: CBuffer):
     dA = bf16_to_device(A)
     st = bm.bm_syrk_bf16(uplo, trans, n, k, alpha, dA.data_ptr(), A.shape[1], beta, cbuf.ptr, cbuf.ldc,
                          bm.BM_C_BF16 if cbuf.bf16 else bm.BM_C_F32, t.cuda.current_stream().cuda_stream)
+    assert st == bm.BM_OK, bm.bm_status_string(st)
+    t.cuda.synchronize()
+    check_no_device_error()
+    return cbuf.result()
+
+
+def run_gemm_e4m3(m, n, k, alpha, A, B, beta, cbuf: CBuffer, workspace=None):
+    """C = alpha * A B^T + beta * C with E4M3 codes A [m, k], B [n, k] (row lengths = leading dimensions)."""
+    import blas3_tensor_core_gb300 as bm
+    t = torch()
+    dA = u8_to_device(A)
+    dB = u8_to_device(B)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    st = bm.bm_gemm_e4m3(m, n, k, alpha, dA.data_ptr(), A.shape[1], dB.data_ptr(), B.shape[1], beta, cbuf.ptr,
+                         cbuf.ldc, bm.BM_C_BF16 if cbuf.bf16 else bm.BM_C_F32, ws_ptr, ws_bytes,
+                         t.cuda.current_stream().cuda_stream)
     assert st == bm.BM_OK, bm.bm_status_string(st)
     t.cuda.synchronize()
     check_no_device_error()

@@ -103,6 +103,22 @@ def test_syrk_argument_errors(lib):
     assert s(n=0, ldc=1) == bm.BM_OK
 
 
+def test_e4m3_argument_errors(lib):
+    def g8(m=64, n=64, k=64, A=0x1000, lda=None, B=0x2000, ldb=None, C=0x3000, ldc=None, ct=0):
+        lda = lda if lda is not None else k
+        ldb = ldb if ldb is not None else k
+        ldc = ldc if ldc is not None else n
+        return bm.bm_gemm_e4m3(m, n, k, 1.0, A, lda, B, ldb, 0.0, C, ldc, ct, None, 0, None)
+    assert g8(m=-1) == bm.BM_ERR_INVALID_VALUE
+    assert g8(lda=32) == bm.BM_ERR_INVALID_VALUE     # lda < k
+    assert g8(ldb=63) == bm.BM_ERR_INVALID_VALUE
+    assert g8(k=72, lda=72, ldb=80) == bm.BM_ERR_MISALIGNED   # 72-byte rows
+    assert g8(A=0x1008) == bm.BM_ERR_MISALIGNED
+    assert g8(n=0, ldc=1) == bm.BM_OK
+    assert bm.bm_gemm_e4m3_workspace_size(512, 512, 16384) > 0     # 128 k-blocks of 128: split pays
+    assert bm.bm_gemm_e4m3_workspace_size(4096, 4096, 4096) == bm.bm_gemm_bf16_workspace_size(4096, 4096, 2048)
+
+
 def test_syr2k_argument_errors(lib):
     def s2(uplo=0, trans=0, n=64, k=64, A=0x1000, lda=None, B=0x2000, ldb=None, C=0x3000, ldc=None, ct=0):
         lda = lda if lda is not None else (n if trans else k)

@@ -1,0 +1,98 @@
+"""FP8 E4M3 GEMM parity (C = alpha * A B^T + beta * C): the CUDA path through the
+C ABI against the CPU oracle, on a GB300.
+
+Exact-integer inputs (|x| <= 8, exact in E4M3) pin the kind::f8f6f4 instruction
+descriptor and the 128-element k-blocks bit for bit on every tile variant;
+Gaussian inputs use the tolerance 1e-3 * |alpha| * sum|a*b| (+ 2^-8 |ref| for
+BF16 output).
+"""
+
+import numpy as np
+import pytest
+
+import bm_inputs as gen
+import oracle
+from gpu_helpers import (VARIANT_IDS, VARIANTS, CBuffer, assert_parity, c_input_values, run_gemm_e4m3, tile_samples,
+                         tile_variant, torch)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from blas3_tensor_core_gb300 import build
+    build.build()
+    assert torch().cuda.is_available()
+
+
+def _codes(rows, cols, dist, seed, std=1.0, lo=-8, hi=8):
+    codes = gen.matrix_e4m3(rows, cols, dist, seed, std, lo, hi)
+    pad = (-cols) % 16 + 16
+    return gen.pad_ld(codes, cols + pad, np.uint8(0x7F))  # NaN padding: never read
+
+
+def _ldc(n, bf16):
+    per = 8 if bf16 else 4
+    return n + (-n) % per + per
+
+
+@pytest.mark.parametrize("variant", VARIANTS, ids=VARIANT_IDS)
+@pytest.mark.parametrize("shape", [(256, 256, 256), (200, 300, 136), (129, 520, 64), (1, 8, 16), (520, 264, 200)])
+def test_e4m3_exact_integer_bitwise(shape, variant):
+    m, n, k = shape
+    A = _codes(m, k, "int", 5)
+    B = _codes(n, k, "int", 6)
+    cbuf = CBuffer(m, n, _ldc(n, False), False, init=np.full((m, n), np.nan, np.float32))
+    with tile_variant(variant):
+        got, raw = run_gemm_e4m3(m, n, k, 1.0, A, B, 0.0, cbuf)
+    ref, _ = oracle.default().gemm_e4m3(m, n, k, 1.0, A, B)
+    assert np.array_equal(got, ref), f"max |diff| {np.max(np.abs(got - ref))}"
+    cbuf.assert_guard_intact(raw)
+
+
+@pytest.mark.parametrize("bf16_out,beta", [(False, 0.0), (False, 1.0), (True, 0.0), (True, -0.5)])
+def test_e4m3_gaussian_ragged(bf16_out, beta):
+    m, n, k = 640, 520, 392
+    A = _codes(m, k, "normal", 11)
+    B = _codes(n, k, "normal", 12, std=0.25)
+    c0 = gen.matrix_f32(m, n, "normal", seed=13)
+    c_init = gen.f32_to_bf16_bits(c0) if bf16_out else c0
+    cbuf = CBuffer(m, n, _ldc(n, bf16_out), bf16_out, init=c_init)
+    got, raw = run_gemm_e4m3(m, n, k, 0.75, A, B, beta, cbuf)
+    ref, bound = oracle.default().gemm_e4m3(m, n, k, 0.75, A, B, beta, c_init if beta != 0 else None)
+    assert_parity(got, ref, bound, 0.75, beta, c_input_values(c_init, bf16_out), bf16_out, "e4m3 ragged")
+    cbuf.assert_guard_intact(raw)
+
+
+def test_e4m3_split_k_and_deterministic():
+    import blas3_tensor_core_gb300 as bm
+    t = torch()
+    m, n, k = 512, 512, 16384
+    A = _codes(m, k, "normal", 21)
+    B = _codes(n, k, "normal", 22)
+    need = bm.bm_gemm_e4m3_workspace_size(m, n, k)
+    assert need > 0
+    ws = t.empty(need // 4, dtype=t.float32, device="cuda")
+    outs = []
+    for _ in range(2):
+        cbuf = CBuffer(m, n, n, True)
+        got, raw = run_gemm_e4m3(m, n, k, 1.0, A, B, 0.0, cbuf, workspace=ws)
+        cbuf.assert_guard_intact(raw)
+        outs.append(got)
+    assert np.array_equal(outs[0], outs[1])
+    rows, cols = tile_samples(m, n, per_tile=64, seed=7)
+    ref, bound = oracle.default().gemm_e4m3_entries(k, 1.0, A, B, rows, cols)
+    assert_parity(outs[0][rows, cols], ref, bound, 1.0, 0.0, None, True, "e4m3 split-K")
+
+
+def test_e4m3_full_size_4096_sampled():
+    m = n = k = 4096
+    A = gen.matrix_e4m3(m, k, "normal", 1)
+    B = gen.matrix_e4m3(n, k, "normal", 2)
+    cbuf = CBuffer(m, n, n, True, extra_rows=1)
+    got, raw = run_gemm_e4m3(m, n, k, 1.0, A, B, 0.0, cbuf)
+    assert np.all(np.isfinite(got))
+    rows, cols = tile_samples(m, n, per_tile=4, seed=5)
+    ref, bound = oracle.default().gemm_e4m3_entries(k, 1.0, A, B, rows, cols)
+    assert_parity(got[rows, cols], ref, bound, 1.0, 0.0, None, True, "e4m3 4096^3")
+    cbuf.assert_guard_intact(raw)
