@@ -21,7 +21,7 @@
 //   halves the B operand bytes that the tensor core reads from shared memory
 //   per MMA (8 KB instead of 12 KB for a K = 16 step).
 //
-// Roles (192 threads per CTA):
+// Roles (320 threads per CTA):
 //   warp 0, one lane  TMA producer: fills a STAGES-deep ring of shared-memory
 //                     stages guarded by full/empty mbarriers (PAIR = 2: both
 //                     CTAs' copies complete bytes on CTA 0's full barrier).
@@ -30,10 +30,13 @@
 //                     x BN fp32 columns per CTA); tcgen05.commit releases the
 //                     stage (in both CTAs) and, at the end of a tile, signals
 //                     the accumulator full. Warp 1 allocates and frees TMEM.
-//   warps 2-5         epilogue: TMEM -> registers (tcgen05.ld 32x32b), alpha,
-//                     transpose through shared memory, then coalesced 16-byte
-//                     loads of C (beta != 0) and stores of C; the SYRK
-//                     triangle and the ragged edges are masked per element.
+//   warps 2-9         epilogue, two warps per TMEM lane quadrant (warp w reads
+//                     lanes 32 (w % 4) ..): TMEM -> registers (tcgen05.ld
+//                     32x32b), alpha, then either a 128B-swizzled staging
+//                     block stored by TMA (beta == 0 GEMM, split partials) or
+//                     a transpose through shared memory with coalesced 16-byte
+//                     loads of C (beta != 0) and stores; the SYRK triangle and
+//                     the ragged edges of that path are masked per element.
 // Tiles are handed out persistently (cluster c takes units c, c + clusters,
 // ...), in grouped-raster order for GEMM and row by row over the referenced
 // triangle for SYRK (tiles strictly on the other side of the diagonal are never

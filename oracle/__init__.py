@@ -71,6 +71,7 @@ class Oracle:
         self.path = lib_path
         lib = ctypes.CDLL(lib_path)
         lib.oracle_num_threads.restype = _c_int
+        lib.oracle_set_num_threads.argtypes = [_c_int]
         lib.oracle_gemm.argtypes = [_c_i64, _c_i64, _c_i64, _c_int, _c_int, _c_dbl,
                                     _c_vp, _c_i64, _c_vp, _c_i64, _c_dbl,
                                     _c_vp, _c_i64, _c_int, _c_vp, _c_vp, _c_i64]
@@ -127,6 +128,10 @@ class Oracle:
 
     def num_threads(self) -> int:
         return int(self._lib.oracle_num_threads())
+
+    def set_num_threads(self, n: int) -> None:
+        """Threads of later calls (the results do not depend on it)."""
+        self._lib.oracle_set_num_threads(int(n))
 
     # -- GEMM ----------------------------------------------------------------
     def gemm(self, m, n, k, transA, transB, alpha, A, B, beta=0.0, C=None):

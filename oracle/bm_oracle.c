@@ -185,6 +185,17 @@ int oracle_num_threads(void)
 #endif
 }
 
+/* Threads for later parallel regions (host plumbing; no effect on any result). */
+void oracle_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0)
+        omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 /* Full GEMM: ref and bound are m x n row-major with leading dimension ldr. */
 void oracle_gemm(int64_t m, int64_t n, int64_t k, int transA, int transB, double alpha,
                  const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb, double beta,
