@@ -25,13 +25,14 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr int kGroupM = 16;
 
-// Kernel variants: output tile (rows x BN), ring depth, CTAs per tile.
-//   kSingle256: 128 x 256 per CTA, 4 stages of 48 KB
-//   kSingle128: 128 x 128 per CTA, 6 stages of 32 KB (narrow outputs)
-//   kPair256:   256 x 256 per CTA pair (cta_group::2), 6 stages of 32 KB per CTA
+// Kernel variants: output tile (rows x BN), ring depth, CTAs per tile, k-blocks per stage.
+//   kSingle256: 128 x 256 per CTA, 4 stages of one k-block (48 KB)
+//   kSingle128: 128 x 128 per CTA, 3 stages of two k-blocks (64 KB; narrow outputs)
+//   kPair256:   256 x 256 per CTA pair (cta_group::2), 3 stages of two k-blocks (64 KB per CTA)
 enum Variant { kSingle256 = 0, kSingle128 = 1, kPair256 = 2, kNumVariants = 3 };
 constexpr int kVariantBN[kNumVariants] = {256, 128, 256};
-constexpr int kVariantStages[kNumVariants] = {4, 6, 6};
+constexpr int kVariantStages[kNumVariants] = {4, 3, 3};
+constexpr int kVariantStageKBlocks[kNumVariants] = {1, 2, 2};
 constexpr int kVariantPair[kNumVariants] = {1, 1, 2};
 
 struct DeviceState {
@@ -54,9 +55,9 @@ template <int ELEM>
 const void *variant_kernel_t(int v)
 {
     switch (v) {
-    case kSingle256: return reinterpret_cast<const void *>(&bm::bm_gemm_tcgen05_kernel<256, 4, 1, ELEM>);
-    case kSingle128: return reinterpret_cast<const void *>(&bm::bm_gemm_tcgen05_kernel<128, 6, 1, ELEM>);
-    default: return reinterpret_cast<const void *>(&bm::bm_gemm_tcgen05_kernel<256, 6, 2, ELEM>);
+    case kSingle256: return reinterpret_cast<const void *>(&bm::bm_gemm_tcgen05_kernel<256, 4, 1, ELEM, 1>);
+    case kSingle128: return reinterpret_cast<const void *>(&bm::bm_gemm_tcgen05_kernel<128, 3, 1, ELEM, 2>);
+    default: return reinterpret_cast<const void *>(&bm::bm_gemm_tcgen05_kernel<256, 3, 2, ELEM, 2>);
     }
 }
 
@@ -69,9 +70,9 @@ const void *variant_kernel(int v, int elem = bm::ELEM_BF16)
 int variant_smem(int v)
 {
     switch (v) {
-    case kSingle256: return bm::KernelCfg<256, 4, 1, bm::ELEM_BF16>::SMEM_BYTES;
-    case kSingle128: return bm::KernelCfg<128, 6, 1, bm::ELEM_BF16>::SMEM_BYTES;
-    default: return bm::KernelCfg<256, 6, 2, bm::ELEM_BF16>::SMEM_BYTES;
+    case kSingle256: return bm::KernelCfg<256, 4, 1, bm::ELEM_BF16, 1>::SMEM_BYTES;
+    case kSingle128: return bm::KernelCfg<128, 3, 1, bm::ELEM_BF16, 2>::SMEM_BYTES;
+    default: return bm::KernelCfg<256, 3, 2, bm::ELEM_BF16, 2>::SMEM_BYTES;
     }
 }
 
@@ -226,6 +227,54 @@ bool encode_operand(CUtensorMap *map, const void *base, bool mn_major, int64_t r
     return encode_bf16_2d(map, base, k, rows, ld, 64, tile_rows);
 }
 
+// Stage box of one operand (replaces *map on success): a 3-D map whose single
+// copy brings this CTA's `rows` rows for all `kps` k-blocks of a stage, in the
+// kernel's stage layout. K-major operand [mn][k]: dims (k within a k-block,
+// row, k-block), strides (ld, one k-block); needs K to be whole k-blocks so no
+// row's copy runs past its K. M/N-major operand [k][mn]: dims (m or n within a
+// 64-wide chunk, k, chunk), strides (ld, 128 bytes); needs whole chunks. The
+// middle dimension has the largest stride, which the encoder accepts. Returns
+// false (map untouched) when the shape does not qualify or nothing is gained
+// over the 2-D boxes (one k-block, one chunk).
+bool encode_stage_box(CUtensorMap *map, const void *base, int elem, bool mn_major, int64_t mn, int64_t k, int64_t ld,
+                      int rows, int kps)
+{
+    const int64_t esz = elem == bm::ELEM_E4M3 ? 1 : 2;
+    const int64_t kb_elems = bm::kblock_elems(elem);
+    CUtensorMap m;
+    cuuint64_t dims[3], strides[2];
+    cuuint32_t box[3];
+    if (mn_major) {
+        if (elem != bm::ELEM_BF16 || mn % 64 != 0 || (kps == 1 && rows == 64)) return false;
+        dims[0] = 64;
+        dims[1] = static_cast<cuuint64_t>(k);
+        dims[2] = static_cast<cuuint64_t>(mn / 64);
+        strides[0] = static_cast<cuuint64_t>(ld * esz);
+        strides[1] = 128;
+        box[0] = 64;
+        box[1] = static_cast<cuuint32_t>(64 * kps);
+        box[2] = static_cast<cuuint32_t>(rows / 64);
+    } else {
+        if (kps == 1 || k % kb_elems != 0) return false;
+        dims[0] = static_cast<cuuint64_t>(kb_elems);
+        dims[1] = static_cast<cuuint64_t>(mn);
+        dims[2] = static_cast<cuuint64_t>(k / kb_elems);
+        strides[0] = static_cast<cuuint64_t>(ld * esz);
+        strides[1] = static_cast<cuuint64_t>(kb_elems * esz);
+        box[0] = static_cast<cuuint32_t>(kb_elems);
+        box[1] = static_cast<cuuint32_t>(rows);
+        box[2] = static_cast<cuuint32_t>(kps);
+    }
+    cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = g_encode(&m, elem == bm::ELEM_E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                                3, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return false;
+    *map = m;
+    return true;
+}
+
 struct Plan {
     int variant = kSingle256;
     int tile_m = bm::CTA_M, bn = 256, stages = 4, pair = 1;
@@ -361,9 +410,9 @@ cudaError_t launch_main(const cudaLaunchConfig_t &cfg, int variant, const CUtens
                         const CUtensorMap &tc, const CUtensorMap &tp, const bm::GemmParams &prm)
 {
     switch (variant) {
-    case kSingle256: return cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<256, 4, 1, ELEM>, ta, tb, tc, tp, prm);
-    case kSingle128: return cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<128, 6, 1, ELEM>, ta, tb, tc, tp, prm);
-    default: return cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<256, 6, 2, ELEM>, ta, tb, tc, tp, prm);
+    case kSingle256: return cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<256, 4, 1, ELEM, 1>, ta, tb, tc, tp, prm);
+    case kSingle128: return cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<128, 3, 1, ELEM, 2>, ta, tb, tc, tp, prm);
+    default: return cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<256, 3, 2, ELEM, 2>, ta, tb, tc, tp, prm);
     }
 }
 
@@ -486,6 +535,7 @@ void export_plan(const Plan &pl, bm_plan *plan)
     plan->cta_pair = pl.pair;
     plan->kernels = pl.k_splits > 1 ? 2 : 1;
     plan->workspace_bytes = pl.k_splits > 1 ? pl.ws_bytes : 0;
+    plan->stage_kblocks = kVariantStageKBlocks[pl.variant];
 }
 
 // Pair-cluster capacity for planning without a device (host-only planning): one per SM pair.
@@ -652,6 +702,9 @@ bm_status bm_gemm_bf16(int64_t m, int64_t n, int64_t k, bm_op transA, bm_op tran
     if (!encode_operand(&tb, B, b_mn, n, k, ldb, static_cast<uint32_t>(pl.bn / pl.pair))) return BM_ERR_CUDA;
     prm.a_mn_major = a_mn;
     prm.b_mn_major = b_mn;
+    const int kps = kVariantStageKBlocks[pl.variant];
+    prm.a_box3 = encode_stage_box(&ta, A, bm::ELEM_BF16, a_mn, m, k, lda, bm::CTA_M, kps);
+    prm.b_box3 = encode_stage_box(&tb, B, bm::ELEM_BF16, b_mn, n, k, ldb, pl.bn / pl.pair, kps);
     fill_params(prm, pl);
     prm.partial = pl.k_splits > 1 ? static_cast<float *>(workspace) : nullptr;
     return launch(pl, ta, tb, prm, cs);
@@ -697,6 +750,9 @@ bm_status bm_gemm_bf16_noalloc(int64_t m, int64_t n, int64_t k, bm_op transA, bm
     if (!encode_operand(&tb, B, b_mn, n, k, ldb, static_cast<uint32_t>(pl.bn / pl.pair))) return BM_ERR_CUDA;
     prm.a_mn_major = a_mn;
     prm.b_mn_major = b_mn;
+    const int kps = kVariantStageKBlocks[pl.variant];
+    prm.a_box3 = encode_stage_box(&ta, A, bm::ELEM_BF16, a_mn, m, k, lda, bm::CTA_M, kps);
+    prm.b_box3 = encode_stage_box(&tb, B, bm::ELEM_BF16, b_mn, n, k, ldb, pl.bn / pl.pair, kps);
     fill_params(prm, pl);
     prm.partial = pl.k_splits > 1 ? scratch : nullptr;
     return launch(pl, ta, tb, prm, cs);
@@ -732,6 +788,9 @@ bm_status bm_syrk_bf16(bm_uplo uplo, bm_op trans, int64_t n, int64_t k, float al
     if (!encode_operand(&tb, A, mn, n, k, lda, static_cast<uint32_t>(pl.bn / pl.pair))) return BM_ERR_CUDA;
     prm.a_mn_major = mn;
     prm.b_mn_major = mn;
+    const int kps = kVariantStageKBlocks[pl.variant];
+    prm.a_box3 = encode_stage_box(&ta, A, bm::ELEM_BF16, mn, n, k, lda, bm::CTA_M, kps);
+    prm.b_box3 = encode_stage_box(&tb, A, bm::ELEM_BF16, mn, n, k, lda, pl.bn / pl.pair, kps);
     fill_params(prm, pl);
     return launch(pl, ta, tb, prm, cs);
 }
@@ -807,6 +866,9 @@ bm_status bm_gemm_e4m3(int64_t m, int64_t n, int64_t k, float alpha, const void 
         return BM_ERR_CUDA;
     prm.a_mn_major = 0;
     prm.b_mn_major = 0;
+    const int kps = kVariantStageKBlocks[pl.variant];
+    prm.a_box3 = encode_stage_box(&ta, A, bm::ELEM_E4M3, false, m, k, lda, bm::CTA_M, kps);
+    prm.b_box3 = encode_stage_box(&tb, B, bm::ELEM_E4M3, false, n, k, ldb, pl.bn / pl.pair, kps);
     fill_params(prm, pl);
     prm.partial = pl.k_splits > 1 ? static_cast<float *>(workspace) : nullptr;
     return launch(pl, ta, tb, prm, cs, bm::ELEM_E4M3);

@@ -25,8 +25,9 @@
 //   warp 0, one lane  TMA producer: fills a STAGES-deep ring of shared-memory
 //                     stages guarded by full/empty mbarriers (PAIR = 2: both
 //                     CTAs' copies complete bytes on CTA 0's full barrier).
-//   warp 1, one lane  MMA issuer (CTA 0 only): 4 x tcgen05.mma (K = 16 each)
-//                     per stage into one of two TMEM accumulators (128 lanes
+//   warp 1            MMA issuer (CTA 0 only; the warp waits, lane 0 issues):
+//                     4 x tcgen05.mma (K = 16 each) per k-block, KPS k-blocks
+//                     per stage, into one of two TMEM accumulators (128 lanes
 //                     x BN fp32 columns per CTA); tcgen05.commit releases the
 //                     stage (in both CTAs) and, at the end of a tile, signals
 //                     the accumulator full. Warp 1 allocates and frees TMEM.
@@ -97,17 +98,33 @@ struct GemmParams {
     int store_c_tma;   // beta == 0, GEMM: tmC maps C for TMA stores (box 128 bytes x 32 rows, 128B swizzle)
     int syr2k_kb;      // SYR2K: k-blocks of one product; later k-blocks swap the roles of tmA and tmB
     int store_p_tma;   // split units: tmP maps the partial slots for TMA stores (fp32, box 32 x 32, 128B swizzle)
+    int a_box3;        // tmA is a stage box: one 3-D copy brings a CTA's A tile for a whole stage
+    int b_box3;        // same for tmB
 };
 
-template <int BN, int STAGES, int PAIR, int ELEM>
+// KPS: k-blocks per ring stage. With two k-blocks a stage, the MMA thread waits
+// on a full barrier and commits once per 8 MMAs instead of once per 4; every
+// such handshake leaves the tensor pipe idle for a while, so this pays wherever
+// the ring still holds three stages.
+//
+// Stage layout (one CTA): the A tile of each k-block, then the B tile of each
+// k-block. A K-major tile is rows x 128 bytes (8-row swizzle atoms, 1024 bytes
+// apart); k-block s of it starts s tile sizes in. An M/N-major tile is split
+// into chunks of 64 rows of M or N; chunk c holds the 64 x KPS k-rows of all
+// the stage's k-blocks (128 bytes each), so k-block s starts 8 KB into it and
+// the chunks are KPS x 8 KB apart. A 3-D "stage box" copy writes exactly this
+// layout for a whole operand and stage; without one, each k-block (and chunk)
+// is copied with a 2-D box into its place.
+template <int BN, int STAGES, int PAIR, int ELEM, int KPS>
 struct KernelCfg {
     static constexpr int TILE_M = CTA_M * PAIR;  // output rows per tile
     static constexpr int KB_ELEMS = kblock_elems(ELEM);  // K elements per k-block (128 bytes)
     static constexpr int B_ROWS = BN / PAIR;     // rows of op(B)^T staged by each CTA
     static constexpr int A_BYTES = CTA_M * TILE_K * 2;  // 128 rows x 128 bytes of K, any element type
     static constexpr int B_BYTES = B_ROWS * TILE_K * 2;
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int TX_BYTES = STAGE_BYTES * PAIR;  // bytes that complete one full barrier
+    static constexpr int STAGE_BYTES = KPS * (A_BYTES + B_BYTES);
+    static constexpr int B_OFFSET = KPS * A_BYTES;       // B tiles follow the stage's A tiles
+    static constexpr int CHUNK_BYTES = KPS * 8192;      // one 64-row M/N chunk of all k-blocks of a stage
     static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
     static constexpr int EPI_BYTES = NUM_EPI_WARPS * EPI_WARP_FLOATS * 4;
     static constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, acc full x2, acc empty x2, drain
@@ -116,6 +133,7 @@ struct KernelCfg {
     static constexpr int TMEM_COLS = 2 * BN;  // two accumulators
     static_assert(BN == 128 || BN == 256, "BN");
     static_assert(PAIR == 1 || PAIR == 2, "PAIR");
+    static_assert(KPS == 1 || KPS == 2, "k-blocks per stage");
     static_assert(B_ROWS % 64 == 0, "B rows per CTA");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 };
@@ -380,12 +398,61 @@ __device__ __forceinline__ bool full_vector(const GemmParams &p, int64_t i, int6
 }
 
 // ---------------------------------------------------------------- roles
-template <int BN, int STAGES, int PAIR, int ELEM>
+// One operand tile copy: 2-D box (x, y) into dst, CTA-local or counted on the
+// pair's barrier.
+template <int PAIR>
+__device__ __forceinline__ void load_box(uint32_t dst, const CUtensorMap *map, uint32_t bar, int32_t x, int32_t y)
+{
+    if constexpr (PAIR == 1) tma_load_2d(dst, map, bar, x, y);
+    else tma_load_2d_pair(dst, map, bar, x, y);
+}
+
+template <int PAIR>
+__device__ __forceinline__ void load_box3(uint32_t dst, const CUtensorMap *map, uint32_t bar, int32_t x, int32_t y,
+                                          int32_t z)
+{
+    if constexpr (PAIR == 1) tma_load_3d(dst, map, bar, x, y, z);
+    else tma_load_3d_pair(dst, map, bar, x, y, z);
+}
+
+// Copies of one operand (`rows` rows of op(X) starting at row0, this CTA's
+// share) for the KPS k-blocks kb, kb + 1, ... of a stage into the region at
+// dst, in the stage layout above. A stage box is one 3-D copy: K-major maps
+// are (k in k-block, row, k-block), M/N-major maps (m or n in chunk, k,
+// chunk). Otherwise one 2-D copy per k-block (and per chunk). SYR2K swaps the
+// roles of tmA and tmB from k-block syr2k_kb on (stage boxes are not used there).
+template <int PAIR, int KPS, int ROWS, int KB_ELEMS>
+__device__ __forceinline__ void load_operand(uint32_t dst, const CUtensorMap *map, const CUtensorMap *alt,
+                                             bool box3, bool mn_major, uint32_t bar, int32_t row0, int kb,
+                                             int syr2k_kb)
+{
+    if (box3) {
+        if (mn_major) load_box3<PAIR>(dst, map, bar, 0, kb * KB_ELEMS, row0 / 64);
+        else load_box3<PAIR>(dst, map, bar, 0, row0, kb);
+        return;
+    }
+#pragma unroll
+    for (int sub = 0; sub < KPS; ++sub) {
+        const int kbs = kb + sub;
+        const bool swap = syr2k_kb > 0 && kbs >= syr2k_kb;
+        const CUtensorMap *m = swap ? alt : map;
+        const int32_t kx = (swap ? kbs - syr2k_kb : kbs) * KB_ELEMS;
+        if (mn_major) {
+#pragma unroll
+            for (int c = 0; c < ROWS / 64; ++c)
+                load_box<PAIR>(dst + c * KPS * 8192 + sub * 8192, m, bar, row0 + 64 * c, kx);
+        } else {
+            load_box<PAIR>(dst + sub * ROWS * 128, m, bar, kx, row0);
+        }
+    }
+}
+
+template <int BN, int STAGES, int PAIR, int ELEM, int KPS>
 __device__ __forceinline__ void run_producer(const CUtensorMap *tmA, const CUtensorMap *tmB, const CUtensorMap *tmC,
                                              const GemmParams &p, uint32_t ring, uint32_t bar0, uint32_t rank,
                                              volatile int *abort_flag)
 {
-    using Cfg = KernelCfg<BN, STAGES, PAIR, ELEM>;
+    using Cfg = KernelCfg<BN, STAGES, PAIR, ELEM, KPS>;
     const int64_t units = p.num_units;
     int stage = 0;
     uint32_t phase = 0;
@@ -399,57 +466,30 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmA, const CUten
         const int32_t row_b = static_cast<int32_t>(w.tn * BN + rank * Cfg::B_ROWS);
         // The epilogue of this tile will read this CTA's 128 rows of C: start pulling them into L2.
         if (p.prefetch_c && w.slot < 0) tma_prefetch_l2_2d(tmC, static_cast<int32_t>(w.tn * BN), row_a);
-        for (int kb = kb0; kb < kb1; ++kb) {
+        for (int kb = kb0; kb < kb1; kb += KPS) {
             const uint32_t empty = bar0 + 8u * (STAGES + stage);
             if (!wait_one<PAIR == 2>(empty, phase ^ 1u, abort_flag, p.timeout_ns)) {
                 ok = false;
                 break;
             }
+            // Every stage copies KPS whole k-blocks; those past K (or past this
+            // unit's K range, in the last stage of an odd-length unit) are zeros
+            // or unused, but their bytes still count on the barrier.
             const uint32_t full = bar0 + 8u * stage;
             if (rank == 0) {
-                mbar_arrive_expect_tx(full, Cfg::TX_BYTES);
+                mbar_arrive_expect_tx(full, static_cast<uint32_t>(Cfg::STAGE_BYTES * PAIR));
                 armed |= 1u << stage;
                 armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
             }
-            const uint32_t sa = ring + stage * Cfg::STAGE_BYTES;
-            const uint32_t sb = sa + Cfg::A_BYTES;
-            // SYR2K: the first syr2k_kb k-blocks accumulate op(A) op(B)^T, the rest op(B) op(A)^T
-            const bool swap = p.syr2k_kb > 0 && kb >= p.syr2k_kb;
-            const CUtensorMap *mapA = swap ? tmB : tmA;
-            const CUtensorMap *mapB = swap ? tmA : tmB;
-            const int32_t kx = (swap ? kb - p.syr2k_kb : kb) * Cfg::KB_ELEMS;
             if (!(p.debug_stall && first)) {
                 issued_any = true;
-                if constexpr (PAIR == 1) {
-                    if (p.a_mn_major) {  // A stored [k][m]: two 64-wide chunks along M
-                        tma_load_2d(sa, mapA, full, row_a, kx);
-                        tma_load_2d(sa + 8192, mapA, full, row_a + 64, kx);
-                    } else {  // A stored [m][k]: one 64 x 128 box
-                        tma_load_2d(sa, mapA, full, kx, row_a);
-                    }
-                    if (p.b_mn_major) {  // B stored [k][n]: chunks of 64 along N
-#pragma unroll
-                        for (int c = 0; c < Cfg::B_ROWS / 64; ++c)
-                            tma_load_2d(sb + 8192 * c, mapB, full, row_b + 64 * c, kx);
-                    } else {  // B stored [n][k]: one 64 x B_ROWS box
-                        tma_load_2d(sb, mapB, full, kx, row_b);
-                    }
-                } else {
-                    const uint32_t full0 = map_shared_to_rank(full, 0);  // CTA 0 counts both CTAs' bytes
-                    if (p.a_mn_major) {
-                        tma_load_2d_pair(sa, mapA, full0, row_a, kx);
-                        tma_load_2d_pair(sa + 8192, mapA, full0, row_a + 64, kx);
-                    } else {
-                        tma_load_2d_pair(sa, mapA, full0, kx, row_a);
-                    }
-                    if (p.b_mn_major) {
-#pragma unroll
-                        for (int c = 0; c < Cfg::B_ROWS / 64; ++c)
-                            tma_load_2d_pair(sb + 8192 * c, mapB, full0, row_b + 64 * c, kx);
-                    } else {
-                        tma_load_2d_pair(sb, mapB, full0, kx, row_b);
-                    }
-                }
+                // the pair's CTA 0 counts both CTAs' bytes
+                const uint32_t bar = PAIR == 2 ? map_shared_to_rank(full, 0) : full;
+                const uint32_t sa = ring + stage * Cfg::STAGE_BYTES;
+                load_operand<PAIR, KPS, CTA_M, Cfg::KB_ELEMS>(sa, tmA, tmB, p.a_box3 != 0, p.a_mn_major != 0, bar,
+                                                              row_a, kb, p.syr2k_kb);
+                load_operand<PAIR, KPS, Cfg::B_ROWS, Cfg::KB_ELEMS>(sa + Cfg::B_OFFSET, tmB, tmA, p.b_box3 != 0,
+                                                                    p.b_mn_major != 0, bar, row_b, kb, p.syr2k_kb);
             }
             first = false;
             if (++stage == STAGES) {
@@ -467,11 +507,13 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmA, const CUten
     }
 }
 
-template <int BN, int STAGES, int PAIR, int ELEM>
+template <int BN, int STAGES, int PAIR, int ELEM, int KPS>
+// The whole warp runs the loop and waits; lane 0 issues the MMAs and commits
+// (a converged warp keeps the issue stream tighter than a lone diverged lane).
 __device__ __forceinline__ void run_mma(const GemmParams &p, uint32_t ring, uint32_t bar0, uint32_t tmem_base,
-                                        volatile int *abort_flag)
+                                        volatile int *abort_flag, int lane)
 {
-    using Cfg = KernelCfg<BN, STAGES, PAIR, ELEM>;
+    using Cfg = KernelCfg<BN, STAGES, PAIR, ELEM, KPS>;
     const int64_t units = p.num_units;
     const uint32_t idesc = idesc_f32acc(Cfg::TILE_M, BN, ELEM == ELEM_E4M3 ? 0u : 1u, p.a_mn_major, p.b_mn_major);
     int stage = 0, acc = 0;
@@ -488,35 +530,47 @@ __device__ __forceinline__ void run_mma(const GemmParams &p, uint32_t ring, uint
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int kb = kb0; kb < kb1; ++kb) {
+        for (int kb = kb0; kb < kb1; kb += KPS) {
             if (!wait_one(bar0 + 8u * stage, phase, abort_flag, p.timeout_ns)) {
                 ok = false;
                 break;
             }
             tc_fence_after_sync();
-            const uint32_t sa = ring + stage * Cfg::STAGE_BYTES;
-            const uint32_t sb = sa + Cfg::A_BYTES;
+            const int nkb = kb1 - kb < KPS ? kb1 - kb : KPS;
+            const uint32_t st = ring + stage * Cfg::STAGE_BYTES;
+            for (int sub = 0; sub < nkb; ++sub) {
+                // k-block `sub` of the stage: K-major tiles one tile size further on,
+                // M/N-major ones 64 k-rows (8 KB) further into each chunk
+                const uint32_t sa = st + (p.a_mn_major ? 8192u * sub : static_cast<uint32_t>(Cfg::A_BYTES) * sub);
+                const uint32_t sb = st + Cfg::B_OFFSET +
+                                    (p.b_mn_major ? 8192u * sub : static_cast<uint32_t>(Cfg::B_BYTES) * sub);
 #pragma unroll
-            for (int kk = 0; kk < TILE_K / UMMA_K; ++kk) {
-                // K-major: the next 16 k sit 32 bytes further along the swizzled row.
-                // M/N-major: the next 16 k are the next two 1024-byte row groups.
-                const uint64_t ad = p.a_mn_major ? smem_desc_sw128(sa + 2048u * kk, 8192u, 1024u)
-                                                 : smem_desc_sw128(sa + 32u * kk, 16u, 1024u);
-                const uint64_t bd = p.b_mn_major ? smem_desc_sw128(sb + 2048u * kk, 8192u, 1024u)
-                                                 : smem_desc_sw128(sb + 32u * kk, 16u, 1024u);
-                const uint32_t accumulate = (kb > kb0 || kk > 0) ? 1u : 0u;
-                if constexpr (ELEM == ELEM_E4M3) {
-                    if constexpr (PAIR == 1) umma_f8(d_tmem, ad, bd, idesc, accumulate);
-                    else umma_f8_pair(d_tmem, ad, bd, idesc, accumulate);
-                } else {
-                    if constexpr (PAIR == 1) umma_bf16(d_tmem, ad, bd, idesc, accumulate);
-                    else umma_bf16_pair(d_tmem, ad, bd, idesc, accumulate);
+                for (int kk = 0; kk < TILE_K / UMMA_K; ++kk) {
+                    // K-major: the next 16 k sit 32 bytes further along the swizzled row.
+                    // M/N-major: the next 16 k are the next two 1024-byte row groups;
+                    // the next 64 rows of M or N are one chunk (KPS x 8 KB) further.
+                    const uint64_t ad = p.a_mn_major ? smem_desc_sw128(sa + 2048u * kk, Cfg::CHUNK_BYTES, 1024u)
+                                                     : smem_desc_sw128(sa + 32u * kk, 16u, 1024u);
+                    const uint64_t bd = p.b_mn_major ? smem_desc_sw128(sb + 2048u * kk, Cfg::CHUNK_BYTES, 1024u)
+                                                     : smem_desc_sw128(sb + 32u * kk, 16u, 1024u);
+                    const uint32_t accumulate = (kb > kb0 || sub > 0 || kk > 0) ? 1u : 0u;
+                    if (lane == 0) {
+                        if constexpr (ELEM == ELEM_E4M3) {
+                            if constexpr (PAIR == 1) umma_f8(d_tmem, ad, bd, idesc, accumulate);
+                            else umma_f8_pair(d_tmem, ad, bd, idesc, accumulate);
+                        } else {
+                            if constexpr (PAIR == 1) umma_bf16(d_tmem, ad, bd, idesc, accumulate);
+                            else umma_bf16_pair(d_tmem, ad, bd, idesc, accumulate);
+                        }
+                    }
                 }
             }
             issued_any = true;
             // the stage is free (in both CTAs) once these MMAs finish
-            if constexpr (PAIR == 1) umma_commit(bar0 + 8u * (STAGES + stage));
-            else umma_commit_pair(bar0 + 8u * (STAGES + stage), 0x3);
+            if (lane == 0) {
+                if constexpr (PAIR == 1) umma_commit(bar0 + 8u * (STAGES + stage));
+                else umma_commit_pair(bar0 + 8u * (STAGES + stage), 0x3);
+            }
             if (++stage == STAGES) {
                 stage = 0;
                 phase ^= 1u;
@@ -524,8 +578,10 @@ __device__ __forceinline__ void run_mma(const GemmParams &p, uint32_t ring, uint
         }
         if (!ok) break;
         // accumulator ready for the epilogue (of both CTAs)
-        if constexpr (PAIR == 1) umma_commit(bar0 + 8u * (2 * STAGES + acc));
-        else umma_commit_pair(bar0 + 8u * (2 * STAGES + acc), 0x3);
+        if (lane == 0) {
+            if constexpr (PAIR == 1) umma_commit(bar0 + 8u * (2 * STAGES + acc));
+            else umma_commit_pair(bar0 + 8u * (2 * STAGES + acc), 0x3);
+        }
         if (++acc == 2) {
             acc = 0;
             acc_phase ^= 1u;
@@ -535,20 +591,22 @@ __device__ __forceinline__ void run_mma(const GemmParams &p, uint32_t ring, uint
         signal_timeout(p, abort_flag);
         if (issued_any) {  // drain: MMAs in flight must finish before TMEM is freed
             const uint32_t drain = bar0 + 8u * (2 * STAGES + 4);
-            if constexpr (PAIR == 1) umma_commit(drain);
-            else umma_commit_pair(drain, 0x1);
+            if (lane == 0) {
+                if constexpr (PAIR == 1) umma_commit(drain);
+                else umma_commit_pair(drain, 0x1);
+            }
             wait_one(drain, 0u, nullptr, p.timeout_ns);
         }
     }
 }
 
-template <int BN, int STAGES, int PAIR, int ELEM>
+template <int BN, int STAGES, int PAIR, int ELEM, int KPS>
 __device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUtensorMap *tmP, const GemmParams &p,
                                              uint32_t bar0,
                                              uint32_t tmem_base, float *stage_buf, uint32_t rank,
                                              volatile int *abort_flag, int warp, int lane)
 {
-    using Cfg = KernelCfg<BN, STAGES, PAIR, ELEM>;
+    using Cfg = KernelCfg<BN, STAGES, PAIR, ELEM, KPS>;
     const int64_t units = p.num_units;
     const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31 are this warp's rows
     const int half = (warp - 2) >> 2;  // which of the two warps on this quadrant: even or odd chunks
@@ -716,13 +774,13 @@ __device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUten
 }
 
 // ---------------------------------------------------------------- kernels
-template <int BN, int STAGES, int PAIR, int ELEM>
+template <int BN, int STAGES, int PAIR, int ELEM, int KPS>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     bm_gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                            const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmP,
                            const GemmParams p)
 {
-    using Cfg = KernelCfg<BN, STAGES, PAIR, ELEM>;
+    using Cfg = KernelCfg<BN, STAGES, PAIR, ELEM, KPS>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
@@ -776,11 +834,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     griddep_wait();
 
     if (warp == 0) {
-        if (lane == 0) run_producer<BN, STAGES, PAIR, ELEM>(&tmA, &tmB, &tmC, p, ring, bar0, rank, abort_flag);
+        if (lane == 0) run_producer<BN, STAGES, PAIR, ELEM, KPS>(&tmA, &tmB, &tmC, p, ring, bar0, rank, abort_flag);
     } else if (warp == 1) {
-        if (lane == 0 && rank == 0) run_mma<BN, STAGES, PAIR, ELEM>(p, ring, bar0, tmem_base, abort_flag);
+        if (rank == 0) run_mma<BN, STAGES, PAIR, ELEM, KPS>(p, ring, bar0, tmem_base, abort_flag, lane);
     } else {
-        run_epilogue<BN, STAGES, PAIR, ELEM>(&tmC, &tmP, p, bar0, tmem_base, epi + (warp - 2) * EPI_WARP_FLOATS, rank,
+        run_epilogue<BN, STAGES, PAIR, ELEM, KPS>(&tmC, &tmP, p, bar0, tmem_base, epi + (warp - 2) * EPI_WARP_FLOATS, rank,
                                        abort_flag,
                                        warp, lane);
     }

@@ -227,7 +227,8 @@ BM_API const char *bm_status_string(bm_status status);
 
 /*
  * Resolved launch plan of a GEMM or SYRK, for reports and tests: output tile
- * (tile_m x tile_n, k-block tile_k), ring stages, number of output tiles
+ * (tile_m x tile_n, k-block tile_k), ring stages (of stage_kblocks k-blocks
+ * each), number of output tiles
  * visited, K splits and how many tiles are split (the tiles of a last, partly
  * filled wave, or all tiles when there are too few to fill the GPU), CTAs
  * launched, CTAs per output tile (2 = an SM pair working on one tile), and
@@ -245,6 +246,7 @@ typedef struct {
     int32_t kernels;
     size_t workspace_bytes;
     int64_t split_tiles;
+    int32_t stage_kblocks;
 } bm_plan;
 
 BM_API bm_status bm_gemm_bf16_plan(int64_t m, int64_t n, int64_t k, size_t workspace_bytes, bm_plan *plan);

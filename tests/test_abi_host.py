@@ -145,7 +145,7 @@ def test_gemm_plans(lib):
     st, p = bm.bm_gemm_bf16_plan(4096, 4096, 4096, 0)
     assert st == 0 and (p.tile_m, p.tile_n, p.tile_k, p.cta_pair) == (256, 256, 64, 2)
     assert p.tiles == 16 * 16 and p.k_splits == 1 and p.kernels == 1
-    assert p.ctas == 152 and p.stages == 6
+    assert p.ctas == 152 and (p.stages, p.stage_kblocks) == (3, 2)  # 3 x 2 x 32 KB ring per CTA
     st, p = bm.bm_gemm_bf16_plan(2048, 5120, 5120, 0)
     assert p.tiles == 8 * 20 and p.cta_pair == 2
     # small outputs: 128-row tiles on single SMs
