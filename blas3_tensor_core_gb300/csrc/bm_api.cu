@@ -190,14 +190,16 @@ bool encode_c_prefetch(CUtensorMap *map, void *C, bm_ctype ct, int64_t m, int64_
     return r == CUDA_SUCCESS;
 }
 
-// Map of C for the epilogue's TMA stores: box of 128 bytes (64 bf16 or 32 fp32
-// columns) x 32 rows, 128-byte swizzle (the staging layout the epilogue writes).
-bool encode_c_store(CUtensorMap *map, void *C, bm_ctype ct, int64_t m, int64_t n, int64_t ldc)
+// Map of C for the epilogue's TMA copies: box of 128 bytes (64 bf16 or 32 fp32
+// columns) x `rows` rows, 128-byte swizzle (the staging layout the epilogue
+// writes). 32 rows: one warp's stores (beta == 0); 128 rows: one CTA's rows,
+// loaded and stored by a half of the epilogue (beta != 0).
+bool encode_c_tile(CUtensorMap *map, void *C, bm_ctype ct, int64_t m, int64_t n, int64_t ldc, uint32_t rows)
 {
     const cuuint64_t esz = ct == BM_C_BF16 ? 2u : 4u;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(m)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldc) * esz};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esz), 32u};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esz), rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(map, ct == BM_C_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                           2, C, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -206,7 +208,7 @@ bool encode_c_store(CUtensorMap *map, void *C, bm_ctype ct, int64_t m, int64_t n
 }
 
 // Map of the fp32 partial slots [slots * tile rows][tile columns] for the
-// epilogue's TMA stores: box 32 x 32, 128-byte swizzle.
+// epilogue's per-warp TMA stores: box 32 x 32, 128-byte swizzle.
 bool encode_slots(CUtensorMap *map, void *partial, int64_t rows, int64_t cols)
 {
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
@@ -407,31 +409,35 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 template <int ELEM>
 cudaError_t launch_main(const cudaLaunchConfig_t &cfg, int variant, const CUtensorMap &ta, const CUtensorMap &tb,
-                        const CUtensorMap &tc, const CUtensorMap &tp, const bm::GemmParams &prm)
+                        const CUtensorMap &tc, const CUtensorMap &tp, const CUtensorMap &tcp,
+                        const bm::GemmParams &prm)
 {
     switch (variant) {
-    case kSingle256: return cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<256, 4, 1, ELEM, 1>, ta, tb, tc, tp, prm);
-    case kSingle128: return cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<128, 3, 1, ELEM, 2>, ta, tb, tc, tp, prm);
-    default: return cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<256, 3, 2, ELEM, 2>, ta, tb, tc, tp, prm);
+    case kSingle256:
+        return cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<256, 4, 1, ELEM, 1>, ta, tb, tc, tp, tcp, prm);
+    case kSingle128:
+        return cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<128, 3, 1, ELEM, 2>, ta, tb, tc, tp, tcp, prm);
+    default:
+        return cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<256, 3, 2, ELEM, 2>, ta, tb, tc, tp, tcp, prm);
     }
 }
 
 bm_status launch(const Plan &pl, const CUtensorMap &ta, const CUtensorMap &tb, bm::GemmParams &prm,
                  cudaStream_t stream, int elem = bm::ELEM_BF16)
 {
-    // beta != 0: the epilogue reads C, so each whole tile's C is prefetched into L2.
-    // beta == 0 (GEMM): the epilogue stores C with TMA through a swizzled map instead.
-    CUtensorMap tc;
+    // The epilogue moves C with TMA copies through a swizzled map (GEMM tiles, and
+    // SYRK tiles inside the triangle); with beta != 0 each whole tile's C is also
+    // prefetched into L2 while its mainloop runs.
+    CUtensorMap tc, tcp;
     std::memset(&tc, 0, sizeof(tc));
+    std::memset(&tcp, 0, sizeof(tcp));
     prm.prefetch_c = 0;
-    prm.store_c_tma = 0;
+    prm.tma_c = 0;
     const bm_ctype ct = prm.c_bf16 ? BM_C_BF16 : BM_C_F32;
-    if (prm.beta != 0.0f) {
-        if (encode_c_prefetch(&tc, prm.C, ct, prm.m, prm.n, prm.ldc, static_cast<uint32_t>(pl.bn)))
-            prm.prefetch_c = 1;
-    } else if (prm.mode == bm::MODE_GEMM) {
-        if (encode_c_store(&tc, prm.C, ct, prm.m, prm.n, prm.ldc)) prm.store_c_tma = 1;
-    }
+    if (prm.beta != 0.0f &&
+        encode_c_prefetch(&tcp, prm.C, ct, prm.m, prm.n, prm.ldc, static_cast<uint32_t>(pl.bn)))
+        prm.prefetch_c = 1;
+    if (encode_c_tile(&tc, prm.C, ct, prm.m, prm.n, prm.ldc, prm.beta != 0.0f ? bm::CTA_M : 32u)) prm.tma_c = 1;
     CUtensorMap tp;
     std::memset(&tp, 0, sizeof(tp));
     prm.store_p_tma = 0;
@@ -457,8 +463,9 @@ bm_status launch(const Plan &pl, const CUtensorMap &ta, const CUtensorMap &tb, b
         attr[1].val.clusterDim.z = 1;
         cfg.numAttrs = 2;
     }
-    const cudaError_t err = elem == bm::ELEM_E4M3 ? launch_main<bm::ELEM_E4M3>(cfg, pl.variant, ta, tb, tc, tp, prm)
-                                                  : launch_main<bm::ELEM_BF16>(cfg, pl.variant, ta, tb, tc, tp, prm);
+    const cudaError_t err = elem == bm::ELEM_E4M3
+                                ? launch_main<bm::ELEM_E4M3>(cfg, pl.variant, ta, tb, tc, tp, tcp, prm)
+                                : launch_main<bm::ELEM_BF16>(cfg, pl.variant, ta, tb, tc, tp, tcp, prm);
     if (err != cudaSuccess) {
         cudaGetLastError();
         return BM_ERR_CUDA;

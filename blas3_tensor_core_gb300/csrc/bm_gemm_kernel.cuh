@@ -72,6 +72,9 @@ __host__ __device__ constexpr int kblock_elems(int elem) { return elem == ELEM_E
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
 constexpr int EPI_WARP_FLOATS = 32 * 32;  // one 32 x 32 fp32 staging block per epilogue warp
+// The four warps of one half of the epilogue (one per quadrant) share their
+// staging blocks as one 128-row x 128-byte block.
+constexpr int GROUP_BLOCK_BYTES = 4 * EPI_WARP_FLOATS * 4;
 
 struct GemmParams {
     int64_t m, n, k;   // output rows / columns (SYRK: m == n), reduction length
@@ -94,8 +97,10 @@ struct GemmParams {
     int *status;       // device status word (first error wins)
     uint64_t timeout_ns;
     int debug_stall;   // test hook: the first stage's copy is never issued
-    int prefetch_c;    // beta != 0: tmC maps C for L2 prefetch (box tile columns x 128 rows)
-    int store_c_tma;   // beta == 0, GEMM: tmC maps C for TMA stores (box 128 bytes x 32 rows, 128B swizzle)
+    int prefetch_c;    // beta != 0: tmCP maps C for L2 prefetch (box tile columns x 128 rows)
+    int tma_c;         // tmC maps C for the epilogue's TMA copies (128B swizzle, box 128 bytes x
+                       // 32 rows for per-warp stores when beta == 0, x 128 rows for the group
+                       // load-combine-store when beta != 0)
     int syr2k_kb;      // SYR2K: k-blocks of one product; later k-blocks swap the roles of tmA and tmB
     int store_p_tma;   // split units: tmP maps the partial slots for TMA stores (fp32, box 32 x 32, 128B swizzle)
     int a_box3;        // tmA is a stage box: one 3-D copy brings a CTA's A tile for a whole stage
@@ -127,7 +132,8 @@ struct KernelCfg {
     static constexpr int CHUNK_BYTES = KPS * 8192;      // one 64-row M/N chunk of all k-blocks of a stage
     static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
     static constexpr int EPI_BYTES = NUM_EPI_WARPS * EPI_WARP_FLOATS * 4;
-    static constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, acc full x2, acc empty x2, drain
+    // full, empty, acc full x2, acc empty x2, drain, C load x2 (one per epilogue half)
+    static constexpr int NUM_BARS = 2 * STAGES + 7;
     static constexpr int BAR_BYTES = 8 * NUM_BARS + 16;
     static constexpr int SMEM_BYTES = 1024 + RING_BYTES + EPI_BYTES + BAR_BYTES;
     static constexpr int TMEM_COLS = 2 * BN;  // two accumulators
@@ -158,6 +164,15 @@ __host__ __device__ inline void syrk_row_tiles(int mode, int64_t tm, int64_t til
         lo = (TM * tm) / BN;
         hi = tiles_n - 1;
     }
+}
+
+// Does tile (tm, tn) (TM x BN) lie entirely in the referenced SYRK triangle?
+template <int TM, int BN>
+__device__ __forceinline__ bool tile_inside_triangle(int mode, int64_t tm, int64_t tn)
+{
+    if (mode == MODE_SYRK_LOWER) return tm * TM >= (tn + 1) * BN - 1;  // smallest row >= largest column
+    if (mode == MODE_SYRK_UPPER) return (tm + 1) * TM - 1 <= tn * BN;  // largest row <= smallest column
+    return true;
 }
 
 // Tile t -> (tile row, tile column): grouped raster for GEMM, row by row over
@@ -388,6 +403,22 @@ __device__ __forceinline__ void write_c4_preloaded(const GemmParams &p, int64_t 
     }
 }
 
+// Two bf16 outputs from two fp32 accumulators and two old bf16 values (packed,
+// low half first): beta * c + alpha * acc in fp32, rounded to nearest even.
+// A bf16 value is the upper 16 bits of the fp32 with the same value.
+__device__ __forceinline__ uint32_t combine_bf16x2(const GemmParams &p, uint32_t acc0, uint32_t acc1, uint32_t old)
+{
+    const float v0 = fmaf(p.beta, __uint_as_float(old << 16), p.alpha * __uint_as_float(acc0));
+    const float v1 = fmaf(p.beta, __uint_as_float(old & 0xFFFF0000u), p.alpha * __uint_as_float(acc1));
+    const __nv_bfloat162 h = __floats2bfloat162_rn(v0, v1);
+    return static_cast<uint32_t>(__bfloat16_as_ushort(h.x)) | (static_cast<uint32_t>(__bfloat16_as_ushort(h.y)) << 16);
+}
+
+__device__ __forceinline__ uint32_t combine_f32(const GemmParams &p, uint32_t acc, uint32_t old)
+{
+    return __float_as_uint(fmaf(p.beta, __uint_as_float(old), p.alpha * __uint_as_float(acc)));
+}
+
 // Is C[i, j..j+3] a full vector inside the output (no edge, no triangle mask)?
 __device__ __forceinline__ bool full_vector(const GemmParams &p, int64_t i, int64_t j)
 {
@@ -448,7 +479,7 @@ __device__ __forceinline__ void load_operand(uint32_t dst, const CUtensorMap *ma
 }
 
 template <int BN, int STAGES, int PAIR, int ELEM, int KPS>
-__device__ __forceinline__ void run_producer(const CUtensorMap *tmA, const CUtensorMap *tmB, const CUtensorMap *tmC,
+__device__ __forceinline__ void run_producer(const CUtensorMap *tmA, const CUtensorMap *tmB, const CUtensorMap *tmCP,
                                              const GemmParams &p, uint32_t ring, uint32_t bar0, uint32_t rank,
                                              volatile int *abort_flag)
 {
@@ -465,7 +496,7 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmA, const CUten
         const int32_t row_a = static_cast<int32_t>(w.tm * Cfg::TILE_M + rank * CTA_M);
         const int32_t row_b = static_cast<int32_t>(w.tn * BN + rank * Cfg::B_ROWS);
         // The epilogue of this tile will read this CTA's 128 rows of C: start pulling them into L2.
-        if (p.prefetch_c && w.slot < 0) tma_prefetch_l2_2d(tmC, static_cast<int32_t>(w.tn * BN), row_a);
+        if (p.prefetch_c && w.slot < 0) tma_prefetch_l2_2d(tmCP, static_cast<int32_t>(w.tn * BN), row_a);
         for (int kb = kb0; kb < kb1; kb += KPS) {
             const uint32_t empty = bar0 + 8u * (STAGES + stage);
             if (!wait_one<PAIR == 2>(empty, phase ^ 1u, abort_flag, p.timeout_ns)) {
@@ -602,20 +633,34 @@ __device__ __forceinline__ void run_mma(const GemmParams &p, uint32_t ring, uint
 
 template <int BN, int STAGES, int PAIR, int ELEM, int KPS>
 __device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUtensorMap *tmP, const GemmParams &p,
-                                             uint32_t bar0,
-                                             uint32_t tmem_base, float *stage_buf, uint32_t rank,
+                                             uint32_t bar0, uint32_t tmem_base, float *epi, uint32_t rank,
                                              volatile int *abort_flag, int warp, int lane)
 {
     using Cfg = KernelCfg<BN, STAGES, PAIR, ELEM, KPS>;
     const int64_t units = p.num_units;
     const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31 are this warp's rows
     const int half = (warp - 2) >> 2;  // which of the two warps on this quadrant: even or odd chunks
+    const int group_bar = 1 + half;    // named barrier of the four warps of this half
+    float *stage_buf = epi + (warp - 2) * EPI_WARP_FLOATS;  // this warp's own block (per-warp path)
     const bool beta_nonzero = p.beta != 0.0f;
+    const bool issuer = quad == 0 && lane == 0;  // issues this half's TMA copies in the group path
     int acc = 0;
-    uint32_t acc_phase = 0;
+    uint32_t acc_phase = 0, c_phase = 0;
     for (int64_t u = first_unit<PAIR>(); u < units; u += unit_stride<PAIR>()) {
         const Unit w = map_unit<Cfg::TILE_M, BN>(p, u);
-        if (!wait_warp<PAIR == 2>(bar0 + 8u * (2 * STAGES + acc), acc_phase, abort_flag, p.timeout_ns)) {
+        const bool to_slot = w.slot >= 0;
+        // Paths: beta != 0 tiles of GEMM (and SYRK tiles inside the triangle) go through
+        // the group path (TMA load of C, combine, TMA store); beta == 0 tiles and split
+        // units through the per-warp TMA-store path; SYRK tiles across the diagonal
+        // through the per-warp transposing path with per-element masks.
+        const bool inside = tile_inside_triangle<Cfg::TILE_M, BN>(p.mode, w.tm, w.tn);
+        const bool group = !to_slot && beta_nonzero && p.tma_c && inside;  // the same for every warp
+        const bool warp_tma = to_slot ? p.store_p_tma != 0 : (!beta_nonzero && p.tma_c && inside);
+        bool ready = wait_warp<PAIR == 2>(bar0 + 8u * (2 * STAGES + acc), acc_phase, abort_flag, p.timeout_ns);
+        // A half that will meet at named barriers decides together, so that none of its
+        // warps is left waiting at one.
+        if (group) ready = group_all(ready, group_bar, 128);
+        if (!ready) {
             if (lane == 0) signal_timeout(p, abort_flag);
             break;
         }
@@ -628,8 +673,95 @@ __device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUten
         const int64_t row0 = w.tm * Cfg::TILE_M + rank * CTA_M + quad * 32;
         const int64_t col0 = w.tn * BN;
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN);
-        const bool to_slot = w.slot >= 0;
-        if (to_slot ? p.store_p_tma : p.store_c_tma) {
+        if (group) {
+            // Per chunk of 128 bytes per row (64 bf16 or 32 fp32 columns), one thread of
+            // this half loads the chunk of C (its 128 rows) into one 128B-swizzled
+            // staging block with a single TMA copy; the four warps each combine their
+            // 32 rows in place (beta * c + alpha * acc, as the other paths) and one
+            // TMA copy stores the block back (the map clips rows >= m and columns >= n).
+            const CUtensorMap *map = tmC;
+            const bool bf16_out = p.c_bf16 != 0;
+            const int cw = bf16_out ? 64 : 32;
+            const int nchunks = BN / cw;
+            uint8_t *block = reinterpret_cast<uint8_t *>(epi) + half * GROUP_BLOCK_BYTES;
+            const uint32_t block_addr = smem_addr(block);
+            uint4 *myrow = reinterpret_cast<uint4 *>(block + (quad * 32 + lane) * 128);
+            const int32_t ys = static_cast<int32_t>(w.tm * Cfg::TILE_M + rank * CTA_M);
+            const bool rows_in = ys < p.m;
+            const uint32_t cbar = bar0 + 8u * (2 * STAGES + 5 + half);
+            bool gok = true, loading = false;
+            for (int c = half; c < nchunks; c += 2) {
+                const int32_t xs = static_cast<int32_t>(col0 + static_cast<int64_t>(c) * cw);
+                const bool live = rows_in && xs < p.n;  // the same for the whole half
+                if (issuer && live) {
+                    mbar_arrive_expect_tx(cbar, GROUP_BLOCK_BYTES);
+                    tma_load_2d(block_addr, map, cbar, xs, ys);
+                    loading = true;
+                }
+                bool ok = true;
+                if (live) {
+                    ok = wait_warp<false>(cbar, c_phase, abort_flag, p.timeout_ns);
+                    c_phase ^= 1u;
+                }
+                // 32 accumulator columns at a time: 16-byte units 0-3 of the row (bf16) or
+                // all 8 (fp32, one pass)
+                for (int part = 0; part < cw / 32; ++part) {
+                    uint32_t r[32];
+                    tmem_load_32cols(taddr + static_cast<uint32_t>(c * cw + 32 * part), r);
+                    if (ok) {
+                        if (bf16_out) {
+#pragma unroll
+                            for (int jj = 0; jj < 4; ++jj) {
+                                uint4 *slot = myrow + ((4 * part + jj) ^ (lane & 7));
+                                const uint4 old = *slot;
+                                uint4 q;
+                                q.x = combine_bf16x2(p, r[8 * jj + 0], r[8 * jj + 1], old.x);
+                                q.y = combine_bf16x2(p, r[8 * jj + 2], r[8 * jj + 3], old.y);
+                                q.z = combine_bf16x2(p, r[8 * jj + 4], r[8 * jj + 5], old.z);
+                                q.w = combine_bf16x2(p, r[8 * jj + 6], r[8 * jj + 7], old.w);
+                                *slot = q;
+                            }
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                uint4 *slot = myrow + (j ^ (lane & 7));
+                                const uint4 old = *slot;
+                                uint4 q;
+                                q.x = combine_f32(p, r[4 * j + 0], old.x);
+                                q.y = combine_f32(p, r[4 * j + 1], old.y);
+                                q.z = combine_f32(p, r[4 * j + 2], old.z);
+                                q.w = combine_f32(p, r[4 * j + 3], old.w);
+                                *slot = q;
+                            }
+                        }
+                    }
+                }
+                if (c + 2 >= nchunks) {  // this warp's last chunk of the tile: release the accumulator
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) {
+                        const uint32_t acc_empty = bar0 + 8u * (2 * STAGES + 2 + acc);
+                        if constexpr (PAIR == 1) mbar_arrive(acc_empty);
+                        else mbar_arrive_remote(map_shared_to_rank(acc_empty, 0));
+                    }
+                }
+                fence_proxy_async_shared();
+                gok = group_all(ok, group_bar, 128);  // every row of the block is written
+                if (!gok) break;
+                loading = false;
+                if (issuer && live) {
+                    tma_store_2d(map, block_addr, xs, ys);
+                    bulk_commit_group();
+                    bulk_wait_group_read0();  // the store has read the block
+                }
+                group_sync(group_bar, 128);  // the block may be written again
+            }
+            if (!gok) {
+                if (lane == 0) signal_timeout(p, abort_flag);
+                if (issuer && loading) spin_ns(100000);  // a C copy may still land in the block
+                break;
+            }
+        } else if (warp_tma) {
             // Chunks of 128 bytes per row (64 bf16 or 32 fp32 columns), 32 rows: each lane
             // converts its row into a 128B-swizzled staging block, one lane stores it with
             // TMA, into C (the map clips rows >= m and columns >= n) or into the unit's
@@ -770,7 +902,7 @@ __device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUten
             acc_phase ^= 1u;
         }
     }
-    if ((p.store_c_tma || p.store_p_tma) && lane == 0) bulk_wait_group0();  // stores done before exit
+    if ((p.tma_c || p.store_p_tma) && issuer) bulk_wait_group0();  // stores done before exit
 }
 
 // ---------------------------------------------------------------- kernels
@@ -778,7 +910,7 @@ template <int BN, int STAGES, int PAIR, int ELEM, int KPS>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     bm_gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                            const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmP,
-                           const GemmParams p)
+                           const __grid_constant__ CUtensorMap tmCP, const GemmParams p)
 {
     using Cfg = KernelCfg<BN, STAGES, PAIR, ELEM, KPS>;
     extern __shared__ uint8_t smem_raw[];
@@ -805,13 +937,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(bar0 + 8u * (2 * STAGES + 2 + b), NUM_EPI_WARPS * PAIR);  // accumulator empty
         }
         mbar_init(bar0 + 8u * (2 * STAGES + 4), 1);  // drain (abort path only)
+        mbar_init(bar0 + 8u * (2 * STAGES + 5), 1);  // C load, epilogue half 0
+        mbar_init(bar0 + 8u * (2 * STAGES + 6), 1);  // C load, epilogue half 1
         *abort_flag = 0;
         fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
         tma_prefetch_map(&tmA);
         tma_prefetch_map(&tmB);
-        if (p.prefetch_c || p.store_c_tma) tma_prefetch_map(&tmC);
+        if (p.tma_c) tma_prefetch_map(&tmC);
+        if (p.prefetch_c) tma_prefetch_map(&tmCP);
         if (p.store_p_tma) tma_prefetch_map(&tmP);
     }
     if (warp == 1) {
@@ -834,11 +969,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     griddep_wait();
 
     if (warp == 0) {
-        if (lane == 0) run_producer<BN, STAGES, PAIR, ELEM, KPS>(&tmA, &tmB, &tmC, p, ring, bar0, rank, abort_flag);
+        if (lane == 0) run_producer<BN, STAGES, PAIR, ELEM, KPS>(&tmA, &tmB, &tmCP, p, ring, bar0, rank, abort_flag);
     } else if (warp == 1) {
         if (rank == 0) run_mma<BN, STAGES, PAIR, ELEM, KPS>(p, ring, bar0, tmem_base, abort_flag, lane);
     } else {
-        run_epilogue<BN, STAGES, PAIR, ELEM, KPS>(&tmC, &tmP, p, bar0, tmem_base, epi + (warp - 2) * EPI_WARP_FLOATS, rank,
+        run_epilogue<BN, STAGES, PAIR, ELEM, KPS>(&tmC, &tmP, p, bar0, tmem_base, epi, rank,
                                        abort_flag,
                                        warp, lane);
     }

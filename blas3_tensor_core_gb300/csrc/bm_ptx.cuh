@@ -62,6 +62,27 @@ __device__ __forceinline__ uint32_t map_shared_to_rank(uint32_t addr, uint32_t r
     return r;
 }
 
+// Named barrier over `nthreads` threads (a multiple of 32); id 0 is __syncthreads.
+__device__ __forceinline__ void group_sync(int id, int nthreads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Named barrier that also returns the AND of `v` over its threads.
+__device__ __forceinline__ bool group_all(bool v, int id, int nthreads)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.and.pred p, %2, %3, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
+
 // ---------------------------------------------------------------- programmatic dependent launch
 // Lets the next kernel on the stream (launched with programmatic stream
 // serialisation) be scheduled onto SMs as this grid's CTAs finish.
