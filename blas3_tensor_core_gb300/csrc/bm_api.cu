@@ -175,21 +175,6 @@ bool encode_bf16_2d(CUtensorMap *map, const void *base, int64_t inner, int64_t o
     return encode_operand_2d(map, base, bm::ELEM_BF16, inner, outer, ld, box_inner, box_outer);
 }
 
-// Map of C used only to prefetch each CTA's output rows into L2 (box: tile
-// columns x 128 rows, no swizzle).
-bool encode_c_prefetch(CUtensorMap *map, void *C, bm_ctype ct, int64_t m, int64_t n, int64_t ldc, uint32_t cols)
-{
-    const cuuint64_t esz = ct == BM_C_BF16 ? 2u : 4u;
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(m)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldc) * esz};
-    cuuint32_t box[2] = {cols, static_cast<cuuint32_t>(bm::CTA_M)};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(map, ct == BM_C_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
-                          2, C, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
 // Map of C for the epilogue's TMA copies: box of 128 bytes (64 bf16 or 32 fp32
 // columns) x `rows` rows, 128-byte swizzle (the staging layout the epilogue
 // writes). 32 rows: one warp's stores (beta == 0); 128 rows: one CTA's rows,
@@ -409,16 +394,15 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 template <int ELEM>
 cudaError_t launch_main(const cudaLaunchConfig_t &cfg, int variant, const CUtensorMap &ta, const CUtensorMap &tb,
-                        const CUtensorMap &tc, const CUtensorMap &tp, const CUtensorMap &tcp,
-                        const bm::GemmParams &prm)
+                        const CUtensorMap &tc, const CUtensorMap &tp, const bm::GemmParams &prm)
 {
     switch (variant) {
     case kSingle256:
-        return cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<256, 4, 1, ELEM, 1>, ta, tb, tc, tp, tcp, prm);
+        return cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<256, 4, 1, ELEM, 1>, ta, tb, tc, tp, prm);
     case kSingle128:
-        return cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<128, 3, 1, ELEM, 2>, ta, tb, tc, tp, tcp, prm);
+        return cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<128, 3, 1, ELEM, 2>, ta, tb, tc, tp, prm);
     default:
-        return cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<256, 3, 2, ELEM, 2>, ta, tb, tc, tp, tcp, prm);
+        return cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<256, 3, 2, ELEM, 2>, ta, tb, tc, tp, prm);
     }
 }
 
@@ -426,17 +410,13 @@ bm_status launch(const Plan &pl, const CUtensorMap &ta, const CUtensorMap &tb, b
                  cudaStream_t stream, int elem = bm::ELEM_BF16)
 {
     // The epilogue moves C with TMA copies through a swizzled map (GEMM tiles, and
-    // SYRK tiles inside the triangle); with beta != 0 each whole tile's C is also
-    // prefetched into L2 while its mainloop runs.
-    CUtensorMap tc, tcp;
+    // SYRK tiles inside the triangle). C is not prefetched into L2 ahead of the
+    // epilogue: a prefetch copy occupies the same TMA unit as the operand copies
+    // and cost more mainloop time than the load latency it hid.
+    CUtensorMap tc;
     std::memset(&tc, 0, sizeof(tc));
-    std::memset(&tcp, 0, sizeof(tcp));
-    prm.prefetch_c = 0;
     prm.tma_c = 0;
     const bm_ctype ct = prm.c_bf16 ? BM_C_BF16 : BM_C_F32;
-    if (prm.beta != 0.0f &&
-        encode_c_prefetch(&tcp, prm.C, ct, prm.m, prm.n, prm.ldc, static_cast<uint32_t>(pl.bn)))
-        prm.prefetch_c = 1;
     if (encode_c_tile(&tc, prm.C, ct, prm.m, prm.n, prm.ldc, prm.beta != 0.0f ? bm::CTA_M : 32u)) prm.tma_c = 1;
     CUtensorMap tp;
     std::memset(&tp, 0, sizeof(tp));
@@ -464,8 +444,8 @@ bm_status launch(const Plan &pl, const CUtensorMap &ta, const CUtensorMap &tb, b
         cfg.numAttrs = 2;
     }
     const cudaError_t err = elem == bm::ELEM_E4M3
-                                ? launch_main<bm::ELEM_E4M3>(cfg, pl.variant, ta, tb, tc, tp, tcp, prm)
-                                : launch_main<bm::ELEM_BF16>(cfg, pl.variant, ta, tb, tc, tp, tcp, prm);
+                                ? launch_main<bm::ELEM_E4M3>(cfg, pl.variant, ta, tb, tc, tp, prm)
+                                : launch_main<bm::ELEM_BF16>(cfg, pl.variant, ta, tb, tc, tp, prm);
     if (err != cudaSuccess) {
         cudaGetLastError();
         return BM_ERR_CUDA;

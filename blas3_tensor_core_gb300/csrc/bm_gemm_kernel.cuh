@@ -97,7 +97,6 @@ struct GemmParams {
     int *status;       // device status word (first error wins)
     uint64_t timeout_ns;
     int debug_stall;   // test hook: the first stage's copy is never issued
-    int prefetch_c;    // beta != 0: tmCP maps C for L2 prefetch (box tile columns x 128 rows)
     int tma_c;         // tmC maps C for the epilogue's TMA copies (128B swizzle, box 128 bytes x
                        // 32 rows for per-warp stores when beta == 0, x 128 rows for the group
                        // load-combine-store when beta != 0)
@@ -479,7 +478,7 @@ __device__ __forceinline__ void load_operand(uint32_t dst, const CUtensorMap *ma
 }
 
 template <int BN, int STAGES, int PAIR, int ELEM, int KPS>
-__device__ __forceinline__ void run_producer(const CUtensorMap *tmA, const CUtensorMap *tmB, const CUtensorMap *tmCP,
+__device__ __forceinline__ void run_producer(const CUtensorMap *tmA, const CUtensorMap *tmB,
                                              const GemmParams &p, uint32_t ring, uint32_t bar0, uint32_t rank,
                                              volatile int *abort_flag)
 {
@@ -495,8 +494,6 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmA, const CUten
         const int kb1 = w.kb1;
         const int32_t row_a = static_cast<int32_t>(w.tm * Cfg::TILE_M + rank * CTA_M);
         const int32_t row_b = static_cast<int32_t>(w.tn * BN + rank * Cfg::B_ROWS);
-        // The epilogue of this tile will read this CTA's 128 rows of C: start pulling them into L2.
-        if (p.prefetch_c && w.slot < 0) tma_prefetch_l2_2d(tmCP, static_cast<int32_t>(w.tn * BN), row_a);
         for (int kb = kb0; kb < kb1; kb += KPS) {
             const uint32_t empty = bar0 + 8u * (STAGES + stage);
             if (!wait_one<PAIR == 2>(empty, phase ^ 1u, abort_flag, p.timeout_ns)) {
@@ -910,7 +907,7 @@ template <int BN, int STAGES, int PAIR, int ELEM, int KPS>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     bm_gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                            const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmP,
-                           const __grid_constant__ CUtensorMap tmCP, const GemmParams p)
+                           const GemmParams p)
 {
     using Cfg = KernelCfg<BN, STAGES, PAIR, ELEM, KPS>;
     extern __shared__ uint8_t smem_raw[];
@@ -946,7 +943,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tma_prefetch_map(&tmA);
         tma_prefetch_map(&tmB);
         if (p.tma_c) tma_prefetch_map(&tmC);
-        if (p.prefetch_c) tma_prefetch_map(&tmCP);
         if (p.store_p_tma) tma_prefetch_map(&tmP);
     }
     if (warp == 1) {
@@ -969,7 +965,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     griddep_wait();
 
     if (warp == 0) {
-        if (lane == 0) run_producer<BN, STAGES, PAIR, ELEM, KPS>(&tmA, &tmB, &tmCP, p, ring, bar0, rank, abort_flag);
+        if (lane == 0) run_producer<BN, STAGES, PAIR, ELEM, KPS>(&tmA, &tmB, p, ring, bar0, rank, abort_flag);
     } else if (warp == 1) {
         if (rank == 0) run_mma<BN, STAGES, PAIR, ELEM, KPS>(p, ring, bar0, tmem_base, abort_flag, lane);
     } else {
