@@ -818,6 +818,19 @@ bm_status bm_syr2k_bf16(bm_uplo uplo, bm_op trans, int64_t n, int64_t k, float a
     prm.b_mn_major = mn;
     fill_params(prm, pl);
     prm.syr2k_kb = pl.kb_total / 2;
+    // Stage boxes when no stage straddles the swap of A and B (both maps then serve
+    // as stage boxes of 128 rows in both roles).
+    const int kps = kVariantStageKBlocks[pl.variant];
+    if (prm.syr2k_kb % kps == 0) {
+        CUtensorMap ta3 = ta, tb3 = tb;
+        if (encode_stage_box(&ta3, A, bm::ELEM_BF16, mn, n, k, lda, bm::CTA_M, kps) &&
+            encode_stage_box(&tb3, B, bm::ELEM_BF16, mn, n, k, ldb, bm::CTA_M, kps)) {
+            ta = ta3;
+            tb = tb3;
+            prm.a_box3 = 1;
+            prm.b_box3 = 1;
+        }
+    }
     return launch(pl, ta, tb, prm, cs);
 }
 

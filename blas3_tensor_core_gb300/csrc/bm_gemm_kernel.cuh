@@ -450,15 +450,19 @@ __device__ __forceinline__ void load_box3(uint32_t dst, const CUtensorMap *map, 
 // dst, in the stage layout above. A stage box is one 3-D copy: K-major maps
 // are (k in k-block, row, k-block), M/N-major maps (m or n in chunk, k,
 // chunk). Otherwise one 2-D copy per k-block (and per chunk). SYR2K swaps the
-// roles of tmA and tmB from k-block syr2k_kb on (stage boxes are not used there).
+// roles of tmA and tmB from k-block syr2k_kb on; with stage boxes the host only
+// allows this when syr2k_kb is a whole number of stages.
 template <int PAIR, int KPS, int ROWS, int KB_ELEMS>
 __device__ __forceinline__ void load_operand(uint32_t dst, const CUtensorMap *map, const CUtensorMap *alt,
                                              bool box3, bool mn_major, uint32_t bar, int32_t row0, int kb,
                                              int syr2k_kb)
 {
     if (box3) {
-        if (mn_major) load_box3<PAIR>(dst, map, bar, 0, kb * KB_ELEMS, row0 / 64);
-        else load_box3<PAIR>(dst, map, bar, 0, row0, kb);
+        const bool swap = syr2k_kb > 0 && kb >= syr2k_kb;
+        const CUtensorMap *m = swap ? alt : map;
+        const int kbs = swap ? kb - syr2k_kb : kb;
+        if (mn_major) load_box3<PAIR>(dst, m, bar, 0, kbs * KB_ELEMS, row0 / 64);
+        else load_box3<PAIR>(dst, m, bar, 0, row0, kbs);
         return;
     }
 #pragma unroll

@@ -39,7 +39,9 @@ def _ab(n, k, trans, dist, seed, std=1.0, lo=-1.0, hi=1.0):
 # variants: automatic, single-SM 128x128 (128x256 falls back to it), SM-pair 256x256
 @pytest.mark.parametrize("variant", [0, 2, 3], ids=["auto", "single128x128", "pair256x256"])
 @pytest.mark.parametrize("uplo,trans", list(itertools.product((0, 1), (0, 1))))
-@pytest.mark.parametrize("n,k", [(300, 136), (256, 64), (520, 200)])
+# (320, 256): K is a whole number of two-k-block stages and n of 64-wide chunks, so both
+# operands use stage-box copies on either side of the A/B swap
+@pytest.mark.parametrize("n,k", [(300, 136), (256, 64), (520, 200), (320, 256)])
 def test_syr2k_exact_integer(uplo, trans, n, k, variant):
     A, B = _ab(n, k, trans, "int", seed=15, lo=-8, hi=8)
     c0 = gen.integers(16, n * n, -50, 50).reshape(n, n).astype(np.float32)
