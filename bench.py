@@ -654,6 +654,9 @@ def parse_args(argv=None):
     ap.add_argument("--sweep-steps", type=int, default=200)
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--all-configs", action="store_true", help="also time the backward pair, 256^3 and SYRK")
+    ap.add_argument("--workload", default=None,
+                    help="time only this named sweep / extra / SYRK / SYR2K workload (for profiling); prints "
+                         "one JSON line for it instead of the bench line")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--reference-budget-s", type=float, default=120.0)
@@ -665,12 +668,37 @@ def parse_args(argv=None):
     return args
 
 
+def workload_only(args, dist):
+    """--workload NAME: W warm-up and K timed steps of one named workload (used for ncu captures)."""
+    import torch
+    torch.cuda.set_device(dist.local)
+    import blas3_tensor_core_gb300 as bm
+    if not os.path.exists(bm.library_path):
+        from blas3_tensor_core_gb300 import build
+        build.build()
+    peaks = load_peaks()
+    if args.workload in (SYRK_CFG["name"], "syr2k_lower_8192x4096_f32c_beta1"):
+        a = argparse.Namespace(**vars(args))
+        a.sweep_steps = max(4 * (args.steps - 1), 0)
+        return syrk_point(a, dist, peaks, two_products=args.workload.startswith("syr2k"))
+    cfg = next((c for c in [MAIN] + SWEEP + EXTRA if c["name"] == args.workload), None)
+    if cfg is None:
+        raise SystemExit(f"unknown workload {args.workload!r}")
+    wl = GemmWorkload(cfg, torch)
+    ms = timed_steps(wl, args.steps, args.warmup, dist)
+    t = ms / args.steps * 1e-3
+    return {"workload": cfg["name"], "us_per_step": round(t * 1e6, 3), "tflops": round(wl.flops() / t / 1e12, 2),
+            "steps": args.steps, "warmup": args.warmup, "plan": wl.plan.as_dict()}
+
+
 def main(argv=None):
     args = parse_args(argv)
     dist = Dist()
     try:
         if args.impl == "reference":
             line = reference_arm(args, dist)
+        elif args.workload:
+            line = workload_only(args, dist)
         else:
             line = run_gpu_arm(args, dist)
         if dist.rank == 0 and line is not None:

@@ -269,6 +269,7 @@ struct Plan {
     int64_t full_tiles = 0, num_units = 0;  // whole tiles first; the rest are split k_splits ways
     int k_splits = 1, kb_per_split = 0, kb_total = 0;
     int ctas = 0;
+    int64_t syrk_cross = 0;  // SYRK: tiles crossing the diagonal
     size_t ws_bytes = 0;
 };
 
@@ -285,6 +286,20 @@ void set_variant(Plan &pl, int v)
     pl.stages = kVariantStages[v];
     pl.pair = kVariantPair[v];
     pl.tile_m = bm::CTA_M * pl.pair;
+}
+
+// Tiles of the triangle that cross the diagonal.
+int64_t syrk_cross_count(int mode, int64_t tiles_m, int64_t tiles_n, int tile_m, int bn)
+{
+    int64_t total = 0;
+    for (int64_t tm = 0; tm < tiles_m; ++tm) {
+        int64_t lo, hi, clo, chi;
+        if (tile_m == 256) bm::syrk_row_crossing<256, 256>(mode, tm, tiles_n, lo, hi, clo, chi);
+        else if (bn == 128) bm::syrk_row_crossing<128, 128>(mode, tm, tiles_n, lo, hi, clo, chi);
+        else bm::syrk_row_crossing<128, 256>(mode, tm, tiles_n, lo, hi, clo, chi);
+        if (chi >= clo) total += chi - clo + 1;
+    }
+    return total;
 }
 
 int64_t syrk_tile_count(int mode, int64_t tiles_m, int64_t tiles_n, int tile_m, int bn)
@@ -383,6 +398,7 @@ Plan plan_syrk(int mode, int64_t n, int64_t k, int sms, int pair_clusters, bool 
     pl.tiles_m = ceil_div(n, pl.tile_m);
     pl.tiles_n = ceil_div(n, pl.bn);
     pl.num_tiles = syrk_tile_count(mode, pl.tiles_m, pl.tiles_n, pl.tile_m, pl.bn);
+    pl.syrk_cross = syrk_cross_count(mode, pl.tiles_m, pl.tiles_n, pl.tile_m, pl.bn);
     pl.full_tiles = pl.num_tiles;
     pl.kb_total = static_cast<int>(ceil_div(std::max<int64_t>(k, 1), bm::TILE_K)) * (two_products ? 2 : 1);
     pl.kb_per_split = pl.kb_total;
@@ -507,6 +523,7 @@ void fill_params(bm::GemmParams &prm, const Plan &pl)
     prm.k_splits = pl.k_splits;
     prm.kb_per_split = pl.kb_per_split;
     prm.kb_total = pl.kb_total;
+    prm.syrk_cross = pl.syrk_cross;
 }
 
 void export_plan(const Plan &pl, bm_plan *plan)

@@ -102,6 +102,7 @@ struct GemmParams {
                        // load-combine-store when beta != 0)
     int syr2k_kb;      // SYR2K: k-blocks of one product; later k-blocks swap the roles of tmA and tmB
     int store_p_tma;   // split units: tmP maps the partial slots for TMA stores (fp32, box 32 x 32, 128B swizzle)
+    int64_t syrk_cross; // SYRK: number of tiles crossing the diagonal (visited first)
     int a_box3;        // tmA is a stage box: one 3-D copy brings a CTA's A tile for a whole stage
     int b_box3;        // same for tmB
 };
@@ -167,11 +168,32 @@ __host__ __device__ inline void syrk_row_tiles(int mode, int64_t tm, int64_t til
 
 // Does tile (tm, tn) (TM x BN) lie entirely in the referenced SYRK triangle?
 template <int TM, int BN>
-__device__ __forceinline__ bool tile_inside_triangle(int mode, int64_t tm, int64_t tn)
+__host__ __device__ inline bool tile_inside_triangle(int mode, int64_t tm, int64_t tn)
 {
     if (mode == MODE_SYRK_LOWER) return tm * TM >= (tn + 1) * BN - 1;  // smallest row >= largest column
     if (mode == MODE_SYRK_UPPER) return (tm + 1) * TM - 1 <= tn * BN;  // largest row <= smallest column
     return true;
+}
+
+// Tiles [lo, hi] of tile row tm touch the triangle; of those, [cross_lo, cross_hi]
+// (possibly empty: cross_lo > cross_hi) cross the diagonal and the rest lie
+// inside it (tile_inside_triangle).
+template <int TM, int BN>
+__host__ __device__ inline void syrk_row_crossing(int mode, int64_t tm, int64_t tiles_n, int64_t &lo, int64_t &hi,
+                                                  int64_t &cross_lo, int64_t &cross_hi)
+{
+    syrk_row_tiles<TM, BN>(mode, tm, tiles_n, lo, hi);
+    if (mode == MODE_SYRK_LOWER) {
+        // inside: (tn + 1) * BN - 1 <= tm * TM
+        const int64_t in_hi = (tm * TM + 1) / BN - 1;
+        cross_lo = in_hi + 1 > lo ? in_hi + 1 : lo;
+        cross_hi = hi;
+    } else {
+        // inside: (tm + 1) * TM - 1 <= tn * BN
+        const int64_t in_lo = ((tm + 1) * TM - 1 + BN - 1) / BN;
+        cross_lo = lo;
+        cross_hi = in_lo - 1 < hi ? in_lo - 1 : hi;
+    }
 }
 
 // Tile t -> (tile row, tile column): grouped raster for GEMM, row by row over
@@ -190,14 +212,22 @@ __device__ __forceinline__ void tile_coords(const GemmParams &p, int64_t t, int6
         tm = first + local % rows;
         tn = local / rows;
     } else {
-        int64_t rem = t;
+        // SYRK: first the syrk_cross tiles that cross the diagonal (their epilogue masks
+        // each element and is slower, so it should overlap later tiles' mainloops
+        // rather than end the kernel), then the tiles inside the triangle; each part
+        // row by row.
+        const bool cross = t < p.syrk_cross;
+        int64_t rem = cross ? t : t - p.syrk_cross;
         for (int64_t r = 0; r < p.tiles_m; ++r) {
-            int64_t lo, hi;
-            syrk_row_tiles<TM, BN>(p.mode, r, p.tiles_n, lo, hi);
-            const int64_t cnt = hi - lo + 1;
+            int64_t lo, hi, clo, chi;
+            syrk_row_crossing<TM, BN>(p.mode, r, p.tiles_n, lo, hi, clo, chi);
+            const int64_t ncross = chi >= clo ? chi - clo + 1 : 0;
+            const int64_t cnt = cross ? ncross : (hi - lo + 1) - ncross;
             if (rem < cnt) {
                 tm = r;
-                tn = lo + rem;
+                if (cross) tn = clo + rem;
+                else if (p.mode == MODE_SYRK_LOWER) tn = lo + rem;  // inside tiles precede the crossing ones
+                else tn = (ncross > 0 ? chi + 1 : lo) + rem;        // inside tiles follow the crossing ones
                 break;
             }
             rem -= cnt;
