@@ -792,6 +792,92 @@ __device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUten
                 if (issuer && loading) spin_ns(100000);  // a C copy may still land in the block
                 break;
             }
+        } else if (!inside && p.tma_c) {
+            // SYRK tile across the diagonal: registers straight to C. Per chunk of 128
+            // bytes per row (64 bf16 or 32 fp32 columns), lane l owns row row0 + l of
+            // this warp's 32 x chunk block. A block wholly outside the triangle is
+            // skipped; one wholly inside (and inside m x n) moves with 16-byte loads
+            // and stores; the block on the diagonal (and any block at the edge of C)
+            // goes element by element. The other triangle is neither read nor written.
+            const bool bf16_out = p.c_bf16 != 0;
+            const int cw = bf16_out ? 64 : 32;
+            const int nchunks = BN / cw;
+            const int64_t gi = row0 + lane;
+            const bool lower = p.mode == MODE_SYRK_LOWER;
+            for (int c = half; c < nchunks; c += 2) {
+                // 32 columns at a time: [xp, xp + 32) of rows [row0, row0 + 32)
+                for (int part = 0; part < cw / 32; ++part) {
+                    const int64_t xp = col0 + static_cast<int64_t>(c) * cw + 32 * part;
+                    const bool outside = lower ? row0 + 31 < xp : row0 > xp + 31;
+                    const bool full = (lower ? row0 >= xp + 31 : row0 + 31 <= xp) && row0 + 32 <= p.m &&
+                                      xp + 32 <= p.n;
+                    uint32_t r[32];
+                    if (!outside) tmem_load_32cols(taddr + static_cast<uint32_t>(c * cw + 32 * part), r);
+                    if (c + 2 >= nchunks && part == cw / 32 - 1) {  // this warp's accumulator part is read
+                        tc_fence_before_sync();
+                        __syncwarp();
+                        if (lane == 0) {
+                            const uint32_t acc_empty = bar0 + 8u * (2 * STAGES + 2 + acc);
+                            if constexpr (PAIR == 1) mbar_arrive(acc_empty);
+                            else mbar_arrive_remote(map_shared_to_rank(acc_empty, 0));
+                        }
+                    }
+                    if (outside) continue;
+                    if (full && bf16_out) {
+                        uint4 *row = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.C) + gi * p.ldc + xp);
+                        uint4 old[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) old[j] = beta_nonzero ? row[j] : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            uint4 q;
+                            q.x = combine_bf16x2(p, r[8 * j + 0], r[8 * j + 1], old[j].x);
+                            q.y = combine_bf16x2(p, r[8 * j + 2], r[8 * j + 3], old[j].y);
+                            q.z = combine_bf16x2(p, r[8 * j + 4], r[8 * j + 5], old[j].z);
+                            q.w = combine_bf16x2(p, r[8 * j + 6], r[8 * j + 7], old[j].w);
+                            row[j] = q;
+                        }
+                    } else if (full) {
+                        uint4 *row = reinterpret_cast<uint4 *>(reinterpret_cast<float *>(p.C) + gi * p.ldc + xp);
+                        uint4 old[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) old[j] = beta_nonzero ? row[j] : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            uint4 q;
+                            q.x = combine_f32(p, r[4 * j + 0], old[j].x);
+                            q.y = combine_f32(p, r[4 * j + 1], old[j].y);
+                            q.z = combine_f32(p, r[4 * j + 2], old[j].z);
+                            q.w = combine_f32(p, r[4 * j + 3], old[j].w);
+                            row[j] = q;
+                        }
+                    } else {
+                        // this lane's columns of the part that are in the output: [e0, e1)
+                        int64_t lo_c = xp, hi_c = xp + 32 < p.n ? xp + 32 : p.n;
+                        if (lower) hi_c = hi_c < gi + 1 ? hi_c : gi + 1;  // j <= i
+                        else lo_c = lo_c > gi ? lo_c : gi;               // j >= i
+                        const int e0 = gi < p.m ? static_cast<int>(lo_c - xp) : 32;
+                        const int e1 = gi < p.m ? static_cast<int>(hi_c - xp) : 0;
+                        if (bf16_out) {
+                            __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.C) + gi * p.ldc + xp;
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) {
+                                if (e < e0 || e >= e1) continue;
+                                const float v = p.alpha * __uint_as_float(r[e]);
+                                dst[e] = __float2bfloat16_rn(beta_nonzero ? fmaf(p.beta, __bfloat162float(dst[e]), v) : v);
+                            }
+                        } else {
+                            float *dst = reinterpret_cast<float *>(p.C) + gi * p.ldc + xp;
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) {
+                                if (e < e0 || e >= e1) continue;
+                                const float v = p.alpha * __uint_as_float(r[e]);
+                                dst[e] = beta_nonzero ? fmaf(p.beta, dst[e], v) : v;
+                            }
+                        }
+                    }
+                }
+            }
         } else if (warp_tma) {
             // Chunks of 128 bytes per row (64 bf16 or 32 fp32 columns), 32 rows: each lane
             // converts its row into a 128B-swizzled staging block, one lane stores it with
