@@ -270,6 +270,8 @@ struct Plan {
     int k_splits = 1, kb_per_split = 0, kb_total = 0;
     int ctas = 0;
     int64_t syrk_cross = 0;  // SYRK: tiles crossing the diagonal
+    int fixup = 0;           // split tiles reduced inside the kernel (no reduce kernel)
+    size_t slot_bytes = 0;   // partial slots at the start of the workspace; fixup counters follow
     size_t ws_bytes = 0;
 };
 
@@ -338,13 +340,22 @@ void try_split(Plan &pl, int64_t split_tiles, int64_t want, size_t budget)
     while (want > 1) {
         const int per = static_cast<int>(ceil_div(pl.kb_total, want));
         const int splits = static_cast<int>(ceil_div(pl.kb_total, per));
-        const size_t need = static_cast<size_t>(splits) * static_cast<size_t>(split_tiles) * slot_bytes;
+        // With whole tiles to run after them, split units go first and reduce in
+        // the kernel (the sums hide behind the next mainloops; one 8-byte counter
+        // per epilogue warp region follows the slots); when every tile is split,
+        // the reduce kernel spreads the sums over the GPU.
+        const bool fixup = split_tiles < pl.num_tiles;
+        const size_t slots = static_cast<size_t>(splits) * static_cast<size_t>(split_tiles) * slot_bytes;
+        const size_t need =
+            slots + (fixup ? static_cast<size_t>(split_tiles) * pl.pair * bm::NUM_EPI_WARPS * 8u : 0u);
         const double gain_us = kKBlockUs * (pl.kb_total - per);
         if (splits > 1 && need <= budget && gain_us >= kSplitMinGainUs) {
             pl.k_splits = splits;
             pl.kb_per_split = per;
             pl.full_tiles = pl.num_tiles - split_tiles;
+            pl.slot_bytes = slots;
             pl.ws_bytes = need;
+            pl.fixup = fixup ? 1 : 0;
             return;
         }
         --want;
@@ -440,6 +451,13 @@ bm_status launch(const Plan &pl, const CUtensorMap &ta, const CUtensorMap &tb, b
     if (prm.k_splits > 1 && prm.partial != nullptr &&
         encode_slots(&tp, prm.partial, (prm.num_tiles - prm.full_tiles) * prm.k_splits * pl.tile_m, pl.bn))
         prm.store_p_tma = 1;
+    prm.fixup = 0;
+    if (pl.fixup && prm.k_splits > 1 && prm.partial != nullptr) {
+        static std::atomic<unsigned long long> seq{0};
+        prm.fixup = 1;
+        prm.fixup_ctr = reinterpret_cast<unsigned long long *>(reinterpret_cast<char *>(prm.partial) + pl.slot_bytes);
+        prm.seq = (seq.fetch_add(1) % ((1ull << 48) - 1)) + 1;  // 1 .. 2^48 - 1
+    }
     if (pl.ctas <= 0) return BM_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
@@ -466,7 +484,7 @@ bm_status launch(const Plan &pl, const CUtensorMap &ta, const CUtensorMap &tb, b
         cudaGetLastError();
         return BM_ERR_CUDA;
     }
-    if (prm.k_splits > 1) {
+    if (prm.k_splits > 1 && !prm.fixup) {
         const int64_t work = (prm.num_tiles - prm.full_tiles) * pl.tile_m * (pl.bn / 4);
         const int blocks = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(ceil_div(work, 256), 8 * 152)));
         cudaLaunchConfig_t rc = {};
@@ -537,7 +555,7 @@ void export_plan(const Plan &pl, bm_plan *plan)
     plan->split_tiles = pl.num_tiles - pl.full_tiles;
     plan->ctas = pl.ctas;
     plan->cta_pair = pl.pair;
-    plan->kernels = pl.k_splits > 1 ? 2 : 1;
+    plan->kernels = pl.k_splits > 1 && !pl.fixup ? 2 : 1;
     plan->workspace_bytes = pl.k_splits > 1 ? pl.ws_bytes : 0;
     plan->stage_kblocks = kVariantStageKBlocks[pl.variant];
 }

@@ -105,6 +105,12 @@ struct GemmParams {
     int64_t syrk_cross; // SYRK: number of tiles crossing the diagonal (visited first)
     int a_box3;        // tmA is a stage box: one 3-D copy brings a CTA's A tile for a whole stage
     int b_box3;        // same for tmB
+    // In-kernel split-K reduction: split units run first; per epilogue warp region
+    // of a split tile, the last of the k_splits units to store its partial sums the
+    // slots and writes C (no reduce kernel). Counters are (seq << 16 | arrivals).
+    int fixup;
+    unsigned long long *fixup_ctr;  // split tiles x PAIR x NUM_EPI_WARPS counters
+    unsigned long long seq;         // this launch's tag, 1 .. 2^48 - 1
 };
 
 // KPS: k-blocks per ring stage. With two k-blocks a stage, the MMA thread waits
@@ -235,21 +241,25 @@ __device__ __forceinline__ void tile_coords(const GemmParams &p, int64_t t, int6
     }
 }
 
-// Work unit u: a whole tile (u < full_tiles), or one K range of a split tile.
-// Split tiles come last, so with units handed out round-robin they fill the
-// otherwise partly idle last wave.
+// Work unit u: a whole tile, or one K range of a split tile. With the reduce
+// kernel the split units come last, so with units handed out round-robin they
+// fill the otherwise partly idle last wave. With the in-kernel reduction they
+// come first: the reduction then runs in the epilogue while the next tile's
+// mainloop proceeds, instead of after the last wave.
 template <int TM, int BN>
 __device__ __forceinline__ Unit map_unit(const GemmParams &p, int64_t u)
 {
     Unit r;
     int64_t t;
-    if (u < p.full_tiles) {
-        t = u;
+    const int64_t split_units = p.num_units - p.full_tiles;
+    const bool whole = p.fixup ? u >= split_units : u < p.full_tiles;
+    if (whole) {
+        t = p.fixup ? u - split_units : u;
         r.kb0 = 0;
         r.kb1 = p.kb_total;
         r.slot = -1;
     } else {
-        const int64_t v = u - p.full_tiles;
+        const int64_t v = p.fixup ? u : u - p.full_tiles;
         const int64_t local = v / p.k_splits;
         const int split = static_cast<int>(v - local * p.k_splits);
         t = p.full_tiles + local;
@@ -455,6 +465,86 @@ __device__ __forceinline__ bool full_vector(const GemmParams &p, int64_t i, int6
     if (p.mode == MODE_SYRK_LOWER) all = all && (i >= j + 3);
     if (p.mode == MODE_SYRK_UPPER) all = all && (i <= j);
     return all;
+}
+
+// ---------------------------------------------------------------- in-kernel split-K reduction
+// One arrival at a region counter. The value is (tag << 16) | arrivals; a tag
+// other than this launch's (a reset counter, a launch that stopped early, or
+// workspace bytes left by other use) counts as no arrivals yet. Returns this
+// arrival's number, 1 .. k_splits. Each failed compare-and-swap means another
+// arrival went in, so the loop ends within k_splits attempts.
+__device__ __forceinline__ int fixup_arrive(unsigned long long *ctr, unsigned long long seq, int k_splits)
+{
+    unsigned long long cur = atomicAdd(ctr, 0ull);
+    for (int i = 0; i <= k_splits; ++i) {
+        const int n = (cur >> 16) == seq ? static_cast<int>(cur & 0xFFFFull) + 1 : 1;
+        const unsigned long long want = (seq << 16) | static_cast<unsigned long long>(n);
+        const unsigned long long prev = atomicCAS(ctr, cur, want);
+        if (prev == cur) return n;
+        cur = prev;
+    }
+    return 0;
+}
+
+// Called by an epilogue warp once its 32 rows x (BN / 2) columns of a split
+// unit's partial are stored (plain stores). The last of the tile's k_splits
+// units to get here sums that region over the slots in split order (the order
+// of bm_splitk_reduce_kernel, so results are the same bit for bit), adds
+// beta * C and writes C; the others return at once. Nothing waits.
+template <int TM, int BN, int PAIR>
+__device__ __forceinline__ void fixup_region(const GemmParams &p, int64_t tm, int64_t tn, int64_t slot, uint32_t rank,
+                                          int quad, int half, int warp, int lane)
+{
+    const int64_t local = slot / p.k_splits;
+    unsigned long long *ctr = p.fixup_ctr + (local * PAIR + rank) * NUM_EPI_WARPS + (warp - 2);
+    __threadfence();  // this lane's partial stores, before the arrival (release)
+    __syncwarp();
+    int n = 0;
+    if (lane == 0) {
+        __threadfence();
+        n = fixup_arrive(ctr, p.seq, p.k_splits);
+        if (n == p.k_splits) atomicExch(ctr, 0ull);  // every arrival is in: reset for the next launch
+    }
+    n = __shfl_sync(0xffffffffu, n, 0);
+    if (n != p.k_splits) return;
+    __threadfence();  // the other units' partials, after the arrivals (acquire)
+    const int row_in_tile = static_cast<int>(rank) * CTA_M + quad * 32;
+    const int64_t row0 = tm * TM + row_in_tile;
+    const int64_t col0 = tn * BN;
+    const int64_t slot_elems = static_cast<int64_t>(TM) * BN;
+    const float *base = p.partial + local * p.k_splits * slot_elems + static_cast<int64_t>(row_in_tile) * BN;
+    const int cc = lane & 7;
+#pragma unroll 1
+    for (int ch = half; ch < BN / 32; ch += 2) {
+        // 8 lanes cover one 32-column row segment, 4 rows per step, as in the stores
+        const int64_t off = static_cast<int64_t>(lane >> 3) * BN + ch * 32 + cc * 4;
+        float4 acc[8];
+#pragma unroll
+        for (int step = 0; step < 8; ++step)
+            acc[step] = __ldcg(reinterpret_cast<const float4 *>(base + off + step * 4 * BN));
+#pragma unroll 1
+        for (int sp = 1; sp < p.k_splits; ++sp) {
+            const float *src = base + sp * slot_elems + off;
+            float4 t[8];
+#pragma unroll
+            for (int step = 0; step < 8; ++step) t[step] = __ldcg(reinterpret_cast<const float4 *>(src + step * 4 * BN));
+#pragma unroll
+            for (int step = 0; step < 8; ++step) {
+                acc[step].x += t[step].x;
+                acc[step].y += t[step].y;
+                acc[step].z += t[step].z;
+                acc[step].w += t[step].w;
+            }
+        }
+#pragma unroll
+        for (int step = 0; step < 8; ++step) {
+            const int64_t gi = row0 + step * 4 + (lane >> 3);
+            const int64_t gj = col0 + ch * 32 + cc * 4;
+            if (gi >= p.m || gj >= p.n) continue;
+            float v[4] = {acc[step].x, acc[step].y, acc[step].z, acc[step].w};
+            write_c4(p, gi, gj, v);
+        }
+    }
 }
 
 // ---------------------------------------------------------------- roles
@@ -686,7 +776,9 @@ __device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUten
         // through the per-warp transposing path with per-element masks.
         const bool inside = tile_inside_triangle<Cfg::TILE_M, BN>(p.mode, w.tm, w.tn);
         const bool group = !to_slot && beta_nonzero && p.tma_c && inside;  // the same for every warp
-        const bool warp_tma = to_slot ? p.store_p_tma != 0 : (!beta_nonzero && p.tma_c && inside);
+        // (split units of the in-kernel reduction store their partials with plain
+        // stores, which the arrival's fence orders before the counter update)
+        const bool warp_tma = to_slot ? (p.store_p_tma != 0 && !p.fixup) : (!beta_nonzero && p.tma_c && inside);
         bool ready = wait_warp<PAIR == 2>(bar0 + 8u * (2 * STAGES + acc), acc_phase, abort_flag, p.timeout_ns);
         // A half that will meet at named barriers decides together, so that none of its
         // warps is left waiting at one.
@@ -1013,6 +1105,7 @@ __device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUten
             }
             __syncwarp();
         }
+        if (to_slot && p.fixup) fixup_region<Cfg::TILE_M, BN, PAIR>(p, w.tm, w.tn, w.slot, rank, quad, half, warp, lane);
         }
         if (++acc == 2) {
             acc = 0;

@@ -86,7 +86,16 @@ typedef enum { BM_LOWER = 0, BM_UPPER = 1 } bm_uplo;
  *   split; the result is correct either way. The size the planner would like
  *   is bm_gemm_bf16_workspace_size(); less is accepted (fewer or no splits).
  *   The workspace must be 256-byte aligned; its contents need not be
- *   initialised and are overwritten.
+ *   initialised and are overwritten. When only some tiles are split, the
+ *   split parts run first and the last part of each region to finish sums
+ *   the partials inside the GEMM kernel; the workspace then also holds one
+ *   8-byte counter per region, tagged with a per-call number, so stale or
+ *   random bytes are never taken for this call's counts. A call captured in
+ *   a CUDA graph keeps its number on every replay; each counter is reset
+ *   when its region is summed, so replays start clean. (A replay that
+ *   follows a replay stopped by a device-side wait limit, BM_ERR_TIMEOUT,
+ *   may find counters that replay left behind: re-capture after a timeout.)
+ *   When every tile is split, a second kernel sums the partials.
  *
  *   Returns BM_OK once the work is queued on `stream`.
  */
@@ -230,9 +239,10 @@ BM_API const char *bm_status_string(bm_status status);
  * (tile_m x tile_n, k-block tile_k), ring stages (of stage_kblocks k-blocks
  * each), number of output tiles
  * visited, K splits and how many tiles are split (the tiles of a last, partly
- * filled wave, or all tiles when there are too few to fill the GPU), CTAs
- * launched, CTAs per output tile (2 = an SM pair working on one tile), and
- * the number of kernels one call launches. Performs the same size checks as
+ * filled wave, summed inside the GEMM kernel, or all tiles when there are too
+ * few to fill the GPU, summed by a second kernel), CTAs launched, CTAs per
+ * output tile (2 = an SM pair working on one tile), and the number of kernels
+ * one call launches. Performs the same size checks as
  * the call (no pointers are given). On a machine without a usable GPU the
  * plan assumes 152 SMs.
  */

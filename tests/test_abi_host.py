@@ -159,6 +159,7 @@ def test_gemm_plans(lib):
     need = bm.bm_gemm_bf16_workspace_size(512, 512, 8192)
     assert need > 0
     st, p = bm.bm_gemm_bf16_plan(512, 512, 8192, need)
+    # every tile split: the partial slots only, summed by the reduce kernel
     assert p.k_splits > 1 and p.kernels == 2 and p.workspace_bytes == need
     assert p.workspace_bytes == p.k_splits * 512 * 512 * 4
     st, p = bm.bm_gemm_bf16_plan(512, 512, 8192, need // 2)      # less workspace: fewer splits
@@ -172,16 +173,21 @@ def test_gemm_plans(lib):
 
 def test_tail_split_plans(lib):
     # 4096^3 on SM pairs: 256 tiles = 3 full waves of 76 + 28; the 28 are split in two along K
+    # and summed inside the kernel: two fp32 slots per split tile, then one 8-byte counter per
+    # epilogue warp region (2 CTAs x 8 warps per tile); one kernel, no reduce launch
     need = bm.bm_gemm_bf16_workspace_size(4096, 4096, 4096)
-    assert need == 2 * 28 * 256 * 256 * 4
+    assert need == 2 * 28 * 256 * 256 * 4 + 28 * 2 * 8 * 8
     p = bm.bm_gemm_bf16_plan(4096, 4096, 4096, need)[1]
-    assert (p.split_tiles, p.k_splits, p.kernels, p.ctas) == (28, 2, 2, 152)
+    assert (p.split_tiles, p.k_splits, p.kernels, p.ctas) == (28, 2, 1, 152)
+    # one byte short of the counters: no split
+    assert bm.bm_gemm_bf16_plan(4096, 4096, 4096, need - 1)[1].k_splits == 1
     # no workspace: whole tiles only
     p = bm.bm_gemm_bf16_plan(4096, 4096, 4096, 0)[1]
     assert (p.split_tiles, p.k_splits, p.kernels) == (0, 1, 1)
-    # dX 2048x5120x5120: 160 tiles = 2 waves + 8; split 8 ways within the 16 MiB tail budget
+    # dX 2048x5120x5120: 160 tiles = 2 waves + 8; split 7 ways within the 16 MiB tail budget
+    # (8 ways would need 16 MiB of slots plus the counters)
     p = bm.bm_gemm_bf16_plan(2048, 5120, 5120, 1 << 30)[1]
-    assert (p.split_tiles, p.k_splits) == (8, 8) and p.workspace_bytes <= 16 << 20
+    assert (p.split_tiles, p.k_splits, p.kernels) == (8, 7, 1) and p.workspace_bytes <= 16 << 20
     # a short K saves too little mainloop time to pay for the extra reduce
     p = bm.bm_gemm_bf16_plan(5120, 5120, 2048, 1 << 30)[1]     # 400 tiles = 5 waves + 20
     assert p.split_tiles == 0 and p.k_splits == 1

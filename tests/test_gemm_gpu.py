@@ -186,7 +186,14 @@ def test_split_k_matches_oracle_and_is_deterministic(variant):
 
 @pytest.mark.parametrize("variant", [0, 1], ids=["auto", "single128x256"])
 def test_tail_split_exact_and_deterministic(variant):
-    """The tiles of a partly filled last wave are split along K over the idle SMs."""
+    """The tiles of a partly filled last wave are split along K over the idle SMs.
+
+    Their units run first, and per 32-row region of a split tile the last unit to
+    store its partial sums the slots and writes C inside the kernel. The region
+    counters sit in the workspace after the slots and carry a per-launch tag, so
+    the workspace may start with any bytes: it is filled with random bits here
+    before the first call, and with a stale-looking pattern before the third.
+    """
     import blas3_tensor_core_gb300 as bm
     t = torch()
     m, n, k = 2560, 2048, 3072  # SM pairs: 80 tiles = 76 + 4; single SMs: 160 tiles = 152 + 8
@@ -195,17 +202,98 @@ def test_tail_split_exact_and_deterministic(variant):
     with tile_variant(variant):
         need = bm.bm_gemm_bf16_workspace_size(m, n, k)
         plan = bm.bm_gemm_bf16_plan(m, n, k, need)[1]
-        assert plan.split_tiles > 0 and plan.k_splits > 1 and plan.kernels == 2
+        assert plan.split_tiles > 0 and plan.k_splits > 1 and plan.kernels == 1
         ws = t.empty(need // 4, dtype=t.float32, device="cuda")
+        g = t.Generator(device="cuda")
+        g.manual_seed(5)
+        ws.view(t.int32).copy_(t.randint(-2**31, 2**31 - 1, (need // 4,), dtype=t.int32, device="cuda", generator=g))
+        slot_bytes = plan.k_splits * plan.split_tiles * plan.tile_m * plan.tile_n * 4
+        assert need - slot_bytes == plan.split_tiles * plan.cta_pair * 8 * 8  # one counter per warp region
         outs = []
-        for _ in range(2):
+        for i in range(3):
+            if i == 2:  # every counter as an earlier launch (tag 1) left it after one arrival
+                ws.view(t.int64)[slot_bytes // 8:].fill_((1 << 16) | 1)
             cbuf = CBuffer(m, n, n, False, init=c0)
             got, raw = run_gemm(m, n, k, 0, 0, 1.0, A, B, -1.0, cbuf, workspace=ws)
             cbuf.assert_guard_intact(raw)
             outs.append(got)
-    assert np.array_equal(outs[0], outs[1])
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
     ref, _ = orc().gemm(m, n, k, 0, 0, 1.0, A, B, -1.0, c0)
     assert np.array_equal(outs[0], ref)
+
+
+def test_tail_split_ragged_many_splits_bf16_beta():
+    """Ragged m, n and k; the 4 tail tiles split 10 ways and summed in the kernel, into bf16 C with beta."""
+    import blas3_tensor_core_gb300 as bm
+    t = torch()
+    m, n, k = 2500, 2000, 3000  # 10 x 8 pair tiles = 76 + 4
+    alpha, beta = 0.75, 0.5
+    A, B = _operands(m, n, k, 0, 0, "normal", seed=85)
+    c_init = gen.matrix_bf16(m, n, "normal", seed=86)
+    need = bm.bm_gemm_bf16_workspace_size(m, n, k)
+    plan = bm.bm_gemm_bf16_plan(m, n, k, need)[1]
+    assert (plan.split_tiles, plan.k_splits, plan.kernels) == (4, 10, 1)
+    ws = t.full((need // 4,), float("nan"), dtype=t.float32, device="cuda")
+    cbuf = CBuffer(m, n, _ldc(n, True), True, init=c_init)
+    got, raw = run_gemm(m, n, k, 0, 0, alpha, A, B, beta, cbuf, workspace=ws)
+    cbuf.assert_guard_intact(raw)
+    band_r = np.repeat(np.arange(1280, m), 256)  # the split tiles: last tile column, last 4 tile rows
+    band_c = np.tile(np.arange(n - 256, n), m - 1280)
+    rows, cols = tile_samples(m, n, per_tile=8, seed=13, extra=(band_r, band_c))
+    ref, bound = orc().gemm_entries(k, 0, 0, alpha, A, B, rows, cols, beta, c_init)
+    assert_parity(got[rows, cols], ref, bound, alpha, beta, c_input_values(c_init, True)[rows, cols], True,
+                  "tail split x10")
+
+
+@pytest.mark.parametrize("bf16_out", [False, True])
+def test_tail_split_graph_replays(bf16_out):
+    """A CUDA graph replays its calls with the tags they were captured with; the
+    last unit of each region resets its counter, so every replay starts clean.
+    New inputs are copied into the captured buffers before each replay."""
+    import blas3_tensor_core_gb300 as bm
+    from gpu_helpers import bf16_to_device, device_to_numpy
+    t = torch()
+    m, n, k = 2560, 2048, 3072  # 80 pair tiles = 76 + 4; the 4 are split
+    need = bm.bm_gemm_bf16_workspace_size(m, n, k)
+    assert bm.bm_gemm_bf16_plan(m, n, k, need)[1].kernels == 1
+    ws = t.zeros(need // 4, dtype=t.float32, device="cuda")
+    dA = t.empty((m, k), dtype=t.bfloat16, device="cuda")
+    dB = t.empty((k, n), dtype=t.bfloat16, device="cuda")
+    dC = t.empty((m, n), dtype=t.bfloat16 if bf16_out else t.float32, device="cuda")
+    ct = bm.BM_C_BF16 if bf16_out else bm.BM_C_F32
+
+    def call(h):
+        assert bm.bm_gemm_bf16(m, n, k, 0, 0, 1.0, dA.data_ptr(), k, dB.data_ptr(), n, 0.0, dC.data_ptr(), n, ct,
+                               ws.data_ptr(), need, h) == bm.BM_OK
+
+    side = t.cuda.Stream()
+    side.wait_stream(t.cuda.current_stream())
+    with t.cuda.stream(side):
+        call(side.cuda_stream)  # first-call set-up outside the capture
+    t.cuda.current_stream().wait_stream(side)
+    t.cuda.synchronize()
+    graph = t.cuda.CUDAGraph()
+    with t.cuda.graph(graph):
+        call(t.cuda.current_stream().cuda_stream)
+    # the split tiles are the last ones of the raster: the last tile column, lower rows;
+    # all of the last 256 columns, and samples elsewhere
+    band_r = np.repeat(np.arange(m), 256)
+    band_c = np.tile(np.arange(n - 256, n), m)
+    rows, cols = tile_samples(m, n, per_tile=24, seed=12, extra=(band_r, band_c))
+    for rep in range(3):
+        A = operand(m, k, "int", 100 + rep, lo=-4, hi=4)
+        B = operand(k, n, "int", 200 + rep, lo=-4, hi=4)
+        dA.copy_(bf16_to_device(A))
+        dB.copy_(bf16_to_device(B))
+        graph.replay()
+        t.cuda.synchronize()
+        assert bm.bm_get_last_device_error(t.cuda.current_stream().cuda_stream) == bm.BM_OK
+        got = (gen.bf16_bits_to_f32(device_to_numpy(dC)) if bf16_out else dC.cpu().numpy()).astype(np.float64)
+        ref, _ = orc().gemm_entries(k, 0, 0, 1.0, A, B, rows, cols)
+        if bf16_out:
+            ref = gen.bf16_bits_to_f32(gen.f32_to_bf16_bits(ref.astype(np.float32))).astype(np.float64)
+        assert np.array_equal(got[rows, cols], ref), f"replay {rep}"
+    del graph
 
 
 # ----------------------------------------------------------------------------- stream ordering
