@@ -327,9 +327,12 @@ void size_grid(Plan &pl, int sms, int pair_clusters)
 
 // Split the last `split_tiles` tiles of the unit order `want` ways (or fewer)
 // along K, if each part keeps >= 4 k-blocks, the partial slots fit `budget`,
-// and the mainloop time it saves beats the cost of the extra reduce kernel.
-// One 64-deep k-block of a tile takes 4 MMAs of 128 tensor-core cycles, about
-// 0.26 us at 2 GHz; the reduce launch and its traffic cost a few us.
+// and the mainloop time it saves is at least kSplitMinGainUs. One 64-deep
+// k-block of a tile takes 4 MMAs of 128 tensor-core cycles, about 0.26 us at
+// 2 GHz. Summing the partials costs a few us: a second kernel when every tile
+// is split, extra epilogue work inside the kernel for a tail split (a lower
+// threshold there was measured slower at K = 1024 and 2048, where the
+// epilogue already takes longer than a tile's mainloop).
 constexpr double kKBlockUs = 0.256;
 constexpr double kSplitMinGainUs = 6.0;
 

@@ -486,14 +486,49 @@ __device__ __forceinline__ int fixup_arrive(unsigned long long *ctr, unsigned lo
     return 0;
 }
 
+// A full 4-vector of C (no edge, no triangle mask) from its final value: cast
+// and store, no beta term.
+__device__ __forceinline__ void store_c4(const GemmParams &p, int64_t i, int64_t j, float4 v)
+{
+    if (p.c_bf16) {
+        const __nv_bfloat162 r01 = __floats2bfloat162_rn(v.x, v.y);
+        const __nv_bfloat162 r23 = __floats2bfloat162_rn(v.z, v.w);
+        uint2 out;
+        out.x = *reinterpret_cast<const uint32_t *>(&r01);
+        out.y = *reinterpret_cast<const uint32_t *>(&r23);
+        *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(p.C) + i * p.ldc + j) = out;
+    } else {
+        *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.C) + i * p.ldc + j) = v;
+    }
+}
+
+// beta * c + v for a full 4-vector whose old C value (bf16 or fp32 bits) was loaded earlier.
+__device__ __forceinline__ float4 add_beta_c4(const GemmParams &p, float4 v, uint4 old)
+{
+    if (p.c_bf16) {
+        v.x = fmaf(p.beta, __uint_as_float(old.x << 16), v.x);
+        v.y = fmaf(p.beta, __uint_as_float(old.x & 0xFFFF0000u), v.y);
+        v.z = fmaf(p.beta, __uint_as_float(old.y << 16), v.z);
+        v.w = fmaf(p.beta, __uint_as_float(old.y & 0xFFFF0000u), v.w);
+    } else {
+        v.x = fmaf(p.beta, __uint_as_float(old.x), v.x);
+        v.y = fmaf(p.beta, __uint_as_float(old.y), v.y);
+        v.z = fmaf(p.beta, __uint_as_float(old.z), v.z);
+        v.w = fmaf(p.beta, __uint_as_float(old.w), v.w);
+    }
+    return v;
+}
+
 // Called by an epilogue warp once its 32 rows x (BN / 2) columns of a split
 // unit's partial are stored (plain stores). The last of the tile's k_splits
-// units to get here sums that region over the slots in split order (the order
-// of bm_splitk_reduce_kernel, so results are the same bit for bit), adds
-// beta * C and writes C; the others return at once. Nothing waits.
+// units to get here sums that region over the slots in split order and writes
+// C; the others return at once. Nothing waits. With beta != 0 the unit of
+// split 0 has already added beta * C to its partial at every full 4-vector
+// (it read C before it counted itself in, so before anyone writes C); only
+// the vectors at the edges of C take beta here.
 template <int TM, int BN, int PAIR>
 __device__ __forceinline__ void fixup_region(const GemmParams &p, int64_t tm, int64_t tn, int64_t slot, uint32_t rank,
-                                          int quad, int half, int warp, int lane)
+                                             int quad, int half, int warp, int lane)
 {
     const int64_t local = slot / p.k_splits;
     unsigned long long *ctr = p.fixup_ctr + (local * PAIR + rank) * NUM_EPI_WARPS + (warp - 2);
@@ -536,13 +571,17 @@ __device__ __forceinline__ void fixup_region(const GemmParams &p, int64_t tm, in
                 acc[step].w += t[step].w;
             }
         }
+        const int64_t gj = col0 + ch * 32 + cc * 4;
 #pragma unroll
         for (int step = 0; step < 8; ++step) {
             const int64_t gi = row0 + step * 4 + (lane >> 3);
-            const int64_t gj = col0 + ch * 32 + cc * 4;
             if (gi >= p.m || gj >= p.n) continue;
-            float v[4] = {acc[step].x, acc[step].y, acc[step].z, acc[step].w};
-            write_c4(p, gi, gj, v);
+            if (full_vector(p, gi, gj)) {
+                store_c4(p, gi, gj, acc[step]);
+            } else {
+                float v[4] = {acc[step].x, acc[step].y, acc[step].z, acc[step].w};
+                write_c4(p, gi, gj, v);
+            }
         }
     }
 }
@@ -788,7 +827,9 @@ __device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUten
             break;
         }
         tc_fence_after_sync();
-        const bool use_beta_fast = beta_nonzero && w.slot < 0;
+        // split 0 of an in-kernel reduction adds beta * C to its partial (full vectors)
+        const bool fold_beta = to_slot && p.fixup && beta_nonzero && w.kb0 == 0;
+        const bool use_beta_fast = beta_nonzero && (w.slot < 0 || fold_beta);
         // split units: this CTA's rows of the tile's fp32 partial slot
         float *slot_rows = w.slot < 0 ? nullptr
                                       : p.partial + w.slot * static_cast<int64_t>(Cfg::TILE_M * BN) +
@@ -1084,7 +1125,8 @@ __device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUten
                 const float4 v4 = reinterpret_cast<const float4 *>(stage_buf + rr * 32)[cc ^ (rr & 7)];
                 const int64_t gi = row0 + rr;
                 if (slot_rows != nullptr) {  // whole tile row segment, edges included
-                    *reinterpret_cast<float4 *>(slot_rows + rr * BN + ch * 32 + cc * 4) = v4;
+                    const float4 x = fold_beta && full_vector(p, gi, gj0) ? add_beta_c4(p, v4, old[step]) : v4;
+                    *reinterpret_cast<float4 *>(slot_rows + rr * BN + ch * 32 + cc * 4) = x;
                 } else if (full_vector(p, gi, gj0)) {
                     float v[4] = {v4.x, v4.y, v4.z, v4.w};
                     if (use_beta_fast) {
@@ -1222,7 +1264,22 @@ __global__ void __launch_bounds__(256) bm_splitk_reduce_kernel(const GemmParams 
         if (i >= p.m || j >= p.n) continue;
         const float *src = p.partial + local * p.k_splits * slot_elems + static_cast<int64_t>(r) * BN + c;
         float4 s = *reinterpret_cast<const float4 *>(src);
-        for (int sp = 1; sp < p.k_splits; ++sp) {
+        // Loads of up to 8 slots are issued together, then added one after the
+        // other in split order (the sum itself is sequential).
+        int sp = 1;
+        for (; sp + 8 <= p.k_splits; sp += 8) {
+            float4 t[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) t[q] = *reinterpret_cast<const float4 *>(src + (sp + q) * slot_elems);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                s.x += t[q].x;
+                s.y += t[q].y;
+                s.z += t[q].z;
+                s.w += t[q].w;
+            }
+        }
+        for (; sp < p.k_splits; ++sp) {
             const float4 t = *reinterpret_cast<const float4 *>(src + sp * slot_elems);
             s.x += t.x;
             s.y += t.y;
