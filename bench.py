@@ -16,7 +16,8 @@ uses the next of several input sets whose total is larger than twice the L2,
 so no step finds its operands in L2. Clocks and throttle reasons are sampled
 through NVML during the timed region. `e2e` repeats the measurement through
 the same C-ABI call with the inputs in pinned host memory: each step copies
-A and B to the device and C back inside the timed region.
+A and B to the device and C back inside the timed region, pipelined over two
+device buffer sets and three streams (uploads, GEMMs, downloads).
 
 `--impl reference` times the CPU oracle (plain double-precision triple loop)
 on a bounded sample of the same workload; it is the comparison arm, not a
@@ -303,8 +304,11 @@ class GemmWorkload:
         self.ldb = B.shape[1]
 
     def call(self, i, stream_handle):
-        c = self.cfg
         dA, dB, dC = self.sets[i % len(self.sets)]
+        self.call_set(dA, dB, dC, stream_handle)
+
+    def call_set(self, dA, dB, dC, stream_handle):
+        c = self.cfg
         if self.e4m3:
             st = self.bm.bm_gemm_e4m3(c["m"], c["n"], c["k"], 1.0, dA.data_ptr(), self.lda, dB.data_ptr(), self.ldb,
                                       c["beta"], dC.data_ptr(), c["n"],
@@ -389,37 +393,70 @@ def graph_steps(wl, steps):
 
 
 def e2e_steps(wl, steps, warmup, dist):
-    """Same call with pinned host inputs: H2D of A and B and D2H of C inside the timed region."""
+    """Same call with pinned host inputs: H2D of A and B and D2H of C inside the timed region.
+
+    The steps are pipelined the way a stream of GEMMs would be fed: two device
+    buffer sets and three streams, so the upload of step i + 1 and the download
+    of step i - 1 overlap the GEMM of step i. Events order each buffer set's
+    reuse (upload after the GEMM two steps back has read it, GEMM after the
+    download two steps back has read its C). Every step still moves its whole
+    A and B to the device and its whole C back.
+    """
     import numpy as np
     t = wl.t
-    stream = t.cuda.current_stream()
-    h = stream.cuda_stream
+    main = t.cuda.current_stream()
+    h = main.cuda_stream
+    s_in, s_out = t.cuda.Stream(), t.cuda.Stream()
     hA = t.from_numpy(wl.A_host.view(np.int16)).view(t.bfloat16).pin_memory()
     hB = t.from_numpy(wl.B_host.view(np.int16)).view(t.bfloat16).pin_memory()
-    dA, dB, dC = wl.sets[0]
-    hC = t.empty(dC.shape, dtype=dC.dtype).pin_memory()
+    slots = wl.sets[:2]
+    hC = t.empty(slots[0][2].shape, dtype=slots[0][2].dtype).pin_memory()
     hC0 = None
     if wl.C0_host is not None:  # beta != 0: the step's input C travels too
-        hC0 = t.from_numpy(wl.C0_host.view(np.int16)).view(t.bfloat16).to(dC.dtype).pin_memory()
+        hC0 = t.from_numpy(wl.C0_host.view(np.int16)).view(t.bfloat16).to(slots[0][2].dtype).pin_memory()
+    read_done = [t.cuda.Event(), t.cuda.Event()]   # GEMM of the slot's last step has read A, B (and C)
+    out_done = [t.cuda.Event(), t.cuda.Event()]    # download of the slot's last step has read C
+    in_done = [t.cuda.Event(), t.cuda.Event()]
 
-    def step():
-        dA.copy_(hA, non_blocking=True)
-        dB.copy_(hB, non_blocking=True)
-        if hC0 is not None:
-            dC.copy_(hC0, non_blocking=True)
-        wl.call(0, h)
-        hC.copy_(dC, non_blocking=True)
+    def step(i):
+        s = i % 2
+        dA, dB, dC = slots[s]
+        if i >= 2:
+            s_in.wait_event(read_done[s])
+            if hC0 is not None:
+                s_in.wait_event(out_done[s])
+        with t.cuda.stream(s_in):
+            dA.copy_(hA, non_blocking=True)
+            dB.copy_(hB, non_blocking=True)
+            if hC0 is not None:
+                dC.copy_(hC0, non_blocking=True)
+        in_done[s].record(s_in)
+        main.wait_event(in_done[s])
+        if i >= 2:
+            main.wait_event(out_done[s])
+        wl.call_set(dA, dB, dC, h)
+        read_done[s].record(main)
+        s_out.wait_event(read_done[s])
+        with t.cuda.stream(s_out):
+            hC.copy_(dC, non_blocking=True)
+        out_done[s].record(s_out)
 
-    for _ in range(warmup):
-        step()
+    def run(n):
+        s_in.wait_stream(main)
+        s_out.wait_stream(main)
+        for i in range(n):
+            step(i)
+        main.wait_stream(s_in)
+        main.wait_stream(s_out)
+
+    run(warmup)
     t.cuda.synchronize()
     dist.barrier()
     t.cuda.synchronize()
     ev0, ev1 = t.cuda.Event(enable_timing=True), t.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for _ in range(steps):
-        step()
-    ev1.record(stream)
+    ev0.record(main)
+    run(steps)
+    ev1.record(main)
     t.cuda.synchronize()
     dist.barrier()
     ms = dist.max(ev0.elapsed_time(ev1))
@@ -557,7 +594,9 @@ def run_gpu_arm(args, dist):
     e2e_ms, h2d, d2h, _ = e2e_steps(wl, args.e2e_steps, max(3, args.warmup // 10), dist)
     e2e = {"value": round(dist.world * wl.flops() * args.e2e_steps / (e2e_ms * 1e-3) / 1e12, 3), "unit": UNIT,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
-           "ms_per_step": round(e2e_ms / args.e2e_steps, 4)}
+           "ms_per_step": round(e2e_ms / args.e2e_steps, 4),
+           "pipeline": "two device buffer sets; uploads, GEMMs and downloads on three streams, "
+                       "so step i+1's H2D and step i-1's D2H overlap step i's GEMM"}
     sweep = []
     if not args.no_sweep:
         for cfg in SWEEP + (EXTRA if args.all_configs else []):

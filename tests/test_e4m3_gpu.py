@@ -85,6 +85,27 @@ def test_e4m3_split_k_and_deterministic():
     assert_parity(outs[0][rows, cols], ref, bound, 1.0, 0.0, None, True, "e4m3 split-K")
 
 
+def test_e4m3_tail_split_summed_in_kernel():
+    """80 pair tiles = 76 + 4: the 4 tail tiles split 13 ways along K (the 16 MiB tail budget) and summed inside the kernel."""
+    import blas3_tensor_core_gb300 as bm
+    t = torch()
+    m, n, k = 2560, 2048, 8192
+    A = _codes(m, k, "normal", 23)
+    B = _codes(n, k, "normal", 24)
+    need = bm.bm_gemm_e4m3_workspace_size(m, n, k)
+    ws = t.empty(need // 4, dtype=t.float32, device="cuda")
+    cbuf = CBuffer(m, n, n, True)
+    got, raw = run_gemm_e4m3(m, n, k, 1.0, A, B, 0.0, cbuf, workspace=ws)
+    cbuf.assert_guard_intact(raw)
+    # the split tiles are in the last tile column; columns 1823, 1919, 1951 and 2047 fall in
+    # tile-local 32-column chunks 0, 3, 4 and 7, so both epilogue halves of every row are checked
+    band_c = np.repeat(np.array([n - 225, n - 129, n - 97, n - 1]), m)
+    band_r = np.tile(np.arange(m), 4)
+    rows, cols = tile_samples(m, n, per_tile=16, seed=8, extra=(band_r, band_c))
+    ref, bound = oracle.default().gemm_e4m3_entries(k, 1.0, A, B, rows, cols)
+    assert_parity(got[rows, cols], ref, bound, 1.0, 0.0, None, True, "e4m3 tail split")
+
+
 def test_e4m3_full_size_4096_sampled():
     m = n = k = 4096
     A = gen.matrix_e4m3(m, k, "normal", 1)

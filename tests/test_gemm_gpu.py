@@ -184,7 +184,7 @@ def test_split_k_matches_oracle_and_is_deterministic(variant):
     assert_parity(plain[rows, cols], ref, bound, 1.0, 0.0, None, False, "no split")
 
 
-@pytest.mark.parametrize("variant", [0, 1], ids=["auto", "single128x256"])
+@pytest.mark.parametrize("variant", [0, 1, 2], ids=["auto", "single128x256", "single128x128"])
 def test_tail_split_exact_and_deterministic(variant):
     """The tiles of a partly filled last wave are split along K over the idle SMs.
 
