@@ -458,6 +458,38 @@ __device__ __forceinline__ uint32_t combine_f32(const GemmParams &p, uint32_t ac
     return __float_as_uint(fmaf(p.beta, __uint_as_float(old), p.alpha * __uint_as_float(acc)));
 }
 
+// One lane's row of a 32-row x 128-byte staging block, 128B-swizzled (16-byte
+// unit u of row r at slot u ^ (r & 7)): 64 accumulator columns as bf16, or 32
+// as fp32, times alpha when SCALE.
+template <bool SCALE>
+__device__ __forceinline__ void stage_row_bf16(uint4 *srow, const uint32_t (&r)[64], float alpha, int lane)
+{
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        __nv_bfloat162 h[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float x0 = __uint_as_float(r[8 * j + 2 * e]);
+            const float x1 = __uint_as_float(r[8 * j + 2 * e + 1]);
+            h[e] = SCALE ? __floats2bfloat162_rn(alpha * x0, alpha * x1) : __floats2bfloat162_rn(x0, x1);
+        }
+        srow[j ^ (lane & 7)] = *reinterpret_cast<const uint4 *>(h);
+    }
+}
+
+template <bool SCALE>
+__device__ __forceinline__ void stage_row_f32(uint4 *srow, const uint32_t (&r)[64], float alpha, int lane)
+{
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        uint4 q = make_uint4(r[4 * j + 0], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+        if (SCALE)
+            q = make_uint4(__float_as_uint(alpha * __uint_as_float(q.x)), __float_as_uint(alpha * __uint_as_float(q.y)),
+                           __float_as_uint(alpha * __uint_as_float(q.z)), __float_as_uint(alpha * __uint_as_float(q.w)));
+        srow[j ^ (lane & 7)] = q;
+    }
+}
+
 // Is C[i, j..j+3] a full vector inside the output (no edge, no triangle mask)?
 __device__ __forceinline__ bool full_vector(const GemmParams &p, int64_t i, int64_t j)
 {
@@ -707,6 +739,20 @@ __device__ __forceinline__ void run_mma(const GemmParams &p, uint32_t ring, uint
     using Cfg = KernelCfg<BN, STAGES, PAIR, ELEM, KPS>;
     const int64_t units = p.num_units;
     const uint32_t idesc = idesc_f32acc(Cfg::TILE_M, BN, ELEM == ELEM_E4M3 ? 0u : 1u, p.a_mn_major, p.b_mn_major);
+    // Shared-memory descriptors are built once: a template with the start address
+    // left at 0, plus the address >> 4 in the low 14 bits per MMA. Shared addresses
+    // are below 256 KB, so the sum never carries into the next field. Steps, in
+    // 16-byte units: K-major operands advance 32 B per 16 k and one tile per
+    // k-block of the stage; M/N-major ones two 1024-byte row groups per 16 k and
+    // 8 KB per k-block (the next 64 M/N lines are one chunk, KPS x 8 KB, further).
+    // This keeps the issuing warp to a few instructions per MMA: it shares its SM
+    // sub-partition with two epilogue warps.
+    const uint64_t a_tpl = p.a_mn_major ? smem_desc_sw128(0u, Cfg::CHUNK_BYTES, 1024u) : smem_desc_sw128(0u, 16u, 1024u);
+    const uint64_t b_tpl = p.b_mn_major ? smem_desc_sw128(0u, Cfg::CHUNK_BYTES, 1024u) : smem_desc_sw128(0u, 16u, 1024u);
+    const uint32_t a_kk = p.a_mn_major ? 2048u / 16u : 32u / 16u;
+    const uint32_t b_kk = p.b_mn_major ? 2048u / 16u : 32u / 16u;
+    const uint32_t a_sub = p.a_mn_major ? 8192u / 16u : static_cast<uint32_t>(Cfg::A_BYTES) / 16u;
+    const uint32_t b_sub = p.b_mn_major ? 8192u / 16u : static_cast<uint32_t>(Cfg::B_BYTES) / 16u;
     int stage = 0, acc = 0;
     uint32_t phase = 0, acc_phase = 0;
     bool ok = true, issued_any = false;
@@ -730,20 +776,13 @@ __device__ __forceinline__ void run_mma(const GemmParams &p, uint32_t ring, uint
             const int nkb = kb1 - kb < KPS ? kb1 - kb : KPS;
             const uint32_t st = ring + stage * Cfg::STAGE_BYTES;
             for (int sub = 0; sub < nkb; ++sub) {
-                // k-block `sub` of the stage: K-major tiles one tile size further on,
-                // M/N-major ones 64 k-rows (8 KB) further into each chunk
-                const uint32_t sa = st + (p.a_mn_major ? 8192u * sub : static_cast<uint32_t>(Cfg::A_BYTES) * sub);
-                const uint32_t sb = st + Cfg::B_OFFSET +
-                                    (p.b_mn_major ? 8192u * sub : static_cast<uint32_t>(Cfg::B_BYTES) * sub);
+                // k-block `sub` of the stage
+                const uint64_t a0 = a_tpl + (st >> 4) + a_sub * sub;
+                const uint64_t b0 = b_tpl + ((st + Cfg::B_OFFSET) >> 4) + b_sub * sub;
 #pragma unroll
                 for (int kk = 0; kk < TILE_K / UMMA_K; ++kk) {
-                    // K-major: the next 16 k sit 32 bytes further along the swizzled row.
-                    // M/N-major: the next 16 k are the next two 1024-byte row groups;
-                    // the next 64 rows of M or N are one chunk (KPS x 8 KB) further.
-                    const uint64_t ad = p.a_mn_major ? smem_desc_sw128(sa + 2048u * kk, Cfg::CHUNK_BYTES, 1024u)
-                                                     : smem_desc_sw128(sa + 32u * kk, 16u, 1024u);
-                    const uint64_t bd = p.b_mn_major ? smem_desc_sw128(sb + 2048u * kk, Cfg::CHUNK_BYTES, 1024u)
-                                                     : smem_desc_sw128(sb + 32u * kk, 16u, 1024u);
+                    const uint64_t ad = a0 + a_kk * kk;
+                    const uint64_t bd = b0 + b_kk * kk;
                     const uint32_t accumulate = (kb > kb0 || sub > 0 || kk > 0) ? 1u : 0u;
                     if (lane == 0) {
                         if constexpr (ELEM == ELEM_E4M3) {
@@ -1040,23 +1079,14 @@ __device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUten
                 if (lane == 0) bulk_wait_group_read0();  // the previous store has read the staging block
                 __syncwarp();
                 uint4 *srow = reinterpret_cast<uint4 *>(stage_buf) + lane * 8;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    uint4 q;
-                    if (bf16_out) {
-                        __nv_bfloat162 h[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            h[e] = __floats2bfloat162_rn(p.alpha * __uint_as_float(r[8 * j + 2 * e]),
-                                                         p.alpha * __uint_as_float(r[8 * j + 2 * e + 1]));
-                        q = *reinterpret_cast<const uint4 *>(h);
-                    } else {
-                        q = make_uint4(__float_as_uint(p.alpha * __uint_as_float(r[4 * j + 0])),
-                                       __float_as_uint(p.alpha * __uint_as_float(r[4 * j + 1])),
-                                       __float_as_uint(p.alpha * __uint_as_float(r[4 * j + 2])),
-                                       __float_as_uint(p.alpha * __uint_as_float(r[4 * j + 3])));
-                    }
-                    srow[j ^ (lane & 7)] = q;
+                // (alpha == 1 skips the multiplies: fewer instructions for the warps that
+                // share sub-partitions with the producer and MMA warps)
+                if (bf16_out) {
+                    if (p.alpha == 1.0f) stage_row_bf16<false>(srow, r, p.alpha, lane);
+                    else stage_row_bf16<true>(srow, r, p.alpha, lane);
+                } else {
+                    if (p.alpha == 1.0f) stage_row_f32<false>(srow, r, p.alpha, lane);
+                    else stage_row_f32<true>(srow, r, p.alpha, lane);
                 }
                 fence_proxy_async_shared();
                 __syncwarp();
