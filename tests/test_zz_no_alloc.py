@@ -80,6 +80,27 @@ def test_split_k_without_allocation_matches_workspace_path_twice():
         assert ok, (seed, worst, where)
 
 
+def test_tail_split_summed_in_kernel_without_allocation_three_times():
+    """Tail tiles split along K and summed inside the kernel: the partial slots and the
+    region counters both live in the static array. Three calls in a row on different
+    integer inputs (the counters are reset by each call's last units), with beta = 0
+    and beta = -1; small integers make every result exact, so the two entry points
+    must agree bit for bit."""
+    import blas3_tensor_core_gb300 as bm
+    m, n, k = 2560, 2048, 3072
+    st, plan = bm.bm_gemm_bf16_plan(m, n, k, bm.bm_gemm_bf16_workspace_size(m, n, k))
+    assert plan.split_tiles > 0 and plan.k_splits > 1 and plan.kernels == 1
+    assert plan.workspace_bytes <= bm.BM_NOALLOC_SCRATCH_BYTES
+    for seed, beta in ((61, 0.0), (71, -1.0), (81, 0.0)):
+        A = operand(m, k, "int", seed, lo=-4, hi=4)
+        B = operand(k, n, "int", seed + 1, lo=-4, hi=4)
+        c0 = gen.integers(seed + 2, m * n, -50, 50).reshape(m, n).astype(np.float32)
+        dA, dB = bf16_to_device(A), bf16_to_device(B)
+        want, _ = _with_workspace(m, n, k, dA, dB, k, n, 1.0, beta, c0, False)
+        got = _noalloc(m, n, k, dA, dB, k, n, 1.0, beta, c0, False)
+        assert np.array_equal(got, want), seed
+
+
 def test_without_split_and_with_beta():
     m, n, k = 256, 264, 256
     A = operand(m, k, "normal", 31)
