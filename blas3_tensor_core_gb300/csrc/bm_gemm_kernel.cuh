@@ -87,9 +87,9 @@ struct GemmParams {
     int mode;          // MODE_*
     int64_t tiles_m, tiles_n;
     int64_t num_tiles;  // GEMM: tiles_m * tiles_n; SYRK: tiles touching the triangle
-    int64_t full_tiles; // units [0, full_tiles) are whole tiles; each later tile is split k_splits ways
+    int64_t full_tiles; // tiles [0, full_tiles) run whole; each later tile is split k_splits ways
     int64_t num_units;  // full_tiles + (num_tiles - full_tiles) * k_splits
-    int k_splits;       // > 1: split units write fp32 partials that a second kernel sums
+    int k_splits;       // > 1: split units write fp32 partials, summed in this kernel (fixup) or by a second one
     int kb_per_split;   // k-blocks (128 bytes of K each) per split
     int kb_total;       // ceil(k / elements per k-block)
     int group_m;        // grouped raster: tile rows per group
@@ -872,9 +872,10 @@ __device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUten
         const Unit w = map_unit<Cfg::TILE_M, BN>(p, u);
         const bool to_slot = w.slot >= 0;
         // Paths: beta != 0 tiles of GEMM (and SYRK tiles inside the triangle) go through
-        // the group path (TMA load of C, combine, TMA store); beta == 0 tiles and split
-        // units through the per-warp TMA-store path; SYRK tiles across the diagonal
-        // through the per-warp transposing path with per-element masks.
+        // the group path (TMA load of C, combine, TMA store); beta == 0 tiles and the
+        // split units of the reduce-kernel plan through the per-warp TMA-store path; SYRK
+        // tiles across the diagonal through the direct path from registers; split units
+        // of the in-kernel reduction through the per-warp transposing path.
         const bool inside = tile_inside_triangle<Cfg::TILE_M, BN>(p.mode, w.tm, w.tn);
         const bool group = !to_slot && beta_nonzero && p.tma_c && inside;  // the same for every warp
         // (split units of the in-kernel reduction store their partials with plain
