@@ -31,6 +31,7 @@ from __future__ import annotations
 import argparse
 import ctypes
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -99,14 +100,22 @@ def load_peaks():
         return dict(FALLBACK_PEAKS, source="fallback")
 
 
-def kernel_source_hash():
+def _code_only(text):
+    """C++ source without comments and with whitespace runs collapsed, so that
+    comment edits do not mark a profile of unchanged code as stale."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
+def kernel_source_hash(csrc=None):
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "blas3_tensor_core_gb300", "csrc")
+    csrc = csrc or os.path.join(ROOT, "blas3_tensor_core_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
         if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
+            with open(os.path.join(csrc, name), encoding="utf-8") as f:
                 h.update(name.encode())
-                h.update(f.read())
+                h.update(_code_only(f.read()).encode())
     return h.hexdigest()
 
 
