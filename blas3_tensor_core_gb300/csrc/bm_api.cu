@@ -51,19 +51,27 @@ std::atomic<uint32_t> g_timeout_ms{2000};
 std::atomic<int> g_debug_stall{0};
 std::atomic<int> g_tile_override{0};  // 0 = automatic, else 1 + Variant
 
-template <int ELEM>
+template <int ELEM, bool SIMPLE = false>
 const void *variant_kernel_t(int v)
 {
     switch (v) {
-    case kSingle256: return reinterpret_cast<const void *>(&bm::bm_gemm_tcgen05_kernel<256, 4, 1, ELEM, 1>);
-    case kSingle128: return reinterpret_cast<const void *>(&bm::bm_gemm_tcgen05_kernel<128, 3, 1, ELEM, 2>);
-    default: return reinterpret_cast<const void *>(&bm::bm_gemm_tcgen05_kernel<256, 3, 2, ELEM, 2>);
+    case kSingle256: return reinterpret_cast<const void *>(&bm::bm_gemm_tcgen05_kernel<256, 4, 1, ELEM, 1, SIMPLE>);
+    case kSingle128: return reinterpret_cast<const void *>(&bm::bm_gemm_tcgen05_kernel<128, 3, 1, ELEM, 2, SIMPLE>);
+    default: return reinterpret_cast<const void *>(&bm::bm_gemm_tcgen05_kernel<256, 3, 2, ELEM, 2, SIMPLE>);
     }
 }
 
-const void *variant_kernel(int v, int elem = bm::ELEM_BF16)
+// Kernel instantiations: bf16 and E4M3 operands with every epilogue path, and
+// bf16 with the TMA-store epilogue only (SIMPLE, beta == 0 GEMMs).
+constexpr int kNumKernelKinds = 3;
+
+const void *variant_kernel(int v, int kind = 0)
 {
-    return elem == bm::ELEM_E4M3 ? variant_kernel_t<bm::ELEM_E4M3>(v) : variant_kernel_t<bm::ELEM_BF16>(v);
+    switch (kind) {
+    case 1: return variant_kernel_t<bm::ELEM_E4M3>(v);
+    case 2: return variant_kernel_t<bm::ELEM_BF16, true>(v);
+    default: return variant_kernel_t<bm::ELEM_BF16>(v);
+    }
 }
 
 // Shared memory does not depend on the element type (k-blocks are 128 bytes of K).
@@ -111,7 +119,7 @@ bm_status device_state(DeviceState **out)
         if (cudaMemset(st.status, 0, sizeof(int)) != cudaSuccess) return BM_ERR_CUDA;
     }
     if (!st.attrs_set) {
-        for (int e = 0; e < 2; ++e)
+        for (int e = 0; e < kNumKernelKinds; ++e)
             for (int v = 0; v < kNumVariants; ++v)
                 if (cudaFuncSetAttribute(variant_kernel(v, e), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          variant_smem(v)) != cudaSuccess)
@@ -422,17 +430,17 @@ Plan plan_syrk(int mode, int64_t n, int64_t k, int sms, int pair_clusters, bool 
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-template <int ELEM>
+template <int ELEM, bool SIMPLE = false>
 cudaError_t launch_main(const cudaLaunchConfig_t &cfg, int variant, const CUtensorMap &ta, const CUtensorMap &tb,
                         const CUtensorMap &tc, const CUtensorMap &tp, const bm::GemmParams &prm)
 {
     switch (variant) {
     case kSingle256:
-        return cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<256, 4, 1, ELEM, 1>, ta, tb, tc, tp, prm);
+        return cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<256, 4, 1, ELEM, 1, SIMPLE>, ta, tb, tc, tp, prm);
     case kSingle128:
-        return cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<128, 3, 1, ELEM, 2>, ta, tb, tc, tp, prm);
+        return cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<128, 3, 1, ELEM, 2, SIMPLE>, ta, tb, tc, tp, prm);
     default:
-        return cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<256, 3, 2, ELEM, 2>, ta, tb, tc, tp, prm);
+        return cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<256, 3, 2, ELEM, 2, SIMPLE>, ta, tb, tc, tp, prm);
     }
 }
 
@@ -480,9 +488,14 @@ bm_status launch(const Plan &pl, const CUtensorMap &ta, const CUtensorMap &tb, b
         attr[1].val.clusterDim.z = 1;
         cfg.numAttrs = 2;
     }
-    const cudaError_t err = elem == bm::ELEM_E4M3
-                                ? launch_main<bm::ELEM_E4M3>(cfg, pl.variant, ta, tb, tc, tp, prm)
-                                : launch_main<bm::ELEM_BF16>(cfg, pl.variant, ta, tb, tc, tp, prm);
+    // A beta == 0 GEMM whose every unit takes the TMA-store epilogue (no in-kernel
+    // split-K sum; split units, if any, store through the slot map) runs the
+    // kernel compiled with that path alone.
+    const bool simple = elem == bm::ELEM_BF16 && prm.mode == bm::MODE_GEMM && prm.beta == 0.0f && prm.tma_c &&
+                        !prm.fixup && (prm.k_splits == 1 || prm.store_p_tma);
+    const cudaError_t err = elem == bm::ELEM_E4M3 ? launch_main<bm::ELEM_E4M3>(cfg, pl.variant, ta, tb, tc, tp, prm)
+                            : simple              ? launch_main<bm::ELEM_BF16, true>(cfg, pl.variant, ta, tb, tc, tp, prm)
+                                                  : launch_main<bm::ELEM_BF16>(cfg, pl.variant, ta, tb, tc, tp, prm);
     if (err != cudaSuccess) {
         cudaGetLastError();
         return BM_ERR_CUDA;
@@ -653,7 +666,7 @@ bm_status noalloc_device_setup(DeviceState **out, float **scratch)
         g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
     if (!st.attrs_set) {
-        for (int e = 0; e < 2; ++e)
+        for (int e = 0; e < kNumKernelKinds; ++e)
             for (int v = 0; v < kNumVariants; ++v)
                 if (cudaFuncSetAttribute(variant_kernel(v, e), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          variant_smem(v)) != cudaSuccess)

@@ -853,7 +853,10 @@ __device__ __forceinline__ void run_mma(const GemmParams &p, uint32_t ring, uint
     }
 }
 
-template <int BN, int STAGES, int PAIR, int ELEM, int KPS>
+// SIMPLE: every unit of the launch takes the per-warp TMA-store path (beta == 0
+// GEMM, no in-kernel split-K sum); the other paths are not compiled in, which
+// keeps the epilogue free of register spills.
+template <int BN, int STAGES, int PAIR, int ELEM, int KPS, bool SIMPLE = false>
 __device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUtensorMap *tmP, const GemmParams &p,
                                              uint32_t bar0, uint32_t tmem_base, float *epi, uint32_t rank,
                                              volatile int *abort_flag, int warp, int lane)
@@ -877,10 +880,11 @@ __device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUten
         // tiles across the diagonal through the direct path from registers; split units
         // of the in-kernel reduction through the per-warp transposing path.
         const bool inside = tile_inside_triangle<Cfg::TILE_M, BN>(p.mode, w.tm, w.tn);
-        const bool group = !to_slot && beta_nonzero && p.tma_c && inside;  // the same for every warp
+        const bool group = !SIMPLE && !to_slot && beta_nonzero && p.tma_c && inside;  // the same for every warp
         // (split units of the in-kernel reduction store their partials with plain
         // stores, which the arrival's fence orders before the counter update)
-        const bool warp_tma = to_slot ? (p.store_p_tma != 0 && !p.fixup) : (!beta_nonzero && p.tma_c && inside);
+        const bool warp_tma =
+            SIMPLE || (to_slot ? (p.store_p_tma != 0 && !p.fixup) : (!beta_nonzero && p.tma_c && inside));
         bool ready = wait_warp<PAIR == 2>(bar0 + 8u * (2 * STAGES + acc), acc_phase, abort_flag, p.timeout_ns);
         // A half that will meet at named barriers decides together, so that none of its
         // warps is left waiting at one.
@@ -988,7 +992,7 @@ __device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUten
                 if (issuer && loading) spin_ns(100000);  // a C copy may still land in the block
                 break;
             }
-        } else if (!inside && p.tma_c) {
+        } else if (!SIMPLE && !inside && p.tma_c) {
             // SYRK tile across the diagonal: registers straight to C. Per chunk of 128
             // bytes per row (64 bf16 or 32 fp32 columns), lane l owns row row0 + l of
             // this warp's 32 x chunk block. A block wholly outside the triangle is
@@ -1212,7 +1216,7 @@ __device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUten
 }
 
 // ---------------------------------------------------------------- kernels
-template <int BN, int STAGES, int PAIR, int ELEM, int KPS>
+template <int BN, int STAGES, int PAIR, int ELEM, int KPS, bool SIMPLE = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     bm_gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                            const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmP,
@@ -1284,7 +1288,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else if (warp == 1) {
         if (rank == 0) run_mma<BN, STAGES, PAIR, ELEM, KPS>(p, ring, bar0, tmem_base, abort_flag, lane);
     } else {
-        run_epilogue<BN, STAGES, PAIR, ELEM, KPS>(&tmC, &tmP, p, bar0, tmem_base, epi, rank,
+        run_epilogue<BN, STAGES, PAIR, ELEM, KPS, SIMPLE>(&tmC, &tmP, p, bar0, tmem_base, epi, rank,
                                        abort_flag,
                                        warp, lane);
     }
