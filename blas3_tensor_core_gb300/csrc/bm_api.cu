@@ -51,25 +51,26 @@ std::atomic<uint32_t> g_timeout_ms{2000};
 std::atomic<int> g_debug_stall{0};
 std::atomic<int> g_tile_override{0};  // 0 = automatic, else 1 + Variant
 
-template <int ELEM, bool SIMPLE = false>
+template <int ELEM, int EPI = bm::EPI_FULL>
 const void *variant_kernel_t(int v)
 {
     switch (v) {
-    case kSingle256: return reinterpret_cast<const void *>(&bm::bm_gemm_tcgen05_kernel<256, 4, 1, ELEM, 1, SIMPLE>);
-    case kSingle128: return reinterpret_cast<const void *>(&bm::bm_gemm_tcgen05_kernel<128, 3, 1, ELEM, 2, SIMPLE>);
-    default: return reinterpret_cast<const void *>(&bm::bm_gemm_tcgen05_kernel<256, 3, 2, ELEM, 2, SIMPLE>);
+    case kSingle256: return reinterpret_cast<const void *>(&bm::bm_gemm_tcgen05_kernel<256, 4, 1, ELEM, 1, EPI>);
+    case kSingle128: return reinterpret_cast<const void *>(&bm::bm_gemm_tcgen05_kernel<128, 3, 1, ELEM, 2, EPI>);
+    default: return reinterpret_cast<const void *>(&bm::bm_gemm_tcgen05_kernel<256, 3, 2, ELEM, 2, EPI>);
     }
 }
 
-// Kernel instantiations: bf16 and E4M3 operands with every epilogue path, and
-// bf16 with the TMA-store epilogue only (SIMPLE, beta == 0 GEMMs).
-constexpr int kNumKernelKinds = 3;
+// Kernel copies: bf16 and E4M3 operands with every epilogue path, and bf16 with
+// the store-only (beta == 0) and combine (beta != 0) epilogues.
+constexpr int kNumKernelKinds = 4;
 
 const void *variant_kernel(int v, int kind = 0)
 {
     switch (kind) {
     case 1: return variant_kernel_t<bm::ELEM_E4M3>(v);
-    case 2: return variant_kernel_t<bm::ELEM_BF16, true>(v);
+    case 2: return variant_kernel_t<bm::ELEM_BF16, bm::EPI_STORE>(v);
+    case 3: return variant_kernel_t<bm::ELEM_BF16, bm::EPI_COMBINE>(v);
     default: return variant_kernel_t<bm::ELEM_BF16>(v);
     }
 }
@@ -430,17 +431,17 @@ Plan plan_syrk(int mode, int64_t n, int64_t k, int sms, int pair_clusters, bool 
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-template <int ELEM, bool SIMPLE = false>
+template <int ELEM, int EPI = bm::EPI_FULL>
 cudaError_t launch_main(const cudaLaunchConfig_t &cfg, int variant, const CUtensorMap &ta, const CUtensorMap &tb,
                         const CUtensorMap &tc, const CUtensorMap &tp, const bm::GemmParams &prm)
 {
     switch (variant) {
     case kSingle256:
-        return cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<256, 4, 1, ELEM, 1, SIMPLE>, ta, tb, tc, tp, prm);
+        return cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<256, 4, 1, ELEM, 1, EPI>, ta, tb, tc, tp, prm);
     case kSingle128:
-        return cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<128, 3, 1, ELEM, 2, SIMPLE>, ta, tb, tc, tp, prm);
+        return cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<128, 3, 1, ELEM, 2, EPI>, ta, tb, tc, tp, prm);
     default:
-        return cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<256, 3, 2, ELEM, 2, SIMPLE>, ta, tb, tc, tp, prm);
+        return cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<256, 3, 2, ELEM, 2, EPI>, ta, tb, tc, tp, prm);
     }
 }
 
@@ -488,14 +489,16 @@ bm_status launch(const Plan &pl, const CUtensorMap &ta, const CUtensorMap &tb, b
         attr[1].val.clusterDim.z = 1;
         cfg.numAttrs = 2;
     }
-    // A beta == 0 GEMM whose every unit takes the TMA-store epilogue (no in-kernel
-    // split-K sum; split units, if any, store through the slot map) runs the
-    // kernel compiled with that path alone.
-    const bool simple = elem == bm::ELEM_BF16 && prm.mode == bm::MODE_GEMM && prm.beta == 0.0f && prm.tma_c &&
-                        !prm.fixup && (prm.k_splits == 1 || prm.store_p_tma);
-    const cudaError_t err = elem == bm::ELEM_E4M3 ? launch_main<bm::ELEM_E4M3>(cfg, pl.variant, ta, tb, tc, tp, prm)
-                            : simple              ? launch_main<bm::ELEM_BF16, true>(cfg, pl.variant, ta, tb, tc, tp, prm)
-                                                  : launch_main<bm::ELEM_BF16>(cfg, pl.variant, ta, tb, tc, tp, prm);
+    // A bf16 GEMM without the in-kernel split-K sum (split units, if any, store
+    // through the slot map) runs a kernel copy with only the epilogue paths it
+    // takes: store-only for beta == 0, group combine (+ slot stores) otherwise.
+    const bool lean = elem == bm::ELEM_BF16 && prm.mode == bm::MODE_GEMM && prm.tma_c && !prm.fixup &&
+                      (prm.k_splits == 1 || prm.store_p_tma);
+    cudaError_t err;
+    if (elem == bm::ELEM_E4M3) err = launch_main<bm::ELEM_E4M3>(cfg, pl.variant, ta, tb, tc, tp, prm);
+    else if (lean && prm.beta == 0.0f) err = launch_main<bm::ELEM_BF16, bm::EPI_STORE>(cfg, pl.variant, ta, tb, tc, tp, prm);
+    else if (lean) err = launch_main<bm::ELEM_BF16, bm::EPI_COMBINE>(cfg, pl.variant, ta, tb, tc, tp, prm);
+    else err = launch_main<bm::ELEM_BF16>(cfg, pl.variant, ta, tb, tc, tp, prm);
     if (err != cudaSuccess) {
         cudaGetLastError();
         return BM_ERR_CUDA;

@@ -57,6 +57,7 @@
 namespace bm {
 
 enum : int { MODE_GEMM = 0, MODE_SYRK_LOWER = 1, MODE_SYRK_UPPER = 2 };
+enum : int { EPI_FULL = 0, EPI_STORE = 1, EPI_COMBINE = 2 };  // epilogue paths compiled into a kernel copy
 enum : int { DEV_ERR_TIMEOUT = 5 };
 
 constexpr int CTA_M = 128;  // accumulator rows (TMEM lanes) per CTA
@@ -853,10 +854,13 @@ __device__ __forceinline__ void run_mma(const GemmParams &p, uint32_t ring, uint
     }
 }
 
-// SIMPLE: every unit of the launch takes the per-warp TMA-store path (beta == 0
-// GEMM, no in-kernel split-K sum); the other paths are not compiled in, which
-// keeps the epilogue free of register spills.
-template <int BN, int STAGES, int PAIR, int ELEM, int KPS, bool SIMPLE = false>
+// EPI selects the epilogue paths compiled in. EPI_FULL has them all. The other
+// two serve GEMMs without the in-kernel split-K sum, whose split units (if any)
+// store through the slot map: EPI_STORE (beta == 0) has the per-warp TMA-store
+// path alone, EPI_COMBINE (beta != 0) the group path for whole tiles plus that
+// store path for split units. Leaving the rest out keeps those copies free of
+// register spills.
+template <int BN, int STAGES, int PAIR, int ELEM, int KPS, int EPI = EPI_FULL>
 __device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUtensorMap *tmP, const GemmParams &p,
                                              uint32_t bar0, uint32_t tmem_base, float *epi, uint32_t rank,
                                              volatile int *abort_flag, int warp, int lane)
@@ -880,11 +884,12 @@ __device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUten
         // tiles across the diagonal through the direct path from registers; split units
         // of the in-kernel reduction through the per-warp transposing path.
         const bool inside = tile_inside_triangle<Cfg::TILE_M, BN>(p.mode, w.tm, w.tn);
-        const bool group = !SIMPLE && !to_slot && beta_nonzero && p.tma_c && inside;  // the same for every warp
+        const bool group = EPI == EPI_COMBINE ? !to_slot
+                                              : EPI == EPI_FULL && !to_slot && beta_nonzero && p.tma_c && inside;
         // (split units of the in-kernel reduction store their partials with plain
         // stores, which the arrival's fence orders before the counter update)
         const bool warp_tma =
-            SIMPLE || (to_slot ? (p.store_p_tma != 0 && !p.fixup) : (!beta_nonzero && p.tma_c && inside));
+            EPI != EPI_FULL || (to_slot ? (p.store_p_tma != 0 && !p.fixup) : (!beta_nonzero && p.tma_c && inside));
         bool ready = wait_warp<PAIR == 2>(bar0 + 8u * (2 * STAGES + acc), acc_phase, abort_flag, p.timeout_ns);
         // A half that will meet at named barriers decides together, so that none of its
         // warps is left waiting at one.
@@ -992,7 +997,7 @@ __device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUten
                 if (issuer && loading) spin_ns(100000);  // a C copy may still land in the block
                 break;
             }
-        } else if (!SIMPLE && !inside && p.tma_c) {
+        } else if (EPI == EPI_FULL && !inside && p.tma_c) {
             // SYRK tile across the diagonal: registers straight to C. Per chunk of 128
             // bytes per row (64 bf16 or 32 fp32 columns), lane l owns row row0 + l of
             // this warp's 32 x chunk block. A block wholly outside the triangle is
@@ -1216,7 +1221,7 @@ __device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUten
 }
 
 // ---------------------------------------------------------------- kernels
-template <int BN, int STAGES, int PAIR, int ELEM, int KPS, bool SIMPLE = false>
+template <int BN, int STAGES, int PAIR, int ELEM, int KPS, int EPI = EPI_FULL>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     bm_gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                            const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmP,
@@ -1288,7 +1293,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else if (warp == 1) {
         if (rank == 0) run_mma<BN, STAGES, PAIR, ELEM, KPS>(p, ring, bar0, tmem_base, abort_flag, lane);
     } else {
-        run_epilogue<BN, STAGES, PAIR, ELEM, KPS, SIMPLE>(&tmC, &tmP, p, bar0, tmem_base, epi, rank,
+        run_epilogue<BN, STAGES, PAIR, ELEM, KPS, EPI>(&tmC, &tmP, p, bar0, tmem_base, epi, rank,
                                        abort_flag,
                                        warp, lane);
     }
