@@ -61,8 +61,8 @@ const void *variant_kernel_t(int v)
     }
 }
 
-// Kernel copies: bf16 and E4M3 operands with every epilogue path, and bf16 with
-// the store-only (beta == 0) and combine (beta != 0) epilogues.
+// Kernel copies: bf16 and E4M3 operands with every epilogue path, and bf16 GEMM
+// copies without the SYRK diagonal path (beta == 0 and beta != 0).
 constexpr int kNumKernelKinds = 4;
 
 const void *variant_kernel(int v, int kind = 0)
@@ -489,11 +489,10 @@ bm_status launch(const Plan &pl, const CUtensorMap &ta, const CUtensorMap &tb, b
         attr[1].val.clusterDim.z = 1;
         cfg.numAttrs = 2;
     }
-    // A bf16 GEMM without the in-kernel split-K sum (split units, if any, store
-    // through the slot map) runs a kernel copy with only the epilogue paths it
-    // takes: store-only for beta == 0, group combine (+ slot stores) otherwise.
-    const bool lean = elem == bm::ELEM_BF16 && prm.mode == bm::MODE_GEMM && prm.tma_c && !prm.fixup &&
-                      (prm.k_splits == 1 || prm.store_p_tma);
+    // A bf16 GEMM runs a kernel copy without the SYRK diagonal path: TMA-store
+    // epilogue for beta == 0, group combine otherwise (split units as in the
+    // full kernel).
+    const bool lean = elem == bm::ELEM_BF16 && prm.mode == bm::MODE_GEMM && prm.tma_c;
     cudaError_t err;
     if (elem == bm::ELEM_E4M3) err = launch_main<bm::ELEM_E4M3>(cfg, pl.variant, ta, tb, tc, tp, prm);
     else if (lean && prm.beta == 0.0f) err = launch_main<bm::ELEM_BF16, bm::EPI_STORE>(cfg, pl.variant, ta, tb, tc, tp, prm);

@@ -854,12 +854,12 @@ __device__ __forceinline__ void run_mma(const GemmParams &p, uint32_t ring, uint
     }
 }
 
-// EPI selects the epilogue paths compiled in. EPI_FULL has them all. The other
-// two serve GEMMs without the in-kernel split-K sum, whose split units (if any)
-// store through the slot map: EPI_STORE (beta == 0) has the per-warp TMA-store
-// path alone, EPI_COMBINE (beta != 0) the group path for whole tiles plus that
-// store path for split units. Leaving the rest out keeps those copies free of
-// register spills.
+// EPI selects the epilogue paths compiled in. EPI_FULL has them all (SYRK needs
+// the direct path for tiles across the diagonal). The GEMM copies leave that path
+// out, which keeps them free of register spills: EPI_STORE (beta == 0) stores
+// whole tiles with per-warp TMA stores, EPI_COMBINE (beta != 0) through the
+// group path; split units take the slot-map TMA stores, or the transposing path
+// with the in-kernel sum.
 template <int BN, int STAGES, int PAIR, int ELEM, int KPS, int EPI = EPI_FULL>
 __device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUtensorMap *tmP, const GemmParams &p,
                                              uint32_t bar0, uint32_t tmem_base, float *epi, uint32_t rank,
@@ -886,10 +886,12 @@ __device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUten
         const bool inside = tile_inside_triangle<Cfg::TILE_M, BN>(p.mode, w.tm, w.tn);
         const bool group = EPI == EPI_COMBINE ? !to_slot
                                               : EPI == EPI_FULL && !to_slot && beta_nonzero && p.tma_c && inside;
+        const bool slot_tma = p.store_p_tma != 0 && !p.fixup;  // split units of the reduce-kernel plan
         // (split units of the in-kernel reduction store their partials with plain
         // stores, which the arrival's fence orders before the counter update)
-        const bool warp_tma =
-            EPI != EPI_FULL || (to_slot ? (p.store_p_tma != 0 && !p.fixup) : (!beta_nonzero && p.tma_c && inside));
+        const bool warp_tma = EPI == EPI_STORE   ? !to_slot || slot_tma
+                              : EPI == EPI_COMBINE ? to_slot && slot_tma
+                                                   : (to_slot ? slot_tma : (!beta_nonzero && p.tma_c && inside));
         bool ready = wait_warp<PAIR == 2>(bar0 + 8u * (2 * STAGES + acc), acc_phase, abort_flag, p.timeout_ns);
         // A half that will meet at named barriers decides together, so that none of its
         // warps is left waiting at one.
