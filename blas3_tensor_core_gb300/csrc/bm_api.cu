@@ -336,16 +336,19 @@ void size_grid(Plan &pl, int sms, int pair_clusters)
 
 // Split the last `split_tiles` tiles of the unit order `want` ways (or fewer)
 // along K, if each part keeps >= 4 k-blocks, the partial slots fit `budget`,
-// and the mainloop time it saves is at least kSplitMinGainUs. One 64-deep
+// and the mainloop time it saves is at least `min_gain_us`. One 64-deep
 // k-block of a tile takes 4 MMAs of 128 tensor-core cycles, about 0.26 us at
 // 2 GHz. Summing the partials costs a few us: a second kernel when every tile
-// is split, extra epilogue work inside the kernel for a tail split (a lower
-// threshold there was measured slower at K = 1024 and 2048, where the
-// epilogue already takes longer than a tile's mainloop).
+// is split (kSplitMinGainUs), extra epilogue work inside the kernel for a tail
+// split. Measured for tail splits: with beta == 0 a 3.5 us gain pays (4096^2 x
+// 2048 and the 5120^2 x 2048 TN GEMM ran 9 % and 5 % faster split), 2 us does
+// not (4096^2 x 1024 ran slower); with beta != 0 the split units' combine with
+// C makes 3.5 us lose (dW 5120^2 x 2048 75.3 -> 81.5 us), so it keeps 6 us.
 constexpr double kKBlockUs = 0.256;
 constexpr double kSplitMinGainUs = 6.0;
+constexpr double kTailSplitMinGainUsBeta0 = 3.5;
 
-void try_split(Plan &pl, int64_t split_tiles, int64_t want, size_t budget)
+void try_split(Plan &pl, int64_t split_tiles, int64_t want, size_t budget, double min_gain_us)
 {
     const size_t slot_bytes = static_cast<size_t>(pl.tile_m) * pl.bn * sizeof(float);
     want = std::min<int64_t>(want, pl.kb_total / 4);
@@ -361,7 +364,7 @@ void try_split(Plan &pl, int64_t split_tiles, int64_t want, size_t budget)
         const size_t need =
             slots + (fixup ? static_cast<size_t>(split_tiles) * pl.pair * bm::NUM_EPI_WARPS * 8u : 0u);
         const double gain_us = kKBlockUs * (pl.kb_total - per);
-        if (splits > 1 && need <= budget && gain_us >= kSplitMinGainUs) {
+        if (splits > 1 && need <= budget && gain_us >= min_gain_us) {
             pl.k_splits = splits;
             pl.kb_per_split = per;
             pl.full_tiles = pl.num_tiles - split_tiles;
@@ -376,8 +379,10 @@ void try_split(Plan &pl, int64_t split_tiles, int64_t want, size_t budget)
 
 // Pair tiles (256 x 256 on two SMs) whenever they alone can occupy at least half
 // of the SM pairs; otherwise 128-row tiles on single SMs (more, smaller tiles).
+// beta_nonzero: the call combines with C (tail splits then need a larger gain,
+// as do E4M3 ones, which were not measured with the lower threshold).
 Plan plan_gemm(int64_t m, int64_t n, int64_t k, size_t ws_bytes, int sms, int pair_clusters,
-               int elem = bm::ELEM_BF16)
+               int elem = bm::ELEM_BF16, bool beta_nonzero = false)
 {
     Plan pl;
     const int64_t pair_tiles = ceil_div(m, 256) * ceil_div(n, 256);
@@ -395,11 +400,13 @@ Plan plan_gemm(int64_t m, int64_t n, int64_t k, size_t ws_bytes, int sms, int pa
     if (slots > 0 && pl.kb_total >= 8) {
         if (pl.num_tiles * 2 <= slots) {
             // Too few tiles to fill half the GPU: split every tile along K.
-            try_split(pl, pl.num_tiles, ceil_div(slots, pl.num_tiles), ws_bytes);
+            try_split(pl, pl.num_tiles, ceil_div(slots, pl.num_tiles), ws_bytes, kSplitMinGainUs);
         } else {
             // The last wave is at most half full: split its tiles along K over the idle slots.
             const int64_t tail = pl.num_tiles % slots;
-            if (tail > 0 && tail * 2 <= slots) try_split(pl, tail, slots / tail, std::min(ws_bytes, kTailSplitMaxBytes));
+            if (tail > 0 && tail * 2 <= slots)
+                try_split(pl, tail, slots / tail, std::min(ws_bytes, kTailSplitMaxBytes),
+                          elem == bm::ELEM_BF16 && !beta_nonzero ? kTailSplitMinGainUsBeta0 : kSplitMinGainUs);
         }
     }
     size_grid(pl, sms, pair_clusters);
@@ -734,7 +741,7 @@ bm_status bm_gemm_bf16(int64_t m, int64_t n, int64_t k, bm_op transA, bm_op tran
     if (!products) return launch_scale(prm, cs);
 
     const Plan pl = plan_gemm(m, n, k, workspace != nullptr ? workspace_bytes : 0, st->sm_count,
-                              st->max_pair_clusters);
+                              st->max_pair_clusters, bm::ELEM_BF16, beta != 0.0f);
     CUtensorMap ta, tb;
     const bool a_mn = transA == BM_OP_T, b_mn = transB == BM_OP_N;
     // each CTA stages 128 rows of op(A) and bn / pair rows of op(B)^T
@@ -782,7 +789,7 @@ bm_status bm_gemm_bf16_noalloc(int64_t m, int64_t n, int64_t k, bm_op transA, bm
 
     // The plan bm_gemm_bf16 makes with the workspace it asks for; its partials
     // must fit the static scratch array.
-    const Plan pl = plan_gemm(m, n, k, SIZE_MAX, st->sm_count, st->max_pair_clusters);
+    const Plan pl = plan_gemm(m, n, k, SIZE_MAX, st->sm_count, st->max_pair_clusters, bm::ELEM_BF16, beta != 0.0f);
     if (pl.k_splits > 1 && pl.ws_bytes > BM_NOALLOC_SCRATCH_BYTES) return BM_ERR_WORKSPACE;
     CUtensorMap ta, tb;
     const bool a_mn = transA == BM_OP_T, b_mn = transB == BM_OP_N;

@@ -244,7 +244,9 @@ BM_API const char *bm_status_string(bm_status status);
  * output tile (2 = an SM pair working on one tile), and the number of kernels
  * one call launches. Performs the same size checks as
  * the call (no pointers are given). On a machine without a usable GPU the
- * plan assumes 152 SMs.
+ * plan assumes 152 SMs. A GEMM's plan is the one for beta == 0: with
+ * beta != 0 a tail split needs a larger saving, so such a call may split
+ * fewer tiles (bm_gemm_bf16_workspace_size covers both).
  */
 typedef struct {
     int32_t tile_m, tile_n, tile_k;

@@ -116,7 +116,10 @@ def test_e4m3_argument_errors(lib):
     assert g8(A=0x1008) == bm.BM_ERR_MISALIGNED
     assert g8(n=0, ldc=1) == bm.BM_OK
     assert bm.bm_gemm_e4m3_workspace_size(512, 512, 16384) > 0     # 128 k-blocks of 128: split pays
-    assert bm.bm_gemm_e4m3_workspace_size(4096, 4096, 4096) == bm.bm_gemm_bf16_workspace_size(4096, 4096, 2048)
+    # same bytes per k-block as bf16 with half the K (the lower beta == 0 tail-split threshold is
+    # bf16-only, so compare where both split: a 16 us saving)
+    assert bm.bm_gemm_e4m3_workspace_size(4096, 4096, 8192) == bm.bm_gemm_bf16_workspace_size(4096, 4096, 4096) > 0
+    assert bm.bm_gemm_e4m3_workspace_size(4096, 4096, 4096) == 0    # 4.1 us: below the 6 us E4M3 keeps
 
 
 def test_syr2k_argument_errors(lib):
@@ -188,13 +191,16 @@ def test_tail_split_plans(lib):
     # (8 ways would need 16 MiB of slots plus the counters)
     p = bm.bm_gemm_bf16_plan(2048, 5120, 5120, 1 << 30)[1]
     assert (p.split_tiles, p.k_splits, p.kernels) == (8, 7, 1) and p.workspace_bytes <= 16 << 20
-    # a short K saves too little mainloop time to pay for the extra reduce
+    # the tail split must save enough mainloop time: 3.5 us for a beta == 0 bf16 GEMM (the
+    # plan shown), 6 us with beta != 0; 0.256 us per k-block of a tile
     p = bm.bm_gemm_bf16_plan(5120, 5120, 2048, 1 << 30)[1]     # 400 tiles = 5 waves + 20
-    assert p.split_tiles == 0 and p.k_splits == 1
+    assert (p.split_tiles, p.k_splits) == (20, 3)              # 3-way: 21 of 32 k-blocks saved, 5.4 us
     p = bm.bm_gemm_bf16_plan(5120, 5120, 4096, 1 << 30)[1]
     assert p.split_tiles == 20 and p.k_splits == 3
-    p = bm.bm_gemm_bf16_plan(4096, 4096, 1024, 1 << 30)[1]
+    p = bm.bm_gemm_bf16_plan(4096, 4096, 1024, 1 << 30)[1]     # 2-way: 8 k-blocks, 2 us
     assert p.split_tiles == 0
+    p = bm.bm_gemm_bf16_plan(4096, 4096, 2048, 1 << 30)[1]     # 2-way: 16 k-blocks, 4.1 us
+    assert (p.split_tiles, p.k_splits) == (28, 2)
     # a last wave more than half full is not split
     p = bm.bm_gemm_bf16_plan(8192, 8192 - 1024, 4096, 1 << 30)[1]  # 32 x 28 = 896 tiles = 11 waves + 60
     assert p.split_tiles == 0 and p.k_splits == 1
