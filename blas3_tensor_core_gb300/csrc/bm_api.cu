@@ -61,9 +61,10 @@ const void *variant_kernel_t(int v)
     }
 }
 
-// Kernel copies: bf16 and E4M3 operands with every epilogue path, and bf16 GEMM
-// copies without the SYRK diagonal path (beta == 0 and beta != 0).
-constexpr int kNumKernelKinds = 4;
+// Kernel copies: bf16 and E4M3 operands with every epilogue path, bf16 GEMM
+// copies without the SYRK diagonal path (beta == 0 and beta != 0), and the
+// E4M3 beta == 0 one.
+constexpr int kNumKernelKinds = 5;
 
 const void *variant_kernel(int v, int kind = 0)
 {
@@ -71,6 +72,7 @@ const void *variant_kernel(int v, int kind = 0)
     case 1: return variant_kernel_t<bm::ELEM_E4M3>(v);
     case 2: return variant_kernel_t<bm::ELEM_BF16, bm::EPI_STORE>(v);
     case 3: return variant_kernel_t<bm::ELEM_BF16, bm::EPI_COMBINE>(v);
+    case 4: return variant_kernel_t<bm::ELEM_E4M3, bm::EPI_STORE>(v);
     default: return variant_kernel_t<bm::ELEM_BF16>(v);
     }
 }
@@ -496,12 +498,14 @@ bm_status launch(const Plan &pl, const CUtensorMap &ta, const CUtensorMap &tb, b
         attr[1].val.clusterDim.z = 1;
         cfg.numAttrs = 2;
     }
-    // A bf16 GEMM runs a kernel copy without the SYRK diagonal path: TMA-store
-    // epilogue for beta == 0, group combine otherwise (split units as in the
-    // full kernel).
-    const bool lean = elem == bm::ELEM_BF16 && prm.mode == bm::MODE_GEMM && prm.tma_c;
+    // A GEMM runs a kernel copy without the SYRK diagonal path: TMA-store epilogue
+    // for beta == 0, group combine otherwise (split units as in the full kernel;
+    // for E4M3 only the beta == 0 copy exists).
+    const bool lean = prm.mode == bm::MODE_GEMM && prm.tma_c;
     cudaError_t err;
-    if (elem == bm::ELEM_E4M3) err = launch_main<bm::ELEM_E4M3>(cfg, pl.variant, ta, tb, tc, tp, prm);
+    if (elem == bm::ELEM_E4M3 && lean && prm.beta == 0.0f)
+        err = launch_main<bm::ELEM_E4M3, bm::EPI_STORE>(cfg, pl.variant, ta, tb, tc, tp, prm);
+    else if (elem == bm::ELEM_E4M3) err = launch_main<bm::ELEM_E4M3>(cfg, pl.variant, ta, tb, tc, tp, prm);
     else if (lean && prm.beta == 0.0f) err = launch_main<bm::ELEM_BF16, bm::EPI_STORE>(cfg, pl.variant, ta, tb, tc, tp, prm);
     else if (lean) err = launch_main<bm::ELEM_BF16, bm::EPI_COMBINE>(cfg, pl.variant, ta, tb, tc, tp, prm);
     else err = launch_main<bm::ELEM_BF16>(cfg, pl.variant, ta, tb, tc, tp, prm);
