@@ -222,6 +222,34 @@ def test_tail_split_exact_and_deterministic(variant):
     assert np.array_equal(outs[0], ref)
 
 
+@pytest.mark.parametrize("beta", [0.0, 1.0], ids=["beta0", "beta1"])
+def test_tail_split_depends_on_beta(beta):
+    """4096^2 x 2048: the 28 tiles of the last wave save 4.1 us of mainloop by a 2-way K split.
+    That pays when the split tiles need no combine with C (beta == 0, split and summed in the
+    kernel) and not otherwise (beta != 0, whole tiles). Either plan must give the exact result:
+    small integers, checked on every row of four columns through the split tiles (the last two
+    tile columns) and on samples everywhere else."""
+    import blas3_tensor_core_gb300 as bm
+    t = torch()
+    m = n = 4096
+    k = 2048
+    st, plan = bm.bm_gemm_bf16_plan(m, n, k, bm.bm_gemm_bf16_workspace_size(m, n, k))
+    assert (plan.split_tiles, plan.k_splits, plan.kernels) == (28, 2, 1)   # the plan reported is beta == 0's
+    A, B = _operands(m, n, k, 0, 0, "int", seed=87, lo=-2, hi=2)
+    c0 = gen.integers(88, m * n, -30, 30).reshape(m, n).astype(np.float32)
+    need = bm.bm_gemm_bf16_workspace_size(m, n, k)
+    ws = t.empty(need // 4, dtype=t.float32, device="cuda")
+    cbuf = CBuffer(m, n, n, False, init=c0)
+    got, raw = run_gemm(m, n, k, 0, 0, 1.0, A, B, beta, cbuf, workspace=ws)
+    cbuf.assert_guard_intact(raw)
+    cols_full = np.array([3584, 3700, 3840, 4095])
+    band_r = np.tile(np.arange(m), cols_full.size)
+    band_c = np.repeat(cols_full, m)
+    rows, cols = tile_samples(m, n, tile_m=256, tile_n=256, per_tile=8, seed=14, extra=(band_r, band_c))
+    ref, _ = orc().gemm_entries(k, 0, 0, 1.0, A, B, rows, cols, beta, c0 if beta != 0 else None)
+    assert np.array_equal(got[rows, cols], ref)
+
+
 def test_tail_split_ragged_many_splits_bf16_beta():
     """Ragged m, n and k; the 4 tail tiles split 10 ways and summed in the kernel, into bf16 C with beta."""
     import blas3_tensor_core_gb300 as bm
