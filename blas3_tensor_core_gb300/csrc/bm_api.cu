@@ -89,6 +89,36 @@ int variant_smem(int v)
 
 bool fits_int32(int64_t v) { return v >= 0 && v <= 0x7FFFFFFFLL; }
 
+// Once per device: the dynamic shared-memory size of every kernel copy, and how
+// many clusters of the pair kernel fit at once (0: single-CTA tiles only).
+bm_status init_kernel_attrs(DeviceState &st)
+{
+    for (int e = 0; e < kNumKernelKinds; ++e)
+        for (int v = 0; v < kNumVariants; ++v)
+            if (cudaFuncSetAttribute(variant_kernel(v, e), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     variant_smem(v)) != cudaSuccess)
+                return BM_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * (st.sm_count / 2), 1, 1);
+    cfg.blockDim = dim3(bm::NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = variant_smem(kPair256);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, variant_kernel(kPair256), &cfg) != cudaSuccess || clusters <= 0) {
+        cudaGetLastError();
+        clusters = 0;
+    }
+    st.max_pair_clusters = clusters;
+    st.attrs_set = true;
+    return BM_OK;
+}
+
 // Current device, checked for compute capability 10.3; status word allocated.
 bm_status device_state(DeviceState **out)
 {
@@ -122,30 +152,8 @@ bm_status device_state(DeviceState **out)
         if (cudaMemset(st.status, 0, sizeof(int)) != cudaSuccess) return BM_ERR_CUDA;
     }
     if (!st.attrs_set) {
-        for (int e = 0; e < kNumKernelKinds; ++e)
-            for (int v = 0; v < kNumVariants; ++v)
-                if (cudaFuncSetAttribute(variant_kernel(v, e), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         variant_smem(v)) != cudaSuccess)
-                    return BM_ERR_CUDA;
-        cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.gridDim = dim3(2 * (st.sm_count / 2), 1, 1);
-        cfg.blockDim = dim3(bm::NUM_THREADS, 1, 1);
-        cfg.dynamicSmemBytes = variant_smem(kPair256);
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        int clusters = 0;
-        if (cudaOccupancyMaxActiveClusters(&clusters, variant_kernel(kPair256), &cfg) != cudaSuccess ||
-            clusters <= 0) {
-            cudaGetLastError();
-            clusters = 0;  // pair kernel unavailable: single-CTA tiles only
-        }
-        st.max_pair_clusters = clusters;
-        st.attrs_set = true;
+        const bm_status a = init_kernel_attrs(st);
+        if (a != BM_OK) return a;
     }
     *out = &st;
     return BM_OK;
@@ -679,30 +687,8 @@ bm_status noalloc_device_setup(DeviceState **out, float **scratch)
         g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
     if (!st.attrs_set) {
-        for (int e = 0; e < kNumKernelKinds; ++e)
-            for (int v = 0; v < kNumVariants; ++v)
-                if (cudaFuncSetAttribute(variant_kernel(v, e), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         variant_smem(v)) != cudaSuccess)
-                    return BM_ERR_CUDA;
-        cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.gridDim = dim3(2 * (st.sm_count / 2), 1, 1);
-        cfg.blockDim = dim3(bm::NUM_THREADS, 1, 1);
-        cfg.dynamicSmemBytes = variant_smem(kPair256);
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        int clusters = 0;
-        if (cudaOccupancyMaxActiveClusters(&clusters, variant_kernel(kPair256), &cfg) != cudaSuccess ||
-            clusters <= 0) {
-            cudaGetLastError();
-            clusters = 0;
-        }
-        st.max_pair_clusters = clusters;
-        st.attrs_set = true;
+        const bm_status a = init_kernel_attrs(st);
+        if (a != BM_OK) return a;
     }
     if (g_noalloc_scratch_addr[dev] == nullptr) {
         void *addr = nullptr;
