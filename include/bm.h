@@ -34,6 +34,11 @@
  *     a failed launch returns BM_ERR_CUDA. A device-side wait that runs out
  *     of time (see bm_set_wait_timeout_ms) is reported later by
  *     bm_get_last_device_error.
+ *   - Stream order holds as for any kernel: a call reads and writes memory
+ *     only after the work queued before it on `stream` has completed. (Its
+ *     kernel is launched early and prepares meanwhile: barriers, tensor
+ *     memory, and an L2 prefetch of its first A and B tiles, which brings no
+ *     data into the SM and so cannot observe an older value.)
  *   - The device must be compute capability 10.3 (GB300, sm_103a); any other
  *     device gives BM_ERR_ARCH. There is no other code path.
  */
