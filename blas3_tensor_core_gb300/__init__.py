@@ -22,7 +22,7 @@ __all__ = [
     "bm_gemm_bf16", "bm_gemm_bf16_noalloc", "BM_NOALLOC_SCRATCH_BYTES", "bm_syrk_bf16", "bm_syr2k_bf16",
     "bm_gemm_e4m3", "bm_gemm_e4m3_workspace_size", "bm_gemm_bf16_workspace_size", "bm_get_last_device_error",
     "bm_set_wait_timeout_ms", "bm_debug_inject_stall", "bm_status_string", "bm_gemm_bf16_plan",
-    "bm_syrk_bf16_plan", "bm_set_tile_override", "bm_version", "gemm", "syrk", "syr2k", "workspace_size",
+    "bm_syrk_bf16_plan", "bm_syrk_bf16_tile_order", "bm_set_tile_override", "bm_version", "gemm", "syrk", "syr2k", "workspace_size",
 ]
 
 BM_OK, BM_ERR_INVALID_VALUE, BM_ERR_MISALIGNED, BM_ERR_ARCH, BM_ERR_CUDA, BM_ERR_TIMEOUT, BM_ERR_WORKSPACE = range(7)
@@ -98,6 +98,8 @@ def library():
                 lib.bm_gemm_bf16_plan.restype = _i32
                 lib.bm_syrk_bf16_plan.argtypes = [_i32, _i64, _i64, ctypes.POINTER(Plan)]
                 lib.bm_syrk_bf16_plan.restype = _i32
+                lib.bm_syrk_bf16_tile_order.argtypes = [_i32, _i64, _i64, _i64, _vp, _vp]
+                lib.bm_syrk_bf16_tile_order.restype = _i32
                 lib.bm_set_tile_override.argtypes = [_i32]
                 lib.bm_set_tile_override.restype = _i32
                 lib.bm_version.argtypes = []
@@ -172,6 +174,18 @@ def bm_syrk_bf16_plan(uplo, n, k):
     plan = Plan()
     st = library().bm_syrk_bf16_plan(uplo, n, k, ctypes.byref(plan))
     return st, plan
+
+
+def bm_syrk_bf16_tile_order(uplo, n, k):
+    """(status, tile rows, tile columns) of the SYRK schedule, as int64 NumPy arrays."""
+    import numpy as np
+    st, plan = bm_syrk_bf16_plan(uplo, n, k)
+    rows = np.zeros(max(plan.tiles, 0), np.int64)
+    cols = np.zeros(max(plan.tiles, 0), np.int64)
+    if st != BM_OK:
+        return st, rows, cols
+    st = library().bm_syrk_bf16_tile_order(uplo, n, k, plan.tiles, rows.ctypes.data, cols.ctypes.data)
+    return st, rows, cols
 
 
 TILE_AUTO, TILE_SINGLE_128x256, TILE_SINGLE_128x128, TILE_PAIR_256x256 = range(4)

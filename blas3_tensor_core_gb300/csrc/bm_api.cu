@@ -39,6 +39,7 @@ struct DeviceState {
     bool ready = false;
     int sm_count = 0;
     int cc_major = 0, cc_minor = 0;
+    int device = -1;
     int *status = nullptr;  // one int, allocated on first use
     bool attrs_set = false;
     int max_pair_clusters = 0;  // co-resident clusters of the pair kernel
@@ -119,8 +120,11 @@ bm_status init_kernel_attrs(DeviceState &st)
     return BM_OK;
 }
 
-// Current device, checked for compute capability 10.3; status word allocated.
-bm_status device_state(DeviceState **out)
+// Current device, checked for compute capability 10.3, with the one-time set-up
+// of its state (tensor-map encoder, kernel attributes). With `alloc_status` the
+// device status word is allocated on first use; without it (the allocation-free
+// entry point) nothing is allocated and the word is used only if it exists.
+bm_status device_state(DeviceState **out, bool alloc_status = true)
 {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
@@ -135,6 +139,7 @@ bm_status device_state(DeviceState **out)
         st.sm_count = prop.multiProcessorCount;
         st.cc_major = prop.major;
         st.cc_minor = prop.minor;
+        st.device = dev;
         st.ready = true;
     }
     if (st.cc_major != 10 || st.cc_minor != 3) return BM_ERR_ARCH;
@@ -147,7 +152,7 @@ bm_status device_state(DeviceState **out)
             return BM_ERR_CUDA;
         g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
-    if (st.status == nullptr) {
+    if (alloc_status && st.status == nullptr) {
         if (cudaMalloc(&st.status, sizeof(int)) != cudaSuccess) return BM_ERR_CUDA;
         if (cudaMemset(st.status, 0, sizeof(int)) != cudaSuccess) return BM_ERR_CUDA;
     }
@@ -288,7 +293,6 @@ struct Plan {
     int64_t full_tiles = 0, num_units = 0;  // whole tiles first; the rest are split k_splits ways
     int k_splits = 1, kb_per_split = 0, kb_total = 0;
     int ctas = 0;
-    int64_t syrk_cross = 0;  // SYRK: tiles crossing the diagonal
     int fixup = 0;           // split tiles reduced inside the kernel (no reduce kernel)
     size_t slot_bytes = 0;   // partial slots at the start of the workspace; fixup counters follow
     size_t ws_bytes = 0;
@@ -309,31 +313,20 @@ void set_variant(Plan &pl, int v)
     pl.tile_m = bm::CTA_M * pl.pair;
 }
 
-// Tiles of the triangle that cross the diagonal.
-int64_t syrk_cross_count(int mode, int64_t tiles_m, int64_t tiles_n, int tile_m, int bn)
-{
-    int64_t total = 0;
-    for (int64_t tm = 0; tm < tiles_m; ++tm) {
-        int64_t lo, hi, clo, chi;
-        if (tile_m == 256) bm::syrk_row_crossing<256, 256>(mode, tm, tiles_n, lo, hi, clo, chi);
-        else if (bn == 128) bm::syrk_row_crossing<128, 128>(mode, tm, tiles_n, lo, hi, clo, chi);
-        else bm::syrk_row_crossing<128, 256>(mode, tm, tiles_n, lo, hi, clo, chi);
-        if (chi >= clo) total += chi - clo + 1;
-    }
-    return total;
-}
-
+// Tiles of the SYRK schedule: one across the diagonal per tile row, then the
+// tiles inside the triangle (closed forms shared with the kernel).
 int64_t syrk_tile_count(int mode, int64_t tiles_m, int64_t tiles_n, int tile_m, int bn)
 {
-    int64_t total = 0;
-    for (int64_t tm = 0; tm < tiles_m; ++tm) {
-        int64_t lo, hi;
-        if (tile_m == 256) bm::syrk_row_tiles<256, 256>(mode, tm, tiles_n, lo, hi);
-        else if (bn == 128) bm::syrk_row_tiles<128, 128>(mode, tm, tiles_n, lo, hi);
-        else bm::syrk_row_tiles<128, 256>(mode, tm, tiles_n, lo, hi);
-        total += hi - lo + 1;
-    }
-    return total;
+    if (tile_m == 256) return tiles_m + bm::syrk_inside_before<256, 256>(mode, tiles_m, tiles_n);
+    if (bn == 128) return tiles_m + bm::syrk_inside_before<128, 128>(mode, tiles_m, tiles_n);
+    return tiles_m + bm::syrk_inside_before<128, 256>(mode, tiles_m, tiles_n);
+}
+
+void syrk_coords(int mode, int64_t tiles_m, int64_t tiles_n, int tile_m, int bn, int64_t t, int64_t &tm, int64_t &tn)
+{
+    if (tile_m == 256) bm::syrk_tile_coords<256, 256>(mode, tiles_m, tiles_n, t, tm, tn);
+    else if (bn == 128) bm::syrk_tile_coords<128, 128>(mode, tiles_m, tiles_n, t, tm, tn);
+    else bm::syrk_tile_coords<128, 256>(mode, tiles_m, tiles_n, t, tm, tn);
 }
 
 // Persistent grid: one CTA (or CTA pair) per SM (pair of SMs), never more than the work units.
@@ -438,7 +431,6 @@ Plan plan_syrk(int mode, int64_t n, int64_t k, int sms, int pair_clusters, bool 
     pl.tiles_m = ceil_div(n, pl.tile_m);
     pl.tiles_n = ceil_div(n, pl.bn);
     pl.num_tiles = syrk_tile_count(mode, pl.tiles_m, pl.tiles_n, pl.tile_m, pl.bn);
-    pl.syrk_cross = syrk_cross_count(mode, pl.tiles_m, pl.tiles_n, pl.tile_m, pl.bn);
     pl.full_tiles = pl.num_tiles;
     pl.kb_total = static_cast<int>(ceil_div(std::max<int64_t>(k, 1), bm::TILE_K)) * (two_products ? 2 : 1);
     pl.kb_per_split = pl.kb_total;
@@ -463,7 +455,7 @@ cudaError_t launch_main(const cudaLaunchConfig_t &cfg, int variant, const CUtens
 }
 
 bm_status launch(const Plan &pl, const CUtensorMap &ta, const CUtensorMap &tb, bm::GemmParams &prm,
-                 cudaStream_t stream, int elem = bm::ELEM_BF16)
+                 cudaStream_t stream, int sms, int elem = bm::ELEM_BF16)
 {
     // The epilogue moves C with TMA copies through a swizzled map (GEMM tiles, and
     // SYRK tiles inside the triangle). C is not prefetched into L2 ahead of the
@@ -523,7 +515,8 @@ bm_status launch(const Plan &pl, const CUtensorMap &ta, const CUtensorMap &tb, b
     }
     if (prm.k_splits > 1 && !prm.fixup) {
         const int64_t work = (prm.num_tiles - prm.full_tiles) * pl.tile_m * (pl.bn / 4);
-        const int blocks = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(ceil_div(work, 256), 8 * 152)));
+        const int blocks =
+            static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(ceil_div(work, 256), 8 * static_cast<int64_t>(sms))));
         cudaLaunchConfig_t rc = {};
         cudaLaunchAttribute ra[1];
         ra[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -548,10 +541,12 @@ bm_status launch(const Plan &pl, const CUtensorMap &ta, const CUtensorMap &tb, b
     return BM_OK;
 }
 
-bm_status launch_scale(bm::GemmParams &prm, cudaStream_t stream)
+// C = beta * C (alpha == 0 or k == 0): a grid-stride kernel of at most 8 blocks per SM.
+bm_status launch_scale(bm::GemmParams &prm, cudaStream_t stream, int sms)
 {
     const int64_t work = prm.m * ceil_div(prm.n, 4);
-    const int blocks = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(ceil_div(work, 256), 8 * 152)));
+    const int blocks =
+        static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(ceil_div(work, 256), 8 * static_cast<int64_t>(sms))));
     cudaLaunchConfig_t rc = {};
     cudaLaunchAttribute ra[1];
     ra[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -578,7 +573,6 @@ void fill_params(bm::GemmParams &prm, const Plan &pl)
     prm.k_splits = pl.k_splits;
     prm.kb_per_split = pl.kb_per_split;
     prm.kb_total = pl.kb_total;
-    prm.syrk_cross = pl.syrk_cross;
 }
 
 void export_plan(const Plan &pl, bm_plan *plan)
@@ -654,52 +648,26 @@ static __device__ __align__(256) float g_noalloc_scratch[BM_NOALLOC_SCRATCH_BYTE
 
 float *g_noalloc_scratch_addr[kMaxDevices] = {};
 
-// Set-up for the allocation-free entry point on the current device: the same
-// device checks and one-time attributes as the other entry points, but no
-// cudaMalloc (the status word is used only if another entry point already
-// created it), and the device address of the scratch array (looked up once per
-// device, with that device current).
+// Set-up for the allocation-free entry point on the current device: the device
+// checks and one-time attributes of the other entry points without any
+// allocation, plus the device address of the scratch array, looked up once per
+// device with that device current.
 bm_status noalloc_device_setup(DeviceState **out, float **scratch)
 {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
-        cudaGetLastError();
-        return BM_ERR_CUDA;
-    }
+    DeviceState *st = nullptr;
+    const bm_status s = device_state(&st, false);
+    if (s != BM_OK) return s;
     std::lock_guard<std::mutex> lock(g_mutex);
-    DeviceState &st = g_devices[dev];
-    if (!st.ready) {
-        cudaDeviceProp prop;
-        if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return BM_ERR_CUDA;
-        st.sm_count = prop.multiProcessorCount;
-        st.cc_major = prop.major;
-        st.cc_minor = prop.minor;
-        st.ready = true;
-    }
-    if (st.cc_major != 10 || st.cc_minor != 3) return BM_ERR_ARCH;
-    if (g_encode == nullptr) {
-        void *fn = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess || fn == nullptr)
-            return BM_ERR_CUDA;
-        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    }
-    if (!st.attrs_set) {
-        const bm_status a = init_kernel_attrs(st);
-        if (a != BM_OK) return a;
-    }
-    if (g_noalloc_scratch_addr[dev] == nullptr) {
+    if (g_noalloc_scratch_addr[st->device] == nullptr) {
         void *addr = nullptr;
         if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || addr == nullptr) {
             cudaGetLastError();
             return BM_ERR_CUDA;
         }
-        g_noalloc_scratch_addr[dev] = static_cast<float *>(addr);
+        g_noalloc_scratch_addr[st->device] = static_cast<float *>(addr);
     }
-    *scratch = g_noalloc_scratch_addr[dev];
-    *out = &st;
+    *scratch = g_noalloc_scratch_addr[st->device];
+    *out = st;
     return BM_OK;
 }
 
@@ -728,7 +696,7 @@ bm_status bm_gemm_bf16(int64_t m, int64_t n, int64_t k, bm_op transA, bm_op tran
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     bm::GemmParams prm = base_params(m, n, k, alpha, beta, C, ldc, c_type, st);
     prm.mode = bm::MODE_GEMM;
-    if (!products) return launch_scale(prm, cs);
+    if (!products) return launch_scale(prm, cs, st->sm_count);
 
     const Plan pl = plan_gemm(m, n, k, workspace != nullptr ? workspace_bytes : 0, st->sm_count,
                               st->max_pair_clusters, bm::ELEM_BF16, beta != 0.0f);
@@ -744,7 +712,7 @@ bm_status bm_gemm_bf16(int64_t m, int64_t n, int64_t k, bm_op transA, bm_op tran
     prm.b_box3 = encode_stage_box(&tb, B, bm::ELEM_BF16, b_mn, n, k, ldb, pl.bn / pl.pair, kps);
     fill_params(prm, pl);
     prm.partial = pl.k_splits > 1 ? static_cast<float *>(workspace) : nullptr;
-    return launch(pl, ta, tb, prm, cs);
+    return launch(pl, ta, tb, prm, cs, st->sm_count);
 }
 
 size_t bm_gemm_bf16_workspace_size(int64_t m, int64_t n, int64_t k)
@@ -775,12 +743,13 @@ bm_status bm_gemm_bf16_noalloc(int64_t m, int64_t n, int64_t k, bm_op transA, bm
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     bm::GemmParams prm = base_params(m, n, k, alpha, beta, C, ldc, c_type, st);
     prm.mode = bm::MODE_GEMM;
-    if (!products) return launch_scale(prm, cs);
+    if (!products) return launch_scale(prm, cs, st->sm_count);
 
-    // The plan bm_gemm_bf16 makes with the workspace it asks for; its partials
-    // must fit the static scratch array.
-    const Plan pl = plan_gemm(m, n, k, SIZE_MAX, st->sm_count, st->max_pair_clusters, bm::ELEM_BF16, beta != 0.0f);
-    if (pl.k_splits > 1 && pl.ws_bytes > BM_NOALLOC_SCRATCH_BYTES) return BM_ERR_WORKSPACE;
+    // The plan bm_gemm_bf16 makes with a workspace the size of the static array:
+    // the planner lowers the split count until the partials fit.
+    const Plan pl = plan_gemm(m, n, k, BM_NOALLOC_SCRATCH_BYTES, st->sm_count, st->max_pair_clusters,
+                              bm::ELEM_BF16, beta != 0.0f);
+    if (pl.k_splits > 1 && pl.ws_bytes > BM_NOALLOC_SCRATCH_BYTES) return BM_ERR_WORKSPACE;  // defensive
     CUtensorMap ta, tb;
     const bool a_mn = transA == BM_OP_T, b_mn = transB == BM_OP_N;
     if (!encode_operand(&ta, A, a_mn, m, k, lda, bm::CTA_M)) return BM_ERR_CUDA;
@@ -792,7 +761,7 @@ bm_status bm_gemm_bf16_noalloc(int64_t m, int64_t n, int64_t k, bm_op transA, bm
     prm.b_box3 = encode_stage_box(&tb, B, bm::ELEM_BF16, b_mn, n, k, ldb, pl.bn / pl.pair, kps);
     fill_params(prm, pl);
     prm.partial = pl.k_splits > 1 ? scratch : nullptr;
-    return launch(pl, ta, tb, prm, cs);
+    return launch(pl, ta, tb, prm, cs, st->sm_count);
 }
 
 bm_status bm_syrk_bf16(bm_uplo uplo, bm_op trans, int64_t n, int64_t k, float alpha, const void *A, int64_t lda,
@@ -816,7 +785,7 @@ bm_status bm_syrk_bf16(bm_uplo uplo, bm_op trans, int64_t n, int64_t k, float al
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     bm::GemmParams prm = base_params(n, n, k, alpha, beta, C, ldc, c_type, st);
     prm.mode = uplo == BM_LOWER ? bm::MODE_SYRK_LOWER : bm::MODE_SYRK_UPPER;
-    if (!products) return launch_scale(prm, cs);
+    if (!products) return launch_scale(prm, cs, st->sm_count);
 
     const Plan pl = plan_syrk(prm.mode, n, k, st->sm_count, st->max_pair_clusters);
     CUtensorMap ta, tb;
@@ -829,7 +798,7 @@ bm_status bm_syrk_bf16(bm_uplo uplo, bm_op trans, int64_t n, int64_t k, float al
     prm.a_box3 = encode_stage_box(&ta, A, bm::ELEM_BF16, mn, n, k, lda, bm::CTA_M, kps);
     prm.b_box3 = encode_stage_box(&tb, A, bm::ELEM_BF16, mn, n, k, lda, pl.bn / pl.pair, kps);
     fill_params(prm, pl);
-    return launch(pl, ta, tb, prm, cs);
+    return launch(pl, ta, tb, prm, cs, st->sm_count);
 }
 
 bm_status bm_syr2k_bf16(bm_uplo uplo, bm_op trans, int64_t n, int64_t k, float alpha, const void *A, int64_t lda,
@@ -856,7 +825,7 @@ bm_status bm_syr2k_bf16(bm_uplo uplo, bm_op trans, int64_t n, int64_t k, float a
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     bm::GemmParams prm = base_params(n, n, k, alpha, beta, C, ldc, c_type, st);
     prm.mode = uplo == BM_LOWER ? bm::MODE_SYRK_LOWER : bm::MODE_SYRK_UPPER;
-    if (!products) return launch_scale(prm, cs);
+    if (!products) return launch_scale(prm, cs, st->sm_count);
 
     const Plan pl = plan_syrk(prm.mode, n, k, st->sm_count, st->max_pair_clusters, true);
     CUtensorMap ta, tb;
@@ -881,7 +850,7 @@ bm_status bm_syr2k_bf16(bm_uplo uplo, bm_op trans, int64_t n, int64_t k, float a
             prm.b_box3 = 1;
         }
     }
-    return launch(pl, ta, tb, prm, cs);
+    return launch(pl, ta, tb, prm, cs, st->sm_count);
 }
 
 bm_status bm_gemm_e4m3(int64_t m, int64_t n, int64_t k, float alpha, const void *A, int64_t lda, const void *B,
@@ -905,7 +874,7 @@ bm_status bm_gemm_e4m3(int64_t m, int64_t n, int64_t k, float alpha, const void 
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     bm::GemmParams prm = base_params(m, n, k, alpha, beta, C, ldc, c_type, st);
     prm.mode = bm::MODE_GEMM;
-    if (!products) return launch_scale(prm, cs);
+    if (!products) return launch_scale(prm, cs, st->sm_count);
 
     const Plan pl = plan_gemm(m, n, k, workspace != nullptr ? workspace_bytes : 0, st->sm_count,
                               st->max_pair_clusters, bm::ELEM_E4M3);
@@ -921,7 +890,7 @@ bm_status bm_gemm_e4m3(int64_t m, int64_t n, int64_t k, float alpha, const void 
     prm.b_box3 = encode_stage_box(&tb, B, bm::ELEM_E4M3, false, n, k, ldb, pl.bn / pl.pair, kps);
     fill_params(prm, pl);
     prm.partial = pl.k_splits > 1 ? static_cast<float *>(workspace) : nullptr;
-    return launch(pl, ta, tb, prm, cs, bm::ELEM_E4M3);
+    return launch(pl, ta, tb, prm, cs, st->sm_count, bm::ELEM_E4M3);
 }
 
 size_t bm_gemm_e4m3_workspace_size(int64_t m, int64_t n, int64_t k)
@@ -961,6 +930,21 @@ bm_status bm_syrk_bf16_plan(bm_uplo uplo, int64_t n, int64_t k, bm_plan *plan)
     export_plan(plan_syrk(uplo == BM_LOWER ? bm::MODE_SYRK_LOWER : bm::MODE_SYRK_UPPER, n, k, sms,
                           pair_clusters_or_default(sms)),
                 plan);
+    return BM_OK;
+}
+
+bm_status bm_syrk_bf16_tile_order(bm_uplo uplo, int64_t n, int64_t k, int64_t count, int64_t *tile_row,
+                                   int64_t *tile_col)
+{
+    if (uplo != BM_LOWER && uplo != BM_UPPER) return BM_ERR_INVALID_VALUE;
+    if (n < 0 || k < 0 || count < 0 || !fits_int32(n) || !fits_int32(k)) return BM_ERR_INVALID_VALUE;
+    if (count > 0 && (tile_row == nullptr || tile_col == nullptr)) return BM_ERR_INVALID_VALUE;
+    if (n == 0 || k == 0) return count == 0 ? BM_OK : BM_ERR_INVALID_VALUE;
+    const int sms = sm_count_or_default();
+    const int mode = uplo == BM_LOWER ? bm::MODE_SYRK_LOWER : bm::MODE_SYRK_UPPER;
+    const Plan pl = plan_syrk(mode, n, k, sms, pair_clusters_or_default(sms));
+    if (count != pl.num_tiles) return BM_ERR_INVALID_VALUE;
+    for (int64_t t = 0; t < count; ++t) syrk_coords(mode, pl.tiles_m, pl.tiles_n, pl.tile_m, pl.bn, t, tile_row[t], tile_col[t]);
     return BM_OK;
 }
 

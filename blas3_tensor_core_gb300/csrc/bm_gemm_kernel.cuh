@@ -103,7 +103,6 @@ struct GemmParams {
                        // load-combine-store when beta != 0)
     int syr2k_kb;      // SYR2K: k-blocks of one product; later k-blocks swap the roles of tmA and tmB
     int store_p_tma;   // split units: tmP maps the partial slots for TMA stores (fp32, box 32 x 32, 128B swizzle)
-    int64_t syrk_cross; // SYRK: number of tiles crossing the diagonal (visited first)
     int a_box3;        // tmA is a stage box: one 3-D copy brings a CTA's A tile for a whole stage
     int b_box3;        // same for tmB
     // In-kernel split-K reduction: split units run first; per epilogue warp region
@@ -158,21 +157,6 @@ struct Unit {
     int64_t slot;     // partial-sum slot (split units only), -1 for a whole tile
 };
 
-// Range of tile columns [lo, hi] of tile row tm (tiles TM x BN) that touch the
-// SYRK triangle.
-template <int TM, int BN>
-__host__ __device__ inline void syrk_row_tiles(int mode, int64_t tm, int64_t tiles_n, int64_t &lo, int64_t &hi)
-{
-    if (mode == MODE_SYRK_LOWER) {  // some row >= some column
-        lo = 0;
-        const int64_t last = (TM * tm + TM - 1) / BN;
-        hi = last < tiles_n - 1 ? last : tiles_n - 1;
-    } else {  // some row <= some column
-        lo = (TM * tm) / BN;
-        hi = tiles_n - 1;
-    }
-}
-
 // Does tile (tm, tn) (TM x BN) lie entirely in the referenced SYRK triangle?
 template <int TM, int BN>
 __host__ __device__ inline bool tile_inside_triangle(int mode, int64_t tm, int64_t tn)
@@ -182,29 +166,61 @@ __host__ __device__ inline bool tile_inside_triangle(int mode, int64_t tm, int64
     return true;
 }
 
-// Tiles [lo, hi] of tile row tm touch the triangle; of those, [cross_lo, cross_hi]
-// (possibly empty: cross_lo > cross_hi) cross the diagonal and the rest lie
-// inside it (tile_inside_triangle).
+// SYRK tile order in closed form. The tile shapes used (TM = BN, or BN = 2 TM)
+// give every tile row tm exactly one tile across the diagonal, in tile column
+// tm / Q with Q = BN / TM; the tiles strictly inside the triangle are, per row,
+// the columns left of it (lower) or right of it (upper). syrk_inside_before(R)
+// counts the inside tiles of rows [0, R).
 template <int TM, int BN>
-__host__ __device__ inline void syrk_row_crossing(int mode, int64_t tm, int64_t tiles_n, int64_t &lo, int64_t &hi,
-                                                  int64_t &cross_lo, int64_t &cross_hi)
+__host__ __device__ inline int64_t syrk_inside_before(int mode, int64_t R, int64_t tiles_n)
 {
-    syrk_row_tiles<TM, BN>(mode, tm, tiles_n, lo, hi);
-    if (mode == MODE_SYRK_LOWER) {
-        // inside: (tn + 1) * BN - 1 <= tm * TM
-        const int64_t in_hi = (tm * TM + 1) / BN - 1;
-        cross_lo = in_hi + 1 > lo ? in_hi + 1 : lo;
-        cross_hi = hi;
-    } else {
-        // inside: (tm + 1) * TM - 1 <= tn * BN
-        const int64_t in_lo = ((tm + 1) * TM - 1 + BN - 1) / BN;
-        cross_lo = lo;
-        cross_hi = in_lo - 1 < hi ? in_lo - 1 : hi;
-    }
+    constexpr int Q = BN / TM;
+    static_assert(Q == 1 || Q == 2, "tile shapes with one diagonal tile per row");
+    // sum over r < R of floor(r / Q)
+    const int64_t h = R >> 1;
+    const int64_t diag = Q == 1 ? R * (R - 1) / 2 : h * (h - 1) + (R & 1) * h;
+    return mode == MODE_SYRK_LOWER ? diag : R * (tiles_n - 1) - diag;
 }
 
-// Tile t -> (tile row, tile column): grouped raster for GEMM, row by row over
-// the triangle for SYRK.
+// Tile t of the SYRK schedule -> (tile row, tile column). The tiles_m tiles
+// across the diagonal come first (their epilogue masks each
+// element and is slower, so it should overlap later tiles' mainloops rather
+// than end the kernel), one per row; then the tiles inside the triangle, row by
+// row. The row of an inside tile inverts the quadratic count above: a square-
+// root estimate, then an exact integer correction of a step or two.
+template <int TM, int BN>
+__host__ __device__ inline void syrk_tile_coords(int mode, int64_t tiles_m, int64_t tiles_n, int64_t t, int64_t &tm,
+                                                 int64_t &tn)
+{
+    constexpr int Q = BN / TM;
+    if (t < tiles_m) {
+        tm = t;
+        tn = t / Q;
+        return;
+    }
+    const int64_t v = t - tiles_m;
+    double est;
+    if (mode == MODE_SYRK_LOWER) {
+        // lower: about R^2 / (2 Q) inside tiles before row R
+        est = Q == 1 ? 0.5 * (1.0 + sqrt(1.0 + 8.0 * static_cast<double>(v)))
+                     : 1.0 + 2.0 * sqrt(static_cast<double>(v));
+    } else {
+        // upper: about R (T - 1/2) - R^2 / (2 Q) before row R, T = tiles_n
+        const double b = static_cast<double>(tiles_n) - 0.5;
+        const double disc = b * b - 2.0 * static_cast<double>(v) / Q;
+        est = Q * (b - sqrt(disc > 0.0 ? disc : 0.0));
+    }
+    int64_t r = static_cast<int64_t>(est);
+    r = r < 0 ? 0 : (r > tiles_m - 1 ? tiles_m - 1 : r);
+    while (r + 1 < tiles_m && syrk_inside_before<TM, BN>(mode, r + 1, tiles_n) <= v) ++r;
+    while (r > 0 && syrk_inside_before<TM, BN>(mode, r, tiles_n) > v) --r;
+    tm = r;
+    const int64_t local = v - syrk_inside_before<TM, BN>(mode, r, tiles_n);
+    tn = mode == MODE_SYRK_LOWER ? local : r / Q + 1 + local;
+}
+
+// Tile t -> (tile row, tile column): grouped raster for GEMM, the closed-form
+// triangle order above for SYRK.
 template <int TM, int BN>
 __device__ __forceinline__ void tile_coords(const GemmParams &p, int64_t t, int64_t &tm, int64_t &tn)
 {
@@ -219,26 +235,7 @@ __device__ __forceinline__ void tile_coords(const GemmParams &p, int64_t t, int6
         tm = first + local % rows;
         tn = local / rows;
     } else {
-        // SYRK: first the syrk_cross tiles that cross the diagonal (their epilogue masks
-        // each element and is slower, so it should overlap later tiles' mainloops
-        // rather than end the kernel), then the tiles inside the triangle; each part
-        // row by row.
-        const bool cross = t < p.syrk_cross;
-        int64_t rem = cross ? t : t - p.syrk_cross;
-        for (int64_t r = 0; r < p.tiles_m; ++r) {
-            int64_t lo, hi, clo, chi;
-            syrk_row_crossing<TM, BN>(p.mode, r, p.tiles_n, lo, hi, clo, chi);
-            const int64_t ncross = chi >= clo ? chi - clo + 1 : 0;
-            const int64_t cnt = cross ? ncross : (hi - lo + 1) - ncross;
-            if (rem < cnt) {
-                tm = r;
-                if (cross) tn = clo + rem;
-                else if (p.mode == MODE_SYRK_LOWER) tn = lo + rem;  // inside tiles precede the crossing ones
-                else tn = (ncross > 0 ? chi + 1 : lo) + rem;        // inside tiles follow the crossing ones
-                break;
-            }
-            rem -= cnt;
-        }
+        syrk_tile_coords<TM, BN>(p.mode, p.tiles_m, p.tiles_n, t, tm, tn);
     }
 }
 

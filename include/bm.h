@@ -125,12 +125,16 @@ BM_API size_t bm_gemm_bf16_workspace_size(int64_t m, int64_t n, int64_t k);
  *
  * Same operation, arguments, layout rules and errors as bm_gemm_bf16, except
  * that there is no workspace argument. When the launch plan splits K (small
- * m * n, long k), the partial sums go to one file-scope device array of
- * BM_NOALLOC_SCRATCH_BYTES that the library holds on every GPU it is loaded
- * on, until the process exits. The plan is the one bm_gemm_bf16 uses with a
- * workspace of bm_gemm_bf16_workspace_size(m, n, k) bytes; if that is more than
- * BM_NOALLOC_SCRATCH_BYTES the call returns BM_ERR_WORKSPACE and launches
- * nothing. The caller still owns and passes A, B and C.
+ * m * n, long k, or the tiles of a partly filled last wave), the partial sums
+ * go to one file-scope device array of BM_NOALLOC_SCRATCH_BYTES that the
+ * library holds on every GPU it is loaded on, until the process exits. The
+ * plan is the one bm_gemm_bf16 makes when given a workspace of
+ * BM_NOALLOC_SCRATCH_BYTES bytes: where a full split would need more, the
+ * planner splits fewer ways so that the partials fit. Like that plan it
+ * depends on beta (a tail split with beta != 0 must save more time, so such a
+ * call may split fewer tiles). BM_ERR_WORKSPACE is returned, with nothing
+ * launched, only if a plan ever exceeded the array, which the planner does
+ * not produce. The caller still owns and passes A, B and C.
  *
  *   - The first call on a device looks up the device address of the array
  *     (cudaGetSymbolAddress) with that device current; make that first call
@@ -268,6 +272,17 @@ typedef struct {
 
 BM_API bm_status bm_gemm_bf16_plan(int64_t m, int64_t n, int64_t k, size_t workspace_bytes, bm_plan *plan);
 BM_API bm_status bm_syrk_bf16_plan(bm_uplo uplo, int64_t n, int64_t k, bm_plan *plan);
+
+/*
+ * Visit order of the output tiles of a SYRK plan (the one bm_syrk_bf16_plan
+ * reports for the same arguments), for reports and tests: tile t of the
+ * persistent schedule covers rows tile_row[t] * tile_m ... and columns
+ * tile_col[t] * tile_n ... of C. The tiles across the diagonal come first, one
+ * per tile row, then the tiles inside the triangle, row by row. `count` must be
+ * the plan's `tiles`; the two arrays are host memory of `count` elements.
+ */
+BM_API bm_status bm_syrk_bf16_tile_order(bm_uplo uplo, int64_t n, int64_t k, int64_t count, int64_t *tile_row,
+                                         int64_t *tile_col);
 
 /* Library version: major * 10000 + minor * 100 + patch. */
 BM_API int bm_version(void);

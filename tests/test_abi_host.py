@@ -250,3 +250,55 @@ def test_tile_override_values(lib):
             assert s.tiles == _syrk_tiles_bruteforce(1000, True, s.tile_m, s.tile_n)
     finally:
         assert bm.bm_set_tile_override(0) == bm.BM_OK
+
+
+def _syrk_order_bruteforce(n, lower, tm_, tn_):
+    """The schedule written out by enumeration: per tile row the tile that crosses the
+    diagonal, then per row the tiles wholly inside the triangle (nominal tile extents)."""
+    rows_t, cols_t = (n + tm_ - 1) // tm_, (n + tn_ - 1) // tn_
+    cross, inside = [], []
+    for r in range(rows_t):
+        for c in range(cols_t):
+            r_lo, r_hi, c_lo, c_hi = r * tm_, r * tm_ + tm_ - 1, c * tn_, c * tn_ + tn_ - 1
+            touches = r_hi >= c_lo if lower else r_lo <= c_hi
+            wholly = r_lo >= c_hi if lower else r_hi <= c_lo
+            if touches and wholly:
+                inside.append((r, c))
+            elif touches:
+                cross.append((r, c))
+    return cross + inside
+
+
+@pytest.mark.parametrize("n", [1, 200, 256, 300, 1000, 1024, 4096, 8192, 12288 + 100, 16384])
+@pytest.mark.parametrize("variant", [1, 2, 3], ids=["single128x256", "single128x128", "pair256x256"])
+def test_syrk_tile_order_closed_form(lib, n, variant):
+    """Every tile index of the kernel's closed-form SYRK schedule maps to the tile the
+    enumeration puts there: the diagonal-crossing tiles first, then the inside ones."""
+    import numpy as np
+    assert bm.bm_set_tile_override(variant) == bm.BM_OK
+    try:
+        for uplo in (bm.BM_LOWER, bm.BM_UPPER):
+            st, p = bm.bm_syrk_bf16_plan(uplo, n, 64)
+            assert st == 0
+            want = _syrk_order_bruteforce(n, uplo == bm.BM_LOWER, p.tile_m, p.tile_n)
+            st, rows, cols = bm.bm_syrk_bf16_tile_order(uplo, n, 64)
+            assert st == 0 and p.tiles == len(want)
+            got = list(zip(rows.tolist(), cols.tolist()))
+            assert got == want
+            # one tile across the diagonal per tile row, in row order
+            tiles_m = (n + p.tile_m - 1) // p.tile_m
+            assert [r for r, _ in want[:tiles_m]] == list(range(tiles_m))
+    finally:
+        bm.bm_set_tile_override(0)
+
+
+def test_syrk_tile_order_argument_errors(lib):
+    import ctypes
+    import numpy as np
+    st, p = bm.bm_syrk_bf16_plan(bm.BM_LOWER, 1000, 64)
+    buf = np.zeros(p.tiles + 1, np.int64)
+    f = bm.library().bm_syrk_bf16_tile_order
+    assert f(bm.BM_LOWER, 1000, 64, p.tiles + 1, buf.ctypes.data, buf.ctypes.data) == bm.BM_ERR_INVALID_VALUE
+    assert f(bm.BM_LOWER, 1000, 64, p.tiles, None, None) == bm.BM_ERR_INVALID_VALUE
+    assert f(7, 1000, 64, p.tiles, buf.ctypes.data, buf.ctypes.data) == bm.BM_ERR_INVALID_VALUE
+    assert f(bm.BM_LOWER, 0, 64, 0, None, None) == bm.BM_OK

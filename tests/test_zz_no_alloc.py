@@ -5,13 +5,21 @@ through its own pool, a plug-in called back by another library without an
 allocator, or a latency-critical path that cannot afford cudaMalloc's implicit
 synchronisation. For them the library keeps its split-K scratch in a static
 device array. These tests call that entry point through the C ABI and compare
-it with bm_gemm_bf16 given a caller-owned workspace, on two calls in a row
-(the array keeps the previous call's contents), and check that a shape whose
-partial sums do not fit the array is refused without touching C.
+it with bm_gemm_bf16 given a caller-owned workspace, and with the CPU oracle,
+on two calls in a row (the array keeps the previous call's contents). A shape
+whose full split would not fit the array is split fewer ways, exactly as
+bm_gemm_bf16 splits it with a workspace of the array's size. A call that is the
+first use of the library in a process, so that no device status word exists
+yet, still returns cleanly from a device-side wait that runs out.
 
 The file name sorts last so that a run that stops at the first failure has
 already run every other test. It depends on no state left by other tests.
 """
+
+import os
+import subprocess
+import sys
+import textwrap
 
 import numpy as np
 import pytest
@@ -64,6 +72,15 @@ def _noalloc(m, n, k, dA, dB, lda, ldb, alpha, beta, c_init, bf16):
     return got
 
 
+def _oracle_check(got, m, n, k, A, B, alpha, beta, c_init, bf16, what):
+    ref, bound = oracle.default().gemm(m, n, k, 0, 0, alpha, A, B, beta, c_init if beta != 0 else None)
+    c_in = None
+    if beta != 0:
+        c_in = gen.bf16_bits_to_f32(c_init).astype(np.float64) if bf16 else np.asarray(c_init, np.float64)
+    ok, worst, where = oracle.compare(got, ref, bound, alpha, beta, c_in, bf16)
+    assert ok, (what, worst, where)
+
+
 def test_split_k_without_allocation_matches_workspace_path_twice():
     import blas3_tensor_core_gb300 as bm
     m, n, k = 512, 520, 2048
@@ -78,6 +95,7 @@ def test_split_k_without_allocation_matches_workspace_path_twice():
         got = _noalloc(m, n, k, dA, dB, k, n, 1.0, 0.0, None, True)
         ok, worst, where = oracle.compare(got, want, _bound(A, B), 1.0, 0.0, None, True)
         assert ok, (seed, worst, where)
+        _oracle_check(got, m, n, k, A, B, 1.0, 0.0, None, True, f"seed {seed}")
 
 
 def test_tail_split_summed_in_kernel_without_allocation_three_times():
@@ -112,20 +130,92 @@ def test_without_split_and_with_beta():
         got = _noalloc(m, n, k, dA, dB, k, n, -0.5, 1.5, c0, False)
         ok, worst, _ = oracle.compare(got, want, _bound(A, B), -0.5, 1.5, c0.astype(np.float64), False)
         assert ok, worst
+        _oracle_check(got, m, n, k, A, B, -0.5, 1.5, c0, False, "beta 1.5")
 
 
-def test_plan_beyond_the_scratch_array_is_refused():
+def test_full_split_beyond_the_array_splits_fewer_ways():
+    """512 x 512 x 8192: a 19-way split of the 8 tiles would need 19.9 MB of partials; within
+    the 16 MiB array the planner splits 16 ways, as bm_gemm_bf16 does with a 16 MiB workspace.
+    Both entry points then run the same plan, so they agree bit for bit, twice in a row."""
     import blas3_tensor_core_gb300 as bm
     t = torch()
     m, n, k = 512, 512, 8192
     assert bm.bm_gemm_bf16_workspace_size(m, n, k) > bm.BM_NOALLOC_SCRATCH_BYTES
-    A = operand(m, k, "normal", 41)
-    B = operand(k, n, "normal", 42)
+    plan = bm.bm_gemm_bf16_plan(m, n, k, bm.BM_NOALLOC_SCRATCH_BYTES)[1]
+    assert plan.k_splits > 1 and plan.workspace_bytes <= bm.BM_NOALLOC_SCRATCH_BYTES
+    ws = t.empty(bm.BM_NOALLOC_SCRATCH_BYTES // 4, dtype=t.float32, device="cuda")
+    for seed in (41, 51):
+        A = operand(m, k, "normal", seed)
+        B = operand(k, n, "normal", seed + 1)
+        dA, dB = bf16_to_device(A), bf16_to_device(B)
+        cw = CBuffer(m, n, n, True, init=np.zeros((m, n), np.uint16))
+        st = bm.bm_gemm_bf16(m, n, k, 0, 0, 1.0, dA.data_ptr(), k, dB.data_ptr(), n, 0.0, cw.ptr, n,
+                             bm.BM_C_BF16, ws.data_ptr(), bm.BM_NOALLOC_SCRATCH_BYTES,
+                             t.cuda.current_stream().cuda_stream)
+        assert st == bm.BM_OK
+        t.cuda.synchronize()
+        want = cw.result()[0]
+        got = _noalloc(m, n, k, dA, dB, k, n, 1.0, 0.0, None, True)
+        assert np.array_equal(got, want), seed
+        _oracle_check(got, m, n, k, A, B, 1.0, 0.0, None, True, f"seed {seed}")
+
+
+_FRESH_PROCESS = textwrap.dedent("""
+    import sys
+    import numpy as np
+    import torch
+    sys.path.insert(0, {root!r})
+    sys.path.insert(0, {tests!r})
+    import blas3_tensor_core_gb300 as bm
+    import oracle
+    from gpu_helpers import CBuffer, bf16_to_device, operand
+    torch.cuda.set_device(0)
+    h = torch.cuda.current_stream().cuda_stream
+    m, n, k = 512, 512, 256
+    A = operand(m, k, "normal", 1)
+    B = operand(k, n, "normal", 2)
     dA, dB = bf16_to_device(A), bf16_to_device(B)
-    cbuf = CBuffer(m, n, n, True, init=np.zeros((m, n), np.uint16))
-    st = bm.bm_gemm_bf16_noalloc(m, n, k, 0, 0, 1.0, dA.data_ptr(), k, dB.data_ptr(), n, 0.0, cbuf.ptr, n,
-                                 bm.BM_C_BF16, t.cuda.current_stream().cuda_stream)
-    assert st == bm.BM_ERR_WORKSPACE
-    t.cuda.synchronize()
-    _, raw = cbuf.result()
-    assert np.array_equal(raw, cbuf.before)
+    c = CBuffer(m, n, n, False, init=np.zeros((m, n), np.float32))
+    bm.bm_set_wait_timeout_ms(50)
+    bm.bm_debug_inject_stall(1)
+    # the first call of the library in this process: no status word exists on the device
+    st = bm.bm_gemm_bf16_noalloc(m, n, k, 0, 0, 1.0, dA.data_ptr(), k, dB.data_ptr(), n, 0.0, c.ptr, n,
+                                 bm.BM_C_F32, h)
+    assert st == bm.BM_OK, st
+    torch.cuda.synchronize()   # the stalled kernel gave up and exited; nothing faulted
+    bm.bm_debug_inject_stall(0)
+    bm.bm_set_wait_timeout_ms(2000)
+    # the timeout had no status word to go to: the word created now starts clear
+    assert bm.bm_get_last_device_error(h) == bm.BM_OK
+    for entry in ("noalloc", "workspace"):
+        c2 = CBuffer(m, n, n, False, init=np.zeros((m, n), np.float32))
+        if entry == "noalloc":
+            st = bm.bm_gemm_bf16_noalloc(m, n, k, 0, 0, 1.0, dA.data_ptr(), k, dB.data_ptr(), n, 0.0, c2.ptr,
+                                         n, bm.BM_C_F32, h)
+        else:
+            st = bm.bm_gemm_bf16(m, n, k, 0, 0, 1.0, dA.data_ptr(), k, dB.data_ptr(), n, 0.0, c2.ptr, n,
+                                 bm.BM_C_F32, None, 0, h)
+        assert st == bm.BM_OK, st
+        assert bm.bm_get_last_device_error(h) == bm.BM_OK
+        got, raw = c2.result()
+        ref, bound = oracle.default().gemm(m, n, k, 0, 0, 1.0, A, B)
+        ok, worst, _ = oracle.compare(got, ref, bound, 1.0)
+        assert ok, (entry, worst)
+        c2.assert_guard_intact(raw)
+    print("fresh-process noalloc timeout ok")
+""")
+
+
+def test_first_call_without_status_word_survives_a_wait_limit():
+    """A device-side wait that runs out in a call made before any status word exists on
+    the device (the allocation-free entry point never creates one): the kernel gives
+    up after its 50 ms limit, frees its tensor memory and exits; the call's timeout is
+    recorded nowhere, and the context stays usable for both entry points. Run in a
+    fresh process so that no earlier test has created the word. The stall is a copy
+    that is never issued; nothing faults or hangs."""
+    tests = os.path.dirname(os.path.abspath(__file__))
+    root = os.path.dirname(tests)
+    script = _FRESH_PROCESS.format(root=root, tests=tests)
+    res = subprocess.run([sys.executable, "-c", script], capture_output=True, text=True, timeout=600)
+    assert res.returncode == 0, res.stdout[-2000:] + res.stderr[-4000:]
+    assert "fresh-process noalloc timeout ok" in res.stdout
