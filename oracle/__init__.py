@@ -19,8 +19,9 @@ operations of the alpha/beta combine (unit roundoff 2^-24 each), which the
 first term omits when alpha*bound is small next to beta*C.
 
 Parity unpinned: none. Every function here is pinned by the tests in
-``tests/test_oracle_pins.py`` (brute force in exact integer arithmetic,
-closed forms, NumPy float64 matmul, and the invariants A*I = A,
+``tests/test_oracle_pins.py`` (brute force in exact integer and rational
+arithmetic, closed forms, NumPy float64 matmul, every E4M3 code, the OCP MX
+conversion's ties, saturation and special groups, and the invariants A*I = A,
 (A*B)^T = B^T*A^T, SYRK = one triangle of GEMM(A, A^T), SYR2K = one triangle of
 GEMM(A, B^T) + GEMM(B, A^T), SYR2K(A, A) = 2 SYRK(A), beta-accumulation = sum of
 two beta=0 calls).
@@ -94,9 +95,17 @@ class Oracle:
         lib.oracle_gemm_e4m3_entries.argtypes = [_c_i64, _c_dbl, _c_vp, _c_i64, _c_vp, _c_i64, _c_dbl,
                                                  _c_vp, _c_i64, _c_int, _c_i64, _c_vp, _c_vp, _c_vp,
                                                  _c_vp]
+        lib.oracle_gemm_mxfp8.argtypes = [_c_i64, _c_i64, _c_i64, _c_dbl, _c_vp, _c_i64, _c_vp, _c_i64,
+                                          _c_vp, _c_i64, _c_vp, _c_i64, _c_dbl, _c_vp, _c_i64, _c_int,
+                                          _c_vp, _c_vp, _c_i64]
+        lib.oracle_gemm_mxfp8_entries.argtypes = [_c_i64, _c_dbl, _c_vp, _c_i64, _c_vp, _c_i64, _c_vp,
+                                                  _c_i64, _c_vp, _c_i64, _c_dbl, _c_vp, _c_i64, _c_int,
+                                                  _c_i64, _c_vp, _c_vp, _c_vp, _c_vp]
+        lib.oracle_quantize_mxfp8.argtypes = [_c_i64, _c_i64, _c_vp, _c_i64, _c_vp, _c_i64, _c_vp, _c_i64]
         for fn in ("oracle_gemm", "oracle_gemm_entries", "oracle_syrk", "oracle_syrk_entries",
                    "oracle_syr2k", "oracle_syr2k_entries", "oracle_gemm_e4m3",
-                   "oracle_gemm_e4m3_entries"):
+                   "oracle_gemm_e4m3_entries", "oracle_gemm_mxfp8", "oracle_gemm_mxfp8_entries",
+                   "oracle_quantize_mxfp8"):
             getattr(lib, fn).restype = None
         self._lib = lib
 
@@ -226,6 +235,67 @@ class Oracle:
                                            rows.ctypes.data, cols.ctypes.data, ref.ctypes.data,
                                            bound.ctypes.data)
         return ref, bound
+
+    # -- GEMM with MXFP8 operands (E4M3 data, one UE8M0 scale per 32 along K) ---------
+    @staticmethod
+    def _scales(S, rows, k):
+        S = np.ascontiguousarray(S)
+        if S.dtype != np.uint8:
+            raise TypeError("scales must be UE8M0 codes (uint8)")
+        if S.shape[0] < rows or S.shape[1] < (k + 31) // 32:
+            raise ValueError("scales must be [rows, >= ceil(k / 32)]")
+        return S
+
+    def gemm_mxfp8(self, m, n, k, alpha, A, SA, B, SB, beta=0.0, C=None):
+        """Full m x n result of alpha * (A . SA)(B . SB)^T + beta * C.
+
+        A [m, k] and B [n, k] hold E4M3 codes; SA [m, ceil(k/32)] and SB [n, ceil(k/32)]
+        hold UE8M0 codes, row-major (each array's row length is its leading dimension).
+        """
+        A = self._e4m3(A)
+        B = self._e4m3(B)
+        SA = self._scales(SA, m, k)
+        SB = self._scales(SB, n, k)
+        Cin, ldc, cbf = self._cin(C, beta)
+        ref = np.empty((m, n), dtype=np.float64)
+        bound = np.empty((m, n), dtype=np.float64)
+        self._lib.oracle_gemm_mxfp8(m, n, k, float(alpha), A.ctypes.data, A.shape[1], SA.ctypes.data,
+                                    SA.shape[1], B.ctypes.data, B.shape[1], SB.ctypes.data, SB.shape[1],
+                                    float(beta), self._ptr(Cin), ldc, cbf, ref.ctypes.data,
+                                    bound.ctypes.data, n)
+        return ref, bound
+
+    def gemm_mxfp8_entries(self, k, alpha, A, SA, B, SB, rows, cols, beta=0.0, C=None):
+        A = self._e4m3(A)
+        B = self._e4m3(B)
+        SA = self._scales(SA, 0, k)
+        SB = self._scales(SB, 0, k)
+        Cin, ldc, cbf = self._cin(C, beta)
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        cols = np.ascontiguousarray(cols, dtype=np.int64)
+        ref = np.empty(rows.shape[0], dtype=np.float64)
+        bound = np.empty(rows.shape[0], dtype=np.float64)
+        self._lib.oracle_gemm_mxfp8_entries(k, float(alpha), A.ctypes.data, A.shape[1], SA.ctypes.data,
+                                            SA.shape[1], B.ctypes.data, B.shape[1], SB.ctypes.data,
+                                            SB.shape[1], float(beta), self._ptr(Cin), ldc, cbf,
+                                            rows.shape[0], rows.ctypes.data, cols.ctypes.data,
+                                            ref.ctypes.data, bound.ctypes.data)
+        return ref, bound
+
+    def quantize_mxfp8(self, X, k=None):
+        """MXFP8 codes of the first k columns of a bf16 matrix X [rows, ld >= k] (k defaults
+        to the row length): (E4M3 codes [rows, k], UE8M0 codes [rows, ceil(k/32)]), one
+        scale per group of 32 along each row."""
+        X = self._bf16(X)
+        rows = X.shape[0]
+        k = X.shape[1] if k is None else int(k)
+        if not 0 <= k <= X.shape[1]:
+            raise ValueError("k must be within the row length")
+        Q = np.empty((rows, k), dtype=np.uint8)
+        S = np.empty((rows, (k + 31) // 32), dtype=np.uint8)
+        self._lib.oracle_quantize_mxfp8(rows, k, X.ctypes.data, X.shape[1], Q.ctypes.data, k,
+                                        S.ctypes.data, S.shape[1])
+        return Q, S
 
     # -- SYR2K ---------------------------------------------------------------
     def syr2k(self, uplo, trans, n, k, alpha, A, B, beta=0.0, C=None):

@@ -25,6 +25,23 @@
  *          FP32-accumulated products of the FP8 paths in "fused A2A/GEMM
  *          Perfetto profile protocol", FP8 section).
  *
+ *   GEMM, MXFP8 operands (the SM103 MXFP8 GEMM of the same page: E4M3 data with
+ *          one UE8M0 scale per group of 32 consecutive elements along K, "K32
+ *          quantization group", "E32"):
+ *          C[i][j] = alpha * sum_p (A[i][p] * 2^(SA[i][p/32] - 127))
+ *                                * (B[j][p] * 2^(SB[j][p/32] - 127)) + beta * C[i][j]
+ *          SA is [m, ceil(k/32)] and SB [n, ceil(k/32)], row-major UE8M0 codes.
+ *
+ *   MXFP8 quantization of a BF16 matrix X [rows, k] (the page's "W quantize
+ *          BF16 -> MXFP8" step: per group of 32 along K, amax reduction, UE8M0
+ *          scale, E4M3 conversion). The page names the steps, not the rule; the
+ *          rule here is the OCP Microscaling (MX) v1.0 conversion: shared
+ *          exponent e = floor(log2(amax)) - 8 (8 = the largest E4M3 exponent),
+ *          clamped to [-127, 127], scale code e + 127, element = X / 2^e rounded
+ *          to the nearest E4M3 value, ties to even, magnitudes above 448
+ *          saturated to 448. A group of zeros gets code 0; a group holding a
+ *          NaN or an infinity gets code 255 (NaN) and NaN elements (0x7F).
+ *
  * Alongside each value the oracle returns bound[i][j] = sum_p |product|, the
  * scale against which the tolerance max|C - C_ref| <= 1e-3 * |alpha| * bound
  * is stated.
@@ -68,6 +85,36 @@ static double e4m3_value(uint8_t code)
     else
         mag = ldexp(1.0 + (double)m / 8.0, e - 7);
     return (code & 0x80) ? -mag : mag;
+}
+
+/* UE8M0 scale code -> 2^(code - 127), exact; code 255 is NaN. */
+static double ue8m0_value(uint8_t code)
+{
+    if (code == 0xFF)
+        return NAN;
+    return ldexp(1.0, (int)code - 127);
+}
+
+/* Nearest E4M3 code to y (a finite double), ties to the even code (the code's
+ * last bit is the mantissa's last bit), magnitudes beyond 448 saturated to 448.
+ * Found by comparing y with every finite non-negative E4M3 value. */
+static uint8_t e4m3_nearest(double y)
+{
+    double mag = fabs(y);
+    int best = 0;
+    double best_err = INFINITY;
+    if (mag >= 448.0) {
+        best = 0x7E;
+    } else {
+        for (int c = 0; c <= 0x7E; ++c) {
+            double err = fabs(e4m3_value((uint8_t)c) - mag);
+            if (err < best_err || (err == best_err && (c & 1) == 0)) {
+                best = c;
+                best_err = err;
+            }
+        }
+    }
+    return (uint8_t)(signbit(y) ? (best | 0x80) : best);
 }
 
 /* Element (r, c) of op(X), X stored row-major with leading dimension ld. */
@@ -137,6 +184,31 @@ static void gemm_e4m3_element(int64_t i, int64_t j, int64_t k, double alpha, con
     if (alpha != 0.0) {
         for (int64_t p = 0; p < k; ++p) {
             double prod = e4m3_value(A[i * lda + p]) * e4m3_value(B[j * ldb + p]);
+            acc += prod;
+            mag += fabs(prod);
+        }
+    }
+    double value = alpha * acc;
+    if (beta != 0.0)
+        value += beta * c_input(C, ldc, c_is_bf16, i, j);
+    *ref = value;
+    *bound = mag;
+}
+
+/* One output element of the MXFP8 GEMM: row i of A and row j of B, each element
+ * times the scale of its group of 32 along K. */
+static void gemm_mxfp8_element(int64_t i, int64_t j, int64_t k, double alpha, const uint8_t *A,
+                               int64_t lda, const uint8_t *SA, int64_t ldsa, const uint8_t *B,
+                               int64_t ldb, const uint8_t *SB, int64_t ldsb, double beta,
+                               const void *C, int64_t ldc, int c_is_bf16, double *ref,
+                               double *bound)
+{
+    double acc = 0.0, mag = 0.0;
+    if (alpha != 0.0) {
+        for (int64_t p = 0; p < k; ++p) {
+            double a = e4m3_value(A[i * lda + p]) * ue8m0_value(SA[i * ldsa + p / 32]);
+            double b = e4m3_value(B[j * ldb + p]) * ue8m0_value(SB[j * ldsb + p / 32]);
+            double prod = a * b;
             acc += prod;
             mag += fabs(prod);
         }
@@ -315,4 +387,72 @@ void oracle_gemm_e4m3_entries(int64_t k, double alpha, const uint8_t *A, int64_t
     for (int64_t t = 0; t < count; ++t)
         gemm_e4m3_element(rows[t], cols[t], k, alpha, A, lda, B, ldb, beta, C, ldc, c_is_bf16,
                           &ref[t], &bound[t]);
+}
+
+/* Full MXFP8 GEMM C = alpha * (A . SA) * (B . SB)^T + beta * C; A [m, k], B [n, k]. */
+void oracle_gemm_mxfp8(int64_t m, int64_t n, int64_t k, double alpha, const uint8_t *A, int64_t lda,
+                       const uint8_t *SA, int64_t ldsa, const uint8_t *B, int64_t ldb,
+                       const uint8_t *SB, int64_t ldsb, double beta, const void *C, int64_t ldc,
+                       int c_is_bf16, double *ref, double *bound, int64_t ldr)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < m; ++i)
+        for (int64_t j = 0; j < n; ++j)
+            gemm_mxfp8_element(i, j, k, alpha, A, lda, SA, ldsa, B, ldb, SB, ldsb, beta, C, ldc,
+                               c_is_bf16, &ref[i * ldr + j], &bound[i * ldr + j]);
+}
+
+/* MXFP8 GEMM at chosen positions. */
+void oracle_gemm_mxfp8_entries(int64_t k, double alpha, const uint8_t *A, int64_t lda,
+                               const uint8_t *SA, int64_t ldsa, const uint8_t *B, int64_t ldb,
+                               const uint8_t *SB, int64_t ldsb, double beta, const void *C,
+                               int64_t ldc, int c_is_bf16, int64_t count, const int64_t *rows,
+                               const int64_t *cols, double *ref, double *bound)
+{
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t t = 0; t < count; ++t)
+        gemm_mxfp8_element(rows[t], cols[t], k, alpha, A, lda, SA, ldsa, B, ldb, SB, ldsb, beta, C,
+                           ldc, c_is_bf16, &ref[t], &bound[t]);
+}
+
+/* MXFP8 quantization of X [rows, k] (bf16 bits, leading dimension ldx) into E4M3
+ * codes Q [rows, k] (ldq) and UE8M0 codes S [rows, ceil(k/32)] (lds), one per
+ * group of 32 consecutive elements of a row (the last group may be shorter). */
+void oracle_quantize_mxfp8(int64_t rows, int64_t k, const uint16_t *X, int64_t ldx, uint8_t *Q,
+                           int64_t ldq, uint8_t *S, int64_t lds)
+{
+    int64_t groups = (k + 31) / 32;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < rows; ++i)
+        for (int64_t g = 0; g < groups; ++g) {
+            int64_t p0 = 32 * g, p1 = p0 + 32 < k ? p0 + 32 : k;
+            double amax = 0.0;
+            int special = 0;
+            for (int64_t p = p0; p < p1; ++p) {
+                double x = bf16_value(X[i * ldx + p]);
+                if (isnan(x) || isinf(x))
+                    special = 1;
+                else if (fabs(x) > amax)
+                    amax = fabs(x);
+            }
+            if (special) {
+                S[i * lds + g] = 0xFF;
+                for (int64_t p = p0; p < p1; ++p)
+                    Q[i * ldq + p] = 0x7F;
+                continue;
+            }
+            int e = -127;
+            if (amax > 0.0) {
+                int ex;
+                frexp(amax, &ex); /* amax = f * 2^ex, f in [0.5, 1): floor(log2(amax)) = ex - 1 */
+                e = (ex - 1) - 8;
+                if (e < -127)
+                    e = -127;
+                if (e > 127)
+                    e = 127;
+            }
+            S[i * lds + g] = (uint8_t)(e + 127);
+            for (int64_t p = p0; p < p1; ++p)
+                Q[i * ldq + p] = e4m3_nearest(ldexp(bf16_value(X[i * ldx + p]), -e));
+        }
 }

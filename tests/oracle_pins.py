@@ -10,7 +10,14 @@ oracle disagrees with
   SYR2K = one triangle of GEMM(A, B^T) + GEMM(B, A^T), SYR2K(A, A) = 2 SYRK(A),
   SYR2K(A, B) = SYR2K(B, A),
   beta=1 accumulation = C0 + a beta=0 call, exact power-of-two alpha scaling,
-* the BLAS conventions for alpha = 0, beta = 0 and k = 0.
+* the BLAS conventions for alpha = 0, beta = 0 and k = 0,
+* for the MXFP8 GEMM: exact rational brute force with power-of-two group
+  scales, unit scales equal to the plain E4M3 GEMM, NumPy on the decoded
+  operands, exact row and operand scaling,
+* for the MXFP8 quantization (OCP MX conversion): every E4M3 code round trips,
+  an exact rational restatement of the rule on random groups, ties to even,
+  saturation, zero / NaN / infinite groups, short last groups and the rounding
+  error bound.
 
 ``tests/test_oracle_mutants.py`` plants plausible mistakes in copies of the
 oracle's C source and checks that every one of them fails at least one pin.
@@ -372,6 +379,206 @@ def pin_e4m3_matches_numpy(o):
     assert np.allclose(bound, np.abs(a) @ np.abs(b).T, rtol=1e-13, atol=0)
 
 
+# --- MXFP8: E4M3 data with one UE8M0 scale per group of 32 along K --------------------
+def _ue8m0(rows, groups, seed, lo=124, hi=130, pad=0):
+    codes = gen.integers(seed, rows * groups, lo, hi).reshape(rows, groups).astype(np.uint8)
+    if pad:
+        codes = gen.pad_ld(codes, groups + pad, np.uint8(0xFF))  # NaN scales: never read
+    return codes
+
+
+def _pow2(e):
+    return Fraction(2) ** int(e)
+
+
+def pin_mxfp8_bruteforce_exact(o):
+    # k crosses group boundaries (33 = 32 + 1, 70 = 2 * 32 + 6, 96 = 3 whole groups)
+    for (m, n, k) in [(1, 1, 1), (2, 3, 33), (3, 2, 70), (2, 2, 96)]:
+        g = (k + 31) // 32
+        A, Av = _int_e4m3((m, k), 300 + k, pad=4)
+        B, Bv = _int_e4m3((n, k), 301 + k, pad=2)
+        SA = _ue8m0(m, g, 302 + k, pad=2)
+        SB = _ue8m0(n, g, 303 + k, pad=1)
+        Cv = gen.integers(304 + k, m * n, -9, 9).reshape(m, n)
+        for alpha, beta in [(Fraction(1), Fraction(0)), (Fraction(-1, 2), Fraction(3))]:
+            ref, bound = o.gemm_mxfp8(m, n, k, float(alpha), A, SA, B, SB, float(beta), Cv.astype(np.float32))
+            for i in range(m):
+                for j in range(n):
+                    terms = [int(Av[i, p]) * _pow2(int(SA[i, p // 32]) - 127) * int(Bv[j, p])
+                             * _pow2(int(SB[j, p // 32]) - 127) for p in range(k)]
+                    assert Fraction(ref[i, j]) == alpha * sum(terms) + beta * int(Cv[i, j]), (m, n, k, i, j)
+                    assert Fraction(bound[i, j]) == sum(abs(t) for t in terms), (m, n, k, i, j)
+
+
+def pin_mxfp8_unit_scales_equal_e4m3(o):
+    # code 127 is 2^0: the block-scaled GEMM must reduce to the (pinned) plain E4M3 GEMM
+    m, n, k = 13, 11, 100
+    A = gen.matrix_e4m3(m, k, "normal", seed=311, std=2.0)
+    B = gen.matrix_e4m3(n, k, "normal", seed=312)
+    ones_a = np.full((m, 4), 127, np.uint8)
+    ones_b = np.full((n, 4), 127, np.uint8)
+    C = gen.matrix_f32(m, n, "normal", seed=313)
+    r, b = o.gemm_mxfp8(m, n, k, 0.25, A, ones_a, B, ones_b, -2.0, C)
+    r8, b8 = o.gemm_e4m3(m, n, k, 0.25, A, B, -2.0, C)
+    assert np.array_equal(r, r8) and np.array_equal(b, b8)
+
+
+def _mx_decode(codes, scales, k):
+    vals = gen.e4m3_bits_to_f32(codes).astype(np.float64)[:, :k]
+    per = np.repeat(np.ldexp(1.0, scales.astype(np.int64) - 127), 32, axis=1)[:, :k]
+    return vals * per
+
+
+def pin_mxfp8_matches_numpy(o):
+    m, n, k = 21, 17, 200
+    g = (k + 31) // 32
+    A = gen.matrix_e4m3(m, k, "normal", seed=321)
+    B = gen.matrix_e4m3(n, k, "uniform", seed=322, lo=-3, hi=3)
+    SA = _ue8m0(m, g, 323, lo=110, hi=140)
+    SB = _ue8m0(n, g, 324, lo=110, hi=140)
+    a, b = _mx_decode(A, SA, k), _mx_decode(B, SB, k)
+    ref, bound = o.gemm_mxfp8(m, n, k, 1.5, A, SA, B, SB)
+    assert np.all(np.abs(ref - 1.5 * a @ b.T) <= 1e-13 * 1.5 * (np.abs(a) @ np.abs(b).T))
+    assert np.allclose(bound, np.abs(a) @ np.abs(b).T, rtol=1e-13, atol=0)
+
+
+def pin_mxfp8_scaling_exact(o):
+    # raising every scale of row i of SA by d multiplies row i of the products by 2^d;
+    # raising every code of SB by 1 doubles every product
+    m, n, k = 9, 7, 96
+    A = gen.matrix_e4m3(m, k, "normal", seed=331)
+    B = gen.matrix_e4m3(n, k, "normal", seed=332)
+    SA = _ue8m0(m, 3, 333)
+    SB = _ue8m0(n, 3, 334)
+    ref, bound = o.gemm_mxfp8(m, n, k, 1.0, A, SA, B, SB)
+    SA2 = SA.copy()
+    SA2[4] += 3
+    r2, b2 = o.gemm_mxfp8(m, n, k, 1.0, A, SA2, B, SB)
+    want = ref.copy()
+    want[4] *= 8.0
+    assert np.array_equal(r2, want)
+    r3, _ = o.gemm_mxfp8(m, n, k, 1.0, A, SA, B, (SB + 1).astype(np.uint8))
+    assert np.array_equal(r3, 2.0 * ref)
+    rows = np.array([0, 4, 8, 3])
+    cols = np.array([6, 0, 2, 3])
+    e, eb = o.gemm_mxfp8_entries(k, 1.0, A, SA, B, SB, rows, cols)
+    assert np.array_equal(e, ref[rows, cols]) and np.array_equal(eb, bound[rows, cols])
+
+
+E4M3_FINITE = [c for c in range(256) if (c & 0x7F) != 0x7F]
+
+
+def _e4m3_frac(c):
+    e, m = (c >> 3) & 0xF, c & 7
+    mag = Fraction(m, 8) * _pow2(-6) if e == 0 else (1 + Fraction(m, 8)) * _pow2(e - 7)
+    return -mag if c & 0x80 else mag
+
+
+def _floor_log2(x: Fraction) -> int:
+    # largest e with 2^e <= x, for x > 0
+    e = x.numerator.bit_length() - x.denominator.bit_length()
+    while _pow2(e) > x:
+        e -= 1
+    while _pow2(e + 1) <= x:
+        e += 1
+    return e
+
+
+def _mx_rule(group_vals):
+    """The OCP MX conversion of one group, restated in exact rationals: (scale code, codes)."""
+    fr = [Fraction(float(v)) for v in group_vals]
+    amax = max((abs(v) for v in fr), default=Fraction(0))
+    e = -127 if amax == 0 else max(-127, min(127, _floor_log2(amax) - 8))
+    out = []
+    for v in fr:
+        y = v / _pow2(e)
+        if abs(y) >= 448:
+            c = 0x7E
+        else:
+            best = min(range(0x7F), key=lambda c: (abs(_e4m3_frac(c) - abs(y)), c & 1))
+            c = best
+        out.append(c | 0x80 if (y < 0 or (y == 0 and np.signbit(float(v)))) else c)
+    return e + 127, out
+
+
+def pin_quantize_every_code_round_trips(o):
+    # a group led by 256 (= 2^8, scale 2^0) carries each finite E4M3 value through unchanged
+    codes = np.array(E4M3_FINITE, dtype=np.uint8)
+    vals = gen.e4m3_bits_to_f32(codes)
+    rows = -(-len(vals) // 31)
+    X = np.zeros((rows, 32), np.float32)
+    X[:, 0] = 256.0
+    flat = np.zeros(rows * 31, np.float32)
+    flat[:len(vals)] = vals
+    X[:, 1:] = flat.reshape(rows, 31)
+    Q, S = o.quantize_mxfp8(gen.f32_to_bf16_bits(X))
+    assert np.all(S == 127)
+    assert np.all(Q[:, 0] == 0x78)
+    got = Q[:, 1:].reshape(-1)[:len(vals)]
+    want = codes.copy()
+    want[want == 0x80] = 0x80  # -0 keeps its sign
+    assert np.array_equal(got, want), np.nonzero(got != want)
+
+
+def pin_quantize_matches_exact_rule(o):
+    rng_rows, k = 6, 70  # groups of 32, 32 and 6
+    X = gen.matrix_bf16(rng_rows, k, "normal", seed=341, std=3.0)
+    X[1] = gen.f32_to_bf16_bits(gen.bf16_bits_to_f32(X[1]) * np.float32(2e-38))   # tiny: scale clamped at 2^-127
+    X[2] = gen.f32_to_bf16_bits(gen.bf16_bits_to_f32(X[2]) * np.float32(1e20))     # large exponents
+    Q, S = o.quantize_mxfp8(gen.pad_ld(X, k + 6, gen.BF16_NAN), k)
+    vals = gen.bf16_bits_to_f32(X)
+    assert np.all(S[1] == 0)  # floor(log2(amax)) - 8 < -127 in every group of row 1
+    for i in range(rng_rows):
+        for g in range(3):
+            code, want = _mx_rule(vals[i, 32 * g:min(k, 32 * g + 32)])
+            assert S[i, g] == code, (i, g, S[i, g], code)
+            assert list(Q[i, 32 * g:min(k, 32 * g + 32)]) == want, (i, g)
+
+
+def pin_quantize_ties_saturation_specials(o):
+    X = np.zeros((5, 40), np.float32)
+    # row 0: amax 256 (scale 2^0); E4M3 steps by 1 in [8, 16) and by 2 in [16, 32), so 8.5
+    # (8|9), 9.5 (9|10) and 17 (16|18) are ties: the even mantissas give 8, 10 and 16
+    X[0, :4] = [256.0, 8.5, 9.5, 17.0]
+    X[0, 32:] = [-1.0, 0.0, 0.0, 0.0, 0.0, 0.0, 0.0, 2.0]   # short last group: amax 2 -> 2^-7
+    # row 1: amax 500 -> scale 2^0 and 500 saturates to 448; 464 (a tie with 480) too
+    X[1, :3] = [500.0, 464.0, -470.0]
+    # row 2: all zero -> code 0, zero elements
+    # row 3: a NaN poisons its group only
+    X[3, :2] = [np.nan, 1.0]
+    X[3, 32] = 3.0
+    # row 4: an infinity
+    X[4, 5] = np.inf
+    Q, S = o.quantize_mxfp8(gen.f32_to_bf16_bits(X))
+    assert S[0, 0] == 127 and list(Q[0, :4]) == [0x78, 0x50, 0x52, 0x58]
+    assert S[0, 1] == 127 - 7 and Q[0, 32] == 0xF0 and Q[0, 39] == 0x78    # -1 and 2 at 2^-7: -128, 256
+    assert S[1, 0] == 127 and list(Q[1, :3]) == [0x7E, 0x7E, 0xFE]
+    assert S[2, 0] == 0 and S[2, 1] == 0 and np.all(Q[2] == 0)
+    assert S[3, 0] == 255 and np.all(Q[3, :32] == 0x7F)
+    assert S[3, 1] == 127 - 7 and Q[3, 32] == 0x7C                        # 3 at 2^-7: 384 = 1.5 * 2^8
+    assert S[4, 0] == 255 and np.all(Q[4, :32] == 0x7F) and S[4, 1] == 0
+
+
+def pin_quantize_error_bound(o):
+    # dequantized elements up to 448 * scale lie within half an E4M3 step: 2^-4 relative
+    # for normal results, 2^-10 * scale absolute below the smallest normal (2^-6 * scale);
+    # larger ones (the scale leaves the group's amax in [256, 512) * scale) saturate to
+    # exactly 448 * scale
+    X = gen.matrix_bf16(64, 96, "normal", seed=351, std=0.7)
+    Q, S = o.quantize_mxfp8(X)
+    x = gen.bf16_bits_to_f32(X).astype(np.float64)
+    d = _mx_decode(Q, S, 96)
+    scale = np.repeat(np.ldexp(1.0, S.astype(np.int64) - 127), 32, axis=1)
+    sat = np.abs(x) > 448.0 * scale
+    assert np.any(sat)
+    assert np.array_equal(d[sat], np.sign(x[sat]) * 448.0 * scale[sat])
+    err_ok = np.abs(d - x) <= np.maximum(2.0 ** -4 * np.abs(x), 2.0 ** -10 * scale)
+    assert np.all(err_ok[~sat])
+    amax = np.abs(x).reshape(64, 3, 32).max(axis=2)
+    assert np.all((np.abs(d).reshape(64, 3, 32).max(axis=2) >= 2.0 ** 8 * np.ldexp(1.0, S.astype(np.int64) - 127)))
+    assert np.all(amax < 2.0 ** 9 * np.ldexp(1.0, S.astype(np.int64) - 127))
+
+
 PINS = [
     pin_gemm_bruteforce_exact,
     pin_syrk_bruteforce_exact,
@@ -392,4 +599,12 @@ PINS = [
     pin_e4m3_bruteforce_exact,
     pin_e4m3_equals_bf16_gemm_on_same_values,
     pin_e4m3_matches_numpy,
+    pin_mxfp8_bruteforce_exact,
+    pin_mxfp8_unit_scales_equal_e4m3,
+    pin_mxfp8_matches_numpy,
+    pin_mxfp8_scaling_exact,
+    pin_quantize_every_code_round_trips,
+    pin_quantize_matches_exact_rule,
+    pin_quantize_ties_saturation_specials,
+    pin_quantize_error_bound,
 ]

@@ -49,6 +49,28 @@ MUTANTS = [
     ("e4m3_b_k_reversed", "e4m3_value(B[j * ldb + p])", "e4m3_value(B[j * ldb + (k - 1 - p)])", 0),
     ("gemm_last_column_skipped", "for (int64_t j = 0; j < n; ++j)\n            gemm_element",
      "for (int64_t j = 0; j + 1 < n; ++j)\n            gemm_element", 0),
+    # MXFP8 GEMM
+    ("mx_group_of_16", "SA[i * ldsa + p / 32]", "SA[i * ldsa + p / 16]", 0),
+    ("mx_b_scale_of_row_i", "SB[j * ldsb + p / 32]", "SB[i * ldsb + p / 32]", 0),
+    ("mx_b_scale_dropped", " * ue8m0_value(SB[j * ldsb + p / 32])", "", 0),
+    ("mx_scale_bias_128", "return ldexp(1.0, (int)code - 127);", "return ldexp(1.0, (int)code - 128);", 0),
+    ("mx_scale_ld_ignored", "SA[i * ldsa + p / 32]", "SA[i * ((k + 31) / 32) + p / 32]", 0),
+    ("mx_group_index_mod", "SB[j * ldsb + p / 32]", "SB[j * ldsb + p % 32 / 8]", 0),
+    ("mx_signed_bound", "            acc += prod;\n            mag += fabs(prod);\n        }\n    }\n    double value = alpha * acc;\n    if (beta != 0.0)\n        value += beta * c_input(C, ldc, c_is_bf16, i, j);\n    *ref = value;\n    *bound = mag;\n}\n\n/* One output element of SYR2K",
+     "            acc += prod;\n            mag += prod;\n        }\n    }\n    double value = alpha * acc;\n    if (beta != 0.0)\n        value += beta * c_input(C, ldc, c_is_bf16, i, j);\n    *ref = value;\n    *bound = mag;\n}\n\n/* One output element of SYR2K", 0),
+    # MXFP8 quantization (OCP MX conversion)
+    ("q_emax_7", "e = (ex - 1) - 8;", "e = (ex - 1) - 7;", 0),
+    ("q_ceil_log2", "e = (ex - 1) - 8;", "e = ex - 8;", 0),
+    ("q_ties_away", "(err == best_err && (c & 1) == 0)", "(err == best_err)", 0),
+    ("q_ties_down", "(err == best_err && (c & 1) == 0)", "(0)", 0),
+    ("q_no_saturation", "        best = 0x7E;\n", "        best = 0x7F;\n", 0),
+    ("q_sign_dropped", "return (uint8_t)(signbit(y) ? (best | 0x80) : best);", "return (uint8_t)best;", 0),
+    ("q_signed_amax", "else if (fabs(x) > amax)\n                    amax = fabs(x);", "else if (x > amax)\n                    amax = x;", 0),
+    ("q_zero_group_code", "int e = -127;\n            if (amax > 0.0) {", "int e = 0;\n            if (amax > 0.0) {", 0),
+    ("q_specials_ignored", "special = 1;", "special = 0;", 0),
+    ("q_no_low_clamp", "if (e < -127)\n                    e = -127;", "if (e < -200)\n                    e = -127;", 0),
+    ("q_amax_half_group", "for (int64_t p = p0; p < p1; ++p) {\n                double x = bf16_value",
+     "for (int64_t p = p0; p < p1 && p < p0 + 16; ++p) {\n                double x = bf16_value", 0),
 ]
 
 
