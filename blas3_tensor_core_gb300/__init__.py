@@ -20,7 +20,8 @@ __all__ = [
     "BM_ERR_TIMEOUT", "BM_ERR_WORKSPACE", "BM_OP_N", "BM_OP_T", "BM_C_F32", "BM_C_BF16",
     "BM_LOWER", "BM_UPPER", "Plan",
     "bm_gemm_bf16", "bm_gemm_bf16_noalloc", "BM_NOALLOC_SCRATCH_BYTES", "bm_syrk_bf16", "bm_syr2k_bf16",
-    "bm_gemm_e4m3", "bm_gemm_e4m3_workspace_size", "bm_gemm_bf16_workspace_size", "bm_get_last_device_error",
+    "bm_gemm_e4m3", "bm_gemm_e4m3_workspace_size", "bm_gemm_mxfp8", "bm_gemm_mxfp8_workspace_size",
+    "bm_gemm_mxfp8_plan", "mxfp8_scale_bytes", "mxfp8_scale_offset", "bm_gemm_bf16_workspace_size", "bm_get_last_device_error",
     "bm_set_wait_timeout_ms", "bm_debug_inject_stall", "bm_status_string", "bm_gemm_bf16_plan",
     "bm_syrk_bf16_plan", "bm_syrk_bf16_tile_order", "bm_set_tile_override", "bm_version", "gemm", "syrk", "syr2k", "workspace_size",
 ]
@@ -78,6 +79,13 @@ def library():
                 lib.bm_gemm_e4m3.restype = _i32
                 lib.bm_gemm_e4m3_workspace_size.argtypes = [_i64, _i64, _i64]
                 lib.bm_gemm_e4m3_workspace_size.restype = _sz
+                lib.bm_gemm_mxfp8.argtypes = [_i64, _i64, _i64, _f32, _vp, _i64, _vp, _vp, _i64, _vp, _f32, _vp,
+                                              _i64, _i32, _vp, _sz, _vp]
+                lib.bm_gemm_mxfp8.restype = _i32
+                lib.bm_gemm_mxfp8_workspace_size.argtypes = [_i64, _i64, _i64]
+                lib.bm_gemm_mxfp8_workspace_size.restype = _sz
+                lib.bm_gemm_mxfp8_plan.argtypes = [_i64, _i64, _i64, _sz, ctypes.POINTER(Plan)]
+                lib.bm_gemm_mxfp8_plan.restype = _i32
                 lib.bm_syrk_bf16.argtypes = [_i32, _i32, _i64, _i64, _f32, _vp, _i64, _f32, _vp, _i64,
                                              _i32, _vp]
                 lib.bm_syrk_bf16.restype = _i32
@@ -138,6 +146,34 @@ def bm_gemm_e4m3(m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, c_type, workspace
 
 def bm_gemm_e4m3_workspace_size(m, n, k) -> int:
     return library().bm_gemm_e4m3_workspace_size(m, n, k)
+
+
+def bm_gemm_mxfp8(m, n, k, alpha, A, lda, SA, B, ldb, SB, beta, C, ldc, c_type, workspace=None,
+                  workspace_bytes=0, stream=None) -> int:
+    return library().bm_gemm_mxfp8(m, n, k, alpha, A, lda, SA, B, ldb, SB, beta, C, ldc, c_type, workspace,
+                                   workspace_bytes, stream)
+
+
+def bm_gemm_mxfp8_workspace_size(m, n, k) -> int:
+    return library().bm_gemm_mxfp8_workspace_size(m, n, k)
+
+
+def bm_gemm_mxfp8_plan(m, n, k, workspace_bytes=0):
+    plan = Plan()
+    st = library().bm_gemm_mxfp8_plan(m, n, k, workspace_bytes, ctypes.byref(plan))
+    return st, plan
+
+
+def mxfp8_scale_bytes(rows, k) -> int:
+    """Size of an MXFP8 scale array in the tiled layout: ceil(rows/128) x ceil(k/128) atoms of 512 bytes."""
+    return -(-rows // 128) * -(-k // 128) * 512
+
+
+def mxfp8_scale_offset(r, g, k):
+    """Byte offset of the scale of row r, group g (elements 32 g .. 32 g + 31) in the tiled layout
+    (works elementwise on NumPy integer arrays)."""
+    katoms = -(-k // 128)
+    return ((r // 128) * katoms + g // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + g % 4
 
 
 def bm_syr2k_bf16(uplo, trans, n, k, alpha, A, lda, B, ldb, beta, C, ldc, c_type, stream=None) -> int:

@@ -29,11 +29,16 @@ constexpr int kGroupM = 16;
 //   kSingle256: 128 x 256 per CTA, 4 stages of one k-block (48 KB)
 //   kSingle128: 128 x 128 per CTA, 3 stages of two k-blocks (64 KB; narrow outputs)
 //   kPair256:   256 x 256 per CTA pair (cta_group::2), 3 stages of two k-blocks (64 KB per CTA)
-enum Variant { kSingle256 = 0, kSingle128 = 1, kPair256 = 2, kNumVariants = 3 };
-constexpr int kVariantBN[kNumVariants] = {256, 128, 256};
-constexpr int kVariantStages[kNumVariants] = {4, 3, 3};
-constexpr int kVariantStageKBlocks[kNumVariants] = {1, 2, 2};
-constexpr int kVariantPair[kNumVariants] = {1, 1, 2};
+// MXFP8 (the scale factors take tensor-memory columns beside the two accumulators,
+// so the tiles are 128 wide):
+//   kSingle128Mx: 128 x 128 per CTA, 5 stages of one k-block (33 KB with scales)
+//   kPair128Mx:   256 x 128 per CTA pair, 3 stages of two k-blocks (50 KB per CTA)
+enum Variant { kSingle256 = 0, kSingle128 = 1, kPair256 = 2, kSingle128Mx = 3, kPair128Mx = 4, kNumVariants = 5 };
+constexpr int kVariantBN[kNumVariants] = {256, 128, 256, 128, 128};
+constexpr int kVariantStages[kNumVariants] = {4, 3, 3, 5, 3};
+constexpr int kVariantStageKBlocks[kNumVariants] = {1, 2, 2, 1, 2};
+constexpr int kVariantPair[kNumVariants] = {1, 1, 2, 1, 2};
+bool variant_scaled(int v) { return v == kSingle128Mx || v == kPair128Mx; }
 
 struct DeviceState {
     bool ready = false;
@@ -42,7 +47,8 @@ struct DeviceState {
     int device = -1;
     int *status = nullptr;  // one int, allocated on first use
     bool attrs_set = false;
-    int max_pair_clusters = 0;  // co-resident clusters of the pair kernel
+    int max_pair_clusters = 0;     // co-resident clusters of the pair kernel
+    int max_pair_clusters_mx = 0;  // same for the MXFP8 pair kernel
 };
 
 std::mutex g_mutex;
@@ -55,17 +61,24 @@ std::atomic<int> g_tile_override{0};  // 0 = automatic, else 1 + Variant
 template <int ELEM, int EPI = bm::EPI_FULL>
 const void *variant_kernel_t(int v)
 {
-    switch (v) {
-    case kSingle256: return reinterpret_cast<const void *>(&bm::bm_gemm_tcgen05_kernel<256, 4, 1, ELEM, 1, EPI>);
-    case kSingle128: return reinterpret_cast<const void *>(&bm::bm_gemm_tcgen05_kernel<128, 3, 1, ELEM, 2, EPI>);
-    default: return reinterpret_cast<const void *>(&bm::bm_gemm_tcgen05_kernel<256, 3, 2, ELEM, 2, EPI>);
+    if constexpr (ELEM == bm::ELEM_MXF8) {
+        if (v == kSingle128Mx) return reinterpret_cast<const void *>(&bm::bm_gemm_tcgen05_kernel<128, 5, 1, ELEM, 1, EPI>);
+        return reinterpret_cast<const void *>(&bm::bm_gemm_tcgen05_kernel<128, 3, 2, ELEM, 2, EPI>);
+    } else {
+        switch (v) {
+        case kSingle256: return reinterpret_cast<const void *>(&bm::bm_gemm_tcgen05_kernel<256, 4, 1, ELEM, 1, EPI>);
+        case kSingle128: return reinterpret_cast<const void *>(&bm::bm_gemm_tcgen05_kernel<128, 3, 1, ELEM, 2, EPI>);
+        default: return reinterpret_cast<const void *>(&bm::bm_gemm_tcgen05_kernel<256, 3, 2, ELEM, 2, EPI>);
+        }
     }
 }
 
 // Kernel copies: bf16 and E4M3 operands with every epilogue path, bf16 GEMM
-// copies without the SYRK diagonal path (beta == 0 and beta != 0), and the
-// E4M3 beta == 0 one.
-constexpr int kNumKernelKinds = 5;
+// copies without the SYRK diagonal path (beta == 0 and beta != 0), the E4M3
+// beta == 0 one, and the MXFP8 ones (kinds 5, 6) of the MXFP8 variants.
+constexpr int kNumKernelKinds = 7;
+
+bool kind_fits(int v, int kind) { return (kind >= 5) == variant_scaled(v); }
 
 const void *variant_kernel(int v, int kind = 0)
 {
@@ -74,31 +87,34 @@ const void *variant_kernel(int v, int kind = 0)
     case 2: return variant_kernel_t<bm::ELEM_BF16, bm::EPI_STORE>(v);
     case 3: return variant_kernel_t<bm::ELEM_BF16, bm::EPI_COMBINE>(v);
     case 4: return variant_kernel_t<bm::ELEM_E4M3, bm::EPI_STORE>(v);
+    case 5: return variant_kernel_t<bm::ELEM_MXF8>(v);
+    case 6: return variant_kernel_t<bm::ELEM_MXF8, bm::EPI_STORE>(v);
     default: return variant_kernel_t<bm::ELEM_BF16>(v);
     }
 }
 
-// Shared memory does not depend on the element type (k-blocks are 128 bytes of K).
+// Shared memory of bf16 and E4M3 kernels is the same (k-blocks are 128 bytes of
+// K); the MXFP8 variants add the scale atoms.
 int variant_smem(int v)
 {
     switch (v) {
     case kSingle256: return bm::KernelCfg<256, 4, 1, bm::ELEM_BF16, 1>::SMEM_BYTES;
     case kSingle128: return bm::KernelCfg<128, 3, 1, bm::ELEM_BF16, 2>::SMEM_BYTES;
+    case kSingle128Mx: return bm::KernelCfg<128, 5, 1, bm::ELEM_MXF8, 1>::SMEM_BYTES;
+    case kPair128Mx: return bm::KernelCfg<128, 3, 2, bm::ELEM_MXF8, 2>::SMEM_BYTES;
     default: return bm::KernelCfg<256, 3, 2, bm::ELEM_BF16, 2>::SMEM_BYTES;
     }
 }
 
 bool fits_int32(int64_t v) { return v >= 0 && v <= 0x7FFFFFFFLL; }
 
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
 // Once per device: the dynamic shared-memory size of every kernel copy, and how
 // many clusters of the pair kernel fit at once (0: single-CTA tiles only).
-bm_status init_kernel_attrs(DeviceState &st)
+// Co-resident clusters of two CTAs of a pair kernel (0 if none fit).
+int pair_cluster_capacity(const DeviceState &st, int v, int kind)
 {
-    for (int e = 0; e < kNumKernelKinds; ++e)
-        for (int v = 0; v < kNumVariants; ++v)
-            if (cudaFuncSetAttribute(variant_kernel(v, e), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     variant_smem(v)) != cudaSuccess)
-                return BM_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -107,15 +123,26 @@ bm_status init_kernel_attrs(DeviceState &st)
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3(2 * (st.sm_count / 2), 1, 1);
     cfg.blockDim = dim3(bm::NUM_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = variant_smem(kPair256);
+    cfg.dynamicSmemBytes = variant_smem(v);
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, variant_kernel(kPair256), &cfg) != cudaSuccess || clusters <= 0) {
+    if (cudaOccupancyMaxActiveClusters(&clusters, variant_kernel(v, kind), &cfg) != cudaSuccess || clusters <= 0) {
         cudaGetLastError();
         clusters = 0;
     }
-    st.max_pair_clusters = clusters;
+    return clusters;
+}
+
+bm_status init_kernel_attrs(DeviceState &st)
+{
+    for (int e = 0; e < kNumKernelKinds; ++e)
+        for (int v = 0; v < kNumVariants; ++v)
+            if (kind_fits(v, e) && cudaFuncSetAttribute(variant_kernel(v, e), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                        variant_smem(v)) != cudaSuccess)
+                return BM_ERR_CUDA;
+    st.max_pair_clusters = pair_cluster_capacity(st, kPair256, 0);
+    st.max_pair_clusters_mx = pair_cluster_capacity(st, kPair128Mx, 5);
     st.attrs_set = true;
     return BM_OK;
 }
@@ -230,6 +257,25 @@ bool encode_slots(CUtensorMap *map, void *partial, int64_t rows, int64_t cols)
     return r == CUDA_SUCCESS;
 }
 
+// Map of an MXFP8 scale array: ceil(rows / 128) x ceil(k / 128) atoms of 512
+// bytes, atom (row block, k-block) at ((row block) * ceil(k / 128) + k-block) * 512,
+// seen as a 4-D tensor of bytes (256, 2, k-block, row block) so that one box brings
+// `kps` k-blocks of `row_blocks` row blocks (atoms land in the order row block,
+// k-block). Boxes past the last k-block or row block read zeros.
+bool encode_scales(CUtensorMap *map, const void *sf, int64_t rows, int64_t k, int kps, int row_blocks)
+{
+    const int64_t katoms = ceil_div(k, 128);
+    cuuint64_t dims[4] = {256, 2, static_cast<cuuint64_t>(katoms), static_cast<cuuint64_t>(ceil_div(rows, 128))};
+    cuuint64_t strides[3] = {256, static_cast<cuuint64_t>(bm::SF_ATOM_BYTES),
+                             static_cast<cuuint64_t>(katoms * bm::SF_ATOM_BYTES)};
+    cuuint32_t box[4] = {256, 2, static_cast<cuuint32_t>(kps), static_cast<cuuint32_t>(row_blocks)};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(sf), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // Operand tile maps. K-major: box 64 (k) x rows; M/N-major: box 64 (m or n) x 64 (k).
 bool encode_operand(CUtensorMap *map, const void *base, bool mn_major, int64_t rows, int64_t k, int64_t ld,
                     uint32_t tile_rows)
@@ -302,7 +348,6 @@ struct Plan {
 // outputs is not capped).
 constexpr size_t kTailSplitMaxBytes = 16u << 20;
 
-int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 void set_variant(Plan &pl, int v)
 {
@@ -388,11 +433,21 @@ Plan plan_gemm(int64_t m, int64_t n, int64_t k, size_t ws_bytes, int sms, int pa
                int elem = bm::ELEM_BF16, bool beta_nonzero = false)
 {
     Plan pl;
-    const int64_t pair_tiles = ceil_div(m, 256) * ceil_div(n, 256);
     const int forced = g_tile_override.load() - 1;
-    if (forced >= 0 && (forced != kPair256 || pair_clusters > 0)) set_variant(pl, forced);
-    else if (pair_clusters > 0 && m > bm::CTA_M && n > 128 && pair_tiles * 2 >= pair_clusters) set_variant(pl, kPair256);
-    else set_variant(pl, n <= 128 ? kSingle128 : kSingle256);
+    if (elem == bm::ELEM_MXF8) {
+        // MXFP8 tiles are 128 wide: 256 x 128 on SM pairs when those tiles alone fill
+        // half the pairs, else 128 x 128 on single SMs (an override of 3 asks for the
+        // pair, 1 or 2 for single SMs)
+        const int64_t pair_tiles = ceil_div(m, 256) * ceil_div(n, 128);
+        if (forced >= 0) set_variant(pl, forced == kPair256 && pair_clusters > 0 ? kPair128Mx : kSingle128Mx);
+        else if (pair_clusters > 0 && m > bm::CTA_M && pair_tiles * 2 >= pair_clusters) set_variant(pl, kPair128Mx);
+        else set_variant(pl, kSingle128Mx);
+    } else {
+        const int64_t pair_tiles = ceil_div(m, 256) * ceil_div(n, 256);
+        if (forced >= 0 && (forced != kPair256 || pair_clusters > 0)) set_variant(pl, forced);
+        else if (pair_clusters > 0 && m > bm::CTA_M && n > 128 && pair_tiles * 2 >= pair_clusters) set_variant(pl, kPair256);
+        else set_variant(pl, n <= 128 ? kSingle128 : kSingle256);
+    }
     pl.tiles_m = ceil_div(m, pl.tile_m);
     pl.tiles_n = ceil_div(n, pl.bn);
     pl.num_tiles = pl.tiles_m * pl.tiles_n;
@@ -440,22 +495,39 @@ Plan plan_syrk(int mode, int64_t n, int64_t k, int sms, int pair_clusters, bool 
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Tensor maps of one launch: operands, C, partial slots, MXFP8 scale atoms.
+struct Maps {
+    CUtensorMap a, b, c, p, sa, sb;
+};
+
 template <int ELEM, int EPI = bm::EPI_FULL>
-cudaError_t launch_main(const cudaLaunchConfig_t &cfg, int variant, const CUtensorMap &ta, const CUtensorMap &tb,
-                        const CUtensorMap &tc, const CUtensorMap &tp, const bm::GemmParams &prm)
+cudaError_t launch_main(const cudaLaunchConfig_t &cfg, int variant, const Maps &t, const bm::GemmParams &prm)
 {
-    switch (variant) {
-    case kSingle256:
-        return cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<256, 4, 1, ELEM, 1, EPI>, ta, tb, tc, tp, prm);
-    case kSingle128:
-        return cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<128, 3, 1, ELEM, 2, EPI>, ta, tb, tc, tp, prm);
-    default:
-        return cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<256, 3, 2, ELEM, 2, EPI>, ta, tb, tc, tp, prm);
+    if constexpr (ELEM == bm::ELEM_MXF8) {
+        if (variant == kSingle128Mx)
+            return cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<128, 5, 1, ELEM, 1, EPI>, t.a, t.b, t.c, t.p,
+                                      t.sa, t.sb, prm);
+        return cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<128, 3, 2, ELEM, 2, EPI>, t.a, t.b, t.c, t.p, t.sa,
+                                  t.sb, prm);
+    } else {
+        switch (variant) {
+        case kSingle256:
+            return cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<256, 4, 1, ELEM, 1, EPI>, t.a, t.b, t.c, t.p,
+                                      t.sa, t.sb, prm);
+        case kSingle128:
+            return cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<128, 3, 1, ELEM, 2, EPI>, t.a, t.b, t.c, t.p,
+                                      t.sa, t.sb, prm);
+        default:
+            return cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<256, 3, 2, ELEM, 2, EPI>, t.a, t.b, t.c, t.p,
+                                      t.sa, t.sb, prm);
+        }
     }
 }
 
+// sa, sb: the MXFP8 scale maps (elem == ELEM_MXF8 only).
 bm_status launch(const Plan &pl, const CUtensorMap &ta, const CUtensorMap &tb, bm::GemmParams &prm,
-                 cudaStream_t stream, int sms, int elem = bm::ELEM_BF16)
+                 cudaStream_t stream, int sms, int elem = bm::ELEM_BF16, const CUtensorMap *sa = nullptr,
+                 const CUtensorMap *sb = nullptr)
 {
     // The epilogue moves C with TMA copies through a swizzled map (GEMM tiles, and
     // SYRK tiles inside the triangle). C is not prefetched into L2 ahead of the
@@ -503,12 +575,24 @@ bm_status launch(const Plan &pl, const CUtensorMap &ta, const CUtensorMap &tb, b
     // for E4M3 only the beta == 0 copy exists).
     const bool lean = prm.mode == bm::MODE_GEMM && prm.tma_c;
     cudaError_t err;
-    if (elem == bm::ELEM_E4M3 && lean && prm.beta == 0.0f)
-        err = launch_main<bm::ELEM_E4M3, bm::EPI_STORE>(cfg, pl.variant, ta, tb, tc, tp, prm);
-    else if (elem == bm::ELEM_E4M3) err = launch_main<bm::ELEM_E4M3>(cfg, pl.variant, ta, tb, tc, tp, prm);
-    else if (lean && prm.beta == 0.0f) err = launch_main<bm::ELEM_BF16, bm::EPI_STORE>(cfg, pl.variant, ta, tb, tc, tp, prm);
-    else if (lean) err = launch_main<bm::ELEM_BF16, bm::EPI_COMBINE>(cfg, pl.variant, ta, tb, tc, tp, prm);
-    else err = launch_main<bm::ELEM_BF16>(cfg, pl.variant, ta, tb, tc, tp, prm);
+    Maps t;
+    std::memset(&t, 0, sizeof(t));
+    t.a = ta;
+    t.b = tb;
+    t.c = tc;
+    t.p = tp;
+    if (sa != nullptr) t.sa = *sa;
+    if (sb != nullptr) t.sb = *sb;
+    if (elem == bm::ELEM_MXF8 && (sa == nullptr || sb == nullptr)) return BM_ERR_CUDA;
+    if (elem == bm::ELEM_MXF8 && lean && prm.beta == 0.0f)
+        err = launch_main<bm::ELEM_MXF8, bm::EPI_STORE>(cfg, pl.variant, t, prm);
+    else if (elem == bm::ELEM_MXF8) err = launch_main<bm::ELEM_MXF8>(cfg, pl.variant, t, prm);
+    else if (elem == bm::ELEM_E4M3 && lean && prm.beta == 0.0f)
+        err = launch_main<bm::ELEM_E4M3, bm::EPI_STORE>(cfg, pl.variant, t, prm);
+    else if (elem == bm::ELEM_E4M3) err = launch_main<bm::ELEM_E4M3>(cfg, pl.variant, t, prm);
+    else if (lean && prm.beta == 0.0f) err = launch_main<bm::ELEM_BF16, bm::EPI_STORE>(cfg, pl.variant, t, prm);
+    else if (lean) err = launch_main<bm::ELEM_BF16, bm::EPI_COMBINE>(cfg, pl.variant, t, prm);
+    else err = launch_main<bm::ELEM_BF16>(cfg, pl.variant, t, prm);
     if (err != cudaSuccess) {
         cudaGetLastError();
         return BM_ERR_CUDA;
@@ -529,7 +613,9 @@ bm_status launch(const Plan &pl, const CUtensorMap &ta, const CUtensorMap &tb, b
         cudaError_t re;
         switch (pl.variant) {
         case kSingle256: re = cudaLaunchKernelEx(&rc, bm::bm_splitk_reduce_kernel<128, 256>, prm); break;
-        case kSingle128: re = cudaLaunchKernelEx(&rc, bm::bm_splitk_reduce_kernel<128, 128>, prm); break;
+        case kSingle128:
+        case kSingle128Mx: re = cudaLaunchKernelEx(&rc, bm::bm_splitk_reduce_kernel<128, 128>, prm); break;
+        case kPair128Mx: re = cudaLaunchKernelEx(&rc, bm::bm_splitk_reduce_kernel<256, 128>, prm); break;
         default: re = cudaLaunchKernelEx(&rc, bm::bm_splitk_reduce_kernel<256, 256>, prm); break;
         }
         if (re != cudaSuccess) {
@@ -592,12 +678,13 @@ void export_plan(const Plan &pl, bm_plan *plan)
 }
 
 // Pair-cluster capacity for planning without a device (host-only planning): one per SM pair.
-int pair_clusters_or_default(int sms)
+int pair_clusters_or_default(int sms, bool mxfp8 = false)
 {
     int dev = -1;
     if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kMaxDevices) {
         std::lock_guard<std::mutex> lock(g_mutex);
-        if (g_devices[dev].attrs_set) return g_devices[dev].max_pair_clusters;
+        if (g_devices[dev].attrs_set)
+            return mxfp8 ? g_devices[dev].max_pair_clusters_mx : g_devices[dev].max_pair_clusters;
     }
     cudaGetLastError();
     return sms / 2;
@@ -899,6 +986,76 @@ size_t bm_gemm_e4m3_workspace_size(int64_t m, int64_t n, int64_t k)
     const int sms = sm_count_or_default();
     const Plan pl = plan_gemm(m, n, k, SIZE_MAX, sms, pair_clusters_or_default(sms), bm::ELEM_E4M3);
     return pl.k_splits > 1 ? pl.ws_bytes : 0;
+}
+
+bm_status bm_gemm_mxfp8(int64_t m, int64_t n, int64_t k, float alpha, const void *A, int64_t lda, const void *SFA,
+                        const void *B, int64_t ldb, const void *SFB, float beta, void *C, int64_t ldc,
+                        bm_ctype c_type, void *workspace, size_t workspace_bytes, bm_stream_t stream)
+{
+    // A [m, k] and B [n, k] row-major E4M3 codes (both operands K-major), scale atoms beside them
+    bm_status s = check_gemm_args(m, n, k, BM_OP_N, BM_OP_T, lda, ldb, ldc, c_type);
+    if (s != BM_OK) return s;
+    if (workspace_bytes > 0 && (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
+        return BM_ERR_WORKSPACE;
+    if (m == 0 || n == 0) return BM_OK;
+    const bool products = alpha != 0.0f && k > 0;
+    if (C == nullptr || (products && (A == nullptr || B == nullptr || SFA == nullptr || SFB == nullptr)))
+        return BM_ERR_INVALID_VALUE;
+    const int64_t esz = c_type == BM_C_BF16 ? 2 : 4;
+    if (!aligned16(C) || (ldc * esz) % 16 != 0) return BM_ERR_MISALIGNED;
+    if (products && (!aligned16(A) || !aligned16(B) || !aligned16(SFA) || !aligned16(SFB) || lda % 16 != 0 ||
+                     ldb % 16 != 0))
+        return BM_ERR_MISALIGNED;
+    DeviceState *st = nullptr;
+    s = device_state(&st);
+    if (s != BM_OK) return s;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    bm::GemmParams prm = base_params(m, n, k, alpha, beta, C, ldc, c_type, st);
+    prm.mode = bm::MODE_GEMM;
+    if (!products) return launch_scale(prm, cs, st->sm_count);
+
+    const Plan pl = plan_gemm(m, n, k, workspace != nullptr ? workspace_bytes : 0, st->sm_count,
+                              st->max_pair_clusters_mx, bm::ELEM_MXF8);
+    CUtensorMap ta, tb, tsa, tsb;
+    const uint32_t kb = static_cast<uint32_t>(bm::kblock_elems(bm::ELEM_E4M3));
+    if (!encode_operand_2d(&ta, A, bm::ELEM_E4M3, k, m, lda, kb, bm::CTA_M)) return BM_ERR_CUDA;
+    if (!encode_operand_2d(&tb, B, bm::ELEM_E4M3, k, n, ldb, kb, static_cast<uint32_t>(pl.bn / pl.pair)))
+        return BM_ERR_CUDA;
+    const int kps = kVariantStageKBlocks[pl.variant];
+    // each CTA takes the A scales of its 128 rows and the B scales of all the tile's columns
+    if (!encode_scales(&tsa, SFA, m, k, kps, 1)) return BM_ERR_CUDA;
+    if (!encode_scales(&tsb, SFB, n, k, kps, pl.bn / 128)) return BM_ERR_CUDA;
+    prm.a_mn_major = 0;
+    prm.b_mn_major = 0;
+    prm.a_box3 = encode_stage_box(&ta, A, bm::ELEM_E4M3, false, m, k, lda, bm::CTA_M, kps);
+    prm.b_box3 = encode_stage_box(&tb, B, bm::ELEM_E4M3, false, n, k, ldb, pl.bn / pl.pair, kps);
+    fill_params(prm, pl);
+    prm.partial = pl.k_splits > 1 ? static_cast<float *>(workspace) : nullptr;
+    return launch(pl, ta, tb, prm, cs, st->sm_count, bm::ELEM_MXF8, &tsa, &tsb);
+}
+
+size_t bm_gemm_mxfp8_workspace_size(int64_t m, int64_t n, int64_t k)
+{
+    if (m <= 0 || n <= 0 || k <= 0) return 0;
+    const int sms = sm_count_or_default();
+    const Plan pl = plan_gemm(m, n, k, SIZE_MAX, sms, pair_clusters_or_default(sms, true), bm::ELEM_MXF8);
+    return pl.k_splits > 1 ? pl.ws_bytes : 0;
+}
+
+bm_status bm_gemm_mxfp8_plan(int64_t m, int64_t n, int64_t k, size_t workspace_bytes, bm_plan *plan)
+{
+    if (plan == nullptr) return BM_ERR_INVALID_VALUE;
+    if (m < 0 || n < 0 || k < 0 || !fits_int32(m) || !fits_int32(n) || !fits_int32(k)) return BM_ERR_INVALID_VALUE;
+    std::memset(plan, 0, sizeof(*plan));
+    if (m == 0 || n == 0) return BM_OK;
+    if (k == 0) {
+        plan->kernels = 1;
+        return BM_OK;
+    }
+    const int sms = sm_count_or_default();
+    export_plan(plan_gemm(m, n, k, workspace_bytes, sms, pair_clusters_or_default(sms, true), bm::ELEM_MXF8), plan);
+    plan->tile_k = 128;
+    return BM_OK;
 }
 
 bm_status bm_gemm_bf16_plan(int64_t m, int64_t n, int64_t k, size_t workspace_bytes, bm_plan *plan)

@@ -63,11 +63,17 @@ enum : int { DEV_ERR_TIMEOUT = 5 };
 constexpr int CTA_M = 128;  // accumulator rows (TMEM lanes) per CTA
 constexpr int TILE_K = 64;  // bf16 elements = 128 bytes = one swizzle row (a k-block)
 constexpr int UMMA_K = 16;  // bf16 elements of one MMA = 32 bytes
-// Operand element types: bf16 (kind::f16) or FP8 E4M3 (kind::f8f6f4). A k-block
-// is 128 bytes of K either way (64 bf16 or 128 E4M3) and one MMA consumes 32
-// bytes of K, so the shared-memory layout and descriptors are the same.
-enum : int { ELEM_BF16 = 0, ELEM_E4M3 = 1 };
-__host__ __device__ constexpr int kblock_elems(int elem) { return elem == ELEM_E4M3 ? 128 : 64; }
+// Operand element types: bf16 (kind::f16), FP8 E4M3 (kind::f8f6f4), or MXFP8:
+// E4M3 with one UE8M0 scale per 32 elements of K (kind::mxf8f6f4, block-scaled).
+// A k-block is 128 bytes of K in every case (64 bf16 or 128 FP8 elements) and one
+// MMA consumes 32 bytes of K, so the shared-memory layout and descriptors are the
+// same.
+enum : int { ELEM_BF16 = 0, ELEM_E4M3 = 1, ELEM_MXF8 = 2 };
+__host__ __device__ constexpr int kblock_elems(int elem) { return elem == ELEM_BF16 ? 64 : 128; }
+// MXFP8 scale factors travel in atoms of 128 rows x 4 groups of 32 along K (one
+// k-block): 512 bytes, byte (r % 32) * 16 + (r / 32) * 4 + g for row r and group
+// g, the layout that tcgen05.cp 32x128b.warpx4 moves into tensor memory.
+constexpr int SF_ATOM_BYTES = 512;
 // Two epilogue warps per TMEM lane quadrant: warps w and w + 4 read the same 32
 // accumulator rows and split the column chunks between them.
 constexpr int NUM_EPI_WARPS = 8;
@@ -111,6 +117,8 @@ struct GemmParams {
     int fixup;
     unsigned long long *fixup_ctr;  // split tiles x PAIR x NUM_EPI_WARPS counters
     unsigned long long seq;         // this launch's tag, 1 .. 2^48 - 1
+    // MXFP8: tmSA / tmSB map the scale atoms of A and B as (256 bytes, 2, k-block,
+    // 128-row block), one box of KPS k-blocks per stage.
 };
 
 // KPS: k-blocks per ring stage. With two k-blocks a stage, the MMA thread waits
@@ -137,17 +145,30 @@ struct KernelCfg {
     static constexpr int B_OFFSET = KPS * A_BYTES;       // B tiles follow the stage's A tiles
     static constexpr int CHUNK_BYTES = KPS * 8192;      // one 64-row M/N chunk of all k-blocks of a stage
     static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
+    // MXFP8 scale factors per k-block: this CTA's A atom (its 128 rows) and the B
+    // atoms of all BN rows of the tile (each CTA of a pair holds all of them), in
+    // shared memory after the ring and, for the MMAs, in tensor memory after the two
+    // accumulators: four 32-bit columns per atom, one slot per ring k-block.
+    static constexpr bool SCALED = ELEM == ELEM_MXF8;
+    static constexpr int SF_B_ATOMS = BN / 128;
+    static constexpr int SF_KB_BYTES = SCALED ? SF_ATOM_BYTES * (1 + SF_B_ATOMS) : 0;
+    static constexpr int SF_STAGE_BYTES = KPS * SF_KB_BYTES;
+    static constexpr int SF_BYTES = STAGES * SF_STAGE_BYTES;
+    static constexpr int SF_KB_COLS = SCALED ? 4 * (1 + SF_B_ATOMS) : 0;
+    static constexpr int ACC_COLS = 2 * BN;  // two accumulators
     static constexpr int EPI_BYTES = NUM_EPI_WARPS * EPI_WARP_FLOATS * 4;
     // full, empty, acc full x2, acc empty x2, drain, C load x2 (one per epilogue half)
     static constexpr int NUM_BARS = 2 * STAGES + 7;
     static constexpr int BAR_BYTES = 8 * NUM_BARS + 16;
-    static constexpr int SMEM_BYTES = 1024 + RING_BYTES + EPI_BYTES + BAR_BYTES;
-    static constexpr int TMEM_COLS = 2 * BN;  // two accumulators
+    static constexpr int SMEM_BYTES = 1024 + RING_BYTES + SF_BYTES + EPI_BYTES + BAR_BYTES;
+    // allocation: a power of two of at least 32 columns
+    static constexpr int TMEM_COLS = SCALED ? 512 : ACC_COLS;
     static_assert(BN == 128 || BN == 256, "BN");
     static_assert(PAIR == 1 || PAIR == 2, "PAIR");
     static_assert(KPS == 1 || KPS == 2, "k-blocks per stage");
     static_assert(B_ROWS % 64 == 0, "B rows per CTA");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+    static_assert(!SCALED || ACC_COLS + STAGES * KPS * SF_KB_COLS <= TMEM_COLS, "tensor memory");
 };
 
 // ---------------------------------------------------------------- scheduling
@@ -219,9 +240,13 @@ __host__ __device__ inline void syrk_tile_coords(int mode, int64_t tiles_m, int6
     tn = mode == MODE_SYRK_LOWER ? local : r / Q + 1 + local;
 }
 
+// Kernel copies that can run SYRK: bf16 operands with every epilogue path. The
+// others (GEMM-only copies, FP8) leave the triangle order out.
+__host__ __device__ constexpr bool syrk_capable(int elem, int epi) { return elem == ELEM_BF16 && epi == EPI_FULL; }
+
 // Tile t -> (tile row, tile column): grouped raster for GEMM, the closed-form
 // triangle order above for SYRK.
-template <int TM, int BN>
+template <int TM, int BN, bool SYRK = true>
 __device__ __forceinline__ void tile_coords(const GemmParams &p, int64_t t, int64_t &tm, int64_t &tn)
 {
     tm = 0;
@@ -234,7 +259,8 @@ __device__ __forceinline__ void tile_coords(const GemmParams &p, int64_t t, int6
         const int64_t local = t - g * per_group;
         tm = first + local % rows;
         tn = local / rows;
-    } else {
+    } else if constexpr (SYRK && (BN == TM || BN == 2 * TM)) {
+        // (the 256 x 128 MXFP8 tiles never run SYRK)
         syrk_tile_coords<TM, BN>(p.mode, p.tiles_m, p.tiles_n, t, tm, tn);
     }
 }
@@ -244,7 +270,7 @@ __device__ __forceinline__ void tile_coords(const GemmParams &p, int64_t t, int6
 // fill the otherwise partly idle last wave. With the in-kernel reduction they
 // come first: the reduction then runs in the epilogue while the next tile's
 // mainloop proceeds, instead of after the last wave.
-template <int TM, int BN>
+template <int TM, int BN, bool SYRK = true>
 __device__ __forceinline__ Unit map_unit(const GemmParams &p, int64_t u)
 {
     Unit r;
@@ -265,7 +291,7 @@ __device__ __forceinline__ Unit map_unit(const GemmParams &p, int64_t u)
         r.kb1 = min(p.kb_total, r.kb0 + p.kb_per_split);
         r.slot = p.k_splits > 1 ? v : -1;
     }
-    tile_coords<TM, BN>(p, t, r.tm, r.tn);
+    tile_coords<TM, BN, SYRK>(p, t, r.tm, r.tn);
     return r;
 }
 
@@ -675,14 +701,14 @@ __device__ __forceinline__ void load_operand(uint32_t dst, const CUtensorMap *ma
 // load_operand's stage-box branch. Measured: 8 stages beat the ring's 3 at
 // K = 1024 (28.7 vs 29.5 us at 4096^2) and tie elsewhere; 32 stages made dX
 // 5 % slower.
-template <int BN, int STAGES, int PAIR, int ELEM, int KPS>
+template <int BN, int STAGES, int PAIR, int ELEM, int KPS, int EPI>
 __device__ __forceinline__ void prefetch_first_stages(const CUtensorMap *tmA, const CUtensorMap *tmB,
                                                       const GemmParams &p, uint32_t rank)
 {
     using Cfg = KernelCfg<BN, STAGES, PAIR, ELEM, KPS>;
     const int64_t u = first_unit<PAIR>();
     if (u >= p.num_units) return;
-    const Unit w = map_unit<Cfg::TILE_M, BN>(p, u);
+    const Unit w = map_unit<Cfg::TILE_M, BN, syrk_capable(ELEM, EPI)>(p, u);
     const int32_t row_a = static_cast<int32_t>(w.tm * Cfg::TILE_M + rank * CTA_M);
     const int32_t row_b = static_cast<int32_t>(w.tn * BN + rank * Cfg::B_ROWS);
     for (int s = 0, kb = w.kb0; s < 8 && kb < w.kb1; ++s, kb += KPS) {
@@ -693,8 +719,16 @@ __device__ __forceinline__ void prefetch_first_stages(const CUtensorMap *tmA, co
     }
 }
 
-template <int BN, int STAGES, int PAIR, int ELEM, int KPS>
+template <int PAIR>
+__device__ __forceinline__ void load_box4(uint32_t dst, const CUtensorMap *map, uint32_t bar, int32_t z, int32_t w)
+{
+    if constexpr (PAIR == 1) tma_load_4d(dst, map, bar, 0, 0, z, w);
+    else tma_load_4d_pair(dst, map, bar, 0, 0, z, w);
+}
+
+template <int BN, int STAGES, int PAIR, int ELEM, int KPS, int EPI>
 __device__ __forceinline__ void run_producer(const CUtensorMap *tmA, const CUtensorMap *tmB,
+                                             const CUtensorMap *tmSA, const CUtensorMap *tmSB,
                                              const GemmParams &p, uint32_t ring, uint32_t bar0, uint32_t rank,
                                              volatile int *abort_flag)
 {
@@ -705,7 +739,7 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmA, const CUten
     uint32_t armed = 0, armed_parity = 0;  // per stage: armed at least once / parity of last arming
     bool ok = true, first = true, issued_any = false;
     for (int64_t u = first_unit<PAIR>(); u < units && ok; u += unit_stride<PAIR>()) {
-        const Unit w = map_unit<Cfg::TILE_M, BN>(p, u);
+        const Unit w = map_unit<Cfg::TILE_M, BN, syrk_capable(ELEM, EPI)>(p, u);
         const int kb0 = w.kb0;
         const int kb1 = w.kb1;
         const int32_t row_a = static_cast<int32_t>(w.tm * Cfg::TILE_M + rank * CTA_M);
@@ -721,7 +755,7 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmA, const CUten
             // or unused, but their bytes still count on the barrier.
             const uint32_t full = bar0 + 8u * stage;
             if (rank == 0) {
-                mbar_arrive_expect_tx(full, static_cast<uint32_t>(Cfg::STAGE_BYTES * PAIR));
+                mbar_arrive_expect_tx(full, static_cast<uint32_t>((Cfg::STAGE_BYTES + Cfg::SF_STAGE_BYTES) * PAIR));
                 armed |= 1u << stage;
                 armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
             }
@@ -734,6 +768,14 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmA, const CUten
                                                               row_a, kb, p.syr2k_kb);
                 load_operand<PAIR, KPS, Cfg::B_ROWS, Cfg::KB_ELEMS>(sa + Cfg::B_OFFSET, tmB, tmA, p.b_box3 != 0,
                                                                     p.b_mn_major != 0, bar, row_b, kb, p.syr2k_kb);
+                if constexpr (Cfg::SCALED) {
+                    // this CTA's A scale atoms and all B scale atoms of the tile, KPS k-blocks
+                    // (boxes past K or past the last row block are zero-filled and unused)
+                    const uint32_t sf = ring + Cfg::RING_BYTES + stage * Cfg::SF_STAGE_BYTES;
+                    load_box4<PAIR>(sf, tmSA, bar, kb, row_a / 128);
+                    load_box4<PAIR>(sf + KPS * SF_ATOM_BYTES, tmSB, bar, kb,
+                                    static_cast<int32_t>(w.tn * (BN / 128)));
+                }
             }
             first = false;
             if (++stage == STAGES) {
@@ -751,7 +793,7 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmA, const CUten
     }
 }
 
-template <int BN, int STAGES, int PAIR, int ELEM, int KPS>
+template <int BN, int STAGES, int PAIR, int ELEM, int KPS, int EPI>
 // The whole warp runs the loop and waits; lane 0 issues the MMAs and commits
 // (a converged warp keeps the issue stream tighter than a lone diverged lane).
 __device__ __forceinline__ void run_mma(const GemmParams &p, uint32_t ring, uint32_t bar0, uint32_t tmem_base,
@@ -759,7 +801,7 @@ __device__ __forceinline__ void run_mma(const GemmParams &p, uint32_t ring, uint
 {
     using Cfg = KernelCfg<BN, STAGES, PAIR, ELEM, KPS>;
     const int64_t units = p.num_units;
-    const uint32_t idesc = idesc_f32acc(Cfg::TILE_M, BN, ELEM == ELEM_E4M3 ? 0u : 1u, p.a_mn_major, p.b_mn_major);
+    const uint32_t idesc = idesc_f32acc(Cfg::TILE_M, BN, ELEM == ELEM_BF16 ? 1u : 0u, p.a_mn_major, p.b_mn_major);
     // Shared-memory descriptors are built once: a template with the start address
     // left at 0, plus the address >> 4 in the low 14 bits per MMA. Shared addresses
     // are below 256 KB, so the sum never carries into the next field. Steps, in
@@ -778,7 +820,7 @@ __device__ __forceinline__ void run_mma(const GemmParams &p, uint32_t ring, uint
     uint32_t phase = 0, acc_phase = 0;
     bool ok = true, issued_any = false;
     for (int64_t u = first_unit<PAIR>(); u < units && ok; u += unit_stride<PAIR>()) {
-        const Unit w = map_unit<Cfg::TILE_M, BN>(p, u);
+        const Unit w = map_unit<Cfg::TILE_M, BN, syrk_capable(ELEM, EPI)>(p, u);
         const int kb0 = w.kb0;
         const int kb1 = w.kb1;
         const uint32_t acc_empty = bar0 + 8u * (2 * STAGES + 2 + acc);
@@ -800,13 +842,39 @@ __device__ __forceinline__ void run_mma(const GemmParams &p, uint32_t ring, uint
                 // k-block `sub` of the stage
                 const uint64_t a0 = a_tpl + (st >> 4) + a_sub * sub;
                 const uint64_t b0 = b_tpl + ((st + Cfg::B_OFFSET) >> 4) + b_sub * sub;
+                // MXFP8: the k-block's scale atoms into this ring slot's tensor-memory
+                // columns (A's, then B's), ahead of the MMAs that read them. A slot is
+                // rewritten only after the MMAs of its last use have completed: its
+                // stage's full barrier follows the empty barrier those MMAs' commit
+                // arrived on.
+                uint32_t sf_tmem = 0;
+                if constexpr (Cfg::SCALED) {
+                    const uint32_t sf = ring + Cfg::RING_BYTES + stage * Cfg::SF_STAGE_BYTES;
+                    sf_tmem = tmem_base + static_cast<uint32_t>(Cfg::ACC_COLS + (stage * KPS + sub) * Cfg::SF_KB_COLS);
+                    if (lane == 0) {
+#pragma unroll
+                        for (int at = 0; at <= Cfg::SF_B_ATOMS; ++at) {
+                            // atom 0: A's (box offset sub); atoms 1..: B's (box offset KPS + (at-1) KPS + sub)
+                            const uint32_t src = sf + static_cast<uint32_t>(
+                                (at == 0 ? sub : KPS + (at - 1) * KPS + sub) * SF_ATOM_BYTES);
+                            const uint64_t sd = smem_desc_plain(src, 16u, 128u);
+                            if constexpr (PAIR == 1) tmem_cp_32x128b_x4(sf_tmem + 4u * at, sd);
+                            else tmem_cp_32x128b_x4_pair(sf_tmem + 4u * at, sd);
+                        }
+                    }
+                }
 #pragma unroll
                 for (int kk = 0; kk < TILE_K / UMMA_K; ++kk) {
                     const uint64_t ad = a0 + a_kk * kk;
                     const uint64_t bd = b0 + b_kk * kk;
                     const uint32_t accumulate = (kb > kb0 || sub > 0 || kk > 0) ? 1u : 0u;
                     if (lane == 0) {
-                        if constexpr (ELEM == ELEM_E4M3) {
+                        if constexpr (ELEM == ELEM_MXF8) {
+                            // scale byte kk: the kk-th group of 32 elements of this k-block
+                            const uint32_t id = idesc_mxf8(Cfg::TILE_M, BN, static_cast<uint32_t>(kk));
+                            if constexpr (PAIR == 1) umma_mxf8(d_tmem, ad, bd, id, sf_tmem, sf_tmem + 4u, accumulate);
+                            else umma_mxf8_pair(d_tmem, ad, bd, id, sf_tmem, sf_tmem + 4u, accumulate);
+                        } else if constexpr (ELEM == ELEM_E4M3) {
                             if constexpr (PAIR == 1) umma_f8(d_tmem, ad, bd, idesc, accumulate);
                             else umma_f8_pair(d_tmem, ad, bd, idesc, accumulate);
                         } else {
@@ -873,7 +941,7 @@ __device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUten
     int acc = 0;
     uint32_t acc_phase = 0, c_phase = 0;
     for (int64_t u = first_unit<PAIR>(); u < units; u += unit_stride<PAIR>()) {
-        const Unit w = map_unit<Cfg::TILE_M, BN>(p, u);
+        const Unit w = map_unit<Cfg::TILE_M, BN, syrk_capable(ELEM, EPI)>(p, u);
         const bool to_slot = w.slot >= 0;
         // Paths: beta != 0 tiles of GEMM (and SYRK tiles inside the triangle) go through
         // the group path (TMA load of C, combine, TMA store); beta == 0 tiles and the
@@ -1224,6 +1292,7 @@ template <int BN, int STAGES, int PAIR, int ELEM, int KPS, int EPI = EPI_FULL>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     bm_gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                            const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmP,
+                           const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                            const GemmParams p)
 {
     using Cfg = KernelCfg<BN, STAGES, PAIR, ELEM, KPS>;
@@ -1232,8 +1301,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
     uint8_t *smem = smem_raw + pad;
     const uint32_t ring = raw + pad;  // identical offset in both CTAs of a pair
-    float *epi = reinterpret_cast<float *>(smem + Cfg::RING_BYTES);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::RING_BYTES + Cfg::EPI_BYTES);
+    float *epi = reinterpret_cast<float *>(smem + Cfg::RING_BYTES + Cfg::SF_BYTES);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::RING_BYTES + Cfg::SF_BYTES + Cfg::EPI_BYTES);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Cfg::NUM_BARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     const uint32_t bar0 = smem_addr(bars);
@@ -1259,6 +1328,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_map(&tmA);
         tma_prefetch_map(&tmB);
+        if constexpr (Cfg::SCALED) {
+            tma_prefetch_map(&tmSA);
+            tma_prefetch_map(&tmSB);
+        }
         if (p.tma_c) tma_prefetch_map(&tmC);
         if (p.store_p_tma) tma_prefetch_map(&tmP);
     }
@@ -1284,13 +1357,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // first stages into L2 (a prefetch only warms the cache, so
     // it is safe before the wait even if that kernel writes A or B).
     if (warp == 0 && lane == 0 && p.a_box3 && p.b_box3 && p.syr2k_kb == 0)
-        prefetch_first_stages<BN, STAGES, PAIR, ELEM, KPS>(&tmA, &tmB, p, rank);
+        prefetch_first_stages<BN, STAGES, PAIR, ELEM, KPS, EPI>(&tmA, &tmB, p, rank);
     griddep_wait();
 
     if (warp == 0) {
-        if (lane == 0) run_producer<BN, STAGES, PAIR, ELEM, KPS>(&tmA, &tmB, p, ring, bar0, rank, abort_flag);
+        if (lane == 0) run_producer<BN, STAGES, PAIR, ELEM, KPS, EPI>(&tmA, &tmB, &tmSA, &tmSB, p, ring, bar0, rank,
+                                                                        abort_flag);
     } else if (warp == 1) {
-        if (rank == 0) run_mma<BN, STAGES, PAIR, ELEM, KPS>(p, ring, bar0, tmem_base, abort_flag, lane);
+        if (rank == 0) run_mma<BN, STAGES, PAIR, ELEM, KPS, EPI>(p, ring, bar0, tmem_base, abort_flag, lane);
     } else {
         run_epilogue<BN, STAGES, PAIR, ELEM, KPS, EPI>(&tmC, &tmP, p, bar0, tmem_base, epi, rank,
                                        abort_flag,

@@ -209,6 +209,27 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// 4-D tiled copies (MXFP8 scale-factor atoms: several k-blocks and row blocks in one copy).
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int32_t x, int32_t y,
+                                            int32_t z, int32_t w)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const CUtensorMap *map, uint32_t cluster_bar,
+                                                 int32_t x, int32_t y, int32_t z, int32_t w)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(cluster_bar), "r"(x), "r"(y), "r"(z), "r"(w)
+        : "memory");
+}
+
 // 3-D tiled copies (stage boxes: several k-blocks or M/N chunks in one copy);
 // same completion rules as the 2-D forms above.
 // L2 prefetch of one 3-D box (no shared-memory destination, no barrier).
@@ -291,6 +312,51 @@ __device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t a_desc, uint64
         "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
+}
+
+// MXFP8: D (+)= (A . SFA) * (B . SFB), E4M3 inputs with one UE8M0 scale per 32
+// elements of K, FP32 accumulate (kind::mxf8f6f4, block_scale, scale_vec::1X). The
+// scales are read from tensor memory at sfa_tmem / sfb_tmem; the instruction
+// descriptor names the byte of each 32-bit column to use.
+__device__ __forceinline__ void umma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_mxf8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Copy of 32 rows x 16 bytes from shared memory (descriptor s_desc) into four
+// 32-bit tensor-memory columns from taddr, repeated in each of the four 32-lane
+// quadrants: the layout the block-scaled MMA reads scale factors from (row r of a
+// 128-row scale block in lane r % 32 of column r / 32, one byte per group of 32
+// along K). Asynchronous; ordered before later tcgen05.mma of the same thread.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t s_desc)
+{
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(s_desc) : "memory");
+}
+
+// Pair form, issued by CTA 0: each CTA's shared memory at the descriptor's address
+// into its own tensor memory.
+__device__ __forceinline__ void tmem_cp_32x128b_x4_pair(uint32_t taddr, uint64_t s_desc)
+{
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(s_desc) : "memory");
 }
 
 // Arrives once on `bar` when every tcgen05.mma issued so far by this thread is done.
@@ -388,6 +454,32 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
     d |= static_cast<uint64_t>(1) << 46;
     d |= static_cast<uint64_t>(2) << 61;
     return d;
+}
+
+// Shared-memory matrix descriptor without swizzle (layout 0): start address >> 4,
+// leading- and stride-dimension byte offsets >> 4, descriptor version 1. For the
+// scale-factor atoms (32 rows of 16 bytes, rows 16 bytes apart) the 8-row core
+// matrices are 128 bytes apart (SBO); there is a single 16-byte column (LBO
+// unused).
+__device__ __forceinline__ uint64_t smem_desc_plain(uint32_t saddr, uint32_t lbo, uint32_t sbo)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    return d;
+}
+
+// Instruction descriptor of the block-scaled MMA (kind::mxf8f6f4): E4M3 A and B
+// (formats 0 at bits 7-9 and 10-12), K-major, N >> 3 (bits 17-22), UE8M0 scale
+// factors (bit 23), M >> 4 (bits 24-28), and which byte of the 32-bit scale
+// columns this MMA takes: B's at bits 4-5, A's at bits 29-30 (the group of 32
+// along K within a 128-element k-block).
+__host__ __device__ constexpr uint32_t idesc_mxf8(int M, int N, uint32_t sf_byte)
+{
+    return (sf_byte << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) |
+           (static_cast<uint32_t>(M >> 4) << 24) | (sf_byte << 29);
 }
 
 // Instruction descriptor of tcgen05.mma with an FP32 accumulator: D format F32

@@ -178,6 +178,40 @@ BM_API bm_status bm_gemm_e4m3(int64_t m, int64_t n, int64_t k, float alpha, cons
 BM_API size_t bm_gemm_e4m3_workspace_size(int64_t m, int64_t n, int64_t k);
 
 /*
+ * GEMM with MXFP8 operands:  C[m x n] = alpha * (A . SA) * (B . SB)^T + beta * C
+ *
+ *   The block-scaled MXFP8 GEMM of the SM103 path in "fused A2A/GEMM Perfetto
+ *   profile protocol" (MXFP8 GEMM hot-path table; E4M3 data with one UE8M0
+ *   scale per group of 32 consecutive elements along K, "K32 quantization
+ *   group"). Element (i, p) of A stands for A[i][p] * 2^(sa - 127), where sa is
+ *   the UE8M0 code of row i's group p / 32; likewise for B. A is [m, k]
+ *   (lda >= k) and B is [n, k] (ldb >= k), row-major E4M3 codes as for
+ *   bm_gemm_e4m3 (lda, ldb multiples of 16). Products accumulate in FP32 on the
+ *   tensor cores (tcgen05.mma kind::mxf8f6f4, block-scaled); C, alpha, beta,
+ *   the workspace, BLAS rules, errors and stream behaviour are as for
+ *   bm_gemm_bf16.
+ *
+ *   Scale arrays SA (for A's m rows) and SB (for B's n rows): UE8M0 codes
+ *   (value 2^(code - 127); 255 is NaN) in the tiled layout the tensor cores
+ *   read, 16-byte aligned. They hold ceil(rows / 128) x ceil(k / 128) atoms of
+ *   512 bytes; the code of row r, group g (elements 32 g .. 32 g + 31 of the
+ *   row) is at byte
+ *       ((r / 128) * ceil(k / 128) + g / 4) * 512
+ *         + (r % 32) * 16 + ((r % 128) / 32) * 4 + g % 4.
+ *   Entries past the last row or the last group are padding: they must not be
+ *   255 (a NaN scale would turn the zeros they multiply into NaN).
+ *
+ *   Returns BM_OK once the work is queued on `stream`.
+ */
+BM_API bm_status bm_gemm_mxfp8(int64_t m, int64_t n, int64_t k, float alpha, const void *A, int64_t lda,
+                               const void *SA, const void *B, int64_t ldb, const void *SB, float beta, void *C,
+                               int64_t ldc, bm_ctype c_type, void *workspace, size_t workspace_bytes,
+                               bm_stream_t stream);
+
+/* Bytes of workspace that bm_gemm_mxfp8 would use for this shape (0 = none). */
+BM_API size_t bm_gemm_mxfp8_workspace_size(int64_t m, int64_t n, int64_t k);
+
+/*
  * SYRK:  C = alpha * op(A) * op(A)^T + beta * C   on one triangle of C[n x n]
  *
  *   op(A) is n x k: A is stored [n, k] (lda >= k) when trans == BM_OP_N
@@ -272,6 +306,8 @@ typedef struct {
 
 BM_API bm_status bm_gemm_bf16_plan(int64_t m, int64_t n, int64_t k, size_t workspace_bytes, bm_plan *plan);
 BM_API bm_status bm_syrk_bf16_plan(bm_uplo uplo, int64_t n, int64_t k, bm_plan *plan);
+/* Plan of bm_gemm_mxfp8 (tile_k = 128: one k-block is 128 E4M3 elements). */
+BM_API bm_status bm_gemm_mxfp8_plan(int64_t m, int64_t n, int64_t k, size_t workspace_bytes, bm_plan *plan);
 
 /*
  * Visit order of the output tiles of a SYRK plan (the one bm_syrk_bf16_plan

@@ -157,6 +157,38 @@ def run_gemm_e4m3(m, n, k, alpha, A, B, beta, cbuf: CBuffer, workspace=None):
     return cbuf.result()
 
 
+def mxfp8_tiled_scales(S, rows, k, pad_code=0):
+    """UE8M0 codes S [rows, >= ceil(k/32)] (row-major) in the tiled atom layout the library reads;
+    padding entries (rows past `rows`, groups past ceil(k/32)) hold pad_code."""
+    import blas3_tensor_core_gb300 as bm
+    groups = (k + 31) // 32
+    out = np.full(bm.mxfp8_scale_bytes(rows, k), pad_code, np.uint8)
+    r = np.repeat(np.arange(rows, dtype=np.int64), groups)
+    g = np.tile(np.arange(groups, dtype=np.int64), rows)
+    out[bm.mxfp8_scale_offset(r, g, k)] = np.asarray(S)[:rows, :groups].reshape(-1)
+    return out
+
+
+def run_gemm_mxfp8(m, n, k, alpha, A, SA, B, SB, beta, cbuf: CBuffer, workspace=None, pad_code=0):
+    """C = alpha * (A . SA)(B . SB)^T + beta * C; A [m, k], B [n, k] E4M3 codes (row lengths = leading
+    dimensions), SA [m, groups], SB [n, groups] UE8M0 codes, passed in the tiled layout."""
+    import blas3_tensor_core_gb300 as bm
+    t = torch()
+    dA, dB = u8_to_device(A), u8_to_device(B)
+    dSA = u8_to_device(mxfp8_tiled_scales(SA, m, k, pad_code))
+    dSB = u8_to_device(mxfp8_tiled_scales(SB, n, k, pad_code))
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    st = bm.bm_gemm_mxfp8(m, n, k, alpha, dA.data_ptr(), A.shape[1], dSA.data_ptr(), dB.data_ptr(), B.shape[1],
+                          dSB.data_ptr(), beta, cbuf.ptr, cbuf.ldc, bm.BM_C_BF16 if cbuf.bf16 else bm.BM_C_F32,
+                          ws_ptr, ws_bytes, t.cuda.current_stream().cuda_stream)
+    assert st == bm.BM_OK, bm.bm_status_string(st)
+    t.cuda.synchronize()
+    check_no_device_error()
+    return cbuf.result()
+
+
 def run_syr2k(uplo, trans, n, k, alpha, A, B, beta, cbuf: CBuffer):
     import blas3_tensor_core_gb300 as bm
     t = torch()

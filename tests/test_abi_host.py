@@ -122,6 +122,33 @@ def test_e4m3_argument_errors(lib):
     assert bm.bm_gemm_e4m3_workspace_size(4096, 4096, 4096) == 0    # 4.1 us: below the 6 us E4M3 keeps
 
 
+def test_mxfp8_argument_errors_and_plans(lib):
+    def g(m=64, n=64, k=64, A=0x1000, lda=None, SA=0x5000, B=0x2000, ldb=None, SB=0x6000, C=0x3000, ldc=None, ct=0):
+        lda = lda if lda is not None else k
+        ldb = ldb if ldb is not None else k
+        ldc = ldc if ldc is not None else n
+        return bm.bm_gemm_mxfp8(m, n, k, 1.0, A, lda, SA, B, ldb, SB, 0.0, C, ldc, ct, None, 0, None)
+    assert g(m=-1) == bm.BM_ERR_INVALID_VALUE
+    assert g(lda=32) == bm.BM_ERR_INVALID_VALUE
+    assert g(SA=0) == bm.BM_ERR_INVALID_VALUE
+    assert g(SB=0) == bm.BM_ERR_INVALID_VALUE
+    assert g(SA=0x5008) == bm.BM_ERR_MISALIGNED
+    assert g(k=72, lda=72, ldb=80) == bm.BM_ERR_MISALIGNED
+    assert g(n=0, ldc=1) == bm.BM_OK
+    # tiles 128 wide: 256 x 128 on SM pairs, 128 x 128 on single SMs; a k-block is 128 elements
+    st, p = bm.bm_gemm_mxfp8_plan(4096, 4096, 4096, 0)
+    assert st == 0 and (p.tile_m, p.tile_n, p.tile_k, p.cta_pair, p.tiles) == (256, 128, 128, 2, 16 * 32)
+    st, p = bm.bm_gemm_mxfp8_plan(256, 256, 256, 0)
+    assert (p.tile_m, p.tile_n, p.cta_pair, p.tiles) == (128, 128, 1, 4)
+    assert bm.bm_gemm_mxfp8_workspace_size(512, 512, 16384) > 0
+    # the scale-array size and the tiled layout's offsets
+    assert bm.mxfp8_scale_bytes(129, 130) == 2 * 2 * 512
+    assert bm.mxfp8_scale_offset(0, 0, 256) == 0
+    assert bm.mxfp8_scale_offset(1, 0, 256) == 16 and bm.mxfp8_scale_offset(32, 0, 256) == 4
+    assert bm.mxfp8_scale_offset(0, 1, 256) == 1 and bm.mxfp8_scale_offset(0, 4, 256) == 512
+    assert bm.mxfp8_scale_offset(128, 0, 256) == 1024
+
+
 def test_syr2k_argument_errors(lib):
     def s2(uplo=0, trans=0, n=64, k=64, A=0x1000, lda=None, B=0x2000, ldb=None, C=0x3000, ldc=None, ct=0):
         lda = lda if lda is not None else (n if trans else k)
