@@ -1123,7 +1123,7 @@ void bm_debug_inject_stall(int enable) { g_debug_stall.store(enable ? 1 : 0); }
 
 bm_status bm_set_tile_override(int variant)
 {
-    if (variant < 0 || variant > kNumVariants) return BM_ERR_INVALID_VALUE;
+    if (variant < 0 || variant > 3) return BM_ERR_INVALID_VALUE;  // 0 = automatic, 1 + kSingle256 .. kPair256
     g_tile_override.store(variant);
     return BM_OK;
 }

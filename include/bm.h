@@ -268,9 +268,10 @@ BM_API void bm_debug_inject_stall(int enable);
 /*
  * Tile override for ablations and tests (process-wide; 0 = automatic choice,
  * the default). 1: 128 x 256 tiles on single SMs; 2: 128 x 128 tiles on single
- * SMs; 3: 256 x 256 tiles on SM pairs. Results are identical up to FP32
- * summation order; only speed changes. Returns BM_ERR_INVALID_VALUE for other
- * values.
+ * SMs; 3: 256 x 256 tiles on SM pairs. bm_gemm_mxfp8, whose tiles are 128
+ * wide, takes 1 and 2 as 128 x 128 tiles on single SMs and 3 as 256 x 128 tiles
+ * on SM pairs. Results are identical up to FP32 summation order; only speed
+ * changes. Returns BM_ERR_INVALID_VALUE for other values.
  */
 BM_API bm_status bm_set_tile_override(int variant);
 
