@@ -23,7 +23,8 @@ __all__ = [
     "bm_gemm_e4m3", "bm_gemm_e4m3_workspace_size", "bm_gemm_mxfp8", "bm_gemm_mxfp8_workspace_size",
     "bm_gemm_mxfp8_plan", "mxfp8_scale_bytes", "mxfp8_scale_offset", "bm_gemm_bf16_workspace_size", "bm_get_last_device_error",
     "bm_set_wait_timeout_ms", "bm_debug_inject_stall", "bm_status_string", "bm_gemm_bf16_plan",
-    "bm_syrk_bf16_plan", "bm_syrk_bf16_tile_order", "bm_set_tile_override", "bm_version", "gemm", "syrk", "syr2k", "workspace_size",
+    "bm_syrk_bf16_plan", "bm_syrk_bf16_tile_order", "bm_syrk_bf16_workspace_size",
+    "bm_syr2k_bf16_workspace_size", "bm_set_tile_override", "bm_version", "gemm", "syrk", "syr2k", "workspace_size",
 ]
 
 BM_OK, BM_ERR_INVALID_VALUE, BM_ERR_MISALIGNED, BM_ERR_ARCH, BM_ERR_CUDA, BM_ERR_TIMEOUT, BM_ERR_WORKSPACE = range(7)
@@ -87,11 +88,15 @@ def library():
                 lib.bm_gemm_mxfp8_plan.argtypes = [_i64, _i64, _i64, _sz, ctypes.POINTER(Plan)]
                 lib.bm_gemm_mxfp8_plan.restype = _i32
                 lib.bm_syrk_bf16.argtypes = [_i32, _i32, _i64, _i64, _f32, _vp, _i64, _f32, _vp, _i64,
-                                             _i32, _vp]
+                                             _i32, _vp, _sz, _vp]
                 lib.bm_syrk_bf16.restype = _i32
                 lib.bm_syr2k_bf16.argtypes = [_i32, _i32, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp,
-                                              _i64, _i32, _vp]
+                                              _i64, _i32, _vp, _sz, _vp]
                 lib.bm_syr2k_bf16.restype = _i32
+                lib.bm_syrk_bf16_workspace_size.argtypes = [_i32, _i64, _i64]
+                lib.bm_syrk_bf16_workspace_size.restype = _sz
+                lib.bm_syr2k_bf16_workspace_size.argtypes = [_i32, _i64, _i64]
+                lib.bm_syr2k_bf16_workspace_size.restype = _sz
                 lib.bm_gemm_bf16_workspace_size.argtypes = [_i64, _i64, _i64]
                 lib.bm_gemm_bf16_workspace_size.restype = _sz
                 lib.bm_get_last_device_error.argtypes = [_vp]
@@ -104,7 +109,7 @@ def library():
                 lib.bm_status_string.restype = ctypes.c_char_p
                 lib.bm_gemm_bf16_plan.argtypes = [_i64, _i64, _i64, _sz, ctypes.POINTER(Plan)]
                 lib.bm_gemm_bf16_plan.restype = _i32
-                lib.bm_syrk_bf16_plan.argtypes = [_i32, _i64, _i64, ctypes.POINTER(Plan)]
+                lib.bm_syrk_bf16_plan.argtypes = [_i32, _i64, _i64, _sz, ctypes.POINTER(Plan)]
                 lib.bm_syrk_bf16_plan.restype = _i32
                 lib.bm_syrk_bf16_tile_order.argtypes = [_i32, _i64, _i64, _i64, _vp, _vp]
                 lib.bm_syrk_bf16_tile_order.restype = _i32
@@ -134,8 +139,18 @@ def bm_gemm_bf16_noalloc(m, n, k, transA, transB, alpha, A, lda, B, ldb, beta, C
                                           c_type, stream)
 
 
-def bm_syrk_bf16(uplo, trans, n, k, alpha, A, lda, beta, C, ldc, c_type, stream=None) -> int:
-    return library().bm_syrk_bf16(uplo, trans, n, k, alpha, A, lda, beta, C, ldc, c_type, stream)
+def bm_syrk_bf16(uplo, trans, n, k, alpha, A, lda, beta, C, ldc, c_type, workspace=None, workspace_bytes=0,
+                 stream=None) -> int:
+    return library().bm_syrk_bf16(uplo, trans, n, k, alpha, A, lda, beta, C, ldc, c_type, workspace,
+                                  workspace_bytes, stream)
+
+
+def bm_syrk_bf16_workspace_size(uplo, n, k) -> int:
+    return library().bm_syrk_bf16_workspace_size(uplo, n, k)
+
+
+def bm_syr2k_bf16_workspace_size(uplo, n, k) -> int:
+    return library().bm_syr2k_bf16_workspace_size(uplo, n, k)
 
 
 def bm_gemm_e4m3(m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, c_type, workspace=None, workspace_bytes=0,
@@ -176,8 +191,10 @@ def mxfp8_scale_offset(r, g, k):
     return ((r // 128) * katoms + g // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + g % 4
 
 
-def bm_syr2k_bf16(uplo, trans, n, k, alpha, A, lda, B, ldb, beta, C, ldc, c_type, stream=None) -> int:
-    return library().bm_syr2k_bf16(uplo, trans, n, k, alpha, A, lda, B, ldb, beta, C, ldc, c_type, stream)
+def bm_syr2k_bf16(uplo, trans, n, k, alpha, A, lda, B, ldb, beta, C, ldc, c_type, workspace=None,
+                  workspace_bytes=0, stream=None) -> int:
+    return library().bm_syr2k_bf16(uplo, trans, n, k, alpha, A, lda, B, ldb, beta, C, ldc, c_type, workspace,
+                                   workspace_bytes, stream)
 
 
 def bm_gemm_bf16_workspace_size(m, n, k) -> int:
@@ -206,9 +223,9 @@ def bm_gemm_bf16_plan(m, n, k, workspace_bytes=0):
     return st, plan
 
 
-def bm_syrk_bf16_plan(uplo, n, k):
+def bm_syrk_bf16_plan(uplo, n, k, workspace_bytes=0):
     plan = Plan()
-    st = library().bm_syrk_bf16_plan(uplo, n, k, ctypes.byref(plan))
+    st = library().bm_syrk_bf16_plan(uplo, n, k, workspace_bytes, ctypes.byref(plan))
     return st, plan
 
 
@@ -286,7 +303,13 @@ def gemm(A, B, C, alpha=1.0, beta=0.0, transA=False, transB=False, workspace=Non
     return C
 
 
-def syr2k(A, B, C, alpha=1.0, beta=0.0, uplo="L", trans=False, stream=None):
+def _ws(workspace):
+    if workspace is None:
+        return None, 0
+    return workspace.data_ptr(), workspace.numel() * workspace.element_size()
+
+
+def syr2k(A, B, C, alpha=1.0, beta=0.0, uplo="L", trans=False, workspace=None, stream=None):
     """One triangle of C = alpha * (op(A) op(B)^T + op(B) op(A)^T) + beta * C (row-major, bf16 A, B)."""
     import torch
     if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16:
@@ -302,12 +325,12 @@ def syr2k(A, B, C, alpha=1.0, beta=0.0, uplo="L", trans=False, stream=None):
     lo = BM_LOWER if str(uplo).upper().startswith("L") else BM_UPPER
     st = bm_syr2k_bf16(lo, int(bool(trans)), n, k, float(alpha), A.data_ptr(), _rowmajor_ld(A, "A"),
                        B.data_ptr(), _rowmajor_ld(B, "B"), float(beta), C.data_ptr(), _rowmajor_ld(C, "C"),
-                       _ctype(C), _stream_handle(stream))
+                       _ctype(C), *_ws(workspace), _stream_handle(stream))
     _check(st, "bm_syr2k_bf16")
     return C
 
 
-def syrk(A, C, alpha=1.0, beta=0.0, uplo="L", trans=False, stream=None):
+def syrk(A, C, alpha=1.0, beta=0.0, uplo="L", trans=False, workspace=None, stream=None):
     """One triangle of C = alpha * op(A) @ op(A)^T + beta * C (row-major, bf16 A)."""
     import torch
     if A.dtype != torch.bfloat16:
@@ -320,6 +343,7 @@ def syrk(A, C, alpha=1.0, beta=0.0, uplo="L", trans=False, stream=None):
         raise ValueError("inconsistent shapes")
     lo = BM_LOWER if str(uplo).upper().startswith("L") else BM_UPPER
     st = bm_syrk_bf16(lo, int(bool(trans)), n, k, float(alpha), A.data_ptr(), _rowmajor_ld(A, "A"),
-                      float(beta), C.data_ptr(), _rowmajor_ld(C, "C"), _ctype(C), _stream_handle(stream))
+                      float(beta), C.data_ptr(), _rowmajor_ld(C, "C"), _ctype(C), *_ws(workspace),
+                      _stream_handle(stream))
     _check(st, "bm_syrk_bf16")
     return C

@@ -474,7 +474,11 @@ Plan plan_gemm(int64_t m, int64_t n, int64_t k, size_t ws_bytes, int sms, int pa
 // SYRK / SYR2K: tiles touching the triangle. SYR2K runs both products through
 // one accumulator, and its A and B maps serve in both operand roles, so it
 // needs the variants whose A and B tiles have the same 128 rows.
-Plan plan_syrk(int mode, int64_t n, int64_t k, int sms, int pair_clusters, bool two_products = false)
+// The split rules are those of GEMM: every tile is split along K when the
+// triangle's tiles cannot fill half the GPU (a second kernel sums the partials),
+// and the tiles of an at most half-full last wave when that saves at least 6 us
+// (summed inside the kernel; SYRK tiles always take the full epilogue).
+Plan plan_syrk(int mode, int64_t n, int64_t k, size_t ws_bytes, int sms, int pair_clusters, bool two_products = false)
 {
     Plan pl;
     const int64_t tiles = ceil_div(n, 256);
@@ -489,6 +493,16 @@ Plan plan_syrk(int mode, int64_t n, int64_t k, int sms, int pair_clusters, bool 
     pl.full_tiles = pl.num_tiles;
     pl.kb_total = static_cast<int>(ceil_div(std::max<int64_t>(k, 1), bm::TILE_K)) * (two_products ? 2 : 1);
     pl.kb_per_split = pl.kb_total;
+    const int64_t slots = pl.pair == 2 ? pair_clusters : sms;
+    if (slots > 0 && pl.kb_total >= 8) {
+        if (pl.num_tiles * 2 <= slots) {
+            try_split(pl, pl.num_tiles, ceil_div(slots, pl.num_tiles), ws_bytes, kSplitMinGainUs);
+        } else {
+            const int64_t tail = pl.num_tiles % slots;
+            if (tail > 0 && tail * 2 <= slots)
+                try_split(pl, tail, slots / tail, std::min(ws_bytes, kTailSplitMaxBytes), kSplitMinGainUs);
+        }
+    }
     size_grid(pl, sms, pair_clusters);
     return pl;
 }
@@ -852,7 +866,8 @@ bm_status bm_gemm_bf16_noalloc(int64_t m, int64_t n, int64_t k, bm_op transA, bm
 }
 
 bm_status bm_syrk_bf16(bm_uplo uplo, bm_op trans, int64_t n, int64_t k, float alpha, const void *A, int64_t lda,
-                       float beta, void *C, int64_t ldc, bm_ctype c_type, bm_stream_t stream)
+                       float beta, void *C, int64_t ldc, bm_ctype c_type, void *workspace, size_t workspace_bytes,
+                       bm_stream_t stream)
 {
     if (uplo != BM_LOWER && uplo != BM_UPPER) return BM_ERR_INVALID_VALUE;
     if (n < 0 || k < 0 || !fits_int32(n) || !fits_int32(k)) return BM_ERR_INVALID_VALUE;
@@ -860,6 +875,8 @@ bm_status bm_syrk_bf16(bm_uplo uplo, bm_op trans, int64_t n, int64_t k, float al
     if (c_type != BM_C_F32 && c_type != BM_C_BF16) return BM_ERR_INVALID_VALUE;
     const int64_t need_a = trans == BM_OP_N ? k : n;
     if (lda < std::max<int64_t>(1, need_a) || ldc < std::max<int64_t>(1, n)) return BM_ERR_INVALID_VALUE;
+    if (workspace_bytes > 0 && (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
+        return BM_ERR_WORKSPACE;
     if (n == 0) return BM_OK;
     const bool products = alpha != 0.0f && k > 0;
     if (C == nullptr || (products && A == nullptr)) return BM_ERR_INVALID_VALUE;
@@ -874,7 +891,8 @@ bm_status bm_syrk_bf16(bm_uplo uplo, bm_op trans, int64_t n, int64_t k, float al
     prm.mode = uplo == BM_LOWER ? bm::MODE_SYRK_LOWER : bm::MODE_SYRK_UPPER;
     if (!products) return launch_scale(prm, cs, st->sm_count);
 
-    const Plan pl = plan_syrk(prm.mode, n, k, st->sm_count, st->max_pair_clusters);
+    const Plan pl = plan_syrk(prm.mode, n, k, workspace != nullptr ? workspace_bytes : 0, st->sm_count,
+                              st->max_pair_clusters);
     CUtensorMap ta, tb;
     const bool mn = trans == BM_OP_T;  // A stored [k][n]: both operands are M/N-major
     if (!encode_operand(&ta, A, mn, n, k, lda, bm::CTA_M)) return BM_ERR_CUDA;
@@ -885,12 +903,13 @@ bm_status bm_syrk_bf16(bm_uplo uplo, bm_op trans, int64_t n, int64_t k, float al
     prm.a_box3 = encode_stage_box(&ta, A, bm::ELEM_BF16, mn, n, k, lda, bm::CTA_M, kps);
     prm.b_box3 = encode_stage_box(&tb, A, bm::ELEM_BF16, mn, n, k, lda, pl.bn / pl.pair, kps);
     fill_params(prm, pl);
+    prm.partial = pl.k_splits > 1 ? static_cast<float *>(workspace) : nullptr;
     return launch(pl, ta, tb, prm, cs, st->sm_count);
 }
 
 bm_status bm_syr2k_bf16(bm_uplo uplo, bm_op trans, int64_t n, int64_t k, float alpha, const void *A, int64_t lda,
                         const void *B, int64_t ldb, float beta, void *C, int64_t ldc, bm_ctype c_type,
-                        bm_stream_t stream)
+                        void *workspace, size_t workspace_bytes, bm_stream_t stream)
 {
     if (uplo != BM_LOWER && uplo != BM_UPPER) return BM_ERR_INVALID_VALUE;
     if (n < 0 || k < 0 || !fits_int32(n) || !fits_int32(k)) return BM_ERR_INVALID_VALUE;
@@ -899,6 +918,8 @@ bm_status bm_syr2k_bf16(bm_uplo uplo, bm_op trans, int64_t n, int64_t k, float a
     const int64_t need = trans == BM_OP_N ? k : n;
     if (lda < std::max<int64_t>(1, need) || ldb < std::max<int64_t>(1, need) || ldc < std::max<int64_t>(1, n))
         return BM_ERR_INVALID_VALUE;
+    if (workspace_bytes > 0 && (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
+        return BM_ERR_WORKSPACE;
     if (n == 0) return BM_OK;
     const bool products = alpha != 0.0f && k > 0;
     if (C == nullptr || (products && (A == nullptr || B == nullptr))) return BM_ERR_INVALID_VALUE;
@@ -914,7 +935,8 @@ bm_status bm_syr2k_bf16(bm_uplo uplo, bm_op trans, int64_t n, int64_t k, float a
     prm.mode = uplo == BM_LOWER ? bm::MODE_SYRK_LOWER : bm::MODE_SYRK_UPPER;
     if (!products) return launch_scale(prm, cs, st->sm_count);
 
-    const Plan pl = plan_syrk(prm.mode, n, k, st->sm_count, st->max_pair_clusters, true);
+    const Plan pl = plan_syrk(prm.mode, n, k, workspace != nullptr ? workspace_bytes : 0, st->sm_count,
+                              st->max_pair_clusters, true);
     CUtensorMap ta, tb;
     const bool mn = trans == BM_OP_T;  // A, B stored [k][n]: both operands are M/N-major
     // Both maps serve as the A operand (128 rows) and the B operand (bn / pair = 128 rows).
@@ -924,10 +946,12 @@ bm_status bm_syr2k_bf16(bm_uplo uplo, bm_op trans, int64_t n, int64_t k, float a
     prm.b_mn_major = mn;
     fill_params(prm, pl);
     prm.syr2k_kb = pl.kb_total / 2;
+    prm.partial = pl.k_splits > 1 ? static_cast<float *>(workspace) : nullptr;
     // Stage boxes when no stage straddles the swap of A and B (both maps then serve
-    // as stage boxes of 128 rows in both roles).
+    // as stage boxes of 128 rows in both roles): the swap on a stage boundary, and
+    // no K split (a split may start a unit, and so its stages, at any k-block).
     const int kps = kVariantStageKBlocks[pl.variant];
-    if (prm.syr2k_kb % kps == 0) {
+    if (prm.syr2k_kb % kps == 0 && pl.k_splits == 1) {
         CUtensorMap ta3 = ta, tb3 = tb;
         if (encode_stage_box(&ta3, A, bm::ELEM_BF16, mn, n, k, lda, bm::CTA_M, kps) &&
             encode_stage_box(&tb3, B, bm::ELEM_BF16, mn, n, k, ldb, bm::CTA_M, kps)) {
@@ -1073,7 +1097,7 @@ bm_status bm_gemm_bf16_plan(int64_t m, int64_t n, int64_t k, size_t workspace_by
     return BM_OK;
 }
 
-bm_status bm_syrk_bf16_plan(bm_uplo uplo, int64_t n, int64_t k, bm_plan *plan)
+bm_status bm_syrk_bf16_plan(bm_uplo uplo, int64_t n, int64_t k, size_t workspace_bytes, bm_plan *plan)
 {
     if (plan == nullptr || (uplo != BM_LOWER && uplo != BM_UPPER)) return BM_ERR_INVALID_VALUE;
     if (n < 0 || k < 0 || !fits_int32(n) || !fits_int32(k)) return BM_ERR_INVALID_VALUE;
@@ -1084,10 +1108,28 @@ bm_status bm_syrk_bf16_plan(bm_uplo uplo, int64_t n, int64_t k, bm_plan *plan)
         return BM_OK;
     }
     const int sms = sm_count_or_default();
-    export_plan(plan_syrk(uplo == BM_LOWER ? bm::MODE_SYRK_LOWER : bm::MODE_SYRK_UPPER, n, k, sms,
+    export_plan(plan_syrk(uplo == BM_LOWER ? bm::MODE_SYRK_LOWER : bm::MODE_SYRK_UPPER, n, k, workspace_bytes, sms,
                           pair_clusters_or_default(sms)),
                 plan);
     return BM_OK;
+}
+
+size_t bm_syrk_bf16_workspace_size(bm_uplo uplo, int64_t n, int64_t k)
+{
+    if (n <= 0 || k <= 0 || (uplo != BM_LOWER && uplo != BM_UPPER)) return 0;
+    const int sms = sm_count_or_default();
+    const Plan pl = plan_syrk(uplo == BM_LOWER ? bm::MODE_SYRK_LOWER : bm::MODE_SYRK_UPPER, n, k, SIZE_MAX, sms,
+                              pair_clusters_or_default(sms));
+    return pl.k_splits > 1 ? pl.ws_bytes : 0;
+}
+
+size_t bm_syr2k_bf16_workspace_size(bm_uplo uplo, int64_t n, int64_t k)
+{
+    if (n <= 0 || k <= 0 || (uplo != BM_LOWER && uplo != BM_UPPER)) return 0;
+    const int sms = sm_count_or_default();
+    const Plan pl = plan_syrk(uplo == BM_LOWER ? bm::MODE_SYRK_LOWER : bm::MODE_SYRK_UPPER, n, k, SIZE_MAX, sms,
+                              pair_clusters_or_default(sms), true);
+    return pl.k_splits > 1 ? pl.ws_bytes : 0;
 }
 
 bm_status bm_syrk_bf16_tile_order(bm_uplo uplo, int64_t n, int64_t k, int64_t count, int64_t *tile_row,
@@ -1099,7 +1141,7 @@ bm_status bm_syrk_bf16_tile_order(bm_uplo uplo, int64_t n, int64_t k, int64_t co
     if (n == 0 || k == 0) return count == 0 ? BM_OK : BM_ERR_INVALID_VALUE;
     const int sms = sm_count_or_default();
     const int mode = uplo == BM_LOWER ? bm::MODE_SYRK_LOWER : bm::MODE_SYRK_UPPER;
-    const Plan pl = plan_syrk(mode, n, k, sms, pair_clusters_or_default(sms));
+    const Plan pl = plan_syrk(mode, n, k, 0, sms, pair_clusters_or_default(sms));
     if (count != pl.num_tiles) return BM_ERR_INVALID_VALUE;
     for (int64_t t = 0; t < count; ++t) syrk_coords(mode, pl.tiles_m, pl.tiles_n, pl.tile_m, pl.bn, t, tile_row[t], tile_col[t]);
     return BM_OK;

@@ -1064,7 +1064,7 @@ __device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUten
                 if (issuer && loading) spin_ns(100000);  // a C copy may still land in the block
                 break;
             }
-        } else if (EPI == EPI_FULL && !inside && p.tma_c) {
+        } else if (EPI == EPI_FULL && !to_slot && !inside && p.tma_c) {
             // SYRK tile across the diagonal: registers straight to C. Per chunk of 128
             // bytes per row (64 bf16 or 32 fp32 columns), lane l owns row row0 + l of
             // this warp's 32 x chunk block. A block wholly outside the triangle is

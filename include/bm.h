@@ -73,6 +73,10 @@ typedef enum {
 
 typedef enum { BM_OP_N = 0, BM_OP_T = 1 } bm_op;
 typedef enum { BM_C_F32 = 0, BM_C_BF16 = 1 } bm_ctype;
+/* The same element-type enum under the names bm_dtype, BM_F32 and BM_BF16. */
+typedef bm_ctype bm_dtype;
+#define BM_F32 BM_C_F32
+#define BM_BF16 BM_C_BF16
 typedef enum { BM_LOWER = 0, BM_UPPER = 1 } bm_uplo;
 
 /*
@@ -221,11 +225,23 @@ BM_API size_t bm_gemm_mxfp8_workspace_size(int64_t m, int64_t n, int64_t k);
  *   Tiles of C that lie entirely in the other triangle are not computed.
  *   C is [n, n] with ldc >= n.
  *
+ *   workspace / workspace_bytes: optional caller-owned device scratch for FP32
+ *   partial sums, with the rules of bm_gemm_bf16 ("Arguments + workspace" of
+ *   "BLASMp development notes", stage D; the workspace need not be
+ *   initialised): when the triangle has too few tiles to fill the GPU (small n,
+ *   long k) every tile is split along K and a second kernel sums the partials;
+ *   the tiles of a partly filled last wave may be split and summed inside the
+ *   kernel. The sums write only the referenced triangle. NULL/0 disables the
+ *   split; the size the planner would like is bm_syrk_bf16_workspace_size().
+ *
  *   Returns BM_OK once the work is queued on `stream`.
  */
 BM_API bm_status bm_syrk_bf16(bm_uplo uplo, bm_op trans, int64_t n, int64_t k, float alpha,
                               const void *A, int64_t lda, float beta, void *C, int64_t ldc,
-                              bm_ctype c_type, bm_stream_t stream);
+                              bm_ctype c_type, void *workspace, size_t workspace_bytes, bm_stream_t stream);
+
+/* Bytes of workspace that bm_syrk_bf16 would use for this shape (0 = none). */
+BM_API size_t bm_syrk_bf16_workspace_size(bm_uplo uplo, int64_t n, int64_t k);
 
 /*
  * SYR2K:  C = alpha * (op(A) * op(B)^T + op(B) * op(A)^T) + beta * C
@@ -236,13 +252,18 @@ BM_API bm_status bm_syrk_bf16(bm_uplo uplo, bm_op trans, int64_t n, int64_t k, f
  *   op(B) are n x k: A, B are stored [n, k] (lda, ldb >= k) when trans ==
  *   BM_OP_N and [k, n] (lda, ldb >= n) when trans == BM_OP_T. Both products go
  *   through one FP32 accumulator per tile; uplo, the untouched other
- *   triangle, C and the error behaviour are as for bm_syrk_bf16.
+ *   triangle, C, the workspace and the error behaviour are as for bm_syrk_bf16
+ *   (a K split divides the 2k products of a tile).
  *
  *   Returns BM_OK once the work is queued on `stream`.
  */
 BM_API bm_status bm_syr2k_bf16(bm_uplo uplo, bm_op trans, int64_t n, int64_t k, float alpha,
                                const void *A, int64_t lda, const void *B, int64_t ldb, float beta,
-                               void *C, int64_t ldc, bm_ctype c_type, bm_stream_t stream);
+                               void *C, int64_t ldc, bm_ctype c_type, void *workspace, size_t workspace_bytes,
+                               bm_stream_t stream);
+
+/* Bytes of workspace that bm_syr2k_bf16 would use for this shape (0 = none). */
+BM_API size_t bm_syr2k_bf16_workspace_size(bm_uplo uplo, int64_t n, int64_t k);
 
 /*
  * Device-side errors. Every wait inside the kernels (on a shared-memory
@@ -306,13 +327,13 @@ typedef struct {
 } bm_plan;
 
 BM_API bm_status bm_gemm_bf16_plan(int64_t m, int64_t n, int64_t k, size_t workspace_bytes, bm_plan *plan);
-BM_API bm_status bm_syrk_bf16_plan(bm_uplo uplo, int64_t n, int64_t k, bm_plan *plan);
+BM_API bm_status bm_syrk_bf16_plan(bm_uplo uplo, int64_t n, int64_t k, size_t workspace_bytes, bm_plan *plan);
 /* Plan of bm_gemm_mxfp8 (tile_k = 128: one k-block is 128 E4M3 elements). */
 BM_API bm_status bm_gemm_mxfp8_plan(int64_t m, int64_t n, int64_t k, size_t workspace_bytes, bm_plan *plan);
 
 /*
  * Visit order of the output tiles of a SYRK plan (the one bm_syrk_bf16_plan
- * reports for the same arguments), for reports and tests: tile t of the
+ * reports for the same arguments and no workspace), for reports and tests: tile t of the
  * persistent schedule covers rows tile_row[t] * tile_m ... and columns
  * tile_col[t] * tile_n ... of C. The tiles across the diagonal come first, one
  * per tile row, then the tiles inside the triangle, row by row. `count` must be

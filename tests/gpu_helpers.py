@@ -127,12 +127,19 @@ def run_gemm(m, n, k, ta, tb, alpha, A, B, beta, cbuf: CBuffer, workspace=None):
     return cbuf.result()
 
 
-def run_syrk(uplo, trans, n, k, alpha, A, beta, cbuf: CBuffer):
+def _ws_args(workspace):
+    if workspace is None:
+        return None, 0
+    return workspace.data_ptr(), workspace.numel() * workspace.element_size()
+
+
+def run_syrk(uplo, trans, n, k, alpha, A, beta, cbuf: CBuffer, workspace=None):
     import blas3_tensor_core_gb300 as bm
     t = torch()
     dA = bf16_to_device(A)
     st = bm.bm_syrk_bf16(uplo, trans, n, k, alpha, dA.data_ptr(), A.shape[1], beta, cbuf.ptr, cbuf.ldc,
-                         bm.BM_C_BF16 if cbuf.bf16 else bm.BM_C_F32, t.cuda.current_stream().cuda_stream)
+                         bm.BM_C_BF16 if cbuf.bf16 else bm.BM_C_F32, *_ws_args(workspace),
+                         t.cuda.current_stream().cuda_stream)
     assert st == bm.BM_OK, bm.bm_status_string(st)
     t.cuda.synchronize()
     check_no_device_error()
@@ -189,13 +196,13 @@ def run_gemm_mxfp8(m, n, k, alpha, A, SA, B, SB, beta, cbuf: CBuffer, workspace=
     return cbuf.result()
 
 
-def run_syr2k(uplo, trans, n, k, alpha, A, B, beta, cbuf: CBuffer):
+def run_syr2k(uplo, trans, n, k, alpha, A, B, beta, cbuf: CBuffer, workspace=None):
     import blas3_tensor_core_gb300 as bm
     t = torch()
     dA = bf16_to_device(A)
     dB = bf16_to_device(B)
     st = bm.bm_syr2k_bf16(uplo, trans, n, k, alpha, dA.data_ptr(), A.shape[1], dB.data_ptr(), B.shape[1], beta,
-                          cbuf.ptr, cbuf.ldc, bm.BM_C_BF16 if cbuf.bf16 else bm.BM_C_F32,
+                          cbuf.ptr, cbuf.ldc, bm.BM_C_BF16 if cbuf.bf16 else bm.BM_C_F32, *_ws_args(workspace),
                           t.cuda.current_stream().cuda_stream)
     assert st == bm.BM_OK, bm.bm_status_string(st)
     t.cuda.synchronize()

@@ -88,11 +88,27 @@ def test_alpha_zero_skips_operand_checks(lib):
     assert st != bm.BM_ERR_INVALID_VALUE and st != bm.BM_ERR_MISALIGNED
 
 
+def test_syrk_split_plans(lib):
+    """A triangle with too few tiles for the GPU is split along K when a workspace is given:
+    n = 512, k = 8192 has 6 tiles of 128 x 256 (4 across the diagonal, 2 inside)."""
+    for uplo in (bm.BM_LOWER, bm.BM_UPPER):
+        assert bm.bm_syrk_bf16_plan(uplo, 512, 8192, 0)[1].k_splits == 1
+        need = bm.bm_syrk_bf16_workspace_size(uplo, 512, 8192)
+        p = bm.bm_syrk_bf16_plan(uplo, 512, 8192, need)[1]
+        assert (p.tiles, p.cta_pair) == (6, 1)
+        assert p.k_splits > 1 and p.kernels == 2 and p.split_tiles == 6
+        assert p.workspace_bytes == need == p.k_splits * 6 * 128 * 256 * 4
+        assert p.ctas <= 152 and p.ctas == min(152, 6 * p.k_splits)
+    # SYR2K's k-blocks count both products
+    assert bm.bm_syr2k_bf16_workspace_size(bm.BM_LOWER, 512, 4096) > 0
+    assert bm.bm_syrk_bf16_workspace_size(bm.BM_LOWER, 512, 256) == 0      # too short to pay
+
+
 def test_syrk_argument_errors(lib):
     def s(uplo=0, trans=0, n=64, k=64, A=0x1000, lda=None, C=0x3000, ldc=None, ct=0):
         lda = lda if lda is not None else (n if trans else k)
         ldc = ldc if ldc is not None else n
-        return bm.bm_syrk_bf16(uplo, trans, n, k, 1.0, A, lda, 1.0, C, ldc, ct, None)
+        return bm.bm_syrk_bf16(uplo, trans, n, k, 1.0, A, lda, 1.0, C, ldc, ct, None, 0, None)
     assert s(uplo=3) == bm.BM_ERR_INVALID_VALUE
     assert s(trans=5) == bm.BM_ERR_INVALID_VALUE
     assert s(n=-1) == bm.BM_ERR_INVALID_VALUE
@@ -101,6 +117,9 @@ def test_syrk_argument_errors(lib):
     assert s(ldc=32) == bm.BM_ERR_INVALID_VALUE
     assert s(A=0x1002) == bm.BM_ERR_MISALIGNED
     assert s(n=0, ldc=1) == bm.BM_OK
+    assert bm.bm_syrk_bf16(0, 0, 64, 64, 1.0, 0x1000, 64, 1.0, 0x3000, 64, 0, None, 256, None) == bm.BM_ERR_WORKSPACE
+    assert bm.bm_syrk_bf16(0, 0, 64, 64, 1.0, 0x1000, 64, 1.0, 0x3000, 64, 0, 0x4010, 256, None) \
+        == bm.BM_ERR_WORKSPACE
 
 
 def test_e4m3_argument_errors(lib):
@@ -154,7 +173,7 @@ def test_syr2k_argument_errors(lib):
         lda = lda if lda is not None else (n if trans else k)
         ldb = ldb if ldb is not None else (n if trans else k)
         ldc = ldc if ldc is not None else n
-        return bm.bm_syr2k_bf16(uplo, trans, n, k, 1.0, A, lda, B, ldb, 1.0, C, ldc, ct, None)
+        return bm.bm_syr2k_bf16(uplo, trans, n, k, 1.0, A, lda, B, ldb, 1.0, C, ldc, ct, None, 0, None)
     assert s2(uplo=2) == bm.BM_ERR_INVALID_VALUE
     assert s2(trans=3) == bm.BM_ERR_INVALID_VALUE
     assert s2(k=-1) == bm.BM_ERR_INVALID_VALUE
@@ -231,8 +250,8 @@ def test_tail_split_plans(lib):
     # a last wave more than half full is not split
     p = bm.bm_gemm_bf16_plan(8192, 8192 - 1024, 4096, 1 << 30)[1]  # 32 x 28 = 896 tiles = 11 waves + 60
     assert p.split_tiles == 0 and p.k_splits == 1
-    # SYRK never splits
-    assert bm.bm_syrk_bf16_plan(bm.BM_LOWER, 8192, 4096)[1].k_splits == 1
+    # SYRK 8192 x 4096: 528 pair tiles = 6 waves + 72, a last wave more than half full
+    assert bm.bm_syrk_bf16_plan(bm.BM_LOWER, 8192, 4096, 1 << 30)[1].k_splits == 1
     assert bm.bm_gemm_bf16_plan(-1, 4, 4, 0)[0] == bm.BM_ERR_INVALID_VALUE
 
 

@@ -30,3 +30,35 @@ def test_committed_summary_names_its_hash_and_traffic():
     fields = dict(line.split(":", 1) for line in text.splitlines() if ":" in line and not line.startswith(" "))
     assert len(fields["kernel_source_sha256"].strip()) == 64
     assert float(fields["dram_bytes_per_launch"]) > 100e6  # at least the algorithmic 100.7 MB of a 4096^3 call
+
+
+def test_percentiles_interpolate_between_order_statistics():
+    import bench
+    v = [5.0, 1.0, 3.0, 2.0, 4.0]
+    assert bench.percentile(v, 0) == 1.0 and bench.percentile(v, 100) == 5.0
+    assert bench.percentile(v, 50) == 3.0
+    assert abs(bench.percentile(v, 95) - 4.8) < 1e-12
+    assert bench.percentile([7.0], 95) == 7.0
+
+
+def test_config_list_covers_every_configured_workload():
+    """C1 256^3, C2 4096^3, the ten sweep shapes, both backward GEMMs and the SYRK, each once."""
+    import bench
+    labels = [lab for lab, _ in bench.CONFIG_ORDER]
+    names = [c["name"] for _, c in bench.CONFIG_ORDER]
+    assert len(set(names)) == len(names)
+    assert labels.count("C1") == 1 and labels.count("C2") == 1 and labels.count("C3") == 10
+    assert labels.count("C4a") == labels.count("C4b") == labels.count("C5") == 1
+    sweep = {(c["m"], c["k"]) for lab, c in bench.CONFIG_ORDER if lab == "C3"}
+    assert sweep == {(mn, k) for mn in (512, 4096) for k in (256, 512, 1024, 4096, 8192)}
+    dw = dict(bench.CONFIG_ORDER)["C4b"]
+    assert (dw["m"], dw["n"], dw["k"], dw["ta"], dw["beta"], dw["std"]) == (5120, 5120, 2048, 1, 1.0, 0.02)
+    assert dict(bench.CONFIG_ORDER)["C5"]["n"] == 8192 and dict(bench.CONFIG_ORDER)["C5"]["k"] == 4096
+
+
+def test_both_arms_share_the_config_dict():
+    import bench
+    assert bench.main_config() == bench.main_config()
+    assert bench.main_config()["workload"] == bench.MAIN["name"]
+    # nothing run-specific (L2 sets, plan) inside it: those live beside it in the GPU line
+    assert not {"l2", "plan"} & set(bench.main_config())

@@ -112,3 +112,25 @@ def test_syr2k_large_lower_sampled():
     ref, bound = oracle.default().syr2k_entries(0, 0, k, 1.0, A, B, rows, cols, 1.0, c0)
     assert_parity(got[rows, cols], ref, bound, 1.0, 1.0, c0[rows, cols].astype(np.float64), False, "syr2k 4096")
     cbuf.assert_guard_intact(raw, mask_written=_mask(n, 0))
+
+
+@pytest.mark.parametrize("trans", [0, 1])
+def test_syr2k_split_k_exact(trans):
+    """n = 512, k = 4096: every tile of the triangle is split along the 2k concatenated
+    products (the split boundaries fall anywhere relative to the swap of A and B), and a
+    second kernel sums them. Exact on small integers, upper triangle."""
+    import blas3_tensor_core_gb300 as bm
+    t = torch()
+    n, k = 512, 4096
+    need = bm.bm_syr2k_bf16_workspace_size(1, n, k)
+    assert need > 0
+    A, B = _ab(n, k, trans, "int", seed=71, lo=-4, hi=4)
+    c0 = gen.integers(72, n * n, -50, 50).reshape(n, n).astype(np.float32)
+    c0 = np.tril(c0) + np.tril(c0, -1).T
+    ws = t.full((need // 4,), float("nan"), dtype=t.float32, device="cuda")
+    cbuf = CBuffer(n, n, n + 4, False, init=c0)
+    got, raw = run_syr2k(1, trans, n, k, 1.0, A, B, 1.0, cbuf, workspace=ws)
+    ref, _ = oracle.default().syr2k(1, trans, n, k, 1.0, A, B, 1.0, c0)
+    mask = _mask(n, 1)
+    assert np.array_equal(got[mask], ref[mask])
+    cbuf.assert_guard_intact(raw, mask_written=mask)

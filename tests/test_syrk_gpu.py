@@ -13,7 +13,7 @@ import pytest
 import bm_inputs as gen
 import oracle
 from gpu_helpers import (VARIANT_IDS, VARIANTS, CBuffer, assert_parity, c_input_values, operand, run_syrk,
-                         tile_samples, tile_variant, torch)
+                         tile_variant, torch)
 
 pytestmark = pytest.mark.gpu
 
@@ -83,21 +83,74 @@ def test_syrk_alpha_zero_scales_triangle_only():
     cbuf.assert_guard_intact(raw, mask_written=mask)
 
 
-def test_syrk_full_size_lower_8192x4096():
-    """C[8192, 8192] = A A^T + C, A N(0, 1) [8192, 4096], C symmetric fp32 N(0, 1), lower."""
-    n, k = 8192, 4096
-    A = operand(n, k, "normal", 1)
-    c0 = gen.symmetric_f32(n, seed=3)
-    cbuf = CBuffer(n, n, n, False, init=c0, extra_rows=1)
-    got, raw = run_syrk(0, 0, n, k, 1.0, A, 1.0, cbuf)
+def _random_workspace(nbytes, seed):
+    t = torch()
+    ws = t.empty((nbytes // 4,), dtype=t.float32, device="cuda")
+    g = t.Generator(device="cuda")
+    g.manual_seed(seed)
+    ws.view(t.int32).copy_(t.randint(-2**31, 2**31 - 1, (nbytes // 4,), dtype=t.int32, device="cuda", generator=g))
+    return ws
+
+
+@pytest.mark.parametrize("uplo,trans", list(itertools.product((0, 1), (0, 1))))
+def test_syrk_split_k_small_n_long_k_exact(uplo, trans):
+    """n = 512, k = 8192: the 6 tiles of the triangle cannot fill the GPU, so every tile is
+    split along K into the workspace (filled with random bits first) and a second kernel
+    sums the partials, writing only the triangle. Exact on small integers, twice in a row."""
+    import blas3_tensor_core_gb300 as bm
+    n, k = 512, 8192
+    need = bm.bm_syrk_bf16_workspace_size(uplo, n, k)
+    plan = bm.bm_syrk_bf16_plan(uplo, n, k, need)[1]
+    assert plan.k_splits > 1 and plan.kernels == 2
+    A = _a(n, k, trans, "int", seed=41, lo=-4, hi=4)
+    c0 = gen.integers(42, n * n, -50, 50).reshape(n, n).astype(np.float32)
+    c0 = np.tril(c0) + np.tril(c0, -1).T
+    ws = _random_workspace(need, 43)
+    ref, _ = oracle.default().syrk(uplo, trans, n, k, 1.0, A, -1.0, c0)
+    mask = _mask(n, uplo)
+    for _ in range(2):
+        cbuf = CBuffer(n, n, n + 4, False, init=c0)
+        got, raw = run_syrk(uplo, trans, n, k, 1.0, A, -1.0, cbuf, workspace=ws)
+        assert np.array_equal(got[mask], ref[mask])
+        cbuf.assert_guard_intact(raw, mask_written=mask)
+
+
+@pytest.mark.parametrize("uplo", [0, 1], ids=["lower", "upper"])
+def test_syrk_tail_split_summed_in_kernel_exact(uplo):
+    """n = 3072 on SM pairs: 12 * 13 / 2 = 78 tiles = 76 + 2; the 2 tiles of the last wave
+    are split along K and summed inside the kernel (with beta folded into split 0), which
+    writes only the triangle. Exact on small integers, with a workspace of random bits."""
+    import blas3_tensor_core_gb300 as bm
+    n, k = 3072, 4096
+    need = bm.bm_syrk_bf16_workspace_size(uplo, n, k)
+    plan = bm.bm_syrk_bf16_plan(uplo, n, k, need)[1]
+    assert plan.cta_pair == 2 and plan.tiles == 78
+    assert plan.split_tiles == 2 and plan.k_splits > 1 and plan.kernels == 1
+    A = _a(n, k, 0, "int", seed=51, lo=-3, hi=3)
+    c0 = gen.integers(52, n * n, -50, 50).reshape(n, n).astype(np.float32)
+    c0 = np.tril(c0) + np.tril(c0, -1).T
+    ws = _random_workspace(need, 53)
+    cbuf = CBuffer(n, n, n, False, init=c0)
+    got, raw = run_syrk(uplo, 0, n, k, 1.0, A, 1.0, cbuf, workspace=ws)
+    ref, _ = oracle.default().syrk(uplo, 0, n, k, 1.0, A, 1.0, c0)
+    mask = _mask(n, uplo)
+    assert np.array_equal(got[mask], ref[mask])
+    cbuf.assert_guard_intact(raw, mask_written=mask)
+
+
+@pytest.mark.parametrize("bf16_out", [False, True])
+def test_syrk_split_k_gaussian_beta(bf16_out):
+    import blas3_tensor_core_gb300 as bm
+    n, k = 400, 8000
+    need = bm.bm_syrk_bf16_workspace_size(0, n, k)
+    assert bm.bm_syrk_bf16_plan(0, n, k, need)[1].k_splits > 1
+    A = _a(n, k, 1, "normal", seed=61)
+    c0 = gen.symmetric_f32(n, seed=62)
+    c_init = gen.f32_to_bf16_bits(c0) if bf16_out else c0
+    cbuf = CBuffer(n, n, n + 8, bf16_out, init=c_init)
+    got, raw = run_syrk(0, 1, n, k, 0.5, A, -1.5, cbuf, workspace=_random_workspace(need, 63))
+    ref, bound = oracle.default().syrk(0, 1, n, k, 0.5, A, -1.5, c_init)
     mask = _mask(n, 0)
-    rows, cols = tile_samples(n, n, per_tile=4, seed=6)
-    keep = rows >= cols
-    rows, cols = rows[keep], cols[keep]
-    diag = np.arange(0, n, 97)
-    rows = np.concatenate([rows, diag])
-    cols = np.concatenate([cols, diag])
-    ref, bound = oracle.default().syrk_entries(0, 0, k, 1.0, A, rows, cols, 1.0, c0)
-    assert_parity(got[rows, cols], ref, bound, 1.0, 1.0, c0[rows, cols].astype(np.float64), False, "syrk 8192")
-    assert np.all(np.isfinite(got[mask]))
+    assert_parity(got[mask], ref[mask], bound[mask], 0.5, -1.5, c_input_values(c_init, bf16_out)[mask], bf16_out,
+                  "syrk split")
     cbuf.assert_guard_intact(raw, mask_written=mask)
