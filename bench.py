@@ -13,7 +13,8 @@ the 256^3 uniform GEMM into FP32 C, the 4096^3 GEMM, the K-sweep of section 2.3
 (K in {256, 512, 1024, 4096, 8192} x M = N in {512, 4096}), the backward pair of
 "fused A2A/GEMM Perfetto profile protocol" (dX = dY W, and dW += dY^T X with
 beta = 1 into bf16), lower SYRK 8192 x 4096 with beta = 1 into FP32, and, beyond
-those, lower SYR2K of the same size and the FP8 E4M3 and MXFP8 GEMMs at 4096^3.
+those, lower SYR2K of the same size, the FP8 E4M3 and MXFP8 GEMMs at 4096^3
+and the BF16 -> MXFP8 quantization of a 4096 x 4096 matrix.
 
 Timing: the headline is W warm-up steps, then exactly K steps between two CUDA
 events on the launching stream, bracketed by a barrier and a device
@@ -86,9 +87,10 @@ FP8 = [
 ]
 SYRK_CFG = dict(name="syrk_lower_8192x4096_f32c_beta1", n=8192, k=4096, beta=1.0)
 SYR2K_CFG = dict(name="syr2k_lower_8192x4096_f32c_beta1", n=8192, k=4096, beta=1.0, two=True)
+QUANT_CFG = dict(name="quantize_mxfp8_4096x4096_bf16", rows=4096, k=4096, quant=True)
 # (label, workload) in report order: the configured workloads C1..C5, then the extras
 CONFIG_ORDER = ([("C1", SMALL), ("C2", MAIN)] + [("C3", c) for c in SWEEP] + [("C4a", BWD[0]), ("C4b", BWD[1]),
-                ("C5", SYRK_CFG), ("extra", SYR2K_CFG)] + [("extra", c) for c in FP8])
+                ("C5", SYRK_CFG), ("extra", SYR2K_CFG)] + [("extra", c) for c in FP8] + [("extra", QUANT_CFG)])
 EXTRA = [SMALL] + BWD + FP8  # GEMM workloads beyond the sweep (for --workload)
 
 
@@ -498,7 +500,52 @@ class SyrkWorkload:
         return f"{2 if self.two else 1} n(n+1)k (lower triangle incl. diagonal)"
 
 
+class QuantWorkload:
+    """BF16 [4096, 4096] N(0, 1) -> MXFP8 codes and tiled scales, input sets rotated past L2."""
+
+    def __init__(self, cfg, torch_mod, min_total=2 * L2_BYTES):
+        import numpy as np
+        import bm_inputs as gen
+        import blas3_tensor_core_gb300 as bm
+        t = torch_mod
+        self.t, self.bm, self.cfg, self.name = t, bm, cfg, cfg["name"]
+        rows, k = cfg["rows"], cfg["k"]
+        X = gen.matrix_bf16(rows, k, "normal", seed=1)
+        dX = t.from_numpy(X.view(np.int16)).view(t.bfloat16).cuda()
+        dQ = t.empty((rows, k), dtype=t.uint8, device="cuda")
+        dS = t.empty(bm.mxfp8_scale_bytes(rows, k), dtype=t.uint8, device="cuda")
+        per_set = dX.numel() * 2 + dQ.numel() + dS.numel()
+        nsets = max(2, -(-min_total // per_set))
+        self.sets = [(dX, dQ, dS)] + [(dX.clone(), dQ.clone(), dS.clone()) for _ in range(nsets - 1)]
+        self.plan = None
+
+    def call(self, i, hh):
+        dX, dQ, dS = self.sets[i % len(self.sets)]
+        rows, k = self.cfg["rows"], self.cfg["k"]
+        st = self.bm.bm_quantize_mxfp8(rows, k, dX.data_ptr(), k, dQ.data_ptr(), k, dS.data_ptr(), hh)
+        if st != 0:
+            raise RuntimeError(f"{self.name}: {self.bm.bm_status_string(st)}")
+
+    def flops(self):
+        return 0
+
+    def bytes(self):
+        rows, k = self.cfg["rows"], self.cfg["k"]
+        return rows * k * 3 + self.bm.mxfp8_scale_bytes(rows, k)
+
+    def tensor_peak(self, peaks):
+        return peaks["bf16_tflops"]
+
+    def kind(self):
+        return "bf16 -> mxfp8 quantization"
+
+    def flop_convention(self):
+        return "none (memory-bound: 2 bytes read, 1 + 1/32 written per element)"
+
+
 def make_workload(cfg, torch_mod):
+    if cfg.get("quant"):
+        return QuantWorkload(cfg, torch_mod)
     return SyrkWorkload(cfg, torch_mod) if "m" not in cfg else GemmWorkload(cfg, torch_mod)
 
 
@@ -763,6 +810,10 @@ def config_record(label, wl, stats, peaks, b2b_ms, graph_ms):
     CUDA graph; the roofline fraction at p50 and at the back-to-back average."""
     p50 = stats["p50"] * 1e-3
     tf = wl.flops() / p50 / 1e12
+    plan = {}
+    if wl.plan is not None:
+        plan = {k: getattr(wl.plan, k) for k in ("tile_m", "tile_n", "cta_pair", "tiles", "k_splits",
+                                                  "split_tiles", "kernels", "ctas")}
     gbs = wl.bytes() / p50 / 1e9
     tpeak = wl.tensor_peak(peaks)
     frac_t, frac_h = tf / tpeak, gbs / peaks["hbm_gbs"]
@@ -772,11 +823,11 @@ def config_record(label, wl, stats, peaks, b2b_ms, graph_ms):
            "us_min": round(stats["min"] * 1e3, 3), "us_mean": round(stats["mean"] * 1e3, 3),
            "iterations": stats["n"],
            "tflops_p50": round(tf, 2), "tflops_best": round(wl.flops() / (stats["min"] * 1e-3) / 1e12, 2),
+           "gbs_best": round(wl.bytes() / (stats["min"] * 1e-3) / 1e9, 1),
            "gbs_p50": round(gbs, 1), "frac_tensor_p50": round(frac_t, 4), "frac_hbm_p50": round(frac_h, 4),
            "bound": bound, "roofline_frac_p50": round(frac_t if bound == "tensor" else frac_h, 4),
            "flops": wl.flops(), "algorithmic_bytes": wl.bytes(), "flops_convention": wl.flop_convention(),
-           "plan": {k: getattr(wl.plan, k) for k in ("tile_m", "tile_n", "cta_pair", "tiles", "k_splits",
-                                                     "split_tiles", "kernels", "ctas")}}
+           "plan": plan}
     b2b = b2b_ms * 1e-3
     rec["us_back_to_back"] = round(b2b_ms * 1e3, 3)
     rec["tflops_back_to_back"] = round(wl.flops() / b2b / 1e12, 2)

@@ -21,7 +21,7 @@ __all__ = [
     "BM_LOWER", "BM_UPPER", "Plan",
     "bm_gemm_bf16", "bm_gemm_bf16_noalloc", "BM_NOALLOC_SCRATCH_BYTES", "bm_syrk_bf16", "bm_syr2k_bf16",
     "bm_gemm_e4m3", "bm_gemm_e4m3_workspace_size", "bm_gemm_mxfp8", "bm_gemm_mxfp8_workspace_size",
-    "bm_gemm_mxfp8_plan", "mxfp8_scale_bytes", "mxfp8_scale_offset", "bm_gemm_bf16_workspace_size", "bm_get_last_device_error",
+    "bm_gemm_mxfp8_plan", "bm_quantize_mxfp8", "mxfp8_scale_bytes", "mxfp8_scale_offset", "bm_gemm_bf16_workspace_size", "bm_get_last_device_error",
     "bm_set_wait_timeout_ms", "bm_debug_inject_stall", "bm_status_string", "bm_gemm_bf16_plan",
     "bm_syrk_bf16_plan", "bm_syrk_bf16_tile_order", "bm_syrk_bf16_workspace_size",
     "bm_syr2k_bf16_workspace_size", "bm_set_tile_override", "bm_version", "gemm", "syrk", "syr2k", "workspace_size",
@@ -87,6 +87,8 @@ def library():
                 lib.bm_gemm_mxfp8_workspace_size.restype = _sz
                 lib.bm_gemm_mxfp8_plan.argtypes = [_i64, _i64, _i64, _sz, ctypes.POINTER(Plan)]
                 lib.bm_gemm_mxfp8_plan.restype = _i32
+                lib.bm_quantize_mxfp8.argtypes = [_i64, _i64, _vp, _i64, _vp, _i64, _vp, _vp]
+                lib.bm_quantize_mxfp8.restype = _i32
                 lib.bm_syrk_bf16.argtypes = [_i32, _i32, _i64, _i64, _f32, _vp, _i64, _f32, _vp, _i64,
                                              _i32, _vp, _sz, _vp]
                 lib.bm_syrk_bf16.restype = _i32
@@ -177,6 +179,10 @@ def bm_gemm_mxfp8_plan(m, n, k, workspace_bytes=0):
     plan = Plan()
     st = library().bm_gemm_mxfp8_plan(m, n, k, workspace_bytes, ctypes.byref(plan))
     return st, plan
+
+
+def bm_quantize_mxfp8(rows, k, X, ldx, Q, ldq, S, stream=None) -> int:
+    return library().bm_quantize_mxfp8(rows, k, X, ldx, Q, ldq, S, stream)
 
 
 def mxfp8_scale_bytes(rows, k) -> int:

@@ -19,6 +19,7 @@
 
 #include "bm.h"
 #include "bm_gemm_kernel.cuh"
+#include "bm_quant_kernel.cuh"
 
 namespace {
 
@@ -29,16 +30,19 @@ constexpr int kGroupM = 16;
 //   kSingle256: 128 x 256 per CTA, 4 stages of one k-block (48 KB)
 //   kSingle128: 128 x 128 per CTA, 3 stages of two k-blocks (64 KB; narrow outputs)
 //   kPair256:   256 x 256 per CTA pair (cta_group::2), 3 stages of two k-blocks (64 KB per CTA)
-// MXFP8 (the scale factors take tensor-memory columns beside the two accumulators,
-// so the tiles are 128 wide):
+// MXFP8 (the scale factors take tensor-memory columns beside the accumulators):
 //   kSingle128Mx: 128 x 128 per CTA, 5 stages of one k-block (33 KB with scales)
 //   kPair128Mx:   256 x 128 per CTA pair, 3 stages of two k-blocks (50 KB per CTA)
-enum Variant { kSingle256 = 0, kSingle128 = 1, kPair256 = 2, kSingle128Mx = 3, kPair128Mx = 4, kNumVariants = 5 };
-constexpr int kVariantBN[kNumVariants] = {256, 128, 256, 128, 128};
-constexpr int kVariantStages[kNumVariants] = {4, 3, 3, 5, 3};
-constexpr int kVariantStageKBlocks[kNumVariants] = {1, 2, 2, 1, 2};
-constexpr int kVariantPair[kNumVariants] = {1, 1, 2, 1, 2};
-bool variant_scaled(int v) { return v == kSingle128Mx || v == kPair128Mx; }
+//   kPair256Mx:   256 x 256 per CTA pair, 5 stages of one k-block (33.5 KB per CTA),
+//                 one accumulator (two 256-column ones would fill the tensor memory)
+enum Variant {
+    kSingle256 = 0, kSingle128 = 1, kPair256 = 2, kSingle128Mx = 3, kPair128Mx = 4, kPair256Mx = 5, kNumVariants = 6
+};
+constexpr int kVariantBN[kNumVariants] = {256, 128, 256, 128, 128, 256};
+constexpr int kVariantStages[kNumVariants] = {4, 3, 3, 5, 3, 5};
+constexpr int kVariantStageKBlocks[kNumVariants] = {1, 2, 2, 1, 2, 1};
+constexpr int kVariantPair[kNumVariants] = {1, 1, 2, 1, 2, 2};
+bool variant_scaled(int v) { return v >= kSingle128Mx; }
 
 struct DeviceState {
     bool ready = false;
@@ -48,7 +52,7 @@ struct DeviceState {
     int *status = nullptr;  // one int, allocated on first use
     bool attrs_set = false;
     int max_pair_clusters = 0;     // co-resident clusters of the pair kernel
-    int max_pair_clusters_mx = 0;  // same for the MXFP8 pair kernel
+    int max_pair_clusters_mx = 0;  // same for the MXFP8 pair kernels (the smaller of the two)
 };
 
 std::mutex g_mutex;
@@ -63,6 +67,7 @@ const void *variant_kernel_t(int v)
 {
     if constexpr (ELEM == bm::ELEM_MXF8) {
         if (v == kSingle128Mx) return reinterpret_cast<const void *>(&bm::bm_gemm_tcgen05_kernel<128, 5, 1, ELEM, 1, EPI>);
+        if (v == kPair256Mx) return reinterpret_cast<const void *>(&bm::bm_gemm_tcgen05_kernel<256, 5, 2, ELEM, 1, EPI>);
         return reinterpret_cast<const void *>(&bm::bm_gemm_tcgen05_kernel<128, 3, 2, ELEM, 2, EPI>);
     } else {
         switch (v) {
@@ -102,6 +107,7 @@ int variant_smem(int v)
     case kSingle128: return bm::KernelCfg<128, 3, 1, bm::ELEM_BF16, 2>::SMEM_BYTES;
     case kSingle128Mx: return bm::KernelCfg<128, 5, 1, bm::ELEM_MXF8, 1>::SMEM_BYTES;
     case kPair128Mx: return bm::KernelCfg<128, 3, 2, bm::ELEM_MXF8, 2>::SMEM_BYTES;
+    case kPair256Mx: return bm::KernelCfg<256, 5, 2, bm::ELEM_MXF8, 1>::SMEM_BYTES;
     default: return bm::KernelCfg<256, 3, 2, bm::ELEM_BF16, 2>::SMEM_BYTES;
     }
 }
@@ -142,7 +148,8 @@ bm_status init_kernel_attrs(DeviceState &st)
                                                         variant_smem(v)) != cudaSuccess)
                 return BM_ERR_CUDA;
     st.max_pair_clusters = pair_cluster_capacity(st, kPair256, 0);
-    st.max_pair_clusters_mx = pair_cluster_capacity(st, kPair128Mx, 5);
+    st.max_pair_clusters_mx =
+        std::min(pair_cluster_capacity(st, kPair128Mx, 5), pair_cluster_capacity(st, kPair256Mx, 5));
     st.attrs_set = true;
     return BM_OK;
 }
@@ -435,12 +442,17 @@ Plan plan_gemm(int64_t m, int64_t n, int64_t k, size_t ws_bytes, int sms, int pa
     Plan pl;
     const int forced = g_tile_override.load() - 1;
     if (elem == bm::ELEM_MXF8) {
-        // MXFP8 tiles are 128 wide: 256 x 128 on SM pairs when those tiles alone fill
-        // half the pairs, else 128 x 128 on single SMs (an override of 3 asks for the
-        // pair, 1 or 2 for single SMs)
-        const int64_t pair_tiles = ceil_div(m, 256) * ceil_div(n, 128);
-        if (forced >= 0) set_variant(pl, forced == kPair256 && pair_clusters > 0 ? kPair128Mx : kSingle128Mx);
-        else if (pair_clusters > 0 && m > bm::CTA_M && pair_tiles * 2 >= pair_clusters) set_variant(pl, kPair128Mx);
+        // MXFP8: 256 x 256 tiles on SM pairs when those tiles alone fill half the
+        // pairs, else 256 x 128 pair tiles if those do, else 128 x 128 tiles on
+        // single SMs (overrides: 1 the single-SM tiles, 2 the 256 x 128 pair, 3 the
+        // 256 x 256 pair)
+        const int64_t wide_tiles = ceil_div(m, 256) * ceil_div(n, 256);
+        const int64_t narrow_tiles = ceil_div(m, 256) * ceil_div(n, 128);
+        static const int kMxForced[3] = {kSingle128Mx, kPair128Mx, kPair256Mx};
+        if (forced >= 0) set_variant(pl, pair_clusters > 0 ? kMxForced[forced] : kSingle128Mx);
+        else if (pair_clusters > 0 && m > bm::CTA_M && n > 128 && wide_tiles * 2 >= pair_clusters)
+            set_variant(pl, kPair256Mx);
+        else if (pair_clusters > 0 && m > bm::CTA_M && narrow_tiles * 2 >= pair_clusters) set_variant(pl, kPair128Mx);
         else set_variant(pl, kSingle128Mx);
     } else {
         const int64_t pair_tiles = ceil_div(m, 256) * ceil_div(n, 256);
@@ -520,6 +532,9 @@ cudaError_t launch_main(const cudaLaunchConfig_t &cfg, int variant, const Maps &
     if constexpr (ELEM == bm::ELEM_MXF8) {
         if (variant == kSingle128Mx)
             return cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<128, 5, 1, ELEM, 1, EPI>, t.a, t.b, t.c, t.p,
+                                      t.sa, t.sb, prm);
+        if (variant == kPair256Mx)
+            return cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<256, 5, 2, ELEM, 1, EPI>, t.a, t.b, t.c, t.p,
                                       t.sa, t.sb, prm);
         return cudaLaunchKernelEx(&cfg, bm::bm_gemm_tcgen05_kernel<128, 3, 2, ELEM, 2, EPI>, t.a, t.b, t.c, t.p, t.sa,
                                   t.sb, prm);
@@ -630,6 +645,7 @@ bm_status launch(const Plan &pl, const CUtensorMap &ta, const CUtensorMap &tb, b
         case kSingle128:
         case kSingle128Mx: re = cudaLaunchKernelEx(&rc, bm::bm_splitk_reduce_kernel<128, 128>, prm); break;
         case kPair128Mx: re = cudaLaunchKernelEx(&rc, bm::bm_splitk_reduce_kernel<256, 128>, prm); break;
+        case kPair256Mx: re = cudaLaunchKernelEx(&rc, bm::bm_splitk_reduce_kernel<256, 256>, prm); break;
         default: re = cudaLaunchKernelEx(&rc, bm::bm_splitk_reduce_kernel<256, 256>, prm); break;
         }
         if (re != cudaSuccess) {
@@ -1064,6 +1080,49 @@ size_t bm_gemm_mxfp8_workspace_size(int64_t m, int64_t n, int64_t k)
     const int sms = sm_count_or_default();
     const Plan pl = plan_gemm(m, n, k, SIZE_MAX, sms, pair_clusters_or_default(sms, true), bm::ELEM_MXF8);
     return pl.k_splits > 1 ? pl.ws_bytes : 0;
+}
+
+bm_status bm_quantize_mxfp8(int64_t rows, int64_t k, const void *X, int64_t ldx, void *Q, int64_t ldq, void *S,
+                            bm_stream_t stream)
+{
+    if (rows < 0 || k < 0 || !fits_int32(rows) || !fits_int32(k)) return BM_ERR_INVALID_VALUE;
+    if (ldx < std::max<int64_t>(1, k) || ldq < std::max<int64_t>(1, k)) return BM_ERR_INVALID_VALUE;
+    if (rows == 0 || k == 0) return BM_OK;
+    if (X == nullptr || Q == nullptr || S == nullptr) return BM_ERR_INVALID_VALUE;
+    if (!aligned16(X) || !aligned16(Q) || !aligned16(S) || (ldx * 2) % 16 != 0 || ldq % 16 != 0)
+        return BM_ERR_MISALIGNED;
+    DeviceState *st = nullptr;
+    const bm_status s = device_state(&st);
+    if (s != BM_OK) return s;
+    bm::QuantParams p;
+    p.rows = rows;
+    p.k = k;
+    p.X = static_cast<const uint16_t *>(X);
+    p.ldx = ldx;
+    p.Q = static_cast<uint8_t *>(Q);
+    p.ldq = ldq;
+    p.S = static_cast<uint8_t *>(S);
+    p.groups = ceil_div(k, 32);
+    p.groups_pad = 4 * ceil_div(k, 128);
+    p.rows_pad = 128 * ceil_div(rows, 128);
+    // one thread per group of 32; a grid-stride loop over at most 16 blocks of 256 per SM
+    const int64_t work = p.rows_pad * p.groups_pad;
+    const int blocks =
+        static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(ceil_div(work, 256), 16 * static_cast<int64_t>(st->sm_count))));
+    cudaLaunchConfig_t rc = {};
+    cudaLaunchAttribute ra[1];
+    ra[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    ra[0].val.programmaticStreamSerializationAllowed = 1;
+    rc.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+    rc.blockDim = dim3(256, 1, 1);
+    rc.stream = reinterpret_cast<cudaStream_t>(stream);
+    rc.attrs = ra;
+    rc.numAttrs = 1;
+    if (cudaLaunchKernelEx(&rc, bm::bm_quantize_mxfp8_kernel, p) != cudaSuccess) {
+        cudaGetLastError();
+        return BM_ERR_CUDA;
+    }
+    return BM_OK;
 }
 
 bm_status bm_gemm_mxfp8_plan(int64_t m, int64_t n, int64_t k, size_t workspace_bytes, bm_plan *plan)

@@ -153,9 +153,16 @@ struct KernelCfg {
     static constexpr int SF_B_ATOMS = BN / 128;
     static constexpr int SF_KB_BYTES = SCALED ? SF_ATOM_BYTES * (1 + SF_B_ATOMS) : 0;
     static constexpr int SF_STAGE_BYTES = KPS * SF_KB_BYTES;
-    static constexpr int SF_BYTES = STAGES * SF_STAGE_BYTES;
+    // (rounded up to 1 KB: the epilogue staging blocks that follow are 128B-swizzled
+    // TMA sources and must start on 1024-byte boundaries)
+    static constexpr int SF_BYTES = (STAGES * SF_STAGE_BYTES + 1023) / 1024 * 1024;
     static constexpr int SF_KB_COLS = SCALED ? 4 * (1 + SF_B_ATOMS) : 0;
-    static constexpr int ACC_COLS = 2 * BN;  // two accumulators
+    // Two accumulators (the epilogue drains one while the MMAs fill the other),
+    // except for 256-wide MXFP8 tiles: two 256-column accumulators fill the tensor
+    // memory, so those tiles use one and the next tile's MMAs wait until the
+    // epilogue has read it (its stores still overlap the next mainloop).
+    static constexpr int NUM_ACC = (SCALED && BN == 256) ? 1 : 2;
+    static constexpr int ACC_COLS = NUM_ACC * BN;
     static constexpr int EPI_BYTES = NUM_EPI_WARPS * EPI_WARP_FLOATS * 4;
     // full, empty, acc full x2, acc empty x2, drain, C load x2 (one per epilogue half)
     static constexpr int NUM_BARS = 2 * STAGES + 7;
@@ -168,6 +175,7 @@ struct KernelCfg {
     static_assert(KPS == 1 || KPS == 2, "k-blocks per stage");
     static_assert(B_ROWS % 64 == 0, "B rows per CTA");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+    static_assert((RING_BYTES + SF_BYTES) % 1024 == 0 && EPI_WARP_FLOATS * 4 % 1024 == 0, "swizzled staging alignment");
     static_assert(!SCALED || ACC_COLS + STAGES * KPS * SF_KB_COLS <= TMEM_COLS, "tensor memory");
 };
 
@@ -773,8 +781,7 @@ __device__ __forceinline__ void run_producer(const CUtensorMap *tmA, const CUten
                     // (boxes past K or past the last row block are zero-filled and unused)
                     const uint32_t sf = ring + Cfg::RING_BYTES + stage * Cfg::SF_STAGE_BYTES;
                     load_box4<PAIR>(sf, tmSA, bar, kb, row_a / 128);
-                    load_box4<PAIR>(sf + KPS * SF_ATOM_BYTES, tmSB, bar, kb,
-                                    static_cast<int32_t>(w.tn * (BN / 128)));
+                    load_box4<PAIR>(sf + KPS * SF_ATOM_BYTES, tmSB, bar, kb, static_cast<int32_t>(w.tn * (BN / 128)));
                 }
             }
             first = false;
@@ -901,7 +908,7 @@ __device__ __forceinline__ void run_mma(const GemmParams &p, uint32_t ring, uint
             if constexpr (PAIR == 1) umma_commit(bar0 + 8u * (2 * STAGES + acc));
             else umma_commit_pair(bar0 + 8u * (2 * STAGES + acc), 0x3);
         }
-        if (++acc == 2) {
+        if (++acc == Cfg::NUM_ACC) {
             acc = 0;
             acc_phase ^= 1u;
         }
@@ -1279,7 +1286,7 @@ __device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUten
         }
         if (to_slot && p.fixup) fixup_region<Cfg::TILE_M, BN, PAIR>(p, w.tm, w.tn, w.slot, rank, quad, half, warp, lane);
         }
-        if (++acc == 2) {
+        if (++acc == Cfg::NUM_ACC) {
             acc = 0;
             acc_phase ^= 1u;
         }

@@ -216,6 +216,33 @@ BM_API bm_status bm_gemm_mxfp8(int64_t m, int64_t n, int64_t k, float alpha, con
 BM_API size_t bm_gemm_mxfp8_workspace_size(int64_t m, int64_t n, int64_t k);
 
 /*
+ * MXFP8 quantization of a BF16 matrix: X[rows x k] -> E4M3 codes Q[rows x k]
+ * and UE8M0 scales S, one per group of 32 consecutive elements of a row.
+ *
+ *   The "W quantize BF16 -> MXFP8" step of the SM103 MXFP8 path in "fused
+ *   A2A/GEMM Perfetto profile protocol" (per group of 32: amax reduction, UE8M0
+ *   scale, E4M3 conversion). The page names the steps; the rule is the OCP
+ *   Microscaling (MX) v1.0 conversion: shared exponent e = floor(log2(amax)) - 8
+ *   (8 is the largest E4M3 exponent), clamped to [-127, 127], scale code
+ *   e + 127; each element is X / 2^e rounded to the nearest E4M3 value, ties to
+ *   even, magnitudes beyond 448 saturated to 448. A group of zeros gets code 0;
+ *   a group holding a NaN or an infinity gets code 255 (NaN) and NaN elements
+ *   (0x7F). The last group of a row may be shorter than 32.
+ *
+ *   X is row-major bf16 with ldx >= k (ldx * 2 a multiple of 16 bytes); Q is
+ *   row-major E4M3 with ldq >= k (a multiple of 16); Q's bytes past column k
+ *   are not written. S receives ceil(rows / 128) x ceil(k / 128) atoms of 512
+ *   bytes in the tiled layout of bm_gemm_mxfp8 (padding entries are set to 0),
+ *   so Q and S feed bm_gemm_mxfp8 directly as A and SA, or as B and SB. All
+ *   three pointers are device memory, 16-byte aligned, and must not overlap.
+ *   Errors and stream behaviour as for bm_gemm_bf16.
+ *
+ *   Returns BM_OK once the work is queued on `stream`.
+ */
+BM_API bm_status bm_quantize_mxfp8(int64_t rows, int64_t k, const void *X, int64_t ldx, void *Q, int64_t ldq,
+                                   void *S, bm_stream_t stream);
+
+/*
  * SYRK:  C = alpha * op(A) * op(A)^T + beta * C   on one triangle of C[n x n]
  *
  *   op(A) is n x k: A is stored [n, k] (lda >= k) when trans == BM_OP_N
@@ -289,10 +316,10 @@ BM_API void bm_debug_inject_stall(int enable);
 /*
  * Tile override for ablations and tests (process-wide; 0 = automatic choice,
  * the default). 1: 128 x 256 tiles on single SMs; 2: 128 x 128 tiles on single
- * SMs; 3: 256 x 256 tiles on SM pairs. bm_gemm_mxfp8, whose tiles are 128
- * wide, takes 1 and 2 as 128 x 128 tiles on single SMs and 3 as 256 x 128 tiles
- * on SM pairs. Results are identical up to FP32 summation order; only speed
- * changes. Returns BM_ERR_INVALID_VALUE for other values.
+ * SMs; 3: 256 x 256 tiles on SM pairs. bm_gemm_mxfp8 takes 1 as 128 x 128
+ * tiles on single SMs, 2 as 256 x 128 tiles on SM pairs and 3 as 256 x 256
+ * tiles on SM pairs. Results are identical up to FP32 summation order; only
+ * speed changes. Returns BM_ERR_INVALID_VALUE for other values.
  */
 BM_API bm_status bm_set_tile_override(int variant);
 

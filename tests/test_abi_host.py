@@ -156,7 +156,10 @@ def test_mxfp8_argument_errors_and_plans(lib):
     assert g(n=0, ldc=1) == bm.BM_OK
     # tiles 128 wide: 256 x 128 on SM pairs, 128 x 128 on single SMs; a k-block is 128 elements
     st, p = bm.bm_gemm_mxfp8_plan(4096, 4096, 4096, 0)
-    assert st == 0 and (p.tile_m, p.tile_n, p.tile_k, p.cta_pair, p.tiles) == (256, 128, 128, 2, 16 * 32)
+    assert st == 0 and (p.tile_m, p.tile_n, p.tile_k, p.cta_pair, p.tiles) == (256, 256, 128, 2, 16 * 16)
+    assert (p.stages, p.stage_kblocks) == (5, 1)
+    st, p = bm.bm_gemm_mxfp8_plan(1024, 2048, 4096, 0)   # 32 wide tiles: too few; 64 narrow ones fill
+    assert (p.tile_m, p.tile_n, p.cta_pair, p.tiles) == (256, 128, 2, 64)
     st, p = bm.bm_gemm_mxfp8_plan(256, 256, 256, 0)
     assert (p.tile_m, p.tile_n, p.cta_pair, p.tiles) == (128, 128, 1, 4)
     assert bm.bm_gemm_mxfp8_workspace_size(512, 512, 16384) > 0
@@ -166,6 +169,22 @@ def test_mxfp8_argument_errors_and_plans(lib):
     assert bm.mxfp8_scale_offset(1, 0, 256) == 16 and bm.mxfp8_scale_offset(32, 0, 256) == 4
     assert bm.mxfp8_scale_offset(0, 1, 256) == 1 and bm.mxfp8_scale_offset(0, 4, 256) == 512
     assert bm.mxfp8_scale_offset(128, 0, 256) == 1024
+
+
+def test_quantize_argument_errors(lib):
+    def q(rows=64, k=64, X=0x1000, ldx=None, Q=0x2000, ldq=None, S=0x3000):
+        ldx = ldx if ldx is not None else k
+        ldq = ldq if ldq is not None else k
+        return bm.bm_quantize_mxfp8(rows, k, X, ldx, Q, ldq, S, None)
+    assert q(rows=-1) == bm.BM_ERR_INVALID_VALUE
+    assert q(ldx=32) == bm.BM_ERR_INVALID_VALUE
+    assert q(ldq=32) == bm.BM_ERR_INVALID_VALUE
+    assert q(S=0) == bm.BM_ERR_INVALID_VALUE
+    assert q(X=0x1008) == bm.BM_ERR_MISALIGNED
+    assert q(k=36, ldx=36, ldq=48) == bm.BM_ERR_MISALIGNED       # 72-byte bf16 rows
+    assert q(k=40, ldx=48, ldq=40) == bm.BM_ERR_MISALIGNED       # E4M3 rows not a multiple of 16
+    assert q(S=0x3004) == bm.BM_ERR_MISALIGNED
+    assert q(rows=0) == bm.BM_OK and q(k=0, ldx=1, ldq=1) == bm.BM_OK
 
 
 def test_syr2k_argument_errors(lib):
