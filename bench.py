@@ -962,7 +962,7 @@ def workload_only(args, dist):
     ms = timed_steps(wl, args.steps, args.warmup, dist)
     t = ms / args.steps * 1e-3
     return {"workload": cfg["name"], "us_per_step": round(t * 1e6, 3), "tflops": round(wl.flops() / t / 1e12, 2),
-            "steps": args.steps, "warmup": args.warmup, "plan": wl.plan.as_dict()}
+            "steps": args.steps, "warmup": args.warmup, "plan": wl.plan.as_dict() if wl.plan is not None else None}
 
 
 def main(argv=None):
