@@ -383,3 +383,73 @@ def test_persistent_many_tiles_exact(variant):
     ref_rows, _ = orc().gemm_entries(k, 0, 0, 1.0, A, B, full_rows, full_cols)
     assert np.array_equal(got[full_rows, full_cols], ref_rows)
     cbuf.assert_guard_intact(raw)
+
+
+@pytest.mark.parametrize("variant", [0, 3], ids=["auto", "pair256x256"])
+@pytest.mark.parametrize("beta,bf16_out", [(0.0, True), (-1.0, False)], ids=["beta0_bf16", "beta-1_f32"])
+def test_every_tile_split_exact_and_replayed(variant, beta, bf16_out):
+    """512 x 512 x 8192: too few tiles for the GPU, so every tile is split along K and a
+    second kernel sums the partials. The workspace holds random bits before the first call;
+    a CUDA graph of the call is then replayed three times with new inputs. Small integers
+    make every result exact, into bf16 C with beta = 0 and FP32 C with beta = -1."""
+    import blas3_tensor_core_gb300 as bm
+    from gpu_helpers import bf16_to_device, device_to_numpy
+    t = torch()
+    m, n, k = 512, 512, 8192
+    with tile_variant(variant):
+        need = bm.bm_gemm_bf16_workspace_size(m, n, k)
+        plan = bm.bm_gemm_bf16_plan(m, n, k, need)[1]
+        assert plan.split_tiles == plan.tiles and plan.k_splits > 1 and plan.kernels == 2
+        assert need == plan.k_splits * plan.tiles * plan.tile_m * plan.tile_n * 4
+        ws = t.empty((need // 4,), dtype=t.float32, device="cuda")
+        g = t.Generator(device="cuda")
+        g.manual_seed(7)
+        ws.view(t.int32).copy_(t.randint(-2**31, 2**31 - 1, (need // 4,), dtype=t.int32, device="cuda", generator=g))
+        dA = t.empty((m, k), dtype=t.bfloat16, device="cuda")
+        dB = t.empty((k, n), dtype=t.bfloat16, device="cuda")
+        dC = t.empty((m, n), dtype=t.bfloat16 if bf16_out else t.float32, device="cuda")
+        ct = bm.BM_C_BF16 if bf16_out else bm.BM_C_F32
+
+        def call(h):
+            assert bm.bm_gemm_bf16(m, n, k, 0, 0, 1.0, dA.data_ptr(), k, dB.data_ptr(), n, beta, dC.data_ptr(), n,
+                                   ct, ws.data_ptr(), need, h) == bm.BM_OK
+
+        def check(seed):
+            A = operand(m, k, "int", seed, lo=-4, hi=4)
+            B = operand(k, n, "int", seed + 1, lo=-4, hi=4)
+            c0 = gen.integers(seed + 2, m * n, -40, 40).reshape(m, n).astype(np.float32)
+            dA.copy_(bf16_to_device(A))
+            dB.copy_(bf16_to_device(B))
+            dC.copy_(t.from_numpy(c0).cuda().to(dC.dtype))
+            return A, B, c0
+
+        def compare(A, B, c0, what):
+            got = (gen.bf16_bits_to_f32(device_to_numpy(dC)) if bf16_out else dC.cpu().numpy()).astype(np.float64)
+            ref, _ = orc().gemm(m, n, k, 0, 0, 1.0, A, B, beta, c0 if beta != 0 else None)
+            if bf16_out:
+                ref = gen.bf16_bits_to_f32(gen.f32_to_bf16_bits(ref.astype(np.float32))).astype(np.float64)
+            assert np.array_equal(got, ref), what
+
+        h = t.cuda.current_stream().cuda_stream
+        for rep in range(2):
+            A, B, c0 = check(300 + rep)
+            call(h)
+            t.cuda.synchronize()
+            assert bm.bm_get_last_device_error(h) == bm.BM_OK
+            compare(A, B, c0, f"eager call {rep}")
+        side = t.cuda.Stream()
+        side.wait_stream(t.cuda.current_stream())
+        with t.cuda.stream(side):
+            call(side.cuda_stream)
+        t.cuda.current_stream().wait_stream(side)
+        t.cuda.synchronize()
+        graph = t.cuda.CUDAGraph()
+        with t.cuda.graph(graph):
+            call(t.cuda.current_stream().cuda_stream)
+        for rep in range(3):
+            A, B, c0 = check(400 + rep)
+            graph.replay()
+            t.cuda.synchronize()
+            assert bm.bm_get_last_device_error(h) == bm.BM_OK
+            compare(A, B, c0, f"graph replay {rep}")
+        del graph
