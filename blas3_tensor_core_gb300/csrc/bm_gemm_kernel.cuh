@@ -509,6 +509,28 @@ __device__ __forceinline__ void stage_row_bf16(uint4 *srow, const uint32_t (&r)[
     }
 }
 
+// 64 fp32 accumulator values of a row (times alpha) as 32 packed bf16 pairs, in
+// column order (the lower half of each word is the even column).
+template <bool SCALE>
+__device__ __forceinline__ void pack_row_bf16(uint32_t (&h)[32], const uint32_t (&r)[64], float alpha)
+{
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const float x0 = __uint_as_float(r[2 * i]);
+        const float x1 = __uint_as_float(r[2 * i + 1]);
+        const __nv_bfloat162 b = SCALE ? __floats2bfloat162_rn(alpha * x0, alpha * x1) : __floats2bfloat162_rn(x0, x1);
+        h[i] = *reinterpret_cast<const uint32_t *>(&b);
+    }
+}
+
+// A row of 32 packed bf16 pairs (128 bytes) into the 128B-swizzled staging block:
+// 16-byte unit j of row `lane` goes to slot j ^ (lane & 7).
+__device__ __forceinline__ void stage_row_packed(uint4 *srow, const uint32_t (&h)[32], int lane)
+{
+#pragma unroll
+    for (int j = 0; j < 8; ++j) srow[j ^ (lane & 7)] = make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
+}
+
 template <bool SCALE>
 __device__ __forceinline__ void stage_row_f32(uint4 *srow, const uint32_t (&r)[64], float alpha, int lane)
 {
@@ -1168,44 +1190,84 @@ __device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUten
             const int nchunks = BN / cw;
             const uint32_t stage_addr = smem_addr(stage_buf);
             const int64_t slot_row = to_slot ? w.slot * Cfg::TILE_M + rank * CTA_M + quad * 32 : 0;
-            for (int c = half; c < nchunks; c += 2) {
-                uint32_t r[64];
-                tmem_load_32cols(taddr + static_cast<uint32_t>(c * cw), *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-                if (bf16_out)
-                    tmem_load_32cols(taddr + static_cast<uint32_t>(c * cw + 32),
-                                     *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
-                if (c + 2 >= nchunks) {  // this warp's last chunk of the tile: release the accumulator
-                    tc_fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) {
-                        const uint32_t acc_empty = bar0 + 8u * (2 * STAGES + 2 + acc);
-                        if constexpr (PAIR == 1) mbar_arrive(acc_empty);
-                        else mbar_arrive_remote(map_shared_to_rank(acc_empty, 0));
-                    }
+            constexpr bool kReadAllFirst = BN == 256 && EPI == EPI_STORE;
+            if (kReadAllFirst && bf16_out) {
+                // Both chunks of this warp (64-column chunks half and half + 2) are read from
+                // tensor memory and packed to bf16 before any store, so the accumulator goes
+                // back to the MMA warp without waiting behind a store: the C stores queue on
+                // the SM's TMA unit with the operand copies, and with short K the next tile's
+                // MMAs are ready long before the stores have drained.
+                uint32_t h[2][32];
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    uint32_t r[64];
+                    const uint32_t col = static_cast<uint32_t>((half + 2 * j) * 64);
+                    tmem_load_32cols(taddr + col, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+                    tmem_load_32cols(taddr + col + 32u, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+                    if (p.alpha == 1.0f) pack_row_bf16<false>(h[j], r, p.alpha);
+                    else pack_row_bf16<true>(h[j], r, p.alpha);
                 }
-                if (lane == 0) bulk_wait_group_read0();  // the previous store has read the staging block
-                __syncwarp();
-                uint4 *srow = reinterpret_cast<uint4 *>(stage_buf) + lane * 8;
-                // (alpha == 1 skips the multiplies: fewer instructions for the warps that
-                // share sub-partitions with the producer and MMA warps)
-                if (bf16_out) {
-                    if (p.alpha == 1.0f) stage_row_bf16<false>(srow, r, p.alpha, lane);
-                    else stage_row_bf16<true>(srow, r, p.alpha, lane);
-                } else {
-                    if (p.alpha == 1.0f) stage_row_f32<false>(srow, r, p.alpha, lane);
-                    else stage_row_f32<true>(srow, r, p.alpha, lane);
-                }
-                fence_proxy_async_shared();
+                tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) {
-                    if (to_slot) {
-                        tma_store_2d(map, stage_addr, c * cw, static_cast<int32_t>(slot_row));
+                    const uint32_t acc_empty = bar0 + 8u * (2 * STAGES + 2 + acc);
+                    if constexpr (PAIR == 1) mbar_arrive(acc_empty);
+                    else mbar_arrive_remote(map_shared_to_rank(acc_empty, 0));
+                }
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    if (lane == 0) bulk_wait_group_read0();  // the previous store has read the staging block
+                    __syncwarp();
+                    stage_row_packed(reinterpret_cast<uint4 *>(stage_buf) + lane * 8, h[j], lane);
+                    fence_proxy_async_shared();
+                    __syncwarp();
+                    const int64_t cx = col0 + static_cast<int64_t>(half + 2 * j) * 64;
+                    if (lane == 0 && row0 < p.m && cx < p.n) {
+                        tma_store_2d(map, stage_addr, static_cast<int32_t>(cx), static_cast<int32_t>(row0));
                         bulk_commit_group();
+                    }
+                }
+            } else {
+                for (int c = half; c < nchunks; c += 2) {
+                    uint32_t r[64];
+                    tmem_load_32cols(taddr + static_cast<uint32_t>(c * cw),
+                                     *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+                    if (bf16_out)
+                        tmem_load_32cols(taddr + static_cast<uint32_t>(c * cw + 32),
+                                         *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+                    if (c + 2 >= nchunks) {  // this warp's last chunk of the tile: release the accumulator
+                        tc_fence_before_sync();
+                        __syncwarp();
+                        if (lane == 0) {
+                            const uint32_t acc_empty = bar0 + 8u * (2 * STAGES + 2 + acc);
+                            if constexpr (PAIR == 1) mbar_arrive(acc_empty);
+                            else mbar_arrive_remote(map_shared_to_rank(acc_empty, 0));
+                        }
+                    }
+                    if (lane == 0) bulk_wait_group_read0();  // the previous store has read the staging block
+                    __syncwarp();
+                    uint4 *srow = reinterpret_cast<uint4 *>(stage_buf) + lane * 8;
+                    // (alpha == 1 skips the multiplies: fewer instructions for the warps that
+                    // share sub-partitions with the producer and MMA warps)
+                    if (bf16_out) {
+                        if (p.alpha == 1.0f) stage_row_bf16<false>(srow, r, p.alpha, lane);
+                        else stage_row_bf16<true>(srow, r, p.alpha, lane);
                     } else {
-                        const int64_t cx = col0 + static_cast<int64_t>(c) * cw;
-                        if (row0 < p.m && cx < p.n) {
-                            tma_store_2d(map, stage_addr, static_cast<int32_t>(cx), static_cast<int32_t>(row0));
+                        if (p.alpha == 1.0f) stage_row_f32<false>(srow, r, p.alpha, lane);
+                        else stage_row_f32<true>(srow, r, p.alpha, lane);
+                    }
+                    fence_proxy_async_shared();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (to_slot) {
+                            tma_store_2d(map, stage_addr, c * cw, static_cast<int32_t>(slot_row));
                             bulk_commit_group();
+                        } else {
+                            const int64_t cx = col0 + static_cast<int64_t>(c) * cw;
+                            if (row0 < p.m && cx < p.n) {
+                                tma_store_2d(map, stage_addr, static_cast<int32_t>(cx), static_cast<int32_t>(row0));
+                                bulk_commit_group();
+                            }
                         }
                     }
                 }
@@ -1291,7 +1353,10 @@ __device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUten
             acc_phase ^= 1u;
         }
     }
-    if ((p.tma_c || p.store_p_tma) && issuer) bulk_wait_group0();  // stores done before exit
+    // Every thread that issued bulk stores (lane 0 of each warp in the per-warp path,
+    // the half's issuer in the group path) waits for them: the CTA's shared memory
+    // must outlive the copies that read it.
+    if ((p.tma_c || p.store_p_tma) && lane == 0) bulk_wait_group0();
 }
 
 // ---------------------------------------------------------------- kernels
