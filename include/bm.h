@@ -363,8 +363,12 @@ BM_API bm_status bm_gemm_mxfp8_plan(int64_t m, int64_t n, int64_t k, size_t work
  * reports for the same arguments and no workspace), for reports and tests: tile t of the
  * persistent schedule covers rows tile_row[t] * tile_m ... and columns
  * tile_col[t] * tile_n ... of C. The tiles across the diagonal come first, one
- * per tile row, then the tiles inside the triangle, row by row. `count` must be
- * the plan's `tiles`; the two arrays are host memory of `count` elements.
+ * per tile row, then the tiles inside the triangle. With square tiles
+ * (tile_m == tile_n) those go in groups of 16 tile rows of the lower triangle,
+ * each group column by column and each column's rows in order; the upper
+ * triangle takes the transpose (groups of 16 tile columns, each row by row).
+ * With 128 x 256 tiles they go row by row. `count` must be the plan's `tiles`;
+ * the two arrays are host memory of `count` elements.
  */
 BM_API bm_status bm_syrk_bf16_tile_order(bm_uplo uplo, int64_t n, int64_t k, int64_t count, int64_t *tile_row,
                                          int64_t *tile_col);

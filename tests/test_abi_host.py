@@ -317,9 +317,12 @@ def test_tile_override_values(lib):
         assert bm.bm_set_tile_override(0) == bm.BM_OK
 
 
-def _syrk_order_bruteforce(n, lower, tm_, tn_):
+def _syrk_order_bruteforce(n, lower, tm_, tn_, group=16):
     """The schedule written out by enumeration: per tile row the tile that crosses the
-    diagonal, then per row the tiles wholly inside the triangle (nominal tile extents)."""
+    diagonal, then the tiles wholly inside the triangle (nominal tile extents). Inside
+    tiles: with square tiles, groups of `group` tile rows of the lower triangle, each
+    column by column (rows in order within a column), and for the upper triangle the
+    transpose of that; with 128 x 256 tiles, row by row."""
     rows_t, cols_t = (n + tm_ - 1) // tm_, (n + tn_ - 1) // tn_
     cross, inside = [], []
     for r in range(rows_t):
@@ -331,14 +334,28 @@ def _syrk_order_bruteforce(n, lower, tm_, tn_):
                 inside.append((r, c))
             elif touches:
                 cross.append((r, c))
+    if tm_ == tn_:
+        members = set(inside)
+        grouped = []
+        for r0 in range(0, rows_t, group):
+            r1 = min(r0 + group, rows_t)
+            for c in range(cols_t):
+                for r in range(r0, r1):
+                    t = (r, c) if lower else (c, r)
+                    if t in members:
+                        grouped.append(t)
+        assert sorted(grouped) == sorted(inside)
+        inside = grouped
     return cross + inside
 
 
-@pytest.mark.parametrize("n", [1, 200, 256, 300, 1000, 1024, 4096, 8192, 12288 + 100, 16384])
+@pytest.mark.parametrize("n", [1, 200, 256, 300, 1000, 1024, 2200, 4096, 4352, 8192, 12288 + 100, 16384, 33000])
 @pytest.mark.parametrize("variant", [1, 2, 3], ids=["single128x256", "single128x128", "pair256x256"])
 def test_syrk_tile_order_closed_form(lib, n, variant):
     """Every tile index of the kernel's closed-form SYRK schedule maps to the tile the
-    enumeration puts there: the diagonal-crossing tiles first, then the inside ones."""
+    enumeration puts there: the diagonal-crossing tiles first, then the inside ones
+    (grouped for square tiles). Sizes cover one group, a partial last group (including
+    one of a single tile row) and many groups."""
     import numpy as np
     assert bm.bm_set_tile_override(variant) == bm.BM_OK
     try:
