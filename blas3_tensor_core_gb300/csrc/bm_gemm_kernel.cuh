@@ -1029,6 +1029,11 @@ __device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUten
     const bool issuer = quad == 0 && lane == 0;  // issues this half's TMA copies in the group path
     int acc = 0;
     uint32_t acc_phase = 0, c_phase = 0;
+    // This half's staging block has nothing in flight: no unit yet, or the last unit
+    // took the group path (its stores have read the block and the half has met).
+    // After other paths a warp of the half may still be using its own staging area
+    // inside the block.
+    bool block_free = true;
     for (int64_t u = first_unit<PAIR>(); u < units; u += unit_stride<PAIR>()) {
         const Unit w = map_unit<Cfg::TILE_M, BN, syrk_capable(ELEM, EPI)>(p, u);
         const bool to_slot = w.slot >= 0;
@@ -1046,12 +1051,26 @@ __device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUten
         const bool warp_tma = EPI == EPI_STORE   ? !to_slot || slot_tma
                               : EPI == EPI_COMBINE ? to_slot && slot_tma
                                                    : (to_slot ? slot_tma : (!beta_nonzero && p.tma_c && inside));
+        // Group path: this half's staging block and C-load barrier. When the block is
+        // free, the tile's first chunk of C is loaded before the accumulator is ready,
+        // so that its latency overlaps the tile's last MMAs instead of the epilogue.
+        uint8_t *block = reinterpret_cast<uint8_t *>(epi) + half * GROUP_BLOCK_BYTES;
+        const uint32_t block_addr = smem_addr(block);
+        const uint32_t cbar = bar0 + 8u * (2 * STAGES + 5 + half);
+        const int32_t ys = static_cast<int32_t>(w.tm * Cfg::TILE_M + rank * CTA_M);
+        const int32_t xs0 = static_cast<int32_t>(w.tn * BN + static_cast<int64_t>(half) * (p.c_bf16 ? 64 : 32));
+        const bool pre = group && block_free && issuer && ys < p.m && xs0 < p.n;
+        if (pre) {
+            mbar_arrive_expect_tx(cbar, GROUP_BLOCK_BYTES);
+            tma_load_2d(block_addr, tmC, cbar, xs0, ys);
+        }
         bool ready = wait_warp<PAIR == 2>(bar0 + 8u * (2 * STAGES + acc), acc_phase, abort_flag, p.timeout_ns);
         // A half that will meet at named barriers decides together, so that none of its
         // warps is left waiting at one.
         if (group) ready = group_all(ready, group_bar, 128);
         if (!ready) {
             if (lane == 0) signal_timeout(p, abort_flag);
+            if (pre) spin_ns(100000);  // the C copy may still land in the block
             break;
         }
         tc_fence_after_sync();
@@ -1075,17 +1094,13 @@ __device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUten
             const bool bf16_out = p.c_bf16 != 0;
             const int cw = bf16_out ? 64 : 32;
             const int nchunks = BN / cw;
-            uint8_t *block = reinterpret_cast<uint8_t *>(epi) + half * GROUP_BLOCK_BYTES;
-            const uint32_t block_addr = smem_addr(block);
             uint4 *myrow = reinterpret_cast<uint4 *>(block + (quad * 32 + lane) * 128);
-            const int32_t ys = static_cast<int32_t>(w.tm * Cfg::TILE_M + rank * CTA_M);
             const bool rows_in = ys < p.m;
-            const uint32_t cbar = bar0 + 8u * (2 * STAGES + 5 + half);
-            bool gok = true, loading = false;
+            bool gok = true, loading = pre;
             for (int c = half; c < nchunks; c += 2) {
                 const int32_t xs = static_cast<int32_t>(col0 + static_cast<int64_t>(c) * cw);
                 const bool live = rows_in && xs < p.n;  // the same for the whole half
-                if (issuer && live) {
+                if (issuer && live && !(c == half && pre)) {  // (or it went out before the wait)
                     mbar_arrive_expect_tx(cbar, GROUP_BLOCK_BYTES);
                     tma_load_2d(block_addr, map, cbar, xs, ys);
                     loading = true;
@@ -1408,6 +1423,7 @@ __device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUten
         }
         if (to_slot && p.fixup) fixup_region<Cfg::TILE_M, BN, PAIR>(p, w.tm, w.tn, w.slot, rank, quad, half, warp, lane);
         }
+        block_free = group;
         if (++acc == Cfg::NUM_ACC) {
             acc = 0;
             acc_phase ^= 1u;
