@@ -402,6 +402,12 @@ void size_grid(Plan &pl, int sms, int pair_clusters)
 constexpr double kKBlockUs = 0.256;
 constexpr double kSplitMinGainUs = 6.0;
 constexpr double kTailSplitMinGainUsBeta0 = 3.5;
+// At most this many K splits when every tile is split. Measured on the 8 tiles
+// (128 x 256) of a 512^2 output: 512^2 x 4096 ran 14.9 us with 16 splits, 12.2
+// with 13 (what this cap gives) and 12.5 with 11; 512^2 x 8192 17.2 us with 19
+// splits, 16.7 with 16, 14.2 with 13 and 14.4 with 12. More splits shorten each
+// unit's mainloop but write and re-read more fp32 partial tiles.
+constexpr int64_t kMaxAllSplits = 14;
 
 void try_split(Plan &pl, int64_t split_tiles, int64_t want, size_t budget, double min_gain_us)
 {
@@ -471,7 +477,8 @@ Plan plan_gemm(int64_t m, int64_t n, int64_t k, size_t ws_bytes, int sms, int pa
     if (slots > 0 && pl.kb_total >= 8) {
         if (pl.num_tiles * 2 <= slots) {
             // Too few tiles to fill half the GPU: split every tile along K.
-            try_split(pl, pl.num_tiles, ceil_div(slots, pl.num_tiles), ws_bytes, kSplitMinGainUs);
+            try_split(pl, pl.num_tiles, std::min(kMaxAllSplits, ceil_div(slots, pl.num_tiles)), ws_bytes,
+                      kSplitMinGainUs);
         } else {
             // The last wave is at most half full: split its tiles along K over the idle slots.
             const int64_t tail = pl.num_tiles % slots;

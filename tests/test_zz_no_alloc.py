@@ -134,12 +134,12 @@ def test_without_split_and_with_beta():
 
 
 def test_full_split_beyond_the_array_splits_fewer_ways():
-    """512 x 512 x 8192: a 19-way split of the 8 tiles would need 19.9 MB of partials; within
-    the 16 MiB array the planner splits 16 ways, as bm_gemm_bf16 does with a 16 MiB workspace.
+    """512 x 1024 x 8192: a 10-way split of the 16 tiles would need 21.0 MB of partials; within
+    the 16 MiB array the planner splits 8 ways, as bm_gemm_bf16 does with a 16 MiB workspace.
     Both entry points then run the same plan, so they agree bit for bit, twice in a row."""
     import blas3_tensor_core_gb300 as bm
     t = torch()
-    m, n, k = 512, 512, 8192
+    m, n, k = 512, 1024, 8192
     assert bm.bm_gemm_bf16_workspace_size(m, n, k) > bm.BM_NOALLOC_SCRATCH_BYTES
     plan = bm.bm_gemm_bf16_plan(m, n, k, bm.BM_NOALLOC_SCRATCH_BYTES)[1]
     assert plan.k_splits > 1 and plan.workspace_bytes <= bm.BM_NOALLOC_SCRATCH_BYTES
