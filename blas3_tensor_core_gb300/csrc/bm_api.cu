@@ -408,6 +408,13 @@ constexpr double kTailSplitMinGainUsBeta0 = 3.5;
 // splits, 16.7 with 16, 14.2 with 13 and 14.4 with 12. More splits shorten each
 // unit's mainloop but write and re-read more fp32 partial tiles.
 constexpr int64_t kMaxAllSplits = 14;
+// BF16 GEMMs of at most this many 64-deep k-blocks (K <= 320) run on single-SM
+// 128 x 256 tiles rather than 256 x 256 SM-pair tiles. Measured, pair -> single:
+// 4096^2 x 128 / 256 / 320 13.9 / 15.3 / 16.4 -> 10.9 / 13.3 / 15.3 us; 8192^2 x 256
+// 45.3 -> 37.2 us; 2048^2 x 256 8.1 -> 6.6 us; 8192 x 4096 x 256 23.3 -> 20.6 us.
+// From K = 384 on the pair tiles are faster (4096^2 x 384 16.8 vs 17.1 us, x 512
+// 18.1 vs 19.8 us, 8192^2 x 512 50.2 vs 58.6 us).
+constexpr int64_t kShortKBlocks = 5;
 
 void try_split(Plan &pl, int64_t split_tiles, int64_t want, size_t budget, double min_gain_us)
 {
@@ -463,8 +470,13 @@ Plan plan_gemm(int64_t m, int64_t n, int64_t k, size_t ws_bytes, int sms, int pa
         else set_variant(pl, kSingle128Mx);
     } else {
         const int64_t pair_tiles = ceil_div(m, 256) * ceil_div(n, 256);
+        // BF16 with at most kShortKBlocks k-blocks per tile takes single-SM tiles:
+        // with so few k-blocks the pair's cross-SM handshakes cost more than its
+        // smaller operand traffic saves.
+        const bool short_k = elem == bm::ELEM_BF16 && ceil_div(std::max<int64_t>(k, 1), bm::TILE_K) <= kShortKBlocks;
         if (forced >= 0 && (forced != kPair256 || pair_clusters > 0)) set_variant(pl, forced);
-        else if (pair_clusters > 0 && m > bm::CTA_M && n > 128 && pair_tiles * 2 >= pair_clusters) set_variant(pl, kPair256);
+        else if (pair_clusters > 0 && !short_k && m > bm::CTA_M && n > 128 && pair_tiles * 2 >= pair_clusters)
+            set_variant(pl, kPair256);
         else set_variant(pl, n <= 128 ? kSingle128 : kSingle256);
     }
     pl.tiles_m = ceil_div(m, pl.tile_m);
