@@ -39,9 +39,10 @@
 //                     loads of C (beta != 0) and stores; the SYRK triangle and
 //                     the ragged edges of that path are masked per element.
 // Tiles are handed out persistently (cluster c takes units c, c + clusters,
-// ...), in grouped-raster order for GEMM and row by row over the referenced
-// triangle for SYRK (tiles strictly on the other side of the diagonal are never
-// visited).
+// ...), in grouped-raster order for GEMM and, for SYRK, over the referenced
+// triangle only: the tiles across the diagonal first, then the inside tiles in
+// groups of tile rows (tiles strictly on the other side of the diagonal are
+// never visited).
 //
 // Every barrier wait is bounded: after the wait limit the thread records
 // BM_ERR_TIMEOUT in the device status word and raises a shared abort flag that
@@ -613,6 +614,23 @@ __device__ __forceinline__ bool full_vector(const GemmParams &p, int64_t i, int6
     return all;
 }
 
+// Does the 32 x 32 block at rows r0.., columns c0.. lie wholly outside the
+// referenced SYRK triangle (lower: every column > every row; upper: the mirror)?
+__device__ __forceinline__ bool block_outside_triangle(int mode, int64_t r0, int64_t c0)
+{
+    if (mode == MODE_SYRK_LOWER) return r0 + 31 < c0;
+    if (mode == MODE_SYRK_UPPER) return r0 > c0 + 31;
+    return false;
+}
+
+// Does C[i, j..j+3] lie wholly outside the referenced SYRK triangle?
+__device__ __forceinline__ bool vector_outside_triangle(int mode, int64_t i, int64_t j)
+{
+    if (mode == MODE_SYRK_LOWER) return j > i;
+    if (mode == MODE_SYRK_UPPER) return j + 3 < i;
+    return false;
+}
+
 // ---------------------------------------------------------------- in-kernel split-K reduction
 // One arrival at a region counter. The value is (tag << 16) | arrivals; a tag
 // other than this launch's (a reset counter, a launch that stopped early, or
@@ -1009,11 +1027,11 @@ __device__ __forceinline__ void run_mma(const GemmParams &p, uint32_t ring, uint
 }
 
 // EPI selects the epilogue paths compiled in. EPI_FULL has them all (SYRK needs
-// the direct path for tiles across the diagonal). The GEMM copies leave that path
-// out, which keeps them free of register spills: EPI_STORE (beta == 0) stores
-// whole tiles with per-warp TMA stores, EPI_COMBINE (beta != 0) through the
-// group path; split units take the slot-map TMA stores, or the transposing path
-// with the in-kernel sum.
+// the triangle masks of the transposing path for tiles across the diagonal). The
+// GEMM copies keep only what they use, which keeps them free of register spills:
+// EPI_STORE (beta == 0) stores whole tiles with per-warp TMA stores, EPI_COMBINE
+// (beta != 0) through the group path; split units take the slot-map TMA stores,
+// or the transposing path with the in-kernel sum.
 template <int BN, int STAGES, int PAIR, int ELEM, int KPS, int EPI = EPI_FULL>
 __device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUtensorMap *tmP, const GemmParams &p,
                                              uint32_t bar0, uint32_t tmem_base, float *epi, uint32_t rank,
@@ -1040,8 +1058,8 @@ __device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUten
         // Paths: beta != 0 tiles of GEMM (and SYRK tiles inside the triangle) go through
         // the group path (TMA load of C, combine, TMA store); beta == 0 tiles and the
         // split units of the reduce-kernel plan through the per-warp TMA-store path; SYRK
-        // tiles across the diagonal through the direct path from registers; split units
-        // of the in-kernel reduction through the per-warp transposing path.
+        // tiles across the diagonal, split units of the in-kernel reduction and calls
+        // without a C tensor map through the per-warp transposing path.
         const bool inside = tile_inside_triangle<Cfg::TILE_M, BN>(p.mode, w.tm, w.tn);
         const bool group = EPI == EPI_COMBINE ? !to_slot
                                               : EPI == EPI_FULL && !to_slot && beta_nonzero && p.tma_c && inside;
@@ -1168,92 +1186,6 @@ __device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUten
                 if (issuer && loading) spin_ns(100000);  // a C copy may still land in the block
                 break;
             }
-        } else if (EPI == EPI_FULL && !to_slot && !inside && p.tma_c) {
-            // SYRK tile across the diagonal: registers straight to C. Per chunk of 128
-            // bytes per row (64 bf16 or 32 fp32 columns), lane l owns row row0 + l of
-            // this warp's 32 x chunk block. A block wholly outside the triangle is
-            // skipped; one wholly inside (and inside m x n) moves with 16-byte loads
-            // and stores; the block on the diagonal (and any block at the edge of C)
-            // goes element by element. The other triangle is neither read nor written.
-            const bool bf16_out = p.c_bf16 != 0;
-            const int cw = bf16_out ? 64 : 32;
-            const int nchunks = BN / cw;
-            const int64_t gi = row0 + lane;
-            const bool lower = p.mode == MODE_SYRK_LOWER;
-            for (int c = half; c < nchunks; c += 2) {
-                // 32 columns at a time: [xp, xp + 32) of rows [row0, row0 + 32)
-                for (int part = 0; part < cw / 32; ++part) {
-                    const int64_t xp = col0 + static_cast<int64_t>(c) * cw + 32 * part;
-                    const bool outside = lower ? row0 + 31 < xp : row0 > xp + 31;
-                    const bool full = (lower ? row0 >= xp + 31 : row0 + 31 <= xp) && row0 + 32 <= p.m &&
-                                      xp + 32 <= p.n;
-                    uint32_t r[32];
-                    if (!outside) tmem_load_32cols(taddr + static_cast<uint32_t>(c * cw + 32 * part), r);
-                    if (c + 2 >= nchunks && part == cw / 32 - 1) {  // this warp's accumulator part is read
-                        tc_fence_before_sync();
-                        __syncwarp();
-                        if (lane == 0) {
-                            const uint32_t acc_empty = bar0 + 8u * (2 * STAGES + 2 + acc);
-                            if constexpr (PAIR == 1) mbar_arrive(acc_empty);
-                            else mbar_arrive_remote(map_shared_to_rank(acc_empty, 0));
-                        }
-                    }
-                    if (outside) continue;
-                    if (full && bf16_out) {
-                        uint4 *row = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.C) + gi * p.ldc + xp);
-                        uint4 old[4];
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) old[j] = beta_nonzero ? row[j] : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            uint4 q;
-                            q.x = combine_bf16x2(p, r[8 * j + 0], r[8 * j + 1], old[j].x);
-                            q.y = combine_bf16x2(p, r[8 * j + 2], r[8 * j + 3], old[j].y);
-                            q.z = combine_bf16x2(p, r[8 * j + 4], r[8 * j + 5], old[j].z);
-                            q.w = combine_bf16x2(p, r[8 * j + 6], r[8 * j + 7], old[j].w);
-                            row[j] = q;
-                        }
-                    } else if (full) {
-                        uint4 *row = reinterpret_cast<uint4 *>(reinterpret_cast<float *>(p.C) + gi * p.ldc + xp);
-                        uint4 old[8];
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) old[j] = beta_nonzero ? row[j] : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            uint4 q;
-                            q.x = combine_f32(p, r[4 * j + 0], old[j].x);
-                            q.y = combine_f32(p, r[4 * j + 1], old[j].y);
-                            q.z = combine_f32(p, r[4 * j + 2], old[j].z);
-                            q.w = combine_f32(p, r[4 * j + 3], old[j].w);
-                            row[j] = q;
-                        }
-                    } else {
-                        // this lane's columns of the part that are in the output: [e0, e1)
-                        int64_t lo_c = xp, hi_c = xp + 32 < p.n ? xp + 32 : p.n;
-                        if (lower) hi_c = hi_c < gi + 1 ? hi_c : gi + 1;  // j <= i
-                        else lo_c = lo_c > gi ? lo_c : gi;               // j >= i
-                        const int e0 = gi < p.m ? static_cast<int>(lo_c - xp) : 32;
-                        const int e1 = gi < p.m ? static_cast<int>(hi_c - xp) : 0;
-                        if (bf16_out) {
-                            __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.C) + gi * p.ldc + xp;
-#pragma unroll
-                            for (int e = 0; e < 32; ++e) {
-                                if (e < e0 || e >= e1) continue;
-                                const float v = p.alpha * __uint_as_float(r[e]);
-                                dst[e] = __float2bfloat16_rn(beta_nonzero ? fmaf(p.beta, __bfloat162float(dst[e]), v) : v);
-                            }
-                        } else {
-                            float *dst = reinterpret_cast<float *>(p.C) + gi * p.ldc + xp;
-#pragma unroll
-                            for (int e = 0; e < 32; ++e) {
-                                if (e < e0 || e >= e1) continue;
-                                const float v = p.alpha * __uint_as_float(r[e]);
-                                dst[e] = beta_nonzero ? fmaf(p.beta, dst[e], v) : v;
-                            }
-                        }
-                    }
-                }
-            }
         } else if (warp_tma) {
             // Chunks of 128 bytes per row (64 bf16 or 32 fp32 columns), 32 rows: each lane
             // converts its row into a 128B-swizzled staging block, one lane stores it with
@@ -1361,6 +1293,9 @@ __device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUten
                     else mbar_arrive_remote(map_shared_to_rank(acc_empty, 0));
                 }
             }
+            // SYRK tiles across the diagonal: a block wholly outside the triangle is
+            // skipped (the other triangle is neither read nor written).
+            if (block_outside_triangle(p.mode, row0, col0 + 32 * ch)) continue;
             // Row `lane` of this 32 x 32 block into shared memory; 16-byte chunk c of
             // row r goes to slot c ^ (r & 7) so that both passes are conflict-free.
             float4 *srow = reinterpret_cast<float4 *>(stage_buf + lane * 32);
@@ -1415,7 +1350,7 @@ __device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUten
                     } else {
                         *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.C) + gi * p.ldc + gj0) = v4;
                     }
-                } else if (gi < p.m && gj0 < p.n) {
+                } else if (gi < p.m && gj0 < p.n && !vector_outside_triangle(p.mode, gi, gj0)) {
                     write_c4_edge(p, gi, gj0, v4);
                 }
             }
