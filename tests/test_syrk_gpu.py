@@ -72,6 +72,35 @@ def test_syrk_gaussian(uplo, trans, bf16_out, variant):
     cbuf.assert_guard_intact(raw, mask_written=mask)
 
 
+@pytest.mark.parametrize("variant,n", [(3, 4352), (2, 2176)], ids=["pair256x256", "single128x128"])
+@pytest.mark.parametrize("uplo", [0, 1], ids=["lower", "upper"])
+@pytest.mark.parametrize("beta", [1.0, 0.0])
+def test_syrk_grouped_order_two_groups_exact(variant, n, uplo, beta):
+    """17 tile rows: the inside tiles go in a group of 16 tile rows and a group of one,
+    column by column (the upper triangle in the transposed order). With beta = 1 the
+    inside tiles take the group path, whose first chunk of C is loaded before the
+    accumulator is ready, and the diagonal tiles the transposing path with the blocks
+    outside the triangle skipped. Exact on small integers; the other triangle, the
+    ldc padding and the rows below C stay bit-identical."""
+    import blas3_tensor_core_gb300 as bm
+    k = 136
+    with tile_variant(variant):
+        st, rows, cols = bm.bm_syrk_bf16_tile_order(uplo, n, k)
+        assert st == 0
+    tile = 256 if variant == 3 else 128
+    assert (n + tile - 1) // tile == 17 and len(rows) == 17 + 17 * 16 // 2
+    A = _a(n, k, 0, "int", seed=71, lo=-8, hi=8)
+    c0 = gen.integers(72, n * n, -50, 50).reshape(n, n).astype(np.float32)
+    c0 = np.tril(c0) + np.tril(c0, -1).T
+    cbuf = CBuffer(n, n, n + 4, False, init=c0)
+    with tile_variant(variant):
+        got, raw = run_syrk(uplo, 0, n, k, 1.0, A, beta, cbuf)
+    ref, _ = oracle.default().syrk(uplo, 0, n, k, 1.0, A, beta, c0)
+    mask = _mask(n, uplo)
+    assert np.array_equal(got[mask], ref[mask])
+    cbuf.assert_guard_intact(raw, mask_written=mask)
+
+
 def test_syrk_alpha_zero_scales_triangle_only():
     n, k = 200, 64
     A = np.full((n, 72), gen.BF16_NAN, np.uint16)
