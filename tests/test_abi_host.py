@@ -384,3 +384,27 @@ def test_syrk_tile_order_argument_errors(lib):
     assert f(bm.BM_LOWER, 1000, 64, p.tiles, None, None) == bm.BM_ERR_INVALID_VALUE
     assert f(7, 1000, 64, p.tiles, buf.ctypes.data, buf.ctypes.data) == bm.BM_ERR_INVALID_VALUE
     assert f(bm.BM_LOWER, 0, 64, 0, None, None) == bm.BM_OK
+
+
+def test_short_k_bf16_gemms_plan_single_sm_tiles(lib):
+    """BF16 GEMMs of at most five 64-deep k-blocks (K <= 320) take 128 x 256 single-SM
+    tiles; from six k-blocks on, outputs that fill half the SM pairs take 256 x 256 pairs."""
+    for m, n, k in [(4096, 4096, 256), (4096, 4096, 320), (8192, 8192, 256), (2048, 2048, 64)]:
+        p = bm.bm_gemm_bf16_plan(m, n, k, 0)[1]
+        assert (p.tile_m, p.tile_n, p.cta_pair) == (128, 256, 1), (m, n, k)
+    for m, n, k in [(4096, 4096, 384), (4096, 4096, 512), (8192, 8192, 512)]:
+        p = bm.bm_gemm_bf16_plan(m, n, k, 0)[1]
+        assert (p.tile_m, p.tile_n, p.cta_pair) == (256, 256, 2), (m, n, k)
+
+
+def test_full_splits_capped_at_14_ways(lib):
+    """Every tile of a small output is split along K at most 14 ways: 512^2 x 8192 and
+    x 4096 split their 8 tiles 13 ways; SYRK 512 x 8192 its 6 tiles 13 ways."""
+    for k in (4096, 8192):
+        need = bm.bm_gemm_bf16_workspace_size(512, 512, k)
+        p = bm.bm_gemm_bf16_plan(512, 512, k, need)[1]
+        assert p.tiles == 8 and p.k_splits == 13 and p.kernels == 2, k
+    for uplo in (bm.BM_LOWER, bm.BM_UPPER):
+        need = bm.bm_syrk_bf16_workspace_size(uplo, 512, 8192)
+        p = bm.bm_syrk_bf16_plan(uplo, 512, 8192, need)[1]
+        assert p.tiles == 6 and p.k_splits == 13 and p.kernels == 2
