@@ -272,6 +272,27 @@ def test_tail_split_ragged_many_splits_bf16_beta():
                   "tail split x10")
 
 
+def test_beta_tail_split_then_whole_tiles_whole_output_exact():
+    """beta != 0 with a tail split summed in the kernel: 2560 x 2048 x 3072 has 80 pair
+    tiles = 76 + 4, and the 4 are split 12 ways. The 48 split units go first (transposing
+    path, partials, in-kernel sum) and their SM pairs then run whole tiles through the
+    group path (TMA load of C, combine, store), whose first C chunk is loaded early only
+    when the half's staging block is free. Small integers make every element exact, so
+    the whole output is compared with the oracle bit for bit."""
+    import blas3_tensor_core_gb300 as bm
+    t = torch()
+    m, n, k = 2560, 2048, 3072
+    need = bm.bm_gemm_bf16_workspace_size(m, n, k)
+    A, B = _operands(m, n, k, 0, 0, "int", seed=91, lo=-2, hi=2)
+    c0 = gen.integers(92, m * n, -30, 30).reshape(m, n).astype(np.float32)
+    ws = t.full((need // 4,), float("nan"), dtype=t.float32, device="cuda")
+    cbuf = CBuffer(m, n, n + 4, False, init=c0)
+    got, raw = run_gemm(m, n, k, 0, 0, 1.0, A, B, -1.0, cbuf, workspace=ws)
+    cbuf.assert_guard_intact(raw)
+    ref, _ = orc().gemm(m, n, k, 0, 0, 1.0, A, B, -1.0, c0)
+    assert np.array_equal(got, ref)
+
+
 @pytest.mark.parametrize("bf16_out", [False, True])
 def test_tail_split_graph_replays(bf16_out):
     """A CUDA graph replays its calls with the tags they were captured with; the
