@@ -46,7 +46,7 @@ class Plan(ctypes.Structure):
                 ("stages", ctypes.c_int32), ("tiles", ctypes.c_int64), ("k_splits", ctypes.c_int32),
                 ("ctas", ctypes.c_int32), ("cta_pair", ctypes.c_int32), ("kernels", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_size_t), ("split_tiles", ctypes.c_int64),
-                ("stage_kblocks", ctypes.c_int32)]
+                ("stage_kblocks", ctypes.c_int32), ("n_splits", ctypes.c_int32)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}

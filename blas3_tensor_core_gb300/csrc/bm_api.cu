@@ -345,6 +345,7 @@ struct Plan {
     int64_t tiles_m = 0, tiles_n = 0, num_tiles = 0;
     int64_t full_tiles = 0, num_units = 0;  // whole tiles first; the rest are split k_splits ways
     int k_splits = 1, kb_per_split = 0, kb_total = 0;
+    int n_split = 1;         // 2: the tiles after full_tiles run as two N halves each
     int ctas = 0;
     int fixup = 0;           // split tiles reduced inside the kernel (no reduce kernel)
     size_t slot_bytes = 0;   // partial slots at the start of the workspace; fixup counters follow
@@ -384,7 +385,7 @@ void syrk_coords(int mode, int64_t tiles_m, int64_t tiles_n, int tile_m, int bn,
 // Persistent grid: one CTA (or CTA pair) per SM (pair of SMs), never more than the work units.
 void size_grid(Plan &pl, int sms, int pair_clusters)
 {
-    pl.num_units = pl.full_tiles + (pl.num_tiles - pl.full_tiles) * pl.k_splits;
+    pl.num_units = pl.full_tiles + (pl.num_tiles - pl.full_tiles) * (pl.n_split > 1 ? pl.n_split : pl.k_splits);
     if (pl.pair == 2) pl.ctas = static_cast<int>(2 * std::min<int64_t>(pl.num_units, pair_clusters));
     else pl.ctas = static_cast<int>(std::min<int64_t>(pl.num_units, sms));
 }
@@ -494,9 +495,16 @@ Plan plan_gemm(int64_t m, int64_t n, int64_t k, size_t ws_bytes, int sms, int pa
         } else {
             // The last wave is at most half full: split its tiles along K over the idle slots.
             const int64_t tail = pl.num_tiles % slots;
-            if (tail > 0 && tail * 2 <= slots)
+            if (tail > 0 && tail * 2 <= slots) {
                 try_split(pl, tail, slots / tail, std::min(ws_bytes, kTailSplitMaxBytes),
                           elem != bm::ELEM_E4M3 && !beta_nonzero ? kTailSplitMinGainUsBeta0 : kSplitMinGainUs);
+                // No K split: run each tail tile as two N halves on two SM pairs
+                // (256 x 256 bf16 pair tiles), with no partial sums.
+                if (pl.k_splits == 1 && pl.variant == kPair256 && elem == bm::ELEM_BF16) {
+                    pl.n_split = 2;
+                    pl.full_tiles = pl.num_tiles - tail;
+                }
+            }
         }
     }
     size_grid(pl, sms, pair_clusters);
@@ -590,6 +598,13 @@ bm_status launch(const Plan &pl, const CUtensorMap &ta, const CUtensorMap &tb, b
     prm.tma_c = 0;
     const bm_ctype ct = prm.c_bf16 ? BM_C_BF16 : BM_C_F32;
     if (encode_c_tile(&tc, prm.C, ct, prm.m, prm.n, prm.ldc, prm.beta != 0.0f ? bm::CTA_M : 32u)) prm.tma_c = 1;
+    // Half units place their columns in the TMA-store and group epilogues only: a call
+    // whose C cannot take a tensor map runs its tail tiles whole.
+    if (prm.n_split > 1 && !prm.tma_c) {
+        prm.n_split = 1;
+        prm.full_tiles = prm.num_tiles;
+        prm.num_units = prm.num_tiles;
+    }
     CUtensorMap tp;
     std::memset(&tp, 0, sizeof(tp));
     prm.store_p_tma = 0;
@@ -710,6 +725,7 @@ void fill_params(bm::GemmParams &prm, const Plan &pl)
     prm.full_tiles = pl.full_tiles;
     prm.num_units = pl.num_units;
     prm.k_splits = pl.k_splits;
+    prm.n_split = pl.n_split;
     prm.kb_per_split = pl.kb_per_split;
     prm.kb_total = pl.kb_total;
 }
@@ -728,6 +744,7 @@ void export_plan(const Plan &pl, bm_plan *plan)
     plan->kernels = pl.k_splits > 1 && !pl.fixup ? 2 : 1;
     plan->workspace_bytes = pl.k_splits > 1 ? pl.ws_bytes : 0;
     plan->stage_kblocks = kVariantStageKBlocks[pl.variant];
+    plan->n_splits = pl.n_split;
 }
 
 // Pair-cluster capacity for planning without a device (host-only planning): one per SM pair.

@@ -95,9 +95,11 @@ struct GemmParams {
     int mode;          // MODE_*
     int64_t tiles_m, tiles_n;
     int64_t num_tiles;  // GEMM: tiles_m * tiles_n; SYRK: tiles touching the triangle
-    int64_t full_tiles; // tiles [0, full_tiles) run whole; each later tile is split k_splits ways
-    int64_t num_units;  // full_tiles + (num_tiles - full_tiles) * k_splits
+    int64_t full_tiles; // tiles [0, full_tiles) run whole; each later tile is split k_splits (or n_split) ways
+    int64_t num_units;  // full_tiles + (num_tiles - full_tiles) * (k_splits or n_split)
     int k_splits;       // > 1: split units write fp32 partials, summed in this kernel (fixup) or by a second one
+    int n_split;        // 2: each later tile runs as two units of half its columns (256 x 256 pair
+                        // tiles of GEMM only; MMA N = 128, no partial sums); k_splits is then 1
     int kb_per_split;   // k-blocks (128 bytes of K each) per split
     int kb_total;       // ceil(k / elements per k-block)
     int group_m;        // grouped raster: tile rows per group
@@ -185,6 +187,7 @@ struct Unit {
     int64_t tm, tn;
     int kb0, kb1;     // k-blocks of this unit
     int64_t slot;     // partial-sum slot (split units only), -1 for a whole tile
+    int nh;           // N half of a tile split along N (0 or 1), -1 otherwise
 };
 
 // Does tile (tm, tn) (TM x BN) lie entirely in the referenced SYRK triangle?
@@ -334,9 +337,24 @@ __device__ __forceinline__ void tile_coords(const GemmParams &p, int64_t t, int6
     }
 }
 
-// Work unit u: a whole tile, or one K range of a split tile. With the reduce
-// kernel the split units come last, so with units handed out round-robin they
-// fill the otherwise partly idle last wave. With the in-kernel reduction they
+// Output column of accumulator column j (a multiple of 32) of a unit whose tile
+// starts at column col0. A whole tile maps j to col0 + j. A half unit (nh >= 0;
+// 256-wide tiles on SM pairs) ran its MMAs with N = BN / 2 over rows nh * BN / 4 ..
+// of each CTA's half of the tile's B rows, so its columns [0, BN / 4) are tile
+// columns nh * BN / 4 + [0, BN / 4) and the rest lie BN / 2 further on.
+template <int BN, int PAIR = 2>
+__device__ __forceinline__ int64_t unit_col(int64_t col0, int nh, int j)
+{
+    if constexpr (!(PAIR == 2 && BN == 256)) return col0 + j;  // no half units in other copies
+    if (nh < 0) return col0 + j;
+    constexpr int q = BN / 4;
+    return col0 + static_cast<int64_t>(j / q) * (BN / 2) + nh * q + (j % q);
+}
+
+// Work unit u: a whole tile, one K range of a split tile, or one N half of a
+// tile split along N. With the reduce kernel (and with N halves) the split
+// units come last, so with units handed out round-robin they fill the
+// otherwise partly idle last wave. With the in-kernel reduction they
 // come first: the reduction then runs in the epilogue while the next tile's
 // mainloop proceeds, instead of after the last wave.
 template <int TM, int BN, bool SYRK = true>
@@ -344,21 +362,32 @@ __device__ __forceinline__ Unit map_unit(const GemmParams &p, int64_t u)
 {
     Unit r;
     int64_t t;
-    const int64_t split_units = p.num_units - p.full_tiles;
-    const bool whole = p.fixup ? u >= split_units : u < p.full_tiles;
-    if (whole) {
-        t = p.fixup ? u - split_units : u;
+    r.nh = -1;
+    if (p.n_split > 1) {
+        // whole tiles first; then the two N halves of each later tile, one unit each
+        const int64_t v = u - p.full_tiles;
+        t = v < 0 ? u : p.full_tiles + (v >> 1);
+        r.nh = v < 0 ? -1 : static_cast<int>(v & 1);
         r.kb0 = 0;
         r.kb1 = p.kb_total;
         r.slot = -1;
     } else {
-        const int64_t v = p.fixup ? u : u - p.full_tiles;
-        const int64_t local = v / p.k_splits;
-        const int split = static_cast<int>(v - local * p.k_splits);
-        t = p.full_tiles + local;
-        r.kb0 = split * p.kb_per_split;
-        r.kb1 = min(p.kb_total, r.kb0 + p.kb_per_split);
-        r.slot = p.k_splits > 1 ? v : -1;
+        const int64_t split_units = p.num_units - p.full_tiles;
+        const bool whole = p.fixup ? u >= split_units : u < p.full_tiles;
+        if (whole) {
+            t = p.fixup ? u - split_units : u;
+            r.kb0 = 0;
+            r.kb1 = p.kb_total;
+            r.slot = -1;
+        } else {
+            const int64_t v = p.fixup ? u : u - p.full_tiles;
+            const int64_t local = v / p.k_splits;
+            const int split = static_cast<int>(v - local * p.k_splits);
+            t = p.full_tiles + local;
+            r.kb0 = split * p.kb_per_split;
+            r.kb1 = min(p.kb_total, r.kb0 + p.kb_per_split);
+            r.slot = p.k_splits > 1 ? v : -1;
+        }
     }
     tile_coords<TM, BN, SYRK>(p, t, r.tm, r.tn);
     return r;
@@ -577,6 +606,19 @@ __device__ __forceinline__ void pack_row_bf16(uint32_t (&h)[32], const uint32_t 
 {
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
+        const float x0 = __uint_as_float(r[2 * i]);
+        const float x1 = __uint_as_float(r[2 * i + 1]);
+        const __nv_bfloat162 b = SCALE ? __floats2bfloat162_rn(alpha * x0, alpha * x1) : __floats2bfloat162_rn(x0, x1);
+        h[i] = *reinterpret_cast<const uint32_t *>(&b);
+    }
+}
+
+// 32 fp32 accumulator values (times alpha) as 16 packed bf16 pairs, in column order.
+template <bool SCALE>
+__device__ __forceinline__ void pack_32_bf16(uint32_t *h, const uint32_t (&r)[32], float alpha)
+{
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
         const float x0 = __uint_as_float(r[2 * i]);
         const float x1 = __uint_as_float(r[2 * i + 1]);
         const __nv_bfloat162 b = SCALE ? __floats2bfloat162_rn(alpha * x0, alpha * x1) : __floats2bfloat162_rn(x0, x1);
@@ -908,7 +950,7 @@ __device__ __forceinline__ void run_mma(const GemmParams &p, uint32_t ring, uint
 {
     using Cfg = KernelCfg<BN, STAGES, PAIR, ELEM, KPS>;
     const int64_t units = p.num_units;
-    const uint32_t idesc = idesc_f32acc(Cfg::TILE_M, BN, ELEM == ELEM_BF16 ? 1u : 0u, p.a_mn_major, p.b_mn_major);
+
     // Shared-memory descriptors are built once: a template with the start address
     // left at 0, plus the address >> 4 in the low 14 bits per MMA. Shared addresses
     // are below 256 KB, so the sum never carries into the next field. Steps, in
@@ -937,6 +979,13 @@ __device__ __forceinline__ void run_mma(const GemmParams &p, uint32_t ring, uint
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        // N halves (pair 256 x 256 tiles): N = BN / 2 over rows nh * 64 .. of each CTA's
+        // B tile; the second half starts one 64-row chunk (M/N-major) or 64 x 128 bytes
+        // (K-major) in.
+        const uint32_t idesc = idesc_f32acc(Cfg::TILE_M, w.nh < 0 ? BN : BN / 2, ELEM == ELEM_BF16 ? 1u : 0u,
+                                            p.a_mn_major, p.b_mn_major);
+        const uint32_t b_nh =
+            w.nh > 0 ? (p.b_mn_major ? static_cast<uint32_t>(Cfg::CHUNK_BYTES) : 64u * 128u) / 16u : 0u;
         for (int kb = kb0; kb < kb1; kb += KPS) {
             if (!wait_one(bar0 + 8u * stage, phase, abort_flag, p.timeout_ns)) {
                 ok = false;
@@ -948,7 +997,7 @@ __device__ __forceinline__ void run_mma(const GemmParams &p, uint32_t ring, uint
             for (int sub = 0; sub < nkb; ++sub) {
                 // k-block `sub` of the stage
                 const uint64_t a0 = a_tpl + (st >> 4) + a_sub * sub;
-                const uint64_t b0 = b_tpl + ((st + Cfg::B_OFFSET) >> 4) + b_sub * sub;
+                const uint64_t b0 = b_tpl + ((st + Cfg::B_OFFSET) >> 4) + b_sub * sub + b_nh;
                 // MXFP8: the k-block's scale atoms into this ring slot's tensor-memory
                 // columns (A's, then B's), ahead of the MMAs that read them. A slot is
                 // rewritten only after the MMAs of its last use have completed: its
@@ -1076,7 +1125,7 @@ __device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUten
         const uint32_t block_addr = smem_addr(block);
         const uint32_t cbar = bar0 + 8u * (2 * STAGES + 5 + half);
         const int32_t ys = static_cast<int32_t>(w.tm * Cfg::TILE_M + rank * CTA_M);
-        const int32_t xs0 = static_cast<int32_t>(w.tn * BN + static_cast<int64_t>(half) * (p.c_bf16 ? 64 : 32));
+        const int32_t xs0 = static_cast<int32_t>(unit_col<BN, PAIR>(w.tn * BN, w.nh, half * (p.c_bf16 ? 64 : 32)));
         const bool pre = group && block_free && issuer && ys < p.m && xs0 < p.n;
         if (pre) {
             mbar_arrive_expect_tx(cbar, GROUP_BLOCK_BYTES);
@@ -1101,6 +1150,8 @@ __device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUten
                                             static_cast<int64_t>(rank * CTA_M + quad * 32) * BN;
         const int64_t row0 = w.tm * Cfg::TILE_M + rank * CTA_M + quad * 32;
         const int64_t col0 = w.tn * BN;
+        // accumulator columns of this unit (half units exist only for 256 x 256 pair tiles)
+        const int acc_cols = (PAIR == 2 && BN == 256 && w.nh >= 0) ? BN / 2 : BN;
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN);
         if (group) {
             // Per chunk of 128 bytes per row (64 bf16 or 32 fp32 columns), one thread of
@@ -1111,12 +1162,12 @@ __device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUten
             const CUtensorMap *map = tmC;
             const bool bf16_out = p.c_bf16 != 0;
             const int cw = bf16_out ? 64 : 32;
-            const int nchunks = BN / cw;
+            const int nchunks = acc_cols / cw;
             uint4 *myrow = reinterpret_cast<uint4 *>(block + (quad * 32 + lane) * 128);
             const bool rows_in = ys < p.m;
             bool gok = true, loading = pre;
             for (int c = half; c < nchunks; c += 2) {
-                const int32_t xs = static_cast<int32_t>(col0 + static_cast<int64_t>(c) * cw);
+                const int32_t xs = static_cast<int32_t>(unit_col<BN, PAIR>(col0, w.nh, c * cw));
                 const bool live = rows_in && xs < p.n;  // the same for the whole half
                 if (issuer && live && !(c == half && pre)) {  // (or it went out before the wait)
                     mbar_arrive_expect_tx(cbar, GROUP_BLOCK_BYTES);
@@ -1194,25 +1245,29 @@ __device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUten
             const CUtensorMap *map = to_slot ? tmP : tmC;
             const bool bf16_out = !to_slot && p.c_bf16;
             const int cw = bf16_out ? 64 : 32;
-            const int nchunks = BN / cw;
+            const int nchunks = acc_cols / cw;
             const uint32_t stage_addr = smem_addr(stage_buf);
             const int64_t slot_row = to_slot ? w.slot * Cfg::TILE_M + rank * CTA_M + quad * 32 : 0;
             constexpr bool kReadAllFirst = BN == 256 && EPI == EPI_STORE;
             if (kReadAllFirst && bf16_out) {
-                // Both chunks of this warp (64-column chunks half and half + 2) are read from
-                // tensor memory and packed to bf16 before any store, so the accumulator goes
-                // back to the MMA warp without waiting behind a store: the C stores queue on
-                // the SM's TMA unit with the operand copies, and with short K the next tile's
-                // MMAs are ready long before the stores have drained.
+                // Both chunks of this warp (64-column chunks half and half + 2; a half unit
+                // has only the first) are read from tensor memory and packed to bf16 before
+                // any store, so the accumulator goes back to the MMA warp without waiting
+                // behind a store: the C stores queue on the SM's TMA unit with the operand
+                // copies, and with short K the next tile's MMAs are ready long before the
+                // stores have drained.
+                const bool two = w.nh < 0;
                 uint32_t h[2][32];
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
-                    uint32_t r[64];
-                    const uint32_t col = static_cast<uint32_t>((half + 2 * j) * 64);
-                    tmem_load_32cols(taddr + col, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-                    tmem_load_32cols(taddr + col + 32u, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
-                    if (p.alpha == 1.0f) pack_row_bf16<false>(h[j], r, p.alpha);
-                    else pack_row_bf16<true>(h[j], r, p.alpha);
+                    if (j == 1 && !two) continue;
+#pragma unroll
+                    for (int part = 0; part < 2; ++part) {  // 32 columns at a time
+                        uint32_t r[32];
+                        tmem_load_32cols(taddr + static_cast<uint32_t>((half + 2 * j) * 64 + 32 * part), r);
+                        if (p.alpha == 1.0f) pack_32_bf16<false>(h[j] + 16 * part, r, p.alpha);
+                        else pack_32_bf16<true>(h[j] + 16 * part, r, p.alpha);
+                    }
                 }
                 tc_fence_before_sync();
                 __syncwarp();
@@ -1223,12 +1278,13 @@ __device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUten
                 }
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
+                    if (j == 1 && !two) continue;
                     if (lane == 0) bulk_wait_group_read0();  // the previous store has read the staging block
                     __syncwarp();
                     stage_row_packed(reinterpret_cast<uint4 *>(stage_buf) + lane * 8, h[j], lane);
                     fence_proxy_async_shared();
                     __syncwarp();
-                    const int64_t cx = col0 + static_cast<int64_t>(half + 2 * j) * 64;
+                    const int64_t cx = unit_col<BN, PAIR>(col0, w.nh, (half + 2 * j) * 64);
                     if (lane == 0 && row0 < p.m && cx < p.n) {
                         tma_store_2d(map, stage_addr, static_cast<int32_t>(cx), static_cast<int32_t>(row0));
                         bulk_commit_group();
@@ -1270,7 +1326,7 @@ __device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUten
                             tma_store_2d(map, stage_addr, c * cw, static_cast<int32_t>(slot_row));
                             bulk_commit_group();
                         } else {
-                            const int64_t cx = col0 + static_cast<int64_t>(c) * cw;
+                            const int64_t cx = unit_col<BN, PAIR>(col0, w.nh, c * cw);
                             if (row0 < p.m && cx < p.n) {
                                 tma_store_2d(map, stage_addr, static_cast<int32_t>(cx), static_cast<int32_t>(row0));
                                 bulk_commit_group();

@@ -331,14 +331,17 @@ BM_API const char *bm_status_string(bm_status status);
  * (tile_m x tile_n, k-block tile_k), ring stages (of stage_kblocks k-blocks
  * each), number of output tiles
  * visited, K splits and how many tiles are split (the tiles of a last, partly
- * filled wave, summed inside the GEMM kernel, or all tiles when there are too
- * few to fill the GPU, summed by a second kernel), CTAs launched, CTAs per
- * output tile (2 = an SM pair working on one tile), and the number of kernels
- * one call launches. Performs the same size checks as
+ * filled wave: split along K and summed inside the GEMM kernel, or, for bf16
+ * GEMMs on 256 x 256 pair tiles where no K split pays, run as two halves of
+ * their columns on two SM pairs, n_splits == 2; or all tiles when there are too
+ * few to fill the GPU, split along K and summed by a second kernel), CTAs
+ * launched, CTAs per output tile (2 = an SM pair working on one tile), and the
+ * number of kernels one call launches. Performs the same size checks as
  * the call (no pointers are given). On a machine without a usable GPU the
  * plan assumes 152 SMs. A GEMM's plan is the one for beta == 0: with
- * beta != 0 a tail split needs a larger saving, so such a call may split
- * fewer tiles (bm_gemm_bf16_workspace_size covers both).
+ * beta != 0 a tail split along K needs a larger saving, so such a call may
+ * split its tail tiles into N halves instead (bm_gemm_bf16_workspace_size
+ * covers both).
  */
 typedef struct {
     int32_t tile_m, tile_n, tile_k;
@@ -351,6 +354,7 @@ typedef struct {
     size_t workspace_bytes;
     int64_t split_tiles;
     int32_t stage_kblocks;
+    int32_t n_splits;   /* 2: the split_tiles tiles each run as two halves of their columns (no partials) */
 } bm_plan;
 
 BM_API bm_status bm_gemm_bf16_plan(int64_t m, int64_t n, int64_t k, size_t workspace_bytes, bm_plan *plan);

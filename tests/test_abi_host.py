@@ -247,11 +247,12 @@ def test_tail_split_plans(lib):
     assert need == 2 * 28 * 256 * 256 * 4 + 28 * 2 * 8 * 8
     p = bm.bm_gemm_bf16_plan(4096, 4096, 4096, need)[1]
     assert (p.split_tiles, p.k_splits, p.kernels, p.ctas) == (28, 2, 1, 152)
-    # one byte short of the counters: no split
+    # one byte short of the counters: no K split
     assert bm.bm_gemm_bf16_plan(4096, 4096, 4096, need - 1)[1].k_splits == 1
-    # no workspace: whole tiles only
+    # no workspace: no K split; the 28 tail tiles run as two halves of their columns each
+    # (no partial sums, so no workspace), on 56 SM pairs
     p = bm.bm_gemm_bf16_plan(4096, 4096, 4096, 0)[1]
-    assert (p.split_tiles, p.k_splits, p.kernels) == (0, 1, 1)
+    assert (p.split_tiles, p.k_splits, p.n_splits, p.kernels, p.workspace_bytes) == (28, 1, 2, 1, 0)
     # dX 2048x5120x5120: 160 tiles = 2 waves + 8; split 7 ways within the 16 MiB tail budget
     # (8 ways would need 16 MiB of slots plus the counters)
     p = bm.bm_gemm_bf16_plan(2048, 5120, 5120, 1 << 30)[1]
@@ -262,10 +263,14 @@ def test_tail_split_plans(lib):
     assert (p.split_tiles, p.k_splits) == (20, 3)              # 3-way: 21 of 32 k-blocks saved, 5.4 us
     p = bm.bm_gemm_bf16_plan(5120, 5120, 4096, 1 << 30)[1]
     assert p.split_tiles == 20 and p.k_splits == 3
-    p = bm.bm_gemm_bf16_plan(4096, 4096, 1024, 1 << 30)[1]     # 2-way: 8 k-blocks, 2 us
-    assert p.split_tiles == 0
+    p = bm.bm_gemm_bf16_plan(4096, 4096, 1024, 1 << 30)[1]     # 2-way: 8 k-blocks, 2 us: no K split,
+    assert (p.split_tiles, p.k_splits, p.n_splits) == (28, 1, 2)  # N halves instead
     p = bm.bm_gemm_bf16_plan(4096, 4096, 2048, 1 << 30)[1]     # 2-way: 16 k-blocks, 4.1 us
-    assert (p.split_tiles, p.k_splits) == (28, 2)
+    assert (p.split_tiles, p.k_splits, p.n_splits) == (28, 2, 1)
+    # N halves are for 256 x 256 bf16 pair tiles only: single-SM tiles (short K) and E4M3 keep
+    # whole tail tiles
+    p = bm.bm_gemm_bf16_plan(4096, 4096, 256, 1 << 30)[1]
+    assert p.cta_pair == 1 and p.n_splits == 1
     # a last wave more than half full is not split
     p = bm.bm_gemm_bf16_plan(8192, 8192 - 1024, 4096, 1 << 30)[1]  # 32 x 28 = 896 tiles = 11 waves + 60
     assert p.split_tiles == 0 and p.k_splits == 1

@@ -272,6 +272,32 @@ def test_tail_split_ragged_many_splits_bf16_beta():
                   "tail split x10")
 
 
+@pytest.mark.parametrize("m,n,k,ta,tb", [(2560, 2048, 1024, 0, 0), (2560, 2048, 512, 0, 1), (2560, 2048, 1024, 1, 0),
+                                         (2500, 1976, 1000, 0, 0)],
+                         ids=["nn", "nt_k512", "tn", "ragged"])
+@pytest.mark.parametrize("beta", [0.0, -1.0])
+@pytest.mark.parametrize("bf16_out", [False, True])
+def test_n_half_tail_whole_output_exact(m, n, k, ta, tb, beta, bf16_out):
+    """80 pair tiles = 76 + 4 with too few k-blocks for a K split: each of the 4 tail tiles
+    runs as two units of half its columns (MMA N = 128 over half of each CTA's B rows), on
+    8 SM pairs, with no partial sums. Small integers make every element exact, so the whole
+    output (and the guard band) is compared with the oracle; the ragged shape puts part of
+    the last tile column's halves outside n."""
+    import blas3_tensor_core_gb300 as bm
+    p = bm.bm_gemm_bf16_plan(m, n, k, 0)[1]
+    assert (p.split_tiles, p.k_splits, p.n_splits) == (4, 1, 2)
+    A, B = _operands(m, n, k, ta, tb, "int", seed=95, lo=-3, hi=3)
+    c0 = gen.integers(96, m * n, -30, 30).reshape(m, n).astype(np.float32)
+    c_init = gen.f32_to_bf16_bits(c0) if bf16_out else c0
+    cbuf = CBuffer(m, n, _ldc(n, bf16_out), bf16_out, init=c_init)
+    got, raw = run_gemm(m, n, k, ta, tb, 1.0, A, B, beta, cbuf)
+    cbuf.assert_guard_intact(raw)
+    ref, _ = orc().gemm(m, n, k, ta, tb, 1.0, A, B, beta, c_init if beta != 0.0 else None)
+    if bf16_out:
+        ref = gen.bf16_bits_to_f32(gen.f32_to_bf16_bits(ref.astype(np.float32))).astype(np.float64)
+    assert np.array_equal(got, ref)
+
+
 def test_beta_tail_split_then_whole_tiles_whole_output_exact():
     """beta != 0 with a tail split summed in the kernel: 2560 x 2048 x 3072 has 80 pair
     tiles = 76 + 4, and the 4 are split 12 ways. The 48 split units go first (transposing
