@@ -119,6 +119,25 @@ def test_tail_split_summed_in_kernel_without_allocation_three_times():
         assert np.array_equal(got, want), seed
 
 
+@pytest.mark.parametrize("beta", [0.0, -1.0])
+def test_n_half_tail_without_allocation_exact(beta):
+    """2560 x 2048 x 1024: the 4 tail tiles run as N halves (no partials), which needs no
+    scratch at all; the allocation-free call matches the oracle on every element and the
+    workspace entry point bit for bit."""
+    import blas3_tensor_core_gb300 as bm
+    m, n, k = 2560, 2048, 1024
+    st, plan = bm.bm_gemm_bf16_plan(m, n, k, bm.bm_gemm_bf16_workspace_size(m, n, k))
+    assert (plan.split_tiles, plan.k_splits, plan.n_splits, plan.workspace_bytes) == (4, 1, 2, 0)
+    A = operand(m, k, "int", 97, lo=-3, hi=3)
+    B = operand(k, n, "int", 98, lo=-3, hi=3)
+    c0 = gen.integers(99, m * n, -30, 30).reshape(m, n).astype(np.float32)
+    dA, dB = bf16_to_device(A), bf16_to_device(B)
+    want, _ = _with_workspace(m, n, k, dA, dB, k, n, 1.0, beta, c0, False)
+    got = _noalloc(m, n, k, dA, dB, k, n, 1.0, beta, c0, False)
+    assert np.array_equal(got, want)
+    _oracle_check(got, m, n, k, A, B, 1.0, beta, c0, False, f"beta {beta}")
+
+
 def test_without_split_and_with_beta():
     m, n, k = 256, 264, 256
     A = operand(m, k, "normal", 31)
