@@ -386,7 +386,8 @@ class GemmWorkload:
             st, self.plan = bm.bm_gemm_mxfp8_plan(m, n, k, need)
         elif self.e4m3:
             need = bm.bm_gemm_e4m3_workspace_size(m, n, k)
-            # the plan of an E4M3 GEMM equals that of a bf16 GEMM with half the K (same bytes per k-block)
+            # reported as the plan of a bf16 GEMM with half the K (same bytes per k-block); an E4M3
+            # call keeps the larger tail-split threshold, so its tail may run as N halves instead
             st, self.plan = bm.bm_gemm_bf16_plan(m, n, k // 2, need)
         else:
             need = bm.bm_gemm_bf16_workspace_size(m, n, k)

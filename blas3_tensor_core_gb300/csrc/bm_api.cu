@@ -499,8 +499,10 @@ Plan plan_gemm(int64_t m, int64_t n, int64_t k, size_t ws_bytes, int sms, int pa
                 try_split(pl, tail, slots / tail, std::min(ws_bytes, kTailSplitMaxBytes),
                           elem != bm::ELEM_E4M3 && !beta_nonzero ? kTailSplitMinGainUsBeta0 : kSplitMinGainUs);
                 // No K split: run each tail tile as two N halves on two SM pairs
-                // (256 x 256 bf16 pair tiles), with no partial sums.
-                if (pl.k_splits == 1 && pl.variant == kPair256 && elem == bm::ELEM_BF16) {
+                // (256 x 256 bf16 or E4M3 pair tiles), with no partial sums. E4M3
+                // 4096^3: 46.8 -> 45.5 us.
+                if (pl.k_splits == 1 && pl.variant == kPair256 &&
+                    (elem == bm::ELEM_BF16 || elem == bm::ELEM_E4M3)) {
                     pl.n_split = 2;
                     pl.full_tiles = pl.num_tiles - tail;
                 }

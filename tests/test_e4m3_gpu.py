@@ -104,3 +104,23 @@ def test_e4m3_tail_split_summed_in_kernel():
     rows, cols = tile_samples(m, n, per_tile=16, seed=8, extra=(band_r, band_c))
     ref, bound = oracle.default().gemm_e4m3_entries(k, 1.0, A, B, rows, cols)
     assert_parity(got[rows, cols], ref, bound, 1.0, 0.0, None, True, "e4m3 tail split")
+
+
+@pytest.mark.parametrize("bf16_out,beta", [(False, 0.0), (True, -1.0)])
+def test_e4m3_n_half_tail_whole_output_exact(bf16_out, beta):
+    """80 pair tiles = 76 + 4 with too few k-blocks for a K split: the 4 tail tiles run as
+    two units of half their columns each (MMA N = 128 over half of each CTA's B rows), no
+    partial sums. Small integers (exact in E4M3) make every element exact, so the whole
+    output is compared with the oracle."""
+    m, n, k = 2560, 2048, 1024
+    A = _codes(m, k, "int", 31, lo=-4, hi=4)
+    B = _codes(n, k, "int", 32, lo=-4, hi=4)
+    c0 = gen.integers(33, m * n, -30, 30).reshape(m, n).astype(np.float32)
+    c_init = gen.f32_to_bf16_bits(c0) if bf16_out else c0
+    cbuf = CBuffer(m, n, _ldc(n, bf16_out), bf16_out, init=c_init)
+    got, raw = run_gemm_e4m3(m, n, k, 1.0, A, B, beta, cbuf)
+    cbuf.assert_guard_intact(raw)
+    ref, _ = oracle.default().gemm_e4m3(m, n, k, 1.0, A, B, beta, c_init if beta != 0.0 else None)
+    if bf16_out:
+        ref = gen.bf16_bits_to_f32(gen.f32_to_bf16_bits(ref.astype(np.float32))).astype(np.float64)
+    assert np.array_equal(got, ref)
