@@ -814,7 +814,10 @@ def config_record(label, wl, stats, peaks, b2b_ms, graph_ms):
     plan = {}
     if wl.plan is not None:
         plan = {k: getattr(wl.plan, k) for k in ("tile_m", "tile_n", "cta_pair", "tiles", "k_splits",
-                                                  "split_tiles", "kernels", "ctas")}
+                                                  "n_splits", "split_tiles", "kernels", "ctas")}
+        if getattr(wl, "e4m3", False):
+            plan["note"] = ("bf16 plan of K/2; the E4M3 call keeps a 6 us tail-split threshold, so its "
+                            "tail tiles may run as N halves instead of a K split")
     gbs = wl.bytes() / p50 / 1e9
     tpeak = wl.tensor_peak(peaks)
     frac_t, frac_h = tf / tpeak, gbs / peaks["hbm_gbs"]
