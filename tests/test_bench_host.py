@@ -62,3 +62,49 @@ def test_both_arms_share_the_config_dict():
     assert bench.main_config()["workload"] == bench.MAIN["name"]
     # nothing run-specific (L2 sets, plan) inside it: those live beside it in the GPU line
     assert not {"l2", "plan"} & set(bench.main_config())
+
+
+class _FakeWorkload:
+    """Stands in for a configured workload: fixed flops and bytes, an optional plan."""
+
+    def __init__(self, flops, nbytes, plan=None, e4m3=False):
+        self.name, self._f, self._b, self.plan, self.e4m3 = "fake", flops, nbytes, plan, e4m3
+
+    def flops(self):
+        return self._f
+
+    def bytes(self):
+        return self._b
+
+    def tensor_peak(self, peaks):
+        return peaks["bf16_tflops"]
+
+    def kind(self):
+        return "gemm"
+
+    def flop_convention(self):
+        return "2mnk"
+
+
+def test_config_record_bound_fractions_and_plan():
+    """The bound is whichever peak the workload would take longer at; the fraction is taken against
+    that peak; the plan is copied field by field, with a note on the E4M3 stand-in and none without a plan."""
+    import types
+    import bench
+    peaks = {"bf16_tflops": 2000.0, "hbm_gbs": 8000.0}
+    stats = {"p50": 0.1, "p95": 0.12, "min": 0.09, "mean": 0.1, "n": 20}  # ms
+    keys = ("tile_m", "tile_n", "cta_pair", "tiles", "k_splits", "n_splits", "split_tiles", "kernels", "ctas")
+    plan = types.SimpleNamespace(**{k: i + 1 for i, k in enumerate(keys)})
+
+    dense = bench.config_record("C2", _FakeWorkload(1e11, 1e5, plan), stats, peaks, 0.08, 0.07)
+    assert dense["bound"] == "tensor"
+    assert abs(dense["tflops_p50"] - 1000.0) < 1e-9 and dense["roofline_frac_p50"] == 0.5
+    assert dense["roofline_frac_back_to_back"] == 0.625 and dense["us_per_call_graph"] == 70.0
+    assert dense["plan"] == {k: i + 1 for i, k in enumerate(keys)}
+
+    streaming = bench.config_record("C3", _FakeWorkload(1e9, 4e8, None), stats, peaks, 0.1, 0.1)
+    assert streaming["bound"] == "hbm" and streaming["plan"] == {}
+    assert abs(streaming["gbs_p50"] - 4000.0) < 1e-9 and streaming["roofline_frac_p50"] == 0.5
+
+    fp8 = bench.config_record("F8", _FakeWorkload(1e11, 1e5, plan, e4m3=True), stats, peaks, 0.08, 0.07)
+    assert "K/2" in fp8["plan"]["note"]
