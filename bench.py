@@ -866,7 +866,11 @@ def run_gpu_arm(args, dist):
                 "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4),
                 "algorithmic_flops_per_launch": wl.flops(),
                 "algorithmic_bytes_per_launch": wl.bytes(),
-                "kernel": (f"bm_gemm_tcgen05_kernel<{wl.plan.tile_n},{wl.plan.stages},{wl.plan.cta_pair}>"
+                # template <BN, STAGES, PAIR, ELEM, k-blocks per stage, EPI>: a bf16 GEMM whose C
+                # takes a tensor map runs the TMA-store copy (EPI 1) at beta = 0, the combine copy
+                # (EPI 2) otherwise
+                "kernel": (f"bm_gemm_tcgen05_kernel<{wl.plan.tile_n},{wl.plan.stages},{wl.plan.cta_pair},0,"
+                           f"{wl.plan.stage_kblocks},{1 if MAIN['beta'] == 0 else 2}>"
                            + (" + bm_splitk_reduce_kernel" if wl.plan.kernels > 1 else "")),
                 "traffic_source": traffic_src}
     graph_ms = graph_steps(wl, GRAPH_CALLS)
