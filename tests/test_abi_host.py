@@ -413,3 +413,89 @@ def test_full_splits_capped_at_14_ways(lib):
         need = bm.bm_syrk_bf16_workspace_size(uplo, 512, 8192)
         p = bm.bm_syrk_bf16_plan(uplo, 512, 8192, need)[1]
         assert p.tiles == 6 and p.k_splits == 13 and p.kernels == 2
+
+
+def _cdiv(a, b):
+    return -(-a // b)
+
+
+def _check_plan(p, m, n, k, budget, kblock, pair_slots=76, sms=152, tiles=None):
+    """Invariants every plan keeps, whatever the shape and the workspace offered (tiles: the
+    expected tile count where it is not the whole m x n grid)."""
+    assert p.tiles == (tiles if tiles is not None else _cdiv(m, p.tile_m) * _cdiv(n, p.tile_n))
+    assert p.cta_pair in (1, 2) and (p.cta_pair == 1 or p.tile_m == 256)
+    assert 0 <= p.split_tiles <= p.tiles and p.k_splits >= 1 and p.n_splits in (1, 2)
+    kb = _cdiv(k, kblock)
+    if p.k_splits > 1:
+        per = _cdiv(kb, p.k_splits)
+        assert per >= 4 and _cdiv(kb, per) == p.k_splits      # every part keeps >= 4 k-blocks, none empty
+        assert 0 < p.workspace_bytes <= budget
+        assert p.n_splits == 1
+        if p.kernels == 2:                                      # every tile split, summed by a second kernel
+            assert p.split_tiles == p.tiles and p.k_splits <= 14
+            assert p.workspace_bytes == p.k_splits * p.tiles * p.tile_m * p.tile_n * 4
+        else:                                                   # a tail split, summed inside the kernel
+            assert p.kernels == 1 and 0 < p.split_tiles < p.tiles
+            assert p.workspace_bytes <= 16 << 20
+    else:
+        assert p.workspace_bytes == 0 and p.kernels == 1
+    if p.n_splits == 2:                                         # tail tiles as two N halves: no partials
+        assert (p.cta_pair, p.tile_n, p.k_splits, p.workspace_bytes) == (2, 256, 1, 0)
+        assert 0 < p.split_tiles and p.split_tiles * 2 <= pair_slots
+    if p.k_splits == 1 and p.n_splits == 1:
+        assert p.split_tiles == 0
+    slots = pair_slots if p.cta_pair == 2 else sms
+    if 0 < p.split_tiles < p.tiles:                             # only an at most half-full last wave
+        assert p.split_tiles == p.tiles % slots and p.split_tiles * 2 <= slots
+    units = p.tiles - p.split_tiles + p.split_tiles * max(p.k_splits, p.n_splits)
+    assert p.ctas == (2 * min(units, pair_slots) if p.cta_pair == 2 else min(units, sms))
+
+
+def test_gemm_plan_invariants_over_random_shapes(lib):
+    """Seeded random shapes (sizes from 1 to 16384, K up to 32768) and workspace offers:
+    tile counts, split bounds, workspace sizes, half-column units and the grid agree with
+    the planning rules, and the size query returns what an unlimited offer plans."""
+    import random
+    rng = random.Random(20240611)
+    dims = [1, 7, 64, 100, 128, 129, 255, 256, 257, 511, 512, 1000, 1024, 2048, 3000, 4096, 5120, 8192, 16384]
+    for _ in range(400):
+        m, n = rng.choice(dims), rng.choice(dims)
+        k = rng.choice([1, 63, 64, 256, 320, 384, 512, 1024, 2048, 4096, 5000, 8192, 32768])
+        need = bm.bm_gemm_bf16_workspace_size(m, n, k)
+        unlimited = bm.bm_gemm_bf16_plan(m, n, k, 1 << 40)[1]
+        assert need == unlimited.workspace_bytes
+        for budget in (0, need // 2, need, 1 << 40):
+            st, p = bm.bm_gemm_bf16_plan(m, n, k, budget)
+            assert st == 0
+            _check_plan(p, m, n, k, budget, 64)
+            if budget >= need:                                  # enough workspace: the same plan
+                assert (p.k_splits, p.split_tiles, p.n_splits) == (unlimited.k_splits, unlimited.split_tiles,
+                                                                   unlimited.n_splits)
+        p0 = bm.bm_gemm_bf16_plan(m, n, k, 0)[1]
+        assert p0.k_splits == 1 and p0.workspace_bytes == 0
+
+
+def test_mxfp8_and_syrk_plan_invariants_over_random_shapes(lib):
+    """The same invariants for MXFP8 GEMM plans (128-deep k-blocks, no half-column units) and
+    for SYRK plans (only the triangle's tiles, counted by enumeration)."""
+    import random
+    rng = random.Random(7)
+    dims = [1, 100, 128, 129, 256, 300, 512, 1000, 2048, 4096, 8192]
+    for _ in range(150):
+        m, n = rng.choice(dims), rng.choice(dims)
+        k = rng.choice([32, 128, 512, 1024, 4096, 8192, 32768])
+        need = bm.bm_gemm_mxfp8_workspace_size(m, n, k)
+        for budget in (0, need // 2, need, 1 << 40):
+            st, p = bm.bm_gemm_mxfp8_plan(m, n, k, budget)
+            assert st == 0 and p.tile_k == 128 and p.n_splits == 1
+            assert (p.tile_m, p.tile_n, p.cta_pair) in ((256, 256, 2), (256, 128, 2), (128, 128, 1))
+            _check_plan(p, m, n, k, budget, 128)
+    for n in (1, 100, 256, 300, 513, 1000, 2048, 4100, 8192):
+        for k in (64, 512, 4096, 8192, 32768):
+            for uplo in (bm.BM_LOWER, bm.BM_UPPER):
+                need = bm.bm_syrk_bf16_workspace_size(uplo, n, k)
+                for budget in (0, need, 1 << 40):
+                    st, p = bm.bm_syrk_bf16_plan(uplo, n, k, budget)
+                    assert st == 0 and p.n_splits == 1
+                    expect = _syrk_tiles_bruteforce(n, uplo == bm.BM_LOWER, p.tile_m, p.tile_n)
+                    _check_plan(p, n, n, k, budget, 64, tiles=expect)
