@@ -237,9 +237,15 @@ bool encode_bf16_2d(CUtensorMap *map, const void *base, int64_t inner, int64_t o
 // columns) x `rows` rows, 128-byte swizzle (the staging layout the epilogue
 // writes). 32 rows: one warp's stores (beta == 0); 128 rows: one CTA's rows,
 // loaded and stored by a half of the epilogue (beta != 0).
+// No map when a row of C (n elements) does not end on a 16-byte boundary: a
+// tiled TMA store clips the innermost dimension only to whole 16-byte units, so
+// the last box of a row would also write the columns from n up to the next
+// boundary (measured: fp32 C with n = 2162 had columns 2162 and 2163 of its
+// TMA-stored tiles overwritten). Such calls store C with masked plain stores.
 bool encode_c_tile(CUtensorMap *map, void *C, bm_ctype ct, int64_t m, int64_t n, int64_t ldc, uint32_t rows)
 {
     const cuuint64_t esz = ct == BM_C_BF16 ? 2u : 4u;
+    if ((static_cast<cuuint64_t>(n) * esz) % 16u != 0) return false;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(m)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldc) * esz};
     cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esz), rows};

@@ -28,7 +28,11 @@
  *   - Alignment (the tensor-memory-accelerator rules quoted in the ablation
  *     plan, section 1.3: 16-byte aligned global addresses): A, B and C must be
  *     16-byte aligned and lda*2, ldb*2, ldc*sizeof(C element) multiples of 16
- *     bytes; otherwise BM_ERR_MISALIGNED and nothing is launched.
+ *     bytes; otherwise BM_ERR_MISALIGNED and nothing is launched. The sizes
+ *     m, n, k need no alignment. When a row of C (n elements) does not end
+ *     on a 16-byte boundary, C is written with masked plain stores instead
+ *     of tensor-memory-accelerator stores (a slower epilogue): those stores
+ *     would also write the columns from n up to the next 16-byte boundary.
  *   - Calls are asynchronous on `stream` (NULL = the legacy default stream).
  *     Argument errors are returned synchronously before anything is queued;
  *     a failed launch returns BM_ERR_CUDA. A device-side wait that runs out

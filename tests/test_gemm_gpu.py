@@ -298,6 +298,38 @@ def test_n_half_tail_whole_output_exact(m, n, k, ta, tb, beta, bf16_out):
     assert np.array_equal(got, ref)
 
 
+@pytest.mark.parametrize("m,n,k,beta,bf16_out,ws", [
+    (2600, 2602, 512, 0.0, False, False),    # 121 whole pair tiles, TMA-store path when aligned
+    (2600, 2605, 512, -1.0, True, False),    # the same, group path when aligned
+    (2225, 2162, 2464, 0.0, False, True),    # 81 pair tiles, the last 5 split 8 ways along K
+    (2225, 2163, 2048, -1.0, True, True),
+    (2219, 2162, 569, -1.0, False, False),   # tail tiles planned as N halves, run whole
+    (700, 1029, 320, 0.0, True, False),      # short K: 128 x 256 tiles on single SMs
+], ids=["pair_f32", "pair_bf16_beta", "tail_k_f32", "tail_k_bf16_beta", "n_half_f32_beta", "single_bf16"])
+def test_row_end_off_16_bytes_leaves_columns_past_n_intact(m, n, k, beta, bf16_out, ws):
+    """A row of C that does not end on a 16-byte boundary (fp32 n = 4q + 2 or 3, bf16 n = 8q + 5):
+    a tiled TMA store would also write the columns from n to the next boundary, so these calls
+    store C with masked plain stores. Small integers: the whole output equals the oracle bit
+    for bit, and the columns past n (inside ldc) and the rows below C keep their canaries."""
+    import blas3_tensor_core_gb300 as bm
+    t = torch()
+    A, B = _operands(m, n, k, 0, 1, "int", seed=97, lo=-3, hi=3)
+    c0 = gen.integers(98, m * n, -30, 30).reshape(m, n).astype(np.float32)
+    c_init = gen.f32_to_bf16_bits(c0) if bf16_out else c0
+    cbuf = CBuffer(m, n, _ldc(n, bf16_out), bf16_out, init=c_init)
+    workspace = None
+    if ws:
+        need = bm.bm_gemm_bf16_workspace_size(m, n, k)
+        assert bm.bm_gemm_bf16_plan(m, n, k, need)[1].k_splits > 1
+        workspace = t.full((need // 4,), float("nan"), dtype=t.float32, device="cuda")
+    got, raw = run_gemm(m, n, k, 0, 1, 1.0, A, B, beta, cbuf, workspace=workspace)
+    cbuf.assert_guard_intact(raw)
+    ref, _ = orc().gemm(m, n, k, 0, 1, 1.0, A, B, beta, c_init if beta != 0.0 else None)
+    if bf16_out:
+        ref = gen.bf16_bits_to_f32(gen.f32_to_bf16_bits(ref.astype(np.float32))).astype(np.float64)
+    assert np.array_equal(got, ref)
+
+
 def test_beta_tail_split_then_whole_tiles_whole_output_exact():
     """beta != 0 with a tail split summed in the kernel: 2560 x 2048 x 3072 has 80 pair
     tiles = 76 + 4, and the 4 are split 12 ways. The 48 split units go first (transposing

@@ -101,6 +101,29 @@ def test_syrk_grouped_order_two_groups_exact(variant, n, uplo, beta):
     cbuf.assert_guard_intact(raw, mask_written=mask)
 
 
+@pytest.mark.parametrize("n,bf16_out,beta", [(1002, False, 1.0), (1005, True, 0.0), (2306, False, 0.0)],
+                         ids=["f32_beta1", "bf16_beta0", "f32_pair"])
+@pytest.mark.parametrize("uplo", [0, 1], ids=["lower", "upper"])
+def test_syrk_row_end_off_16_bytes_exact(n, bf16_out, beta, uplo):
+    """Rows of C that do not end on a 16-byte boundary take masked plain stores for every
+    tile (a TMA store would also write the columns from n to the boundary). Exact on small
+    integers; the other triangle, the columns past n and the rows below C stay unchanged."""
+    k = 256
+    A = _a(n, k, 0, "int", seed=73, lo=-8, hi=8)
+    c0 = gen.integers(74, n * n, -50, 50).reshape(n, n).astype(np.float32)
+    c0 = np.tril(c0) + np.tril(c0, -1).T
+    c_init = gen.f32_to_bf16_bits(c0) if bf16_out else c0
+    per = 8 if bf16_out else 4
+    cbuf = CBuffer(n, n, n + (-n) % per + per, bf16_out, init=c_init)
+    got, raw = run_syrk(uplo, 0, n, k, 1.0, A, beta, cbuf)
+    ref, _ = oracle.default().syrk(uplo, 0, n, k, 1.0, A, beta, c_init if beta != 0.0 else None)
+    if bf16_out:
+        ref = gen.bf16_bits_to_f32(gen.f32_to_bf16_bits(ref.astype(np.float32))).astype(np.float64)
+    mask = _mask(n, uplo)
+    assert np.array_equal(got[mask], ref[mask])
+    cbuf.assert_guard_intact(raw, mask_written=mask)
+
+
 def test_syrk_alpha_zero_scales_triangle_only():
     n, k = 200, 64
     A = np.full((n, 72), gen.BF16_NAN, np.uint16)
