@@ -238,3 +238,25 @@ def test_quantize_then_block_scaled_gemm():
     ref, bound = oracle.default().gemm_mxfp8(m, n, k, 1.0, Qa, Sa, Qw, Sw)
     assert_parity(got, ref, bound, 1.0, 0.0, None, True, "quantize + mxfp8 gemm")
     cbuf.assert_guard_intact(raw)
+
+
+@pytest.mark.parametrize("m,n,k,bf16_out,beta", [(520, 262, 192, False, 0.0), (2304, 2306, 256, True, -1.0)],
+                         ids=["single_f32", "pair_bf16_beta"])
+def test_mxfp8_row_end_off_16_bytes_exact(m, n, k, bf16_out, beta):
+    """Rows of C that do not end on a 16-byte boundary are stored with masked plain stores
+    (a TMA store would also write the columns from n to the boundary). Exact data (scales 2^-1
+    .. 2^1): the whole output equals the oracle, and the columns past n and the rows below C
+    are unchanged."""
+    A = _codes(m, k, "int", 31)
+    B = _codes(n, k, "int", 32)
+    SA = _scales(m, k, 33, 126, 128)
+    SB = _scales(n, k, 34, 126, 128)
+    c0 = gen.integers(35, m * n, -30, 30).reshape(m, n).astype(np.float32)
+    c_init = gen.f32_to_bf16_bits(c0) if bf16_out else c0
+    cbuf = CBuffer(m, n, _ldc(n, bf16_out), bf16_out, init=c_init)
+    got, raw = run_gemm_mxfp8(m, n, k, 1.0, A, SA, B, SB, beta, cbuf)
+    cbuf.assert_guard_intact(raw)
+    ref, _ = oracle.default().gemm_mxfp8(m, n, k, 1.0, A, SA, B, SB, beta, c_init if beta != 0 else None)
+    if bf16_out:
+        ref = gen.bf16_bits_to_f32(gen.f32_to_bf16_bits(ref.astype(np.float32))).astype(np.float64)
+    assert np.array_equal(got, ref), _explain(got, ref)
