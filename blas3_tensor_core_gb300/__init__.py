@@ -270,6 +270,21 @@ def _rowmajor_ld(t, name):
     return max(t.stride(0), 1)
 
 
+def _on_current_device(**tensors):
+    """Every tensor must live on the current CUDA device: the library launches there and takes
+    the pointers as device addresses."""
+    import torch
+    for name, t in tensors.items():
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor (got device {t.device})")
+    current = torch.cuda.current_device()
+    for name, t in tensors.items():
+        if t is not None and t.device.index != current:
+            raise ValueError(f"{name} is on {t.device}, the current device is cuda:{current}")
+
+
 def _stream_handle(stream):
     import torch
     s = torch.cuda.current_stream() if stream is None else stream
@@ -299,6 +314,7 @@ def gemm(A, B, C, alpha=1.0, beta=0.0, transA=False, transB=False, workspace=Non
     if (A.shape[1] if transA else A.shape[0]) != m or (B.shape[1] if transB else B.shape[0]) != k \
             or (B.shape[0] if transB else B.shape[1]) != n:
         raise ValueError("inconsistent shapes")
+    _on_current_device(A=A, B=B, C=C, workspace=workspace)
     ws_ptr, ws_bytes = (None, 0) if workspace is None else (workspace.data_ptr(),
                                                               workspace.numel() * workspace.element_size())
     st = bm_gemm_bf16(m, n, k, int(bool(transA)), int(bool(transB)), float(alpha),
@@ -329,6 +345,7 @@ def syr2k(A, B, C, alpha=1.0, beta=0.0, uplo="L", trans=False, workspace=None, s
     if (A.shape[1] if trans else A.shape[0]) != n:
         raise ValueError("inconsistent shapes")
     lo = BM_LOWER if str(uplo).upper().startswith("L") else BM_UPPER
+    _on_current_device(A=A, B=B, C=C, workspace=workspace)
     st = bm_syr2k_bf16(lo, int(bool(trans)), n, k, float(alpha), A.data_ptr(), _rowmajor_ld(A, "A"),
                        B.data_ptr(), _rowmajor_ld(B, "B"), float(beta), C.data_ptr(), _rowmajor_ld(C, "C"),
                        _ctype(C), *_ws(workspace), _stream_handle(stream))
@@ -348,6 +365,7 @@ def syrk(A, C, alpha=1.0, beta=0.0, uplo="L", trans=False, workspace=None, strea
     if (A.shape[1] if trans else A.shape[0]) != n:
         raise ValueError("inconsistent shapes")
     lo = BM_LOWER if str(uplo).upper().startswith("L") else BM_UPPER
+    _on_current_device(A=A, C=C, workspace=workspace)
     st = bm_syrk_bf16(lo, int(bool(trans)), n, k, float(alpha), A.data_ptr(), _rowmajor_ld(A, "A"),
                       float(beta), C.data_ptr(), _rowmajor_ld(C, "C"), _ctype(C), *_ws(workspace),
                       _stream_handle(stream))

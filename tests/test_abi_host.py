@@ -499,3 +499,37 @@ def test_mxfp8_and_syrk_plan_invariants_over_random_shapes(lib):
                     assert st == 0 and p.n_splits == 1
                     expect = _syrk_tiles_bruteforce(n, uplo == bm.BM_LOWER, p.tile_m, p.tile_n)
                     _check_plan(p, n, n, k, budget, 64, tiles=expect)
+
+
+def test_tensor_helpers_reject_bad_arguments_before_any_call():
+    """The torch-tensor helpers check dtype, shapes, layout and device before they reach the
+    C ABI: a host tensor's address must never be passed on as a device pointer."""
+    import torch
+    bf, f32 = torch.bfloat16, torch.float32
+    A, B, C = torch.zeros(4, 8, dtype=bf), torch.zeros(8, 6, dtype=bf), torch.zeros(4, 6, dtype=f32)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        bm.gemm(A, B, C)
+    with pytest.raises(TypeError):
+        bm.gemm(A.float(), B, C)
+    with pytest.raises(TypeError):
+        bm._ctype(C.to(torch.float16))
+    with pytest.raises(ValueError, match="inconsistent"):
+        bm.gemm(A, B, torch.zeros(4, 7, dtype=f32))
+    with pytest.raises(ValueError, match="inconsistent"):
+        bm.gemm(A, B, C, transA=True)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        bm.gemm(A.t().contiguous(), B.t().contiguous(), C, transA=True, transB=True)
+    with pytest.raises(ValueError, match="row-major"):
+        bm._rowmajor_ld(C.t(), "C")
+    assert bm._rowmajor_ld(C, "C") == 6 and bm._rowmajor_ld(torch.zeros(3, 10)[:, :6], "C") == 10
+    S = torch.zeros(4, 4, dtype=f32)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        bm.syrk(A, S)
+    with pytest.raises(ValueError, match="square"):
+        bm.syrk(A, C)
+    with pytest.raises(ValueError, match="inconsistent"):
+        bm.syrk(A, S, trans=True)
+    with pytest.raises(ValueError, match="same shape"):
+        bm.syr2k(A, B, S)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        bm.syr2k(A, A.clone(), S)
