@@ -1158,7 +1158,9 @@ __device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUten
             // this half loads the chunk of C (its 128 rows) into one 128B-swizzled
             // staging block with a single TMA copy; the four warps each combine their
             // 32 rows in place (beta * c + alpha * acc, as the other paths) and one
-            // TMA copy stores the block back (the map clips rows >= m and columns >= n).
+            // TMA copy stores the block back (the map clips rows >= m and columns >= n;
+            // C has a map only when its rows end on a 16-byte boundary, the unit the
+            // store clips columns to).
             const CUtensorMap *map = tmC;
             const bool bf16_out = p.c_bf16 != 0;
             const int cw = bf16_out ? 64 : 32;
@@ -1240,8 +1242,8 @@ __device__ __forceinline__ void run_epilogue(const CUtensorMap *tmC, const CUten
         } else if (warp_tma) {
             // Chunks of 128 bytes per row (64 bf16 or 32 fp32 columns), 32 rows: each lane
             // converts its row into a 128B-swizzled staging block, one lane stores it with
-            // TMA, into C (the map clips rows >= m and columns >= n) or into the unit's
-            // fp32 partial slot.
+            // TMA, into C (the map clips rows >= m and columns >= n; C has a map only
+            // when its rows end on a 16-byte boundary) or into the unit's fp32 partial slot.
             const CUtensorMap *map = to_slot ? tmP : tmC;
             const bool bf16_out = !to_slot && p.c_bf16;
             const int cw = bf16_out ? 64 : 32;
