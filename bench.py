@@ -719,10 +719,16 @@ def oracle_rows_rate(A, B, cfg, budget_s):
     import oracle
     o = oracle.default()
     m, n, k = cfg["m"], cfg["n"], cfg["k"]
-    rows = 4
-    t0 = time.perf_counter()
-    o.gemm(rows, n, k, 0, 0, 1.0, A[:rows], B)
-    dt = max(time.perf_counter() - t0, 1e-6)
+    # calibrate on a probe that gives every oracle thread rows and runs long enough (>= 2 %
+    # of the budget) that the call's fixed cost (thread start-up) does not shrink the sample
+    rows = min(m, 4 * max(1, o.num_threads()))
+    while True:
+        t0 = time.perf_counter()
+        o.gemm(rows, n, k, 0, 0, 1.0, A[:rows], B)
+        dt = max(time.perf_counter() - t0, 1e-6)
+        if dt >= 0.02 * budget_s or rows >= m:
+            break
+        rows = min(m, rows * 4)
     R = int(max(4, min(m, rows * budget_s / dt)))
     t0 = time.perf_counter()
     ref, bound = o.gemm(R, n, k, 0, 0, 1.0, A[:R], B)

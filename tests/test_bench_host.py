@@ -108,3 +108,21 @@ def test_config_record_bound_fractions_and_plan():
 
     fp8 = bench.config_record("F8", _FakeWorkload(1e11, 1e5, plan, e4m3=True), stats, peaks, 0.08, 0.07)
     assert "K/2" in fp8["plan"]["note"]
+
+
+def test_cpu_baseline_sample_is_sized_and_bounded():
+    """The oracle sample of the CPU baseline: calibrated on a probe, capped at the whole
+    matrix, and its rows equal the oracle's full result for those rows."""
+    import numpy as np
+    import bm_inputs as gen
+    import bench
+    import oracle
+    cfg = dict(bench.MAIN, m=96, n=64, k=128)
+    A = gen.matrix_bf16(96, 128, "normal", 1)
+    B = gen.matrix_bf16(128, 64, "normal", 2)
+    r = bench.oracle_rows_rate(A, B, cfg, budget_s=60.0)        # a tiny matrix: the whole of it
+    assert r["rows"] == 96 and r["ref"].shape == (96, 64) and r["tflops"] > 0 and r["cores"] >= 1
+    full, _ = oracle.default().gemm(96, 64, 128, 0, 0, 1.0, A, B)
+    assert np.array_equal(r["ref"], full)
+    r = bench.oracle_rows_rate(A, B, cfg, budget_s=1e-6)         # no budget: the minimum sample
+    assert r["rows"] == 4
