@@ -345,7 +345,8 @@ BM_API const char *bm_status_string(bm_status status);
  * plan assumes 152 SMs. A GEMM's plan is the one for beta == 0: with
  * beta != 0 a tail split along K needs a larger saving, so such a call may
  * split its tail tiles into N halves instead (bm_gemm_bf16_workspace_size
- * covers both).
+ * covers both). The plan does not see C: a call whose rows of C do not end on
+ * a 16-byte boundary runs tiles planned as N halves whole.
  */
 typedef struct {
     int32_t tile_m, tile_n, tile_k;
