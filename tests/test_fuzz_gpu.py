@@ -68,11 +68,15 @@ def _branch(p):
     return "single" if p.cta_pair == 1 else "pair"
 
 
-def test_cases_reach_every_plan():
-    """Host-only: the drawn cases take the schedule their family is meant to reach."""
-    import blas3_tensor_core_gb300 as bm
+@pytest.fixture(scope="module")
+def lib():
     from blas3_tensor_core_gb300 import build
     build.build()
+
+
+def test_cases_reach_every_plan(lib):
+    """Host-only: the drawn cases take the schedule their family is meant to reach."""
+    import blas3_tensor_core_gb300 as bm
     for family, m, n, k, ws, *_ in CASES:
         need = bm.bm_gemm_bf16_workspace_size(m, n, k) if ws else 0
         assert _branch(bm.bm_gemm_bf16_plan(m, n, k, need)[1]) == family, (family, m, n, k, ws)
@@ -80,10 +84,8 @@ def test_cases_reach_every_plan():
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("case", CASES, ids=[f"{c[0]}_{c[1]}x{c[2]}x{c[3]}" for c in CASES])
-def test_random_plan_whole_output_exact(case):
+def test_random_plan_whole_output_exact(case, lib):
     import blas3_tensor_core_gb300 as bm
-    from blas3_tensor_core_gb300 import build
-    build.build()
     t = torch()
     family, m, n, k, ws, ta, tb, alpha, beta, bf16_out, seed = case
     ra, ca = (k, m) if ta else (m, k)
